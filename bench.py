@@ -1,0 +1,352 @@
+"""Benchmark of the Flint MoE FFN layer on B300.
+
+Default workload: the decode stack -- 47 distinct BF16 MoE layers of the
+H=2048 / I=512 / 256+1-expert shape (about 73 GB of weights resident, far
+larger than L2), per-expert router bias ~ N(0, 0.5), T=1 token per layer
+step, the layers applied one after another to the same x.  One step is one
+pass over the 47 layers (47 flint_moe_forward calls, replayed as one CUDA
+graph).  Metric: MoE-layer tokens per second = 47 * T / step time, and us per
+layer; roofline: unique bytes of touched expert weights per layer / us per
+layer, against the measured HBM copy bandwidth.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl flint|reference]
+                    [--workload decode1|decode8|decode32]
+
+--impl reference times the fp64 CPU oracle on the host cores (a bounded
+sample of the same workload per step).  With N > 1 each rank runs its own
+replica of the stack (the layer does not shard; no collective on the data
+path); value is the sum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+N_LAYERS = 47
+EXPERT_BYTES_BF16 = 3 * 2048 * 512 * 2        # 6,291,456
+ROUTER_BYTES = 256 * 2048 * 2 + 256 * 4
+WORKLOADS = {
+    "decode1": {"T": 1, "x": "gauss", "x_seed": 11},
+    "decode8": {"T": 8, "x": "clustered", "x_seed": 12},
+    "decode32": {"T": 32, "x": "clustered", "x_seed": 13},
+}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="flint", choices=["flint", "reference"])
+    ap.add_argument("--workload", default="decode1", choices=sorted(WORKLOADS))
+    ap.add_argument("--layers", type=int, default=N_LAYERS, help=argparse.SUPPRESS)
+    return ap.parse_args()
+
+
+def peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))), "measured"
+    except Exception:
+        return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [v.strip() for v in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(args):
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "flint" else "gloo"
+        if args.impl == "flint":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return ws, rank, local
+
+
+def x_bits_for(wl):
+    from synth import gen
+    if wl["x"] == "gauss":
+        return gen.x_gaussian(wl["x_seed"], wl["T"])
+    return gen.x_clustered(wl["x_seed"], wl["T"])[0]
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the fp64 oracle on the host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args, wl, ws, rank):
+    import numpy as np
+    from oracle.reference import LayerOracle
+    from synth import device
+
+    if rank != 0:
+        return
+    device.build()
+    T = wl["T"]
+    xb = x_bits_for(wl)
+    n_sample = 2   # layers per step: each step is a bounded sample of the stack
+    orcs = []
+    for l in range(n_sample):
+        lw = device.LayerWeights(1, l, True)
+        orc = LayerOracle.from_bf16_layer(lw)
+        orc.forward(xb)    # copies the touched experts to the host (untimed)
+        orcs.append(orc)
+        del lw
+    cores = os.cpu_count() or 1
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        for orc in orcs:
+            orc.forward(xb)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+    step = sum(times) / len(times)
+    value = n_sample * T / step
+    line = {"metric": f"MoE-layer tokens/s, decode stack T={T}", "value": value, "unit": "layer-tokens/s",
+            "impl": "reference", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": step * 1e3, "higher_is_better": True, "scaling": "weak",
+            "us_per_layer": step * 1e6 / n_sample, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"decode stack, {N_LAYERS} BF16 MoE layers, T={T}, sample of {n_sample} layers per step",
+                       "H": 2048, "I": 512, "experts": 257, "top_k": 6},
+            "vs_baseline": None,
+            "cpu_baseline": {"value": value, "unit": "layer-tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{n_sample} layers of the stack at T={T}, touched experts on the host"},
+            "e2e": {"value": value, "unit": "layer-tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# flint arm
+# ---------------------------------------------------------------------------
+
+def cpu_baseline(wl, stack_layers, cores_hint=None):
+    """The oracle, as it stands, on one decode step of a 2-layer sample."""
+    from oracle.reference import LayerOracle
+    T = wl["T"]
+    xb = x_bits_for(wl)
+    n = 2
+    orcs = [LayerOracle.from_bf16_layer(stack_layers[l]) for l in range(n)]
+    for o in orcs:
+        o.forward(xb)                  # host copies of touched experts (untimed)
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        for o in orcs:
+            o.forward(xb)
+        reps += 1
+        if time.perf_counter() - t0 > 10.0 or reps >= 50:
+            break
+    dt = (time.perf_counter() - t0) / reps
+    return {"value": n * T / dt, "unit": "layer-tokens/s", "cores": os.cpu_count() or 1, "kind": "oracle",
+            "sample": f"{n} layers of the decode stack at T={T} (touched experts copied to host, copy untimed), {reps} reps"}
+
+
+def run_flint(args, wl, ws, rank, local):
+    import numpy as np
+    import torch
+    from sparse_moe_transformer_03_b300 import flint
+    from synth import device
+
+    flint.load_library()
+    device.build()
+    T = wl["T"]
+    L = args.layers
+    pk, pk_kind = peaks()
+
+    t_gen = time.perf_counter()
+    layers = [device.LayerWeights(1, l, True) for l in range(L)]
+    torch.cuda.synchronize()
+    t_gen = time.perf_counter() - t_gen
+    handles = [flint.flint_moe_create(lw.router_W, lw.router_b, list(lw.gate_up[:256]), list(lw.down[:256]),
+                                      (lw.gate_up[256], lw.down[256])) for lw in layers]
+    xb = x_bits_for(wl)
+    x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
+    ys = [torch.empty_like(x) for _ in range(L)]
+
+    # unique touched experts per layer (for the algorithmic byte count)
+    uniq = []
+    for h in handles:
+        idx = torch.empty((T, 6), dtype=torch.int32, device="cuda")
+        w = torch.empty((T, 6), dtype=torch.float32, device="cuda")
+        flint.flint_moe_route_only(h, x, None, T, idx, w)
+        uniq.append(len(set(idx.cpu().numpy().ravel().tolist())))
+    bytes_per_step = sum((u + 1) * EXPERT_BYTES_BF16 for u in uniq)
+
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+
+    def step_direct():
+        for l in range(L):
+            flint.flint_moe_forward(handles[l], x, T, ys[l], stream)
+
+    # capture the 47-layer step as one graph
+    with torch.cuda.stream(stream):
+        step_direct()
+        step_direct()
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step_direct()
+    stream.synchronize()
+
+    def timed(fn, n):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        ev[0].record(stream)
+        for _ in range(n):
+            fn()
+        ev[1].record(stream)
+        ev[1].synchronize()
+        return ev[0].elapsed_time(ev[1]) / n
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
+    stream.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        with torch.cuda.stream(stream):
+            ms = timed(graph.replay, args.steps)
+    torch.cuda.synchronize()
+    clocks = clk.summary()
+    with torch.cuda.stream(stream):
+        ms_direct = timed(step_direct, max(3, args.steps // 2))
+
+    # end to end through the C ABI: pinned host x -> device, 47 forwards, all y -> host
+    x_host = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).pin_memory()
+    y_host = torch.empty((L, T, 2048), dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(x)
+
+    def step_e2e():
+        x_dev.copy_(x_host, non_blocking=True)
+        for l in range(L):
+            flint.flint_moe_forward(handles[l], x_dev, T, ys[l], stream)
+        for l in range(L):
+            y_host[l].copy_(ys[l], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        step_e2e()
+        ms_e2e = timed(step_e2e, max(3, args.steps // 2))
+    stream.synchronize()
+
+    if ws > 1:
+        t = torch.tensor([ms, ms_e2e], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms, ms_e2e = t.tolist()
+
+    us_layer = ms * 1e3 / L
+    value = ws * L * T / (ms * 1e-3)
+    achieved = bytes_per_step / (ms * 1e-3) / 1e9
+    peak_hbm = float(pk["hbm_gbs"])
+    line = {
+        "metric": f"MoE-layer tokens/s, decode stack T={T}",
+        "value": value, "unit": "layer-tokens/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded counter-based generator; random-init weights)",
+        "us_per_layer": us_layer, "us_per_layer_no_graph": ms_direct * 1e3 / L,
+        "config": {"workload": f"decode stack: {L} distinct BF16 MoE layers (H=2048, I=512, 256 routed + 1 shared, "
+                               f"top-6 sigmoid, router bias N(0,0.5)), T={T} tokens ({wl['x']} x, seed {wl['x_seed']})",
+                   "weights_resident_gb": round(sum(l.gate_up.numel() * 2 + l.down.numel() * 2 for l in layers) / 1e9, 2),
+                   "l2": "inputs larger than L2 (each layer's weights are read once per step)",
+                   "parallelism": f"replicas x{ws}", "graph": True},
+        "unique_experts_per_layer": {"mean": float(np.mean(uniq)), "min": int(min(uniq)), "max": int(max(uniq))},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak_hbm, "unit": "GB/s",
+                     "frac": achieved / peak_hbm, "traffic": None,
+                     "what": "unique touched expert-weight bytes per layer / us per layer (router+gate_up+down "
+                             f"kernels, overlapped by PDL); peak = {pk_kind} HBM copy bandwidth"},
+        "gpu_launches": 3 * L * args.steps,
+        "clocks": clocks,
+        "e2e": {"value": ws * L * T / (ms_e2e * 1e-3), "unit": "layer-tokens/s",
+                "h2d_bytes_per_step": T * 2048 * 2, "d2h_bytes_per_step": L * T * 2048 * 2},
+        "gen_seconds": round(t_gen, 2),
+    }
+    if rank == 0 and ws == 1:
+        line["cpu_baseline"] = cpu_baseline(wl, layers)
+    for h in handles:
+        flint.flint_moe_destroy(h)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    wl = WORKLOADS[args.workload]
+    ws, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, wl, ws, rank)
+    else:
+        run_flint(args, wl, ws, rank, local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

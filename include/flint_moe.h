@@ -1,0 +1,151 @@
+/*
+ * flint_moe.h -- C ABI of the Flint mixture-of-experts FFN layer for B300
+ * (sm_103a).
+ *
+ * The layer (RecursiveSI/flint, vLLM recipe page, "Overview": a
+ * mixture-of-experts model with 256 experts, top-6 sigmoid routing plus a
+ * shared expert; neoteo.com "Model kodujacy Flint", specification table: six
+ * routed experts per token plus one shared expert that is always active):
+ *
+ *   l[t,e] = sum_h x[t,h] Wr[e,h] + b[e]                (router, fp32 accumulate)
+ *   S_t    = 6 experts with the largest l[t,e]          (equal logits: lower index)
+ *   w[t,j] = sigmoid(l[t,S_tj]) / sum_j' sigmoid(l[t,S_tj'])
+ *   y[t]   = sum_j w[t,j] FFN_{S_tj}(x_t) + FFN_shared(x_t)
+ *   FFN(x) = Wd (silu(Wg x) * (Wu x)),  silu(z) = z / (1 + exp(-z))
+ *
+ * The pages give the expert count, top-6, the sigmoid and the shared expert.
+ * They do not give the hidden size, the expert width, the activation or the
+ * weight normalisation; this library fixes H = 2048, I = 512, SwiGLU experts,
+ * weights renormalised to sum to one and an unweighted shared expert (those
+ * sizes reproduce the pages' 39.8B total / ~2.5B active parameter counts).
+ *
+ * Memory: every pointer below is a DEVICE pointer unless marked "host".  All
+ * matrices are row-major [out][in] (each row contiguous along the reduced
+ * dimension).  bf16 = IEEE binary32's upper 16 bits.  Device buffers must be
+ * 16-byte aligned.
+ *
+ * Errors: every call returns a flint_status_t.  Arguments are checked on the
+ * host before anything is launched.  Kernels report device-side problems
+ * (a bounded wait that ran out, an expert index out of range) in a status
+ * word in mapped host memory; the next call on the handle, flint_moe_route_only
+ * (which synchronises) and flint_moe_destroy return it.  No kernel traps.
+ */
+#ifndef FLINT_MOE_H
+#define FLINT_MOE_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define FLINT_API __attribute__((visibility("default")))
+#else
+#define FLINT_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FLINT_HIDDEN 2048      /* H: model width                           */
+#define FLINT_INTER 512        /* I: expert intermediate width (routed and shared) */
+#define FLINT_EXPERTS 256      /* E: routed experts                        */
+#define FLINT_TOPK 6           /* k: routed experts per token              */
+#define FLINT_CHUNK 8192       /* tokens per internal chunk of a forward   */
+#define FLINT_DECODE_MAX_T 32  /* T <= this takes the weight-streaming path */
+
+typedef struct flint_moe* flint_moe_t;
+
+typedef enum {
+    FLINT_BF16 = 0,   /* bf16 weights, borrowed from the caller            */
+    FLINT_NVFP4 = 1   /* NVFP4 (W4A16) expert weights, repacked and owned   */
+} flint_dtype_t;
+
+typedef enum {
+    FLINT_OK = 0,
+    FLINT_ERR_INVALID_ARG = 1,     /* null / misaligned pointer, bad T, bad dtype     */
+    FLINT_ERR_CUDA = 2,            /* a CUDA runtime or driver call failed            */
+    FLINT_ERR_OOM = 3,             /* device allocation failed in create              */
+    FLINT_ERR_DEVICE_TIMEOUT = 4,  /* a bounded device wait ran out (kernel returned) */
+    FLINT_ERR_DEVICE_BADINDEX = 5, /* a kernel saw an expert/token index out of range */
+    FLINT_ERR_UNSUPPORTED = 6      /* no sm_103a device, or an unsupported request    */
+} flint_status_t;
+
+/* One NVFP4 matrix [R][K] (RecursiveSI/flint vLLM recipe page, "Overview":
+ * the NVFP4 checkpoint is run as W4A16).  packed[R][K/2]: E2M1 codes, the
+ * even column in the low nibble; block_scales[R][K/16]: one E4M3 code per 16
+ * consecutive columns; tensor_scale: fp32.  The weight is
+ * e2m1(q) * e4m3(s_block) * tensor_scale.  The struct itself lives in host
+ * memory; packed and block_scales are device pointers. */
+typedef struct {
+    const uint8_t* packed;
+    const uint8_t* block_scales;
+    float tensor_scale;
+} flint_nvfp4_t;
+
+/* Build a layer handle on the current device.
+ *   out        host: receives the handle.
+ *   router_W   bf16 [256][2048].
+ *   router_b   fp32 [256] per-expert logit bias, or NULL for none.
+ *   gate_up_W  host array of 256 entries, one per routed expert.
+ *              FLINT_BF16: device pointer to bf16 [1024][2048], rows 0..511
+ *              the gate projection, rows 512..1023 the up projection.
+ *              FLINT_NVFP4: host pointer to a flint_nvfp4_t of shape [1024][2048].
+ *   down_W     host array of 256 entries: bf16 [2048][512], or flint_nvfp4_t*.
+ *   shared_W   host array {gate_up, down} of the shared expert, same rules.
+ *   dtype      FLINT_BF16 or FLINT_NVFP4 (the router stays bf16 either way).
+ * Ownership: bf16 weights are borrowed (the caller keeps them alive and
+ * unchanged until destroy).  NVFP4 weights are copied into a layout the handle
+ * owns; the caller may free its buffers on return.  The handle also owns its
+ * pointer tables and a workspace for FLINT_CHUNK tokens.  Synchronises the
+ * device.  Errors: INVALID_ARG, OOM, CUDA, UNSUPPORTED (device is not sm_103). */
+FLINT_API flint_status_t flint_moe_create(flint_moe_t* out, const void* router_W, const float* router_b,
+                                const void* const* gate_up_W, const void* const* down_W,
+                                const void* const* shared_W, flint_dtype_t dtype);
+
+/* y = layer(x) for T >= 1 tokens.
+ *   x  bf16 [T][2048], y bf16 [T][2048] (fully overwritten); x and y must not
+ *   overlap.  Runs asynchronously on stream s; allocates nothing; capturable in
+ *   a CUDA graph.  T <= 32 takes the weight-streaming decode kernels, larger T
+ *   the grouped tensor-core path, in chunks of FLINT_CHUNK tokens.  One handle
+ *   serves one stream at a time (the workspace is per handle).
+ * Errors: INVALID_ARG (null, misaligned, T < 1), CUDA (launch failed), or a
+ * device status left by an earlier call. */
+FLINT_API flint_status_t flint_moe_forward(flint_moe_t h, const void* x, int T, void* y, cudaStream_t s);
+
+/* Routing alone, for testing (synchronises s before returning).
+ *   x       bf16 [T][2048] or NULL.
+ *   logits  fp32 [T][256].  If x is NULL, logits is the INPUT: the router
+ *           matrix and bias are skipped and selection runs on these values.
+ *           If x is non-NULL, logits may be NULL or receives the router's fp32
+ *           logits (bias included).
+ *   idx     int32 [T][6] chosen experts, in decreasing logit order (equal
+ *           logits: lower index first).
+ *   w       fp32 [T][6] renormalised sigmoid weights, same order.
+ *   offsets int32 [257] or NULL: offsets[e] = number of (token, slot) pairs
+ *           choosing an expert below e; offsets[256] = 6T.
+ *   gather_idx int32 [6T] or NULL: pair ids t*6+j grouped by expert, in
+ *           increasing pair id within an expert (a stable counting sort).
+ *   T       1 <= T <= FLINT_CHUNK.
+ * Errors: INVALID_ARG, CUDA, or a device status. */
+FLINT_API flint_status_t flint_moe_route_only(flint_moe_t h, const void* x, float* logits, int T,
+                                    int32_t* idx, float* w, int32_t* offsets,
+                                    int32_t* gather_idx, cudaStream_t s);
+
+/* Synchronise the device, release everything the handle owns and return the
+ * last device status.  NULL is accepted (returns FLINT_OK). */
+FLINT_API flint_status_t flint_moe_destroy(flint_moe_t h);
+
+/* Human-readable name of a status code (static storage). */
+FLINT_API const char* flint_status_string(flint_status_t st);
+
+/* Test hook: launch one kernel that waits on a device flag nothing sets,
+ * with a wait limit of timeout_ns nanoseconds of %globaltimer; returns
+ * FLINT_ERR_DEVICE_TIMEOUT when the bounded wait gives up as designed.
+ * Synchronises s. */
+FLINT_API flint_status_t flint_debug_bounded_wait(uint64_t timeout_ns, cudaStream_t s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLINT_MOE_H */

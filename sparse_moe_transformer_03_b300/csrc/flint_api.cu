@@ -1,0 +1,296 @@
+// flint_api.cu -- the C ABI (include/flint_moe.h): handle creation, argument
+// checking, workspace, dispatch between the decode and the grouped
+// tensor-core paths, and the device status word.
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "../../include/flint_moe.h"
+#include "flint_common.cuh"
+#include "flint_internal.h"
+
+using namespace flint;
+
+struct flint_moe {
+    flint_dtype_t dtype;
+    int device;
+    int num_sms;
+    uint64_t wait_limit_ns;
+
+    // weights
+    const __nv_bfloat16* router_W;
+    const float* router_b;
+    ExpertTables host_tables;      // BF16 pointers (host copy)
+    ExpertTables* dev_tables;      // same, in device memory
+
+    // status word in host-mapped memory
+    uint32_t* status_host;
+    uint32_t* status_dev;
+
+    // workspace
+    void* ws_base;
+    size_t ws_bytes;
+    float* logits;                 // [CHUNK][E]
+    float* x_f32;                  // [DEC_T][H]
+    int32_t* idx;                  // [CHUNK][TOPK]
+    float* w;                      // [CHUNK][TOPK]
+    DecodeTables* dec_tables;
+    float* a_dec;                  // [DEC_PAIRS][I]
+    unsigned* ticket;              // router last-CTA ticket
+    int32_t* local_rank;           // [CHUNK][TOPK]
+    int32_t* blk_counts;           // [CHUNK/128][E]
+    int32_t* blk_base;             // [CHUNK/128][E]
+    int32_t* offsets;              // [E+1]
+    int32_t* gather;               // [CHUNK*TOPK]
+};
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+flint_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? FLINT_OK : FLINT_ERR_CUDA; }
+
+// Take (and clear) a device status left by an earlier call.
+flint_status_t take_device_status(flint_moe* h) {
+    volatile uint32_t* s = h->status_host;
+    const uint32_t v = *s;
+    if (v == 0) return FLINT_OK;
+    *s = 0;
+    if (v == ST_TIMEOUT) return FLINT_ERR_DEVICE_TIMEOUT;
+    if (v == ST_BADINDEX) return FLINT_ERR_DEVICE_BADINDEX;
+    return FLINT_ERR_CUDA;
+}
+
+LaunchCtx ctx_of(const flint_moe* h, cudaStream_t s) {
+    LaunchCtx L;
+    L.stream = s;
+    L.status = h->status_dev;
+    L.wait_limit_ns = h->wait_limit_ns;
+    L.num_sms = h->num_sms;
+    L.pdl = true;
+    return L;
+}
+
+// Bump allocator over one cudaMalloc.
+struct Carve {
+    char* base;
+    size_t off;
+    template <typename T>
+    T* take(size_t count) {
+        off = (off + 255) & ~size_t(255);
+        T* p = reinterpret_cast<T*>(base + off);
+        off += count * sizeof(T);
+        return p;
+    }
+};
+
+void free_handle(flint_moe* h) {
+    if (!h) return;
+    if (h->ws_base) cudaFree(h->ws_base);
+    if (h->dev_tables) cudaFree(h->dev_tables);
+    if (h->status_host) cudaFreeHost(h->status_host);
+    delete h;
+}
+
+void carve_workspace(flint_moe* h, char* base, size_t* bytes_out) {
+    Carve c{base, 0};
+    h->logits = c.take<float>((size_t)CHUNK * E);
+    h->x_f32 = c.take<float>((size_t)DEC_T * H);
+    h->idx = c.take<int32_t>((size_t)CHUNK * TOPK);
+    h->w = c.take<float>((size_t)CHUNK * TOPK);
+    h->dec_tables = c.take<DecodeTables>(1);
+    h->a_dec = c.take<float>((size_t)DEC_PAIRS * I);
+    h->ticket = c.take<unsigned>(64);
+    h->local_rank = c.take<int32_t>((size_t)CHUNK * TOPK);
+    h->blk_counts = c.take<int32_t>((size_t)(CHUNK / 128) * E);
+    h->blk_base = c.take<int32_t>((size_t)(CHUNK / 128) * E);
+    h->offsets = c.take<int32_t>(E + 1);
+    h->gather = c.take<int32_t>((size_t)CHUNK * TOPK);
+    *bytes_out = c.off;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* flint_status_string(flint_status_t st) {
+    switch (st) {
+        case FLINT_OK: return "FLINT_OK";
+        case FLINT_ERR_INVALID_ARG: return "FLINT_ERR_INVALID_ARG";
+        case FLINT_ERR_CUDA: return "FLINT_ERR_CUDA";
+        case FLINT_ERR_OOM: return "FLINT_ERR_OOM";
+        case FLINT_ERR_DEVICE_TIMEOUT: return "FLINT_ERR_DEVICE_TIMEOUT";
+        case FLINT_ERR_DEVICE_BADINDEX: return "FLINT_ERR_DEVICE_BADINDEX";
+        case FLINT_ERR_UNSUPPORTED: return "FLINT_ERR_UNSUPPORTED";
+    }
+    return "FLINT_ERR_UNKNOWN";
+}
+
+flint_status_t flint_moe_create(flint_moe_t* out, const void* router_W, const float* router_b,
+                                const void* const* gate_up_W, const void* const* down_W,
+                                const void* const* shared_W, flint_dtype_t dtype) {
+    if (!out) return FLINT_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!router_W || !gate_up_W || !down_W || !shared_W) return FLINT_ERR_INVALID_ARG;
+    if (dtype != FLINT_BF16 && dtype != FLINT_NVFP4) return FLINT_ERR_INVALID_ARG;
+    if (!aligned16(router_W) || (router_b && !aligned16(router_b))) return FLINT_ERR_INVALID_ARG;
+    for (int e = 0; e < NEXP; ++e) {
+        const void* gu = e < E ? gate_up_W[e] : shared_W[0];
+        const void* dn = e < E ? down_W[e] : shared_W[1];
+        if (!gu || !dn) return FLINT_ERR_INVALID_ARG;
+        if (dtype == FLINT_BF16 && (!aligned16(gu) || !aligned16(dn))) return FLINT_ERR_INVALID_ARG;
+    }
+    if (dtype == FLINT_NVFP4) return FLINT_ERR_UNSUPPORTED;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FLINT_ERR_CUDA;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return FLINT_ERR_CUDA;
+    if (prop.major != 10 || prop.minor != 3) return FLINT_ERR_UNSUPPORTED;
+
+    flint_moe* h = new (std::nothrow) flint_moe();
+    if (!h) return FLINT_ERR_OOM;
+    std::memset(h, 0, sizeof(*h));
+    h->dtype = dtype;
+    h->device = dev;
+    h->num_sms = prop.multiProcessorCount;
+    h->wait_limit_ns = 1000000000ull;   // one second
+    h->router_W = static_cast<const __nv_bfloat16*>(router_W);
+    h->router_b = router_b;
+    for (int e = 0; e < NEXP; ++e) {
+        h->host_tables.gate_up[e] = static_cast<const __nv_bfloat16*>(e < E ? gate_up_W[e] : shared_W[0]);
+        h->host_tables.down[e] = static_cast<const __nv_bfloat16*>(e < E ? down_W[e] : shared_W[1]);
+    }
+
+    flint_status_t st = FLINT_OK;
+    if (cudaMalloc(&h->dev_tables, sizeof(ExpertTables)) != cudaSuccess) st = FLINT_ERR_OOM;
+    if (st == FLINT_OK &&
+        cudaMemcpy(h->dev_tables, &h->host_tables, sizeof(ExpertTables), cudaMemcpyHostToDevice) != cudaSuccess)
+        st = FLINT_ERR_CUDA;
+    if (st == FLINT_OK) {
+        if (cudaHostAlloc(reinterpret_cast<void**>(&h->status_host), 64, cudaHostAllocMapped) != cudaSuccess)
+            st = FLINT_ERR_OOM;
+        else {
+            *h->status_host = 0;
+            if (cudaHostGetDevicePointer(reinterpret_cast<void**>(&h->status_dev), h->status_host, 0) !=
+                cudaSuccess)
+                st = FLINT_ERR_CUDA;
+        }
+    }
+    if (st == FLINT_OK) {
+        size_t bytes = 0;
+        carve_workspace(h, nullptr, &bytes);
+        if (cudaMalloc(&h->ws_base, bytes) != cudaSuccess)
+            st = FLINT_ERR_OOM;
+        else {
+            h->ws_bytes = bytes;
+            carve_workspace(h, static_cast<char*>(h->ws_base), &bytes);
+            if (cudaMemset(h->ws_base, 0, bytes) != cudaSuccess) st = FLINT_ERR_CUDA;
+        }
+    }
+    if (st == FLINT_OK) st = from_cuda(decode_set_attributes());
+    if (st == FLINT_OK) st = from_cuda(cudaDeviceSynchronize());
+    if (st != FLINT_OK) {
+        cudaGetLastError();
+        free_handle(h);
+        return st;
+    }
+    *out = h;
+    return FLINT_OK;
+}
+
+flint_status_t flint_moe_forward(flint_moe_t h, const void* x, int T, void* y, cudaStream_t s) {
+    if (!h || !x || !y || T < 1) return FLINT_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(y)) return FLINT_ERR_INVALID_ARG;
+    const char* xb = static_cast<const char*>(x);
+    const char* yb = static_cast<const char*>(y);
+    const size_t bytes = (size_t)T * H * 2;
+    if (xb < yb + bytes && yb < xb + bytes) return FLINT_ERR_INVALID_ARG;
+    flint_status_t st = take_device_status(h);
+    if (st != FLINT_OK) return st;
+
+    const LaunchCtx L = ctx_of(h, s);
+    const __nv_bfloat16* xs = static_cast<const __nv_bfloat16*>(x);
+    __nv_bfloat16* ys = static_cast<__nv_bfloat16*>(y);
+    if (T <= DEC_T) {
+        cudaError_t e = launch_router_decode(L, xs, T, h->router_W, h->router_b, h->logits, nullptr, h->idx,
+                                             h->w, h->dec_tables, h->ticket);
+        if (e == cudaSuccess) e = launch_decode_experts(L, h->dev_tables, h->dec_tables, xs, h->a_dec, ys, T);
+        return from_cuda(e);
+    }
+    return FLINT_ERR_UNSUPPORTED;
+}
+
+flint_status_t flint_moe_route_only(flint_moe_t h, const void* x, float* logits, int T, int32_t* idx,
+                                    float* w, int32_t* offsets, int32_t* gather_idx, cudaStream_t s) {
+    if (!h || !idx || !w || T < 1 || T > CHUNK) return FLINT_ERR_INVALID_ARG;
+    if (!x && !logits) return FLINT_ERR_INVALID_ARG;
+    if ((x && !aligned16(x)) || (logits && !aligned16(logits))) return FLINT_ERR_INVALID_ARG;
+    flint_status_t st = take_device_status(h);
+    if (st != FLINT_OK) return st;
+
+    const LaunchCtx L = ctx_of(h, s);
+    cudaError_t e = cudaSuccess;
+    if (x) {
+        float* lg = logits ? logits : h->logits;
+        const __nv_bfloat16* xs = static_cast<const __nv_bfloat16*>(x);
+        if (T <= DEC_T) {
+            e = launch_router_decode(L, xs, T, h->router_W, h->router_b, lg, nullptr, idx, w, nullptr,
+                                     h->ticket);
+        } else {
+            e = launch_router_logits_general(L, xs, T, h->router_W, h->router_b, lg);
+            if (e == cudaSuccess) e = launch_select(L, lg, T, idx, w);
+        }
+    } else {
+        e = launch_select(L, logits, T, idx, w);
+    }
+    if (e == cudaSuccess && (offsets || gather_idx)) {
+        int32_t* off = offsets ? offsets : h->offsets;
+        e = launch_permutation(L, idx, T, h->local_rank, h->blk_counts, h->blk_base, off, gather_idx);
+    }
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return FLINT_ERR_CUDA;
+    return take_device_status(h);
+}
+
+flint_status_t flint_moe_destroy(flint_moe_t h) {
+    if (!h) return FLINT_OK;
+    cudaError_t e = cudaDeviceSynchronize();
+    flint_status_t st = take_device_status(h);
+    free_handle(h);
+    if (st == FLINT_OK && e != cudaSuccess) st = FLINT_ERR_CUDA;
+    return st;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// test hook: a bounded wait that nothing satisfies
+// ---------------------------------------------------------------------------
+
+__global__ void bounded_wait_probe_kernel(uint64_t limit_ns, uint32_t* result) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    // nothing arrives on the barrier: phase 0 never completes
+    const bool ok = __syncthreads_and(mbar_wait_bounded(&bar, 0, limit_ns));
+    if (threadIdx.x == 0) *result = ok ? 0u : ST_TIMEOUT;
+}
+
+extern "C" flint_status_t flint_debug_bounded_wait(uint64_t timeout_ns, cudaStream_t s) {
+    if (timeout_ns == 0 || timeout_ns > 10000000000ull) return FLINT_ERR_INVALID_ARG;
+    uint32_t* d = nullptr;
+    if (cudaMalloc(&d, sizeof(uint32_t)) != cudaSuccess) return FLINT_ERR_OOM;
+    uint32_t r = 0xFFFFFFFFu;
+    bounded_wait_probe_kernel<<<1, 32, 0, s>>>(timeout_ns, d);
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&r, d, sizeof r, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    cudaFree(d);
+    if (e != cudaSuccess) return FLINT_ERR_CUDA;
+    if (r == ST_TIMEOUT) return FLINT_ERR_DEVICE_TIMEOUT;
+    return r == 0 ? FLINT_OK : FLINT_ERR_CUDA;
+}

@@ -1,0 +1,54 @@
+// flint_internal.h -- host-side declarations shared by the library's .cu files.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "flint_common.cuh"
+
+namespace flint {
+
+// Launch context of one API call.
+struct LaunchCtx {
+    cudaStream_t stream;
+    uint32_t* status;      // device view of the handle's host-mapped status word
+    uint64_t wait_limit_ns;
+    int num_sms;
+    bool pdl;              // launch kernels as programmatic dependents
+};
+
+// Launch `kern` on L.stream, as a programmatic dependent of the previous
+// kernel on the stream when L.pdl is set.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(const LaunchCtx& L, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = L.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = L.pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
+// router.cu
+cudaError_t launch_router_decode(const LaunchCtx& L, const __nv_bfloat16* x, int T, const __nv_bfloat16* Wr,
+                                 const float* bias, float* logits, float* x_f32, int32_t* idx, float* w,
+                                 DecodeTables* tables, unsigned* ticket);
+cudaError_t launch_router_logits_general(const LaunchCtx& L, const __nv_bfloat16* x, int T,
+                                         const __nv_bfloat16* Wr, const float* bias, float* logits);
+cudaError_t launch_select(const LaunchCtx& L, const float* logits, int T, int32_t* idx, float* w);
+cudaError_t launch_permutation(const LaunchCtx& L, const int32_t* idx, int T, int32_t* local_rank,
+                               int32_t* blk_counts, int32_t* blk_base, int32_t* offsets, int32_t* gather);
+
+// decode.cu
+cudaError_t decode_set_attributes();
+cudaError_t launch_decode_experts(const LaunchCtx& L, const ExpertTables* experts, const DecodeTables* tables,
+                                  const __nv_bfloat16* x, float* a_buf, __nv_bfloat16* y, int T);
+
+}  // namespace flint

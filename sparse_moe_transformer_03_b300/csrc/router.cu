@@ -1,0 +1,398 @@
+// router.cu -- router logits, sigmoid top-6 selection with renormalisation,
+// the decode routing tables and the token->expert permutation.
+//
+// RecursiveSI/flint (vLLM recipe page), "Overview": 256 experts with top-6
+// sigmoid routing plus a shared expert.  The selection ranks experts by the
+// fp32 logit (the sigmoid is increasing, so this is the ranking by score
+// without its fp32 saturation), keeps the lower expert index on equal logits,
+// and renormalises the six sigmoid scores to sum to one.
+#include "flint_common.cuh"
+#include "flint_internal.h"
+
+namespace flint {
+
+// ---------------------------------------------------------------------------
+// warp-wide top-6 of one token's 256 logits
+// ---------------------------------------------------------------------------
+
+// Lane l holds logits of experts l, l+32, ..., l+224.  On return every lane
+// has the six chosen expert ids (decreasing logit, equal logits: lower id
+// first) and their renormalised sigmoid weights.
+__device__ __forceinline__ void warp_top6(const float (&v)[8], int lane, int (&sel)[TOPK], float (&wt)[TOPK]) {
+    uint32_t taken = 0;
+    float selv[TOPK];
+#pragma unroll
+    for (int r = 0; r < TOPK; ++r) {
+        float bv = 0.f;
+        int bi = -1;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            // ids grow with i, so a strict comparison keeps the lower id
+            if (!((taken >> i) & 1u) && (bi < 0 || v[i] > bv)) {
+                bv = v[i];
+                bi = lane + 32 * i;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
+            const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
+            if (oi >= 0 && (bi < 0 || ov > bv || (ov == bv && oi < bi))) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        sel[r] = bi;
+        selv[r] = bv;
+        if (lane == (bi & 31)) taken |= 1u << (bi >> 5);
+    }
+    float s[TOPK], sum = 0.f;
+#pragma unroll
+    for (int r = 0; r < TOPK; ++r) {
+        s[r] = sigmoid_f(selv[r]);
+        sum += s[r];
+    }
+#pragma unroll
+    for (int r = 0; r < TOPK; ++r) wt[r] = s[r] / sum;
+}
+
+// ---------------------------------------------------------------------------
+// decode router: logits for T <= 32, then (last CTA) selection + tables
+// ---------------------------------------------------------------------------
+
+constexpr int RT_WARPS = 4;                    // one expert per warp
+constexpr int RT_CTAS = E / RT_WARPS;          // 64
+
+// Build the decode tables from sel_e/sel_w (smem) -- one CTA.
+__device__ void build_decode_tables(int T, const int* sel_e, const float* sel_w, int* cnt, DecodeTables* tab) {
+    const int tid = threadIdx.x, nt = blockDim.x;
+    for (int e = tid; e < E; e += nt) cnt[e] = 0;
+    __syncthreads();
+    for (int p = tid; p < T * TOPK; p += nt) atomicAdd(&cnt[sel_e[p]], 1);
+    __syncthreads();
+    // warp 0: exclusive scans of presence and counts over experts
+    __shared__ int s_pair0[E];
+    if (tid < 32) {
+        const int lane = tid;
+        int pres = 0, sum = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            pres += cnt[lane * 8 + i] > 0;
+            sum += cnt[lane * 8 + i];
+        }
+        int ip = pres, is = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int a = __shfl_up_sync(0xFFFFFFFFu, ip, o);
+            const int b = __shfl_up_sync(0xFFFFFFFFu, is, o);
+            if (lane >= o) {
+                ip += a;
+                is += b;
+            }
+        }
+        int slot = 1 + ip - pres;   // slot 0 is the shared expert
+        int pair0 = T + is - sum;   // pairs 0..T-1 are the shared expert's
+        for (int i = 0; i < 8; ++i) {
+            const int e = lane * 8 + i;
+            s_pair0[e] = pair0;
+            if (cnt[e] > 0) {
+                tab->slot_expert[slot] = e;
+                tab->slot_pair0[slot] = pair0;
+                ++slot;
+                pair0 += cnt[e];
+            }
+        }
+        if (lane == 31) {
+            tab->n_slots = slot;
+            tab->n_pairs = pair0;
+            tab->slot_pair0[slot] = pair0;
+            tab->T = T;
+            tab->slot_expert[0] = SHARED;
+            tab->slot_pair0[0] = 0;
+        }
+    }
+    for (int t = tid; t < T; t += nt) {
+        tab->pair_token[t] = t;
+        tab->pair_weight[t] = 1.0f;
+    }
+    __syncthreads();
+    for (int p = tid; p < T * TOPK; p += nt) {
+        const int t = p / TOPK, e = sel_e[p];
+        int rank = 0;
+        for (int q = 0; q < t * TOPK; ++q) rank += sel_e[q] == e;
+        const int pair = s_pair0[e] + rank;
+        tab->pair_token[pair] = t;
+        tab->pair_weight[pair] = sel_w[p];
+    }
+}
+
+struct RouterDecodeParams {
+    const __nv_bfloat16* x;  // [T][H]
+    int T;
+    const __nv_bfloat16* Wr; // [E][H]
+    const float* bias;       // [E] or null
+    float* logits;           // [T][E] out (workspace or caller)
+    float* x_f32;            // [T][H] out (fp32 copy of x for the expert kernels) or null
+    int32_t* idx;            // [T][6]
+    float* w;                // [T][6]
+    DecodeTables* tables;    // or null
+    unsigned* ticket;
+};
+
+__global__ void __launch_bounds__(RT_WARPS * 32) router_decode_kernel(RouterDecodeParams p) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e = blockIdx.x * RT_WARPS + warp;
+    // weights are immutable: load the row before waiting on the producer of x
+    uint4 wr[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) wr[i] = ldg16(p.Wr + (size_t)e * H + 8 * (lane + 32 * i));
+    const float b = p.bias ? __ldg(p.bias + e) : 0.f;
+    pdl_trigger();
+    pdl_wait();
+
+    const int T = p.T;
+    for (int t = 0; t < T; ++t) {
+        const __nv_bfloat16* xr = p.x + (size_t)t * H;
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint4 xv = ldg16(xr + 8 * (lane + 32 * i));
+            acc = fmaf(bf_lo(wr[i].x), bf_lo(xv.x), acc);
+            acc = fmaf(bf_hi(wr[i].x), bf_hi(xv.x), acc);
+            acc = fmaf(bf_lo(wr[i].y), bf_lo(xv.y), acc);
+            acc = fmaf(bf_hi(wr[i].y), bf_hi(xv.y), acc);
+            acc = fmaf(bf_lo(wr[i].z), bf_lo(xv.z), acc);
+            acc = fmaf(bf_hi(wr[i].z), bf_hi(xv.z), acc);
+            acc = fmaf(bf_lo(wr[i].w), bf_lo(xv.w), acc);
+            acc = fmaf(bf_hi(wr[i].w), bf_hi(xv.w), acc);
+        }
+        acc = warp_sum(acc);
+        if (lane == 0) p.logits[(size_t)t * E + e] = acc + b;
+    }
+    // fp32 copy of x for the expert kernels (each CTA converts a share)
+    if (p.x_f32) {
+        const int n8 = T * H / 8;
+        for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += gridDim.x * blockDim.x) {
+            const uint4 xv = ldg16(p.x + 8 * (size_t)i);
+            float4 a = make_float4(bf_lo(xv.x), bf_hi(xv.x), bf_lo(xv.y), bf_hi(xv.y));
+            float4 c = make_float4(bf_lo(xv.z), bf_hi(xv.z), bf_lo(xv.w), bf_hi(xv.w));
+            reinterpret_cast<float4*>(p.x_f32)[2 * i] = a;
+            reinterpret_cast<float4*>(p.x_f32)[2 * i + 1] = c;
+        }
+    }
+
+    // the last CTA to finish selects and builds the tables
+    __shared__ int s_last;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned done = atomicAdd(p.ticket, 1u);
+        s_last = (done == gridDim.x - 1);
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+
+    __shared__ int sel_e[DEC_T * TOPK];
+    __shared__ float sel_w[DEC_T * TOPK];
+    __shared__ int cnt[E];
+    for (int t = warp; t < T; t += RT_WARPS) {
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = __ldcg(p.logits + (size_t)t * E + lane + 32 * i);
+        int sel[TOPK];
+        float wt[TOPK];
+        warp_top6(v, lane, sel, wt);
+        if (lane < TOPK) {
+            p.idx[t * TOPK + lane] = sel[lane];
+            p.w[t * TOPK + lane] = wt[lane];
+            sel_e[t * TOPK + lane] = sel[lane];
+            sel_w[t * TOPK + lane] = wt[lane];
+        }
+    }
+    if (threadIdx.x == 0) *p.ticket = 0;  // ready for the next call
+    __syncthreads();
+    if (p.tables) build_decode_tables(T, sel_e, sel_w, cnt, p.tables);
+}
+
+// ---------------------------------------------------------------------------
+// general-T router logits (CUDA cores; used by route-only for T > 32)
+// ---------------------------------------------------------------------------
+
+constexpr int RG_TOK = 8;   // tokens per CTA row of the grid
+
+__global__ void __launch_bounds__(RT_WARPS * 32) router_logits_general_kernel(const __nv_bfloat16* x, int T,
+                                                                            const __nv_bfloat16* Wr,
+                                                                            const float* bias, float* logits) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e = blockIdx.x * RT_WARPS + warp;
+    uint4 wr[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) wr[i] = ldg16(Wr + (size_t)e * H + 8 * (lane + 32 * i));
+    const float b = bias ? __ldg(bias + e) : 0.f;
+    pdl_wait();
+    const int t0 = blockIdx.y * RG_TOK;
+    for (int t = t0; t < min(T, t0 + RG_TOK); ++t) {
+        const __nv_bfloat16* xr = x + (size_t)t * H;
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint4 xv = ldg16(xr + 8 * (lane + 32 * i));
+            acc = fmaf(bf_lo(wr[i].x), bf_lo(xv.x), acc);
+            acc = fmaf(bf_hi(wr[i].x), bf_hi(xv.x), acc);
+            acc = fmaf(bf_lo(wr[i].y), bf_lo(xv.y), acc);
+            acc = fmaf(bf_hi(wr[i].y), bf_hi(xv.y), acc);
+            acc = fmaf(bf_lo(wr[i].z), bf_lo(xv.z), acc);
+            acc = fmaf(bf_hi(wr[i].z), bf_hi(xv.z), acc);
+            acc = fmaf(bf_lo(wr[i].w), bf_lo(xv.w), acc);
+            acc = fmaf(bf_hi(wr[i].w), bf_hi(xv.w), acc);
+        }
+        acc = warp_sum(acc);
+        if (lane == 0) logits[(size_t)t * E + e] = acc + b;
+    }
+}
+
+// one warp per token: selection from fp32 logits
+__global__ void __launch_bounds__(128) select_kernel(const float* logits, int T, int32_t* idx, float* w) {
+    pdl_wait();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 4 + warp;
+    if (t >= T) return;
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __ldcg(logits + (size_t)t * E + lane + 32 * i);
+    int sel[TOPK];
+    float wt[TOPK];
+    warp_top6(v, lane, sel, wt);
+    if (lane < TOPK) {
+        idx[t * TOPK + lane] = sel[lane];
+        w[t * TOPK + lane] = wt[lane];
+    }
+}
+
+// ---------------------------------------------------------------------------
+// permutation: stable counting sort of the (token, slot) pairs by expert
+// ---------------------------------------------------------------------------
+// Blocks of PB_TOK tokens.  perm_local: per block, each pair's rank among the
+// block's earlier pairs of the same expert (from per-expert token bitmasks,
+// so the result is deterministic) and the block's per-expert counts.
+// perm_scan: offsets[e] and each block's base per expert.  perm_scatter:
+// gather[offsets[e] + base[b][e] + rank] = pair id.
+
+constexpr int PB_TOK = 128;
+
+__global__ void __launch_bounds__(PB_TOK) perm_local_kernel(const int32_t* idx, int T, int32_t* local_rank,
+                                                           int32_t* blk_counts, uint32_t* status) {
+    pdl_wait();
+    __shared__ uint32_t mask[E][PB_TOK / 32];
+    const int b = blockIdx.x, tid = threadIdx.x;
+    for (int i = tid; i < E * (PB_TOK / 32); i += PB_TOK) (&mask[0][0])[i] = 0u;
+    __syncthreads();
+    const int t = b * PB_TOK + tid;
+    int sel[TOPK];
+    if (t < T) {
+#pragma unroll
+        for (int j = 0; j < TOPK; ++j) {
+            int e = idx[t * TOPK + j];
+            if (e < 0 || e >= E) {
+                report_status(status, ST_BADINDEX);
+                e = 0;
+            }
+            sel[j] = e;
+            atomicOr(&mask[e][tid >> 5], 1u << (tid & 31));
+        }
+    }
+    __syncthreads();
+    if (t < T) {
+#pragma unroll
+        for (int j = 0; j < TOPK; ++j) {
+            const int e = sel[j];
+            int r = 0;
+            for (int wd = 0; wd < (tid >> 5); ++wd) r += __popc(mask[e][wd]);
+            r += __popc(mask[e][tid >> 5] & ((1u << (tid & 31)) - 1u));
+            local_rank[t * TOPK + j] = r;
+        }
+    }
+    for (int e = tid; e < E; e += PB_TOK) {
+        int c = 0;
+#pragma unroll
+        for (int wd = 0; wd < PB_TOK / 32; ++wd) c += __popc(mask[e][wd]);
+        blk_counts[b * E + e] = c;
+    }
+}
+
+__global__ void __launch_bounds__(E) perm_scan_kernel(const int32_t* blk_counts, int nblk, int32_t* blk_base,
+                                                     int32_t* offsets) {
+    pdl_wait();
+    const int e = threadIdx.x;
+    int run = 0;
+    for (int b = 0; b < nblk; ++b) {
+        blk_base[b * E + e] = run;
+        run += blk_counts[b * E + e];
+    }
+    // exclusive scan of run over the 256 experts
+    __shared__ int warp_tot[E / 32];
+    const int lane = e & 31, wid = e >> 5;
+    int incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int a = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += a;
+    }
+    if (lane == 31) warp_tot[wid] = incl;
+    __syncthreads();
+    int before = 0;
+    for (int i = 0; i < wid; ++i) before += warp_tot[i];
+    offsets[e] = before + incl - run;
+    if (e == E - 1) offsets[E] = before + incl;
+}
+
+__global__ void __launch_bounds__(256) perm_scatter_kernel(const int32_t* idx, const int32_t* local_rank, int T,
+                                                          const int32_t* blk_base, const int32_t* offsets,
+                                                          int32_t* gather) {
+    pdl_wait();
+    const int p = blockIdx.x * blockDim.x + threadIdx.x;
+    if (p >= T * TOPK) return;
+    const int t = p / TOPK;
+    const int b = t / PB_TOK;
+    const int e = idx[p];
+    if (e < 0 || e >= E) return;
+    gather[offsets[e] + blk_base[b * E + e] + local_rank[p]] = p;
+}
+
+// ---------------------------------------------------------------------------
+// host launchers
+// ---------------------------------------------------------------------------
+
+cudaError_t launch_router_decode(const LaunchCtx& L, const __nv_bfloat16* x, int T, const __nv_bfloat16* Wr,
+                                 const float* bias, float* logits, float* x_f32, int32_t* idx, float* w,
+                                 DecodeTables* tables, unsigned* ticket) {
+    RouterDecodeParams p{x, T, Wr, bias, logits, x_f32, idx, w, tables, ticket};
+    return launch_pdl(L, router_decode_kernel, dim3(RT_CTAS), dim3(RT_WARPS * 32), 0, p);
+}
+
+cudaError_t launch_router_logits_general(const LaunchCtx& L, const __nv_bfloat16* x, int T,
+                                         const __nv_bfloat16* Wr, const float* bias, float* logits) {
+    return launch_pdl(L, router_logits_general_kernel, dim3(RT_CTAS, (T + RG_TOK - 1) / RG_TOK),
+                      dim3(RT_WARPS * 32), 0, x, T, Wr, bias, logits);
+}
+
+cudaError_t launch_select(const LaunchCtx& L, const float* logits, int T, int32_t* idx, float* w) {
+    return launch_pdl(L, select_kernel, dim3((T + 3) / 4), dim3(128), 0, logits, T, idx, w);
+}
+
+cudaError_t launch_permutation(const LaunchCtx& L, const int32_t* idx, int T, int32_t* local_rank,
+                               int32_t* blk_counts, int32_t* blk_base, int32_t* offsets, int32_t* gather) {
+    const int nblk = (T + PB_TOK - 1) / PB_TOK;
+    cudaError_t err = launch_pdl(L, perm_local_kernel, dim3(nblk), dim3(PB_TOK), 0, idx, T, local_rank,
+                                 blk_counts, L.status);
+    if (err != cudaSuccess) return err;
+    err = launch_pdl(L, perm_scan_kernel, dim3(1), dim3(E), 0, (const int32_t*)blk_counts, nblk, blk_base,
+                     offsets);
+    if (err != cudaSuccess) return err;
+    if (!gather) return cudaSuccess;
+    return launch_pdl(L, perm_scatter_kernel, dim3((T * TOPK + 255) / 256), dim3(256), 0, idx,
+                      (const int32_t*)local_rank, T, (const int32_t*)blk_base, (const int32_t*)offsets, gather);
+}
+
+}  // namespace flint

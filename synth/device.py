@@ -1,0 +1,108 @@
+"""Device-side input generation (CUDA, ``csrc/synth_gen.cu``) for large weight stacks.
+
+Draws exactly the streams of :mod:`synth.gen` (same keys, same Box-Muller
+normals in double precision, same rounding to bf16), directly into torch
+CUDA tensors.  Input generation only.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+from . import gen
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "csrc", "synth_gen.cu")
+_LIB = os.path.join(_HERE, "libflint_synth.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        nvcc = "/usr/local/cuda/bin/nvcc" if os.path.exists("/usr/local/cuda/bin/nvcc") else "nvcc"
+        subprocess.check_call([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17",
+                               "-shared", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
+                               "-o", _LIB + ".tmp", _SRC])
+        os.replace(_LIB + ".tmp", _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB):
+            raise RuntimeError(f"synth CUDA generator not built ({_LIB}); run __graft_entry__.build()")
+        lib = ctypes.CDLL(_LIB)
+        lib.synth_fill_normal_bf16.restype = ctypes.c_int
+        lib.synth_fill_normal_bf16.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint32,
+                                               ctypes.c_uint32, ctypes.c_uint32, ctypes.c_double, ctypes.c_void_p]
+        lib.synth_fill_normal_f32.restype = ctypes.c_int
+        lib.synth_fill_normal_f32.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32,
+                                              ctypes.c_uint32, ctypes.c_double, ctypes.c_void_p]
+        _lib = lib
+    return _lib
+
+
+def _stream_ptr(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def fill_normal_bf16(t, seed: int, layer: int, tensor: int, std: float, start: int = 0, stream=None):
+    """Fill a contiguous bf16 CUDA tensor with std * N(0,1) of a stream."""
+    import torch
+    assert t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous()
+    rc = _load().synth_fill_normal_bf16(ctypes.c_void_p(t.data_ptr()), t.numel(), start, seed, layer, tensor,
+                                        float(std), _stream_ptr(stream))
+    if rc != 0:
+        raise RuntimeError(f"synth_fill_normal_bf16 failed ({rc})")
+    return t
+
+
+def fill_normal_f32(t, seed: int, layer: int, tensor: int, std: float, stream=None):
+    import torch
+    assert t.is_cuda and t.dtype == torch.float32 and t.is_contiguous()
+    rc = _load().synth_fill_normal_f32(ctypes.c_void_p(t.data_ptr()), t.numel(), seed, layer, tensor, float(std),
+                                       _stream_ptr(stream))
+    if rc != 0:
+        raise RuntimeError(f"synth_fill_normal_f32 failed ({rc})")
+    return t
+
+
+class LayerWeights:
+    """One MoE layer's weights in device memory, generated from (seed, layer).
+
+    gate_up: bf16 [257][2I][H] (index 256 = shared expert), down: bf16
+    [257][H][I], router_W: bf16 [E][H], router_b: fp32 [E] or None."""
+
+    def __init__(self, seed: int, layer: int, with_bias: bool, device="cuda",
+                 E: int = gen.E, H: int = gen.H, I: int = gen.I):
+        import torch
+        self.seed, self.layer, self.E, self.H, self.I = seed, layer, E, H, I
+        self.router_W = torch.empty((E, H), dtype=torch.bfloat16, device=device)
+        fill_normal_bf16(self.router_W, seed, layer, gen.T_ROUTER_W, 1.0 / (H ** 0.5))
+        self.router_b = None
+        if with_bias:
+            self.router_b = torch.empty((E,), dtype=torch.float32, device=device)
+            fill_normal_f32(self.router_b, seed, layer, gen.T_ROUTER_B, gen.BIAS_STD)
+        self.gate_up = torch.empty((E + 1, 2 * I, H), dtype=torch.bfloat16, device=device)
+        self.down = torch.empty((E + 1, H, I), dtype=torch.bfloat16, device=device)
+        for e in range(E + 1):
+            fill_normal_bf16(self.gate_up[e], seed, layer, gen.gate_up_tensor(e), gen.WEIGHT_STD)
+            fill_normal_bf16(self.down[e], seed, layer, gen.down_tensor(e), gen.WEIGHT_STD)
+
+    def expert_bits(self, e: int):
+        """(gate_up, down) of expert e as numpy uint16 bf16 bits (host copies)."""
+        import torch
+        gu = self.gate_up[e].view(torch.int16).cpu().numpy().view("uint16")
+        dn = self.down[e].view(torch.int16).cpu().numpy().view("uint16")
+        return gu, dn
+
+    def router_bits(self):
+        import torch
+        return self.router_W.view(torch.int16).cpu().numpy().view("uint16")
+
+    def bias_host(self):
+        return None if self.router_b is None else self.router_b.cpu().numpy()

@@ -1,0 +1,62 @@
+"""The C-ABI library builds for sm_103a, loads without a GPU, exports every
+symbol include/flint_moe.h declares, and rejects bad arguments on the host
+before touching the device."""
+import ctypes
+import re
+
+import pytest
+
+from sparse_moe_transformer_03_b300 import build as flint_build
+from sparse_moe_transformer_03_b300 import flint
+
+
+@pytest.fixture(scope="module")
+def lib():
+    flint_build.build()
+    return flint.load_library()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = flint.declared_symbols()
+    assert {"flint_moe_create", "flint_moe_forward", "flint_moe_route_only", "flint_moe_destroy"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_header_constants_match_binding():
+    src = open(flint.HEADER).read()
+    consts = dict(re.findall(r"#define (FLINT_\w+) (\d+)", src))
+    assert int(consts["FLINT_HIDDEN"]) == flint.H
+    assert int(consts["FLINT_INTER"]) == flint.I
+    assert int(consts["FLINT_EXPERTS"]) == flint.E
+    assert int(consts["FLINT_TOPK"]) == flint.TOPK
+    assert int(consts["FLINT_CHUNK"]) == flint.CHUNK
+    assert int(consts["FLINT_DECODE_MAX_T"]) == flint.DECODE_MAX_T
+    enums = dict(re.findall(r"(FLINT_(?:OK|ERR_\w+)) = (\d+)", src))
+    assert {int(v): k for k, v in enums.items()} == flint.STATUS
+
+
+def test_status_strings(lib):
+    for code, name in flint.STATUS.items():
+        assert flint.flint_status_string(code) == name
+
+
+def test_host_argument_checks(lib):
+    P = ctypes.c_void_p
+    # null handle / null buffers / bad T: rejected before any CUDA call
+    assert lib.flint_moe_forward(None, P(16), 1, P(4096 * 16), None) == 1
+    assert lib.flint_moe_route_only(None, P(16), None, 1, P(32), P(64), None, None, None) == 1
+    assert lib.flint_moe_destroy(None) == 0
+    h = P()
+    assert lib.flint_moe_create(ctypes.byref(h), None, None, None, None, None, 0) == 1
+    arr = (P * 256)()
+    sh = (P * 2)()
+    assert lib.flint_moe_create(ctypes.byref(h), P(256), None, arr, arr, sh, 0) == 1  # null experts
+    for i in range(256):
+        arr[i] = 4096 * (i + 1)
+    sh[0], sh[1] = 1 << 30, (1 << 30) + 4096
+    assert lib.flint_moe_create(ctypes.byref(h), P(256), None, arr, arr, sh, 7) == 1  # bad dtype
+    assert lib.flint_moe_create(ctypes.byref(h), P(258), None, arr, arr, sh, 0) == 1  # misaligned router
+    arr[3] = 4096 * 4 + 8
+    assert lib.flint_moe_create(ctypes.byref(h), P(256), None, arr, arr, sh, 0) == 1  # misaligned expert
+    assert lib.flint_debug_bounded_wait(0, None) == 1
