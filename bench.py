@@ -23,7 +23,6 @@ import argparse
 import json
 import os
 import statistics
-import subprocess
 import sys
 import time
 
@@ -59,56 +58,118 @@ def peaks():
         return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
 
 
+# NVML clock-event reason bits (nvml.h: nvmlClocksEventReason*)
+_REASON_BITS = {"nvmlClocksEventReasonSwPowerCap": 0x4, "nvmlClocksEventReasonHwSlowdown": 0x8,
+                "nvmlClocksEventReasonSwThermalSlowdown": 0x20, "nvmlClocksEventReasonHwThermalSlowdown": 0x40,
+                "nvmlClocksEventReasonHwPowerBrakeSlowdown": 0x80}
+
+
+class _CtypesNvml:
+    """The few read-only NVML queries the sampler needs, through libnvidia-ml."""
+    NVML_CLOCK_SM = 1
+
+    def __init__(self):
+        import ctypes
+        self.c = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+
+    def nvmlInit(self):
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+
+    def nvmlDeviceGetHandleByPciBusId(self, bus):
+        h = self.c.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), self.c.byref(h)) != 0:
+            raise RuntimeError("nvmlDeviceGetHandleByPciBusId failed")
+        return h
+
+    def _clock(self, fn, h, kind):
+        v = self.c.c_uint()
+        if fn(h, kind, self.c.byref(v)) != 0:
+            raise RuntimeError("nvml clock query failed")
+        return v.value
+
+    def nvmlDeviceGetClockInfo(self, h, kind):
+        return self._clock(self.lib.nvmlDeviceGetClockInfo, h, kind)
+
+    def nvmlDeviceGetMaxClockInfo(self, h, kind):
+        return self._clock(self.lib.nvmlDeviceGetMaxClockInfo, h, kind)
+
+    def nvmlDeviceGetCurrentClocksEventReasons(self, h):
+        v = self.c.c_ulonglong()
+        fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        if fn(h, self.c.byref(v)) != 0:
+            raise RuntimeError("nvml reasons query failed")
+        return v.value
+
+
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    """SM clock and clock-event reasons sampled by NVML every ~2 ms while the
+    timed region runs (read-only queries; nothing is changed on the GPU)."""
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = [("hw_slowdown", "nvmlClocksEventReasonHwSlowdown"),
+               ("hw_thermal_slowdown", "nvmlClocksEventReasonHwThermalSlowdown"),
+               ("sw_thermal_slowdown", "nvmlClocksEventReasonSwThermalSlowdown"),
+               ("sw_power_cap", "nvmlClocksEventReasonSwPowerCap"),
+               ("hw_power_brake", "nvmlClocksEventReasonHwPowerBrakeSlowdown")]
 
-    def __init__(self, gpu_index):
-        self.gpu = gpu_index
-        self.proc = None
+    def __init__(self, torch_device):
+        import threading
+        self.dev = torch_device
+        self.samples = []
+        self.stop = threading.Event()
+        self.thread = None
+        self.err = None
+
+    def _handle(self):
+        import torch
+        pr = torch.cuda.get_device_properties(self.dev)
+        bus = f"{pr.pci_domain_id:08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0"
+        try:
+            import pynvml
+        except ImportError:
+            pynvml = _CtypesNvml()
+        pynvml.nvmlInit()
+        return pynvml, pynvml.nvmlDeviceGetHandleByPciBusId(bus)
+
+    def _run(self):
+        try:
+            nv, h = self._handle()
+            mx = nv.nvmlDeviceGetMaxClockInfo(h, nv.NVML_CLOCK_SM)
+            while not self.stop.is_set():
+                sm = nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM)
+                rs = nv.nvmlDeviceGetCurrentClocksEventReasons(h)
+                self.samples.append((sm, mx, rs))
+                self.stop.wait(0.002)
+        except Exception as e:  # NVML missing: report unsampled
+            self.err = repr(e)
 
     def __enter__(self):
-        try:
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
-                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except Exception:
-            self.proc = None
+        import threading
+        self.thread = threading.Thread(target=self._run, daemon=True)
+        self.thread.start()
+        import time as _t
+        _t.sleep(0.05)
         return self
 
     def __exit__(self, *a):
-        self.lines = []
-        if self.proc:
-            self.proc.terminate()
-            try:
-                out, _ = self.proc.communicate(timeout=5)
-            except Exception:
-                self.proc.kill()
-                out = ""
-            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        self.stop.set()
+        if self.thread:
+            self.thread.join(timeout=5)
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in getattr(self, "lines", []):
-            f = [v.strip() for v in ln.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0,
+                    "error": self.err}
+        reasons = set()
+        for _, _, rs in self.samples:
+            for name, const in self.REASONS:
+                if rs & _REASON_BITS[const]:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(s[0] for s in self.samples),
+                "sm_max_mhz": max(s[1] for s in self.samples), "reasons": sorted(reasons),
+                "samples": len(self.samples), "source": "nvml"}
 
 
 def dist_setup(args):

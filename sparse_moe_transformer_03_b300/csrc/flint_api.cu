@@ -213,9 +213,9 @@ flint_status_t flint_moe_forward(flint_moe_t h, const void* x, int T, void* y, c
     const __nv_bfloat16* xs = static_cast<const __nv_bfloat16*>(x);
     __nv_bfloat16* ys = static_cast<__nv_bfloat16*>(y);
     if (T <= DEC_T) {
-        cudaError_t e = launch_router_decode(L, xs, T, h->router_W, h->router_b, h->logits, nullptr, h->idx,
-                                             h->w, h->dec_tables, h->ticket);
-        if (e == cudaSuccess) e = launch_decode_experts(L, h->dev_tables, h->dec_tables, xs, h->a_dec, ys, T);
+        cudaError_t e = launch_router_logits_decode(L, xs, T, h->router_W, h->router_b, h->logits);
+        if (e == cudaSuccess)
+            e = launch_decode_experts(L, h->dev_tables, h->logits, xs, T, h->dec_tables, h->idx, h->w, h->a_dec, ys);
         return from_cuda(e);
     }
     return FLINT_ERR_UNSUPPORTED;

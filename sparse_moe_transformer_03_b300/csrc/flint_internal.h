@@ -40,6 +40,8 @@ cudaError_t launch_pdl(const LaunchCtx& L, void (*kern)(KArgs...), dim3 grid, di
 cudaError_t launch_router_decode(const LaunchCtx& L, const __nv_bfloat16* x, int T, const __nv_bfloat16* Wr,
                                  const float* bias, float* logits, float* x_f32, int32_t* idx, float* w,
                                  DecodeTables* tables, unsigned* ticket);
+cudaError_t launch_router_logits_decode(const LaunchCtx& L, const __nv_bfloat16* x, int T,
+                                        const __nv_bfloat16* Wr, const float* bias, float* logits);
 cudaError_t launch_router_logits_general(const LaunchCtx& L, const __nv_bfloat16* x, int T,
                                          const __nv_bfloat16* Wr, const float* bias, float* logits);
 cudaError_t launch_select(const LaunchCtx& L, const float* logits, int T, int32_t* idx, float* w);
@@ -48,7 +50,8 @@ cudaError_t launch_permutation(const LaunchCtx& L, const int32_t* idx, int T, in
 
 // decode.cu
 cudaError_t decode_set_attributes();
-cudaError_t launch_decode_experts(const LaunchCtx& L, const ExpertTables* experts, const DecodeTables* tables,
-                                  const __nv_bfloat16* x, float* a_buf, __nv_bfloat16* y, int T);
+cudaError_t launch_decode_experts(const LaunchCtx& L, const ExpertTables* experts, const float* logits,
+                                  const __nv_bfloat16* x, int T, DecodeTables* tables, int32_t* idx, float* w,
+                                  float* a_buf, __nv_bfloat16* y);
 
 }  // namespace flint

@@ -8,53 +8,9 @@
 // and renormalises the six sigmoid scores to sum to one.
 #include "flint_common.cuh"
 #include "flint_internal.h"
+#include "routing.cuh"
 
 namespace flint {
-
-// ---------------------------------------------------------------------------
-// warp-wide top-6 of one token's 256 logits
-// ---------------------------------------------------------------------------
-
-// Lane l holds logits of experts l, l+32, ..., l+224.  On return every lane
-// has the six chosen expert ids (decreasing logit, equal logits: lower id
-// first) and their renormalised sigmoid weights.
-__device__ __forceinline__ void warp_top6(const float (&v)[8], int lane, int (&sel)[TOPK], float (&wt)[TOPK]) {
-    uint32_t taken = 0;
-    float selv[TOPK];
-#pragma unroll
-    for (int r = 0; r < TOPK; ++r) {
-        float bv = 0.f;
-        int bi = -1;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            // ids grow with i, so a strict comparison keeps the lower id
-            if (!((taken >> i) & 1u) && (bi < 0 || v[i] > bv)) {
-                bv = v[i];
-                bi = lane + 32 * i;
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
-            const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
-            if (oi >= 0 && (bi < 0 || ov > bv || (ov == bv && oi < bi))) {
-                bv = ov;
-                bi = oi;
-            }
-        }
-        sel[r] = bi;
-        selv[r] = bv;
-        if (lane == (bi & 31)) taken |= 1u << (bi >> 5);
-    }
-    float s[TOPK], sum = 0.f;
-#pragma unroll
-    for (int r = 0; r < TOPK; ++r) {
-        s[r] = sigmoid_f(selv[r]);
-        sum += s[r];
-    }
-#pragma unroll
-    for (int r = 0; r < TOPK; ++r) wt[r] = s[r] / sum;
-}
 
 // ---------------------------------------------------------------------------
 // decode router: logits for T <= 32, then (last CTA) selection + tables
@@ -62,69 +18,6 @@ __device__ __forceinline__ void warp_top6(const float (&v)[8], int lane, int (&s
 
 constexpr int RT_WARPS = 4;                    // one expert per warp
 constexpr int RT_CTAS = E / RT_WARPS;          // 64
-
-// Build the decode tables from sel_e/sel_w (smem) -- one CTA.
-__device__ void build_decode_tables(int T, const int* sel_e, const float* sel_w, int* cnt, DecodeTables* tab) {
-    const int tid = threadIdx.x, nt = blockDim.x;
-    for (int e = tid; e < E; e += nt) cnt[e] = 0;
-    __syncthreads();
-    for (int p = tid; p < T * TOPK; p += nt) atomicAdd(&cnt[sel_e[p]], 1);
-    __syncthreads();
-    // warp 0: exclusive scans of presence and counts over experts
-    __shared__ int s_pair0[E];
-    if (tid < 32) {
-        const int lane = tid;
-        int pres = 0, sum = 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            pres += cnt[lane * 8 + i] > 0;
-            sum += cnt[lane * 8 + i];
-        }
-        int ip = pres, is = sum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int a = __shfl_up_sync(0xFFFFFFFFu, ip, o);
-            const int b = __shfl_up_sync(0xFFFFFFFFu, is, o);
-            if (lane >= o) {
-                ip += a;
-                is += b;
-            }
-        }
-        int slot = 1 + ip - pres;   // slot 0 is the shared expert
-        int pair0 = T + is - sum;   // pairs 0..T-1 are the shared expert's
-        for (int i = 0; i < 8; ++i) {
-            const int e = lane * 8 + i;
-            s_pair0[e] = pair0;
-            if (cnt[e] > 0) {
-                tab->slot_expert[slot] = e;
-                tab->slot_pair0[slot] = pair0;
-                ++slot;
-                pair0 += cnt[e];
-            }
-        }
-        if (lane == 31) {
-            tab->n_slots = slot;
-            tab->n_pairs = pair0;
-            tab->slot_pair0[slot] = pair0;
-            tab->T = T;
-            tab->slot_expert[0] = SHARED;
-            tab->slot_pair0[0] = 0;
-        }
-    }
-    for (int t = tid; t < T; t += nt) {
-        tab->pair_token[t] = t;
-        tab->pair_weight[t] = 1.0f;
-    }
-    __syncthreads();
-    for (int p = tid; p < T * TOPK; p += nt) {
-        const int t = p / TOPK, e = sel_e[p];
-        int rank = 0;
-        for (int q = 0; q < t * TOPK; ++q) rank += sel_e[q] == e;
-        const int pair = s_pair0[e] + rank;
-        tab->pair_token[pair] = t;
-        tab->pair_weight[pair] = sel_w[p];
-    }
-}
 
 struct RouterDecodeParams {
     const __nv_bfloat16* x;  // [T][H]
@@ -195,7 +88,8 @@ __global__ void __launch_bounds__(RT_WARPS * 32) router_decode_kernel(RouterDeco
 
     __shared__ int sel_e[DEC_T * TOPK];
     __shared__ float sel_w[DEC_T * TOPK];
-    __shared__ int cnt[E];
+    __shared__ uint32_t tmask[E];
+    __shared__ int pair0[E];
     for (int t = warp; t < T; t += RT_WARPS) {
         float v[8];
 #pragma unroll
@@ -204,15 +98,51 @@ __global__ void __launch_bounds__(RT_WARPS * 32) router_decode_kernel(RouterDeco
         float wt[TOPK];
         warp_top6(v, lane, sel, wt);
         if (lane < TOPK) {
-            p.idx[t * TOPK + lane] = sel[lane];
-            p.w[t * TOPK + lane] = wt[lane];
-            sel_e[t * TOPK + lane] = sel[lane];
-            sel_w[t * TOPK + lane] = wt[lane];
+            const int se = pick6(sel, lane);
+            const float sw = pick6(wt, lane);
+            p.idx[t * TOPK + lane] = se;
+            p.w[t * TOPK + lane] = sw;
+            sel_e[t * TOPK + lane] = se;
+            sel_w[t * TOPK + lane] = sw;
         }
     }
     if (threadIdx.x == 0) *p.ticket = 0;  // ready for the next call
     __syncthreads();
-    if (p.tables) build_decode_tables(T, sel_e, sel_w, cnt, p.tables);
+    if (p.tables && warp == 0) build_decode_tables_warp(T, sel_e, sel_w, tmask, pair0, p.tables, lane);
+}
+
+// Logits only (the forward path: the expert kernel selects per CTA).
+__global__ void __launch_bounds__(RT_WARPS * 32) router_logits_decode_kernel(const __nv_bfloat16* x, int T,
+                                                                           const __nv_bfloat16* Wr,
+                                                                           const float* bias, float* logits) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e = blockIdx.x * RT_WARPS + warp;
+    uint4 wr[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) wr[i] = ldg16(Wr + (size_t)e * H + 8 * (lane + 32 * i));
+    const float b = bias ? __ldg(bias + e) : 0.f;
+    pdl_trigger();
+    pdl_wait();
+    for (int t = 0; t < T; ++t) {
+        const __nv_bfloat16* xr = x + (size_t)t * H;
+        uint4 xv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) xv[i] = ldg16(xr + 8 * (lane + 32 * i));
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            acc = fmaf(bf_lo(wr[i].x), bf_lo(xv[i].x), acc);
+            acc = fmaf(bf_hi(wr[i].x), bf_hi(xv[i].x), acc);
+            acc = fmaf(bf_lo(wr[i].y), bf_lo(xv[i].y), acc);
+            acc = fmaf(bf_hi(wr[i].y), bf_hi(xv[i].y), acc);
+            acc = fmaf(bf_lo(wr[i].z), bf_lo(xv[i].z), acc);
+            acc = fmaf(bf_hi(wr[i].z), bf_hi(xv[i].z), acc);
+            acc = fmaf(bf_lo(wr[i].w), bf_lo(xv[i].w), acc);
+            acc = fmaf(bf_hi(wr[i].w), bf_hi(xv[i].w), acc);
+        }
+        acc = warp_sum(acc);
+        if (lane == 0) logits[(size_t)t * E + e] = acc + b;
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -265,8 +195,8 @@ __global__ void __launch_bounds__(128) select_kernel(const float* logits, int T,
     float wt[TOPK];
     warp_top6(v, lane, sel, wt);
     if (lane < TOPK) {
-        idx[t * TOPK + lane] = sel[lane];
-        w[t * TOPK + lane] = wt[lane];
+        idx[t * TOPK + lane] = pick6(sel, lane);
+        w[t * TOPK + lane] = pick6(wt, lane);
     }
 }
 
@@ -369,6 +299,12 @@ cudaError_t launch_router_decode(const LaunchCtx& L, const __nv_bfloat16* x, int
                                  DecodeTables* tables, unsigned* ticket) {
     RouterDecodeParams p{x, T, Wr, bias, logits, x_f32, idx, w, tables, ticket};
     return launch_pdl(L, router_decode_kernel, dim3(RT_CTAS), dim3(RT_WARPS * 32), 0, p);
+}
+
+cudaError_t launch_router_logits_decode(const LaunchCtx& L, const __nv_bfloat16* x, int T,
+                                        const __nv_bfloat16* Wr, const float* bias, float* logits) {
+    return launch_pdl(L, router_logits_decode_kernel, dim3(RT_CTAS), dim3(RT_WARPS * 32), 0, x, T, Wr, bias,
+                      logits);
 }
 
 cudaError_t launch_router_logits_general(const LaunchCtx& L, const __nv_bfloat16* x, int T,

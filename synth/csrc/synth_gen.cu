@@ -62,6 +62,25 @@ __global__ void fill_normal_bf16_kernel(uint16_t* dst, uint64_t n, uint64_t star
     }
 }
 
+// n_tensors consecutive tensors of `elems` elements each; tensor i is the
+// stream (seed, layer, tensor0 + i * tensor_stride)
+__global__ void fill_normal_bf16_batched_kernel(uint16_t* dst, uint32_t n_tensors, uint64_t elems, uint32_t seed,
+                                                uint32_t layer, uint32_t tensor0, uint32_t tensor_stride,
+                                                double std_) {
+    const uint64_t pairs = elems / 2;   // elems is even
+    const uint64_t total = pairs * n_tensors;
+    for (uint64_t q = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; q < total;
+         q += (uint64_t)gridDim.x * blockDim.x) {
+        const uint32_t ti = uint32_t(q / pairs);
+        const uint64_t p = q - uint64_t(ti) * pairs;
+        double z0, z1;
+        normal_pair(stream_key(seed, layer, tensor0 + ti * tensor_stride), p, z0, z1);
+        uint16_t* d = dst + uint64_t(ti) * elems + 2 * p;
+        d[0] = bf16_bits_of(std_ * z0);
+        d[1] = bf16_bits_of(std_ * z1);
+    }
+}
+
 __global__ void fill_normal_f32_kernel(float* dst, uint64_t n, uint64_t key, double std_) {
     for (uint64_t q = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; q < (n + 1) / 2;
          q += (uint64_t)gridDim.x * blockDim.x) {
@@ -88,6 +107,17 @@ SYNTH_API int synth_fill_normal_bf16(void* dst, uint64_t n, uint64_t start, uint
     const uint64_t npairs = (n + (start & 1) + 1) / 2;
     fill_normal_bf16_kernel<<<grid_for(npairs), 256, 0, s>>>(static_cast<uint16_t*>(dst), n, start,
                                                             stream_key(seed, layer, tensor), std_);
+    return cudaGetLastError() == cudaSuccess ? 0 : 2;
+}
+
+// Tensor i of n_tensors (each `elems` bf16, elems even) gets stream
+// (seed, layer, tensor0 + i * tensor_stride).
+SYNTH_API int synth_fill_normal_bf16_batched(void* dst, uint32_t n_tensors, uint64_t elems, uint32_t seed,
+                                             uint32_t layer, uint32_t tensor0, uint32_t tensor_stride, double std_,
+                                             cudaStream_t s) {
+    if (!dst || n_tensors == 0 || elems == 0 || (elems & 1)) return 1;
+    fill_normal_bf16_batched_kernel<<<148 * 16, 256, 0, s>>>(static_cast<uint16_t*>(dst), n_tensors, elems, seed,
+                                                            layer, tensor0, tensor_stride, std_);
     return cudaGetLastError() == cudaSuccess ? 0 : 2;
 }
 

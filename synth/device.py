@@ -37,6 +37,10 @@ def _load():
         lib.synth_fill_normal_bf16.restype = ctypes.c_int
         lib.synth_fill_normal_bf16.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint32,
                                                ctypes.c_uint32, ctypes.c_uint32, ctypes.c_double, ctypes.c_void_p]
+        lib.synth_fill_normal_bf16_batched.restype = ctypes.c_int
+        lib.synth_fill_normal_bf16_batched.argtypes = [ctypes.c_void_p, ctypes.c_uint32, ctypes.c_uint64,
+                                                       ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32,
+                                                       ctypes.c_uint32, ctypes.c_double, ctypes.c_void_p]
         lib.synth_fill_normal_f32.restype = ctypes.c_int
         lib.synth_fill_normal_f32.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32,
                                               ctypes.c_uint32, ctypes.c_double, ctypes.c_void_p]
@@ -58,6 +62,20 @@ def fill_normal_bf16(t, seed: int, layer: int, tensor: int, std: float, start: i
                                         float(std), _stream_ptr(stream))
     if rc != 0:
         raise RuntimeError(f"synth_fill_normal_bf16 failed ({rc})")
+    return t
+
+
+def fill_normal_bf16_batched(t, seed: int, layer: int, tensor0: int, tensor_stride: int, std: float,
+                             stream=None):
+    """Fill t[i] (t of shape [n, ...], contiguous bf16) with stream
+    (seed, layer, tensor0 + i * tensor_stride) for every i."""
+    import torch
+    assert t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous()
+    n = t.shape[0]
+    rc = _load().synth_fill_normal_bf16_batched(ctypes.c_void_p(t.data_ptr()), n, t.numel() // n, seed, layer,
+                                                tensor0, tensor_stride, float(std), _stream_ptr(stream))
+    if rc != 0:
+        raise RuntimeError(f"synth_fill_normal_bf16_batched failed ({rc})")
     return t
 
 
@@ -89,9 +107,8 @@ class LayerWeights:
             fill_normal_f32(self.router_b, seed, layer, gen.T_ROUTER_B, gen.BIAS_STD)
         self.gate_up = torch.empty((E + 1, 2 * I, H), dtype=torch.bfloat16, device=device)
         self.down = torch.empty((E + 1, H, I), dtype=torch.bfloat16, device=device)
-        for e in range(E + 1):
-            fill_normal_bf16(self.gate_up[e], seed, layer, gen.gate_up_tensor(e), gen.WEIGHT_STD)
-            fill_normal_bf16(self.down[e], seed, layer, gen.down_tensor(e), gen.WEIGHT_STD)
+        fill_normal_bf16_batched(self.gate_up, seed, layer, gen.gate_up_tensor(0), 2, gen.WEIGHT_STD)
+        fill_normal_bf16_batched(self.down, seed, layer, gen.down_tensor(0), 2, gen.WEIGHT_STD)
 
     def expert_bits(self, e: int):
         """(gate_up, down) of expert e as numpy uint16 bf16 bits (host copies)."""

@@ -26,3 +26,13 @@ def test_device_generator_matches_host():
     b = torch.empty(256, dtype=torch.float32, device="cuda")
     device.fill_normal_f32(b, 1, 0, gen.T_ROUTER_B, gen.BIAS_STD)
     assert np.allclose(b.cpu().numpy(), gen.router_bias(1, 0), rtol=1e-6, atol=0)
+
+
+def test_batched_generator_matches_per_tensor():
+    device.build()
+    t = torch.empty((3, 64, 32), dtype=torch.bfloat16, device="cuda")
+    device.fill_normal_bf16_batched(t, 2, 4, gen.gate_up_tensor(5), 2, 0.02)
+    for i in range(3):
+        host = gen.normal_bf16(2, 4, gen.gate_up_tensor(5 + i), (64 * 32,), 0.02)
+        got = t[i].reshape(-1).view(torch.int16).cpu().numpy().view(np.uint16)
+        assert (got != host).sum() <= 1
