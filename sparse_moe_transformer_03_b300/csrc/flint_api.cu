@@ -23,6 +23,12 @@ struct flint_moe {
     ExpertTables host_tables;      // BF16 pointers (host copy)
     ExpertTables* dev_tables;      // same, in device memory
 
+    // TMA tensor maps (device arrays) of the expert matrices and the router
+    CUtensorMap* gu_maps;          // [NEXP] boxes 64 x 128
+    CUtensorMap* dn_maps;          // [NEXP] boxes 64 x 128
+    CUtensorMap wr_map;            // boxes 64 x 256
+    CUtensorMap h_map;             // h_perm, boxes 64 x 128
+
     // status word in host-mapped memory
     uint32_t* status_host;
     uint32_t* status_dev;
@@ -42,6 +48,8 @@ struct flint_moe {
     int32_t* blk_base;             // [CHUNK/128][E]
     int32_t* offsets;              // [E+1]
     int32_t* gather;               // [CHUNK*TOPK]
+    __nv_bfloat16* h_perm;         // [(TOPK+1)*CHUNK][I]
+    float* y32;                    // [CHUNK][H]
 };
 
 namespace {
@@ -88,6 +96,8 @@ void free_handle(flint_moe* h) {
     if (!h) return;
     if (h->ws_base) cudaFree(h->ws_base);
     if (h->dev_tables) cudaFree(h->dev_tables);
+    if (h->gu_maps) cudaFree(h->gu_maps);
+    if (h->dn_maps) cudaFree(h->dn_maps);
     if (h->status_host) cudaFreeHost(h->status_host);
     delete h;
 }
@@ -106,6 +116,8 @@ void carve_workspace(flint_moe* h, char* base, size_t* bytes_out) {
     h->blk_base = c.take<int32_t>((size_t)(CHUNK / 128) * E);
     h->offsets = c.take<int32_t>(E + 1);
     h->gather = c.take<int32_t>((size_t)CHUNK * TOPK);
+    h->h_perm = c.take<__nv_bfloat16>((size_t)(TOPK + 1) * CHUNK * I);
+    h->y32 = c.take<float>((size_t)CHUNK * H);
     *bytes_out = c.off;
 }
 
@@ -188,6 +200,29 @@ flint_status_t flint_moe_create(flint_moe_t* out, const void* router_W, const fl
             if (cudaMemset(h->ws_base, 0, bytes) != cudaSuccess) st = FLINT_ERR_CUDA;
         }
     }
+    if (st == FLINT_OK) {
+        // tensor maps of every expert matrix, the router and h_perm
+        CUtensorMap* gu = new (std::nothrow) CUtensorMap[NEXP];
+        CUtensorMap* dn = new (std::nothrow) CUtensorMap[NEXP];
+        bool enc = gu && dn;
+        for (int e = 0; enc && e < NEXP; ++e) {
+            enc = encode_bf16_2d(&gu[e], h->host_tables.gate_up[e], 2 * I, H, H, 128, 64) &&
+                  encode_bf16_2d(&dn[e], h->host_tables.down[e], H, I, I, 128, 64);
+        }
+        enc = enc && encode_bf16_2d(&h->wr_map, h->router_W, E, H, H, E, 64) &&
+              encode_bf16_2d(&h->h_map, h->h_perm, (uint64_t)(TOPK + 1) * CHUNK, I, I, 128, 64);
+        if (!enc) st = FLINT_ERR_CUDA;
+        if (st == FLINT_OK && (cudaMalloc(&h->gu_maps, sizeof(CUtensorMap) * NEXP) != cudaSuccess ||
+                               cudaMalloc(&h->dn_maps, sizeof(CUtensorMap) * NEXP) != cudaSuccess))
+            st = FLINT_ERR_OOM;
+        if (st == FLINT_OK &&
+            (cudaMemcpy(h->gu_maps, gu, sizeof(CUtensorMap) * NEXP, cudaMemcpyHostToDevice) != cudaSuccess ||
+             cudaMemcpy(h->dn_maps, dn, sizeof(CUtensorMap) * NEXP, cudaMemcpyHostToDevice) != cudaSuccess))
+            st = FLINT_ERR_CUDA;
+        delete[] gu;
+        delete[] dn;
+    }
+    if (st == FLINT_OK) st = from_cuda(prefill_set_attributes());
     if (st == FLINT_OK) st = from_cuda(decode_set_attributes());
     if (st == FLINT_OK) st = from_cuda(cudaDeviceSynchronize());
     if (st != FLINT_OK) {
@@ -218,7 +253,26 @@ flint_status_t flint_moe_forward(flint_moe_t h, const void* x, int T, void* y, c
             e = launch_decode_experts(L, h->dev_tables, h->logits, xs, T, h->dec_tables, h->idx, h->w, h->a_dec, ys);
         return from_cuda(e);
     }
-    return FLINT_ERR_UNSUPPORTED;
+    // grouped tensor-core path, chunks of CHUNK tokens
+    for (int t0 = 0; t0 < T; t0 += CHUNK) {
+        const int Tc = T - t0 < CHUNK ? T - t0 : CHUNK;
+        const __nv_bfloat16* xc = xs + (size_t)t0 * H;
+        CUtensorMap xmap, xgmap;
+        if (!encode_bf16_2d(&xmap, xc, Tc, H, H, 128, 64) || !encode_bf16_2d(&xgmap, xc, Tc, H, H, 1, 64))
+            return FLINT_ERR_CUDA;
+        cudaError_t e = cudaMemsetAsync(h->y32, 0, (size_t)Tc * H * sizeof(float), s);
+        if (e == cudaSuccess)
+            e = launch_prefill_router(L, xmap, h->wr_map, Tc, h->router_b, nullptr, h->idx, h->w, h->local_rank,
+                                      h->blk_counts);
+        if (e == cudaSuccess)
+            e = launch_perm_scan_scatter(L, h->idx, Tc, h->local_rank, h->blk_counts, h->blk_base, h->offsets,
+                                         h->gather);
+        if (e == cudaSuccess)
+            e = launch_prefill_experts(L, xgmap, h->h_map, Tc, h->offsets, h->gather, h->w, h->gu_maps, h->dn_maps,
+                                       h->h_perm, h->y32, ys + (size_t)t0 * H);
+        if (e != cudaSuccess) return FLINT_ERR_CUDA;
+    }
+    return FLINT_OK;
 }
 
 flint_status_t flint_moe_route_only(flint_moe_t h, const void* x, float* logits, int T, int32_t* idx,
@@ -238,8 +292,16 @@ flint_status_t flint_moe_route_only(flint_moe_t h, const void* x, float* logits,
             e = launch_router_decode(L, xs, T, h->router_W, h->router_b, lg, nullptr, idx, w, nullptr,
                                      h->ticket);
         } else {
-            e = launch_router_logits_general(L, xs, T, h->router_W, h->router_b, lg);
-            if (e == cudaSuccess) e = launch_select(L, lg, T, idx, w);
+            CUtensorMap xmap;
+            if (!encode_bf16_2d(&xmap, xs, T, H, H, 128, 64)) return FLINT_ERR_CUDA;
+            e = launch_prefill_router(L, xmap, h->wr_map, T, h->router_b, logits, idx, w, h->local_rank,
+                                      h->blk_counts);
+            if (e == cudaSuccess && (offsets || gather_idx))
+                e = launch_perm_scan_scatter(L, idx, T, h->local_rank, h->blk_counts, h->blk_base,
+                                             offsets ? offsets : h->offsets, gather_idx);
+            if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+            if (e != cudaSuccess) return FLINT_ERR_CUDA;
+            return take_device_status(h);
         }
     } else {
         e = launch_select(L, logits, T, idx, w);

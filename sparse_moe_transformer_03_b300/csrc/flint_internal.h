@@ -1,6 +1,7 @@
 // flint_internal.h -- host-side declarations shared by the library's .cu files.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -47,6 +48,24 @@ cudaError_t launch_router_logits_general(const LaunchCtx& L, const __nv_bfloat16
 cudaError_t launch_select(const LaunchCtx& L, const float* logits, int T, int32_t* idx, float* w);
 cudaError_t launch_permutation(const LaunchCtx& L, const int32_t* idx, int T, int32_t* local_rank,
                                int32_t* blk_counts, int32_t* blk_base, int32_t* offsets, int32_t* gather);
+// scan + scatter only (block-local ranks and counts already computed)
+cudaError_t launch_perm_scan_scatter(const LaunchCtx& L, const int32_t* idx, int T, const int32_t* local_rank,
+                                     const int32_t* blk_counts, int32_t* blk_base, int32_t* offsets,
+                                     int32_t* gather);
+
+// tmap.cu
+bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t pitch,
+                    uint32_t box_rows, uint32_t box_cols);
+
+// prefill.cu
+cudaError_t prefill_set_attributes();
+cudaError_t launch_prefill_router(const LaunchCtx& L, const CUtensorMap& x_map, const CUtensorMap& wr_map, int T,
+                                  const float* bias, float* logits, int32_t* idx, float* w, int32_t* local_rank,
+                                  int32_t* blk_counts);
+cudaError_t launch_prefill_experts(const LaunchCtx& L, const CUtensorMap& xg_map, const CUtensorMap& h_map, int T,
+                                   const int32_t* offsets, const int32_t* gather, const float* w_route,
+                                   const CUtensorMap* gu_maps, const CUtensorMap* dn_maps, __nv_bfloat16* h_perm,
+                                   float* y32, __nv_bfloat16* y);
 
 // decode.cu
 cudaError_t decode_set_attributes();

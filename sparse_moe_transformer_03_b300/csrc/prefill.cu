@@ -1,0 +1,686 @@
+// prefill.cu -- the many-token path (T > 32) on the 5th-generation tensor
+// cores: tcgen05.mma with fp32 accumulators in TMEM, operands staged in smem
+// by TMA (tiled loads, and gather4 for the routed token rows).
+//
+//   prefill_router   logits[128 tokens][256 experts] per CTA (K = 2048); the
+//                    epilogue (one thread per token) adds the bias, selects the
+//                    top-6 with equal logits going to the lower expert id,
+//                    renormalises the sigmoid weights and computes each
+//                    (token, slot) pair's rank among the block's pairs of the
+//                    same expert plus the block's per-expert counts.
+//   (scan, scatter)  offsets[257] and the expert-grouped pair list (router.cu)
+//   prefill_gateup   grouped GEMM, "swapped": M = 128 rows of an expert's gate
+//                    (and, in a second accumulator, the matching up) matrix,
+//                    N = up to 128 of the expert's tokens gathered from x,
+//                    K = 2048.  Epilogue: h = silu(gate) * up, bf16, into
+//                    h_perm[slot][512] (routed slots in expert order, then the
+//                    shared expert's T slots).
+//   prefill_down     grouped GEMM: M = 128 rows of the expert's down matrix,
+//                    N = up to 128 slots of h_perm, K = 512.  Epilogue: each
+//                    result times the pair's routing weight (1 for the shared
+//                    expert) is added into y32[token][h] with fp32 reductions.
+//   convert          y = bf16(y32).
+//
+// Warp roles in every GEMM kernel: warp 0 issues TMA (one elected thread),
+// warp 1 allocates TMEM and issues MMAs (one thread), warps 2..5 drain TMEM in
+// the epilogue (warp w reads TMEM lanes 32*(w%4)..+31).  The grouped GEMMs are
+// persistent: CTA c takes units c, c + grid, ... of the list ordered by
+// (expert, row block, token tile), so CTAs working at the same time share the
+// expert's weight tiles through L2.  Every wait is bounded; a timeout sets an
+// abort flag the other roles observe, reports FLINT_ERR_DEVICE_TIMEOUT and the
+// CTA still frees its TMEM.
+//
+// Layer definition: RecursiveSI/flint (vLLM recipe page), "Overview"; SwiGLU
+// experts with H = 2048, I = 512 are this library's reading.
+#include "flint_common.cuh"
+#include "flint_internal.h"
+#include "tc_ptx.cuh"
+
+namespace flint {
+
+constexpr int PF_THREADS = 192;
+constexpr int PF_TILE = 128;                 // rows of every operand tile
+constexpr int PF_BK = 64;                    // K per stage: 128 bytes of bf16
+constexpr int PF_TILE_BYTES = PF_TILE * PF_BK * 2;   // 16 KiB
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+    return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Named barrier of the 128 epilogue threads that also ANDs a predicate, so a
+// decision to give up is taken by all of them together.
+__device__ __forceinline__ bool epi_all(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n barrier.cta.red.and.pred q, 1, 128, p;\n"
+        " selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"(v ? 1u : 0u)
+        : "memory");
+    return r != 0;
+}
+
+// Bounded wait that also gives up when another role has aborted.
+__device__ __forceinline__ bool pf_wait(uint64_t* bar, uint32_t parity, uint64_t limit, volatile int* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 16; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > limit) {
+            *abort = 1;
+            return false;
+        }
+    }
+}
+
+// ===========================================================================
+// router GEMM + top-6 + block-local permutation ranks
+// ===========================================================================
+
+constexpr int RG_STAGES = 4;
+constexpr int RG_B_BYTES = E * PF_BK * 2;                  // 32 KiB: all 256 router rows
+constexpr int RG_STAGE = PF_TILE_BYTES + RG_B_BYTES;       // 48 KiB
+constexpr int RG_SMEM = 1024 + RG_STAGES * RG_STAGE + 256 + E * 4 * 4;
+
+struct RouterGemmParams {
+    int T;
+    const float* bias;        // [E] or null
+    float* logits;            // [T][E] or null (route-only output)
+    int32_t* idx;             // [T][6]
+    float* w;                 // [T][6]
+    int32_t* local_rank;      // [T][6]
+    int32_t* blk_counts;      // [nblk][E]
+    uint32_t* status;
+    uint64_t limit_ns;
+};
+
+__global__ void __launch_bounds__(PF_THREADS, 1)
+    prefill_router_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CUtensorMap wr_map,
+                          RouterGemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align1024(smem_raw);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + RG_STAGES * RG_STAGE);
+    uint64_t* empty = full + RG_STAGES;
+    uint64_t* tfull = empty + RG_STAGES;
+    uint64_t* mdone = tfull + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mdone + 1);
+    volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    uint32_t* mask = reinterpret_cast<uint32_t*>(smem + RG_STAGES * RG_STAGE + 256);   // [E][4]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int blk = blockIdx.x, row0 = blk * PF_TILE;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < RG_STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(tfull, 1);
+        mbar_init(mdone, 1);
+        *abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_slot, 256);
+        tc::tmem_relinquish();
+    }
+    for (int k = threadIdx.x; k < E * 4; k += PF_THREADS) mask[k] = 0u;
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    pdl_wait();      // x may come from the previous kernel
+    pdl_trigger();
+
+    constexpr int KC = H / PF_BK;   // 32
+    if (warp == 0 && lane == 0) {
+        tc::prefetch_tensormap(&x_map);
+        tc::prefetch_tensormap(&wr_map);
+        for (int kc = 0; kc < KC; ++kc) {
+            const int s = kc % RG_STAGES;
+            if (!pf_wait(&empty[s], ((kc / RG_STAGES) & 1) ^ 1, p.limit_ns, abort)) break;
+            uint8_t* st = smem + s * RG_STAGE;
+            mbar_arrive_expect_tx(&full[s], RG_STAGE);
+            tc::tma_load_2d(st, &x_map, kc * PF_BK, row0, &full[s]);
+            tc::tma_load_2d(st + PF_TILE_BYTES, &wr_map, kc * PF_BK, 0, &full[s]);
+        }
+    } else if (warp == 1 && lane == 0) {
+        constexpr uint32_t idesc = tc::idesc_bf16_f32(128, 256);
+        for (int kc = 0; kc < KC; ++kc) {
+            const int s = kc % RG_STAGES;
+            if (!pf_wait(&full[s], (kc / RG_STAGES) & 1, p.limit_ns, abort)) break;
+            tc::fence_after_sync();
+            const uint8_t* st = smem + s * RG_STAGE;
+            const uint64_t a = tc::smem_desc_sw128(st), b = tc::smem_desc_sw128(st + PF_TILE_BYTES);
+#pragma unroll
+            for (int kk = 0; kk < PF_BK / 16; ++kk)
+                tc::mma_bf16(tmem, a + 2 * kk, b + 2 * kk, idesc, (kc | kk) != 0);
+            tc::mma_commit(&empty[s]);
+        }
+        tc::mma_commit(tfull);
+        tc::mma_commit(mdone);
+        mbar_wait_bounded(mdone, 0, p.limit_ns);
+    } else if (warp >= 2) {
+        const int q = warp & 3, row = 32 * q + lane, t = row0 + row;
+        // tcgen05.ld is warp-collective: the warp decides together
+        const bool ok = __all_sync(0xFFFFFFFFu, pf_wait(tfull, 0, p.limit_ns, abort));
+        tc::fence_after_sync();
+        float tv[TOPK];
+        int ti[TOPK];
+#pragma unroll
+        for (int r = 0; r < TOPK; ++r) {
+            tv[r] = -INFINITY;
+            ti[r] = r;
+        }
+        if (ok) {
+#pragma unroll 1
+            for (int c = 0; c < E / 32; ++c) {
+                uint32_t v[32];
+                tc::tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 32 * c, v);
+                tc::tmem_ld_wait();
+                float l[32];
+#pragma unroll
+                for (int m = 0; m < 32; ++m) l[m] = __uint_as_float(v[m]) + (p.bias ? __ldg(p.bias + 32 * c + m) : 0.f);
+                if (p.logits && t < p.T) {
+                    float4* dst = reinterpret_cast<float4*>(p.logits + (size_t)t * E + 32 * c);
+#pragma unroll
+                    for (int m = 0; m < 8; ++m) dst[m] = make_float4(l[4 * m], l[4 * m + 1], l[4 * m + 2], l[4 * m + 3]);
+                }
+                // insertion into the sorted top-6; experts arrive in increasing
+                // id, so a strict comparison keeps the lower id on equal logits
+#pragma unroll
+                for (int m = 0; m < 32; ++m) {
+                    const float x = l[m];
+                    if (x > tv[TOPK - 1]) {
+                        tv[TOPK - 1] = x;
+                        ti[TOPK - 1] = 32 * c + m;
+#pragma unroll
+                        for (int r = TOPK - 1; r > 0; --r) {
+                            if (tv[r] > tv[r - 1]) {
+                                const float a = tv[r];
+                                tv[r] = tv[r - 1];
+                                tv[r - 1] = a;
+                                const int b = ti[r];
+                                ti[r] = ti[r - 1];
+                                ti[r - 1] = b;
+                            }
+                        }
+                    }
+                }
+            }
+        }
+        float s[TOPK], sum = 0.f;
+#pragma unroll
+        for (int r = 0; r < TOPK; ++r) {
+            s[r] = sigmoid_f(tv[r]);
+            sum += s[r];
+        }
+        if (t < p.T) {
+#pragma unroll
+            for (int r = 0; r < TOPK; ++r) {
+                p.idx[t * TOPK + r] = ti[r];
+                p.w[t * TOPK + r] = s[r] / sum;
+                atomicOr(&mask[ti[r] * 4 + (row >> 5)], 1u << (row & 31));
+            }
+        }
+        epi_sync();
+        if (t < p.T) {
+#pragma unroll
+            for (int r = 0; r < TOPK; ++r) {
+                const uint32_t* m = mask + ti[r] * 4;
+                int rank = __popc(m[row >> 5] & ((1u << (row & 31)) - 1u));
+                for (int wd = 0; wd < (row >> 5); ++wd) rank += __popc(m[wd]);
+                p.local_rank[t * TOPK + r] = rank;
+            }
+        }
+        for (int e = row; e < E; e += 128)
+            p.blk_counts[blk * E + e] = __popc(mask[e * 4]) + __popc(mask[e * 4 + 1]) + __popc(mask[e * 4 + 2]) +
+                                        __popc(mask[e * 4 + 3]);
+        if (!ok && row == 0) report_status(p.status, ST_TIMEOUT);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, 256);
+    }
+}
+
+// ===========================================================================
+// grouped expert GEMMs
+// ===========================================================================
+
+struct GroupedParams {
+    int T;
+    const int32_t* offsets;      // [E+1] slot base of each routed expert (6T total)
+    const int32_t* gather;       // [6T] pair ids t*6+j grouped by expert
+    const float* w_route;        // [T][6]
+    const CUtensorMap* gu_maps;  // [NEXP] gate_up matrices, boxes 64 x 128
+    const CUtensorMap* dn_maps;  // [NEXP] down matrices, boxes 64 x 128
+    __nv_bfloat16* h_perm;       // [7T][I]
+    float* y32;                  // [T][H]
+    uint32_t* status;
+    uint64_t limit_ns;
+};
+
+// Per-CTA copy of the unit schedule: expert e covers units
+// [upre[e], upre[e+1]); its slots start at base[e] and number cnt[e].
+struct Sched {
+    int base[NEXP + 1];
+    int cnt[NEXP];
+    int upre[NEXP + 1];
+};
+
+__device__ void build_sched(Sched* S, const GroupedParams& p, int units_per_tile) {
+    const int tid = threadIdx.x;
+    for (int e = tid; e < NEXP; e += blockDim.x) {
+        const int b = e < E ? p.offsets[e] : TOPK * p.T;
+        const int n = e < E ? p.offsets[e + 1] - b : p.T;
+        S->base[e] = b;
+        S->cnt[e] = n;
+    }
+    __syncthreads();
+    if (tid < 32) {
+        // exclusive scan of units over the 257 experts, 9 per lane
+        int loc[9], sum = 0;
+#pragma unroll
+        for (int k = 0; k < 9; ++k) {
+            const int e = tid * 9 + k;
+            loc[k] = e < NEXP ? units_per_tile * ((S->cnt[e] + PF_TILE - 1) / PF_TILE) : 0;
+            sum += loc[k];
+        }
+        int inc = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int a = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+            if (tid >= o) inc += a;
+        }
+        int run = inc - sum;
+#pragma unroll
+        for (int k = 0; k < 9; ++k) {
+            const int e = tid * 9 + k;
+            if (e < NEXP) S->upre[e] = run;
+            run += loc[k];
+        }
+        if (tid == 31) S->upre[NEXP] = run;
+    }
+    __syncthreads();
+}
+
+// expert of unit u (binary search over the prefix)
+__device__ __forceinline__ int unit_expert(const Sched* S, int u) {
+    int lo = 0, hi = NEXP - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (S->upre[mid] <= u) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+struct Unit {
+    int e, blk, tt, base, nvalid, npad;
+};
+
+__device__ __forceinline__ Unit decode_unit(const Sched* S, int u, int blocks) {
+    Unit U;
+    U.e = unit_expert(S, u);
+    const int nt = (S->cnt[U.e] + PF_TILE - 1) / PF_TILE;
+    const int r = u - S->upre[U.e];
+    U.blk = r / nt;
+    U.tt = r - U.blk * nt;
+    U.base = S->base[U.e] + U.tt * PF_TILE;
+    U.nvalid = min(PF_TILE, S->cnt[U.e] - U.tt * PF_TILE);
+    U.npad = (U.nvalid + 15) & ~15;
+    (void)blocks;
+    return U;
+}
+
+// ---------------------------------------------------------------------------
+// GEMM 1: gate/up + SwiGLU
+// ---------------------------------------------------------------------------
+
+constexpr int G1_STAGES = 4;
+constexpr int G1_STAGE = 3 * PF_TILE_BYTES;    // gate tile, up tile, token tile
+constexpr int G1_BLOCKS = I / PF_TILE;         // 4 row blocks of 128
+constexpr int G1_SMEM = 1024 + G1_STAGES * G1_STAGE + 512 + PF_TILE * 4 + (int)sizeof(Sched);
+
+__global__ void __launch_bounds__(PF_THREADS, 1)
+    prefill_gateup_kernel(const __grid_constant__ CUtensorMap xg_map, GroupedParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align1024(smem_raw);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + G1_STAGES * G1_STAGE);
+    uint64_t* empty = full + G1_STAGES;
+    uint64_t* tfull = empty + G1_STAGES;    // [2]
+    uint64_t* tempty = tfull + 2;           // [2]
+    uint64_t* mdone = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mdone + 1);
+    volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int* tok = reinterpret_cast<int*>(smem + G1_STAGES * G1_STAGE + 512);           // [128]
+    Sched* S = reinterpret_cast<Sched*>(tok + PF_TILE);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < G1_STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 4);
+        }
+        mbar_init(mdone, 1);
+        *abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_slot, 512);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    pdl_wait();     // routing, permutation and x are complete
+    pdl_trigger();
+    build_sched(S, p, G1_BLOCKS);
+    const int total = S->upre[NEXP];
+    const int sixT = TOPK * p.T;
+    constexpr int KC = H / PF_BK;   // 32
+
+    if (warp == 0) {
+        if (lane == 0) tc::prefetch_tensormap(&xg_map);
+        int kc_all = 0;
+        for (int u = blockIdx.x; u < total && !__shfl_sync(0xFFFFFFFFu, *abort, 0); u += gridDim.x) {
+            const Unit U = decode_unit(S, u, G1_BLOCKS);
+            // token rows of this tile (padding rows repeat the last valid one)
+#pragma unroll
+            for (int k = 0; k < PF_TILE / 32; ++k) {
+                const int n = lane + 32 * k;
+                const int slot = U.base + min(n, U.nvalid - 1);
+                tok[n] = U.e < E ? __ldg(p.gather + slot) / TOPK : slot - sixT;
+            }
+            __syncwarp();
+            if (lane == 0) {
+                const CUtensorMap* wm = p.gu_maps + U.e;
+                for (int kc = 0; kc < KC; ++kc, ++kc_all) {
+                    const int s = kc_all % G1_STAGES;
+                    if (!pf_wait(&empty[s], ((kc_all / G1_STAGES) & 1) ^ 1, p.limit_ns, abort)) break;
+                    uint8_t* st = smem + s * G1_STAGE;
+                    mbar_arrive_expect_tx(&full[s], 2 * PF_TILE_BYTES + U.npad * PF_BK * 2);
+                    tc::tma_load_2d(st, wm, kc * PF_BK, U.blk * PF_TILE, &full[s]);
+                    tc::tma_load_2d(st + PF_TILE_BYTES, wm, kc * PF_BK, I + U.blk * PF_TILE, &full[s]);
+                    for (int g = 0; g < U.npad / 4; ++g)
+                        tc::tma_gather4(st + 2 * PF_TILE_BYTES + g * 4 * PF_BK * 2, &xg_map, kc * PF_BK, tok[4 * g],
+                                        tok[4 * g + 1], tok[4 * g + 2], tok[4 * g + 3], &full[s]);
+                }
+            }
+            __syncwarp();
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int kc_all = 0, lu = 0;
+            for (int u = blockIdx.x; u < total && !*abort; u += gridDim.x, ++lu) {
+                const Unit U = decode_unit(S, u, G1_BLOCKS);
+                const int b = lu & 1;
+                if (!pf_wait(&tempty[b], ((lu >> 1) & 1) ^ 1, p.limit_ns, abort)) break;
+                tc::fence_after_sync();
+                const uint32_t idesc = tc::idesc_bf16_f32(128, U.npad);
+                const uint32_t dg = tmem + b * 256, du = tmem + b * 256 + 128;
+                for (int kc = 0; kc < KC; ++kc, ++kc_all) {
+                    const int s = kc_all % G1_STAGES;
+                    if (!pf_wait(&full[s], (kc_all / G1_STAGES) & 1, p.limit_ns, abort)) break;
+                    tc::fence_after_sync();
+                    const uint8_t* st = smem + s * G1_STAGE;
+                    const uint64_t ag = tc::smem_desc_sw128(st), au = tc::smem_desc_sw128(st + PF_TILE_BYTES);
+                    const uint64_t bx = tc::smem_desc_sw128(st + 2 * PF_TILE_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < PF_BK / 16; ++kk) {
+                        tc::mma_bf16(dg, ag + 2 * kk, bx + 2 * kk, idesc, (kc | kk) != 0);
+                        tc::mma_bf16(du, au + 2 * kk, bx + 2 * kk, idesc, (kc | kk) != 0);
+                    }
+                    tc::mma_commit(&empty[s]);
+                }
+                tc::mma_commit(&tfull[b]);
+            }
+            // every MMA this thread issued has finished before TMEM is freed
+            tc::mma_commit(mdone);
+            mbar_wait_bounded(mdone, 0, p.limit_ns);
+        }
+        __syncwarp();
+    } else {
+        const int q = warp & 3, row = 32 * q + lane;
+        int lu = 0;
+        for (int u = blockIdx.x; u < total; u += gridDim.x, ++lu) {
+            const Unit U = decode_unit(S, u, G1_BLOCKS);
+            const int b = lu & 1;
+            if (!__all_sync(0xFFFFFFFFu, pf_wait(&tfull[b], (lu >> 1) & 1, p.limit_ns, abort))) break;
+            tc::fence_after_sync();
+            const int j = U.blk * PF_TILE + row;
+            const uint32_t tg = tmem + ((uint32_t)(32 * q) << 16) + b * 256;
+            for (int c0 = 0; c0 < U.npad; c0 += 32) {
+                uint32_t g[32], up[32];
+                tc::tmem_ld32(tg + c0, g);
+                tc::tmem_ld32(tg + 128 + c0, up);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int m = 0; m < 32; ++m) {
+                    const int n = c0 + m;
+                    if (n < U.nvalid) {
+                        const float h = silu_f(__uint_as_float(g[m])) * __uint_as_float(up[m]);
+                        p.h_perm[(size_t)(U.base + n) * I + j] = __float2bfloat16_rn(h);
+                    }
+                }
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[b]);
+        }
+    }
+    if (*abort && threadIdx.x == 0) report_status(p.status, ST_TIMEOUT);
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// GEMM 2: down projection + weighted scatter-add
+// ---------------------------------------------------------------------------
+
+constexpr int G2_STAGES = 6;
+constexpr int G2_STAGE = 2 * PF_TILE_BYTES;    // down tile, activation tile
+constexpr int G2_BLOCKS = H / PF_TILE;         // 16 row blocks of 128
+constexpr int G2_SMEM = 1024 + G2_STAGES * G2_STAGE + 512 + PF_TILE * 8 + (int)sizeof(Sched);
+
+__global__ void __launch_bounds__(PF_THREADS, 1)
+    prefill_down_kernel(const __grid_constant__ CUtensorMap h_map, GroupedParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align1024(smem_raw);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + G2_STAGES * G2_STAGE);
+    uint64_t* empty = full + G2_STAGES;
+    uint64_t* tfull = empty + G2_STAGES;    // [2]
+    uint64_t* tempty = tfull + 2;           // [2]
+    uint64_t* mdone = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mdone + 1);
+    volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int* tok = reinterpret_cast<int*>(smem + G2_STAGES * G2_STAGE + 512);          // [128]
+    float* wgt = reinterpret_cast<float*>(tok + PF_TILE);                           // [128]
+    Sched* S = reinterpret_cast<Sched*>(wgt + PF_TILE);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < G2_STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 4);
+        }
+        mbar_init(mdone, 1);
+        *abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_slot, 256);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    pdl_wait();     // h_perm is complete
+    pdl_trigger();
+    build_sched(S, p, G2_BLOCKS);
+    const int total = S->upre[NEXP];
+    const int sixT = TOPK * p.T;
+    constexpr int KC = I / PF_BK;   // 8
+
+    if (warp == 0) {
+        if (lane == 0) {
+            tc::prefetch_tensormap(&h_map);
+            int kc_all = 0;
+            for (int u = blockIdx.x; u < total && !*abort; u += gridDim.x) {
+                const Unit U = decode_unit(S, u, G2_BLOCKS);
+                const CUtensorMap* wm = p.dn_maps + U.e;
+                for (int kc = 0; kc < KC; ++kc, ++kc_all) {
+                    const int s = kc_all % G2_STAGES;
+                    if (!pf_wait(&empty[s], ((kc_all / G2_STAGES) & 1) ^ 1, p.limit_ns, abort)) break;
+                    uint8_t* st = smem + s * G2_STAGE;
+                    mbar_arrive_expect_tx(&full[s], 2 * PF_TILE_BYTES);
+                    tc::tma_load_2d(st, wm, kc * PF_BK, U.blk * PF_TILE, &full[s]);
+                    tc::tma_load_2d(st + PF_TILE_BYTES, &h_map, kc * PF_BK, U.base, &full[s]);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int kc_all = 0, lu = 0;
+            for (int u = blockIdx.x; u < total && !*abort; u += gridDim.x, ++lu) {
+                const Unit U = decode_unit(S, u, G2_BLOCKS);
+                const int b = lu & 1;
+                if (!pf_wait(&tempty[b], ((lu >> 1) & 1) ^ 1, p.limit_ns, abort)) break;
+                tc::fence_after_sync();
+                const uint32_t idesc = tc::idesc_bf16_f32(128, U.npad);
+                const uint32_t d = tmem + b * 128;
+                for (int kc = 0; kc < KC; ++kc, ++kc_all) {
+                    const int s = kc_all % G2_STAGES;
+                    if (!pf_wait(&full[s], (kc_all / G2_STAGES) & 1, p.limit_ns, abort)) break;
+                    tc::fence_after_sync();
+                    const uint8_t* st = smem + s * G2_STAGE;
+                    const uint64_t a = tc::smem_desc_sw128(st), bh = tc::smem_desc_sw128(st + PF_TILE_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < PF_BK / 16; ++kk)
+                        tc::mma_bf16(d, a + 2 * kk, bh + 2 * kk, idesc, (kc | kk) != 0);
+                    tc::mma_commit(&empty[s]);
+                }
+                tc::mma_commit(&tfull[b]);
+            }
+            // every MMA this thread issued has finished before TMEM is freed
+            tc::mma_commit(mdone);
+            mbar_wait_bounded(mdone, 0, p.limit_ns);
+        }
+        __syncwarp();
+    } else {
+        const int q = warp & 3, row = 32 * q + lane;
+        int lu = 0;
+        for (int u = blockIdx.x; u < total; u += gridDim.x, ++lu) {
+            const Unit U = decode_unit(S, u, G2_BLOCKS);
+            const int b = lu & 1;
+            // token and routing weight of each column of the tile
+            if (row < U.nvalid) {
+                const int slot = U.base + row;
+                if (U.e < E) {
+                    const int pr = __ldg(p.gather + slot);
+                    tok[row] = pr / TOPK;
+                    wgt[row] = __ldg(p.w_route + pr);
+                } else {
+                    tok[row] = slot - sixT;
+                    wgt[row] = 1.f;
+                }
+            }
+            // waits for the accumulator; also publishes tok/wgt to all four warps
+            if (!epi_all(pf_wait(&tfull[b], (lu >> 1) & 1, p.limit_ns, abort))) break;
+            tc::fence_after_sync();
+            const int h = U.blk * PF_TILE + row;
+            const uint32_t td = tmem + ((uint32_t)(32 * q) << 16) + b * 128;
+            for (int c0 = 0; c0 < U.npad; c0 += 32) {
+                uint32_t v[32];
+                tc::tmem_ld32(td + c0, v);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int m = 0; m < 32; ++m) {
+                    const int n = c0 + m;
+                    if (n < U.nvalid) atomicAdd(p.y32 + (size_t)tok[n] * H + h, wgt[n] * __uint_as_float(v[m]));
+                }
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[b]);
+            epi_sync();   // tok/wgt of this unit no longer needed
+        }
+    }
+    if (*abort && threadIdx.x == 0) report_status(p.status, ST_TIMEOUT);
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, 256);
+    }
+}
+
+__global__ void __launch_bounds__(256) convert_y_kernel(const float* y32, __nv_bfloat16* y, int n8) {
+    pdl_wait();
+    pdl_trigger();
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n8) return;
+    const float4 a = __ldcg(reinterpret_cast<const float4*>(y32) + 2 * i);
+    const float4 b = __ldcg(reinterpret_cast<const float4*>(y32) + 2 * i + 1);
+    __nv_bfloat162 o[4] = {__floats2bfloat162_rn(a.x, a.y), __floats2bfloat162_rn(a.z, a.w),
+                           __floats2bfloat162_rn(b.x, b.y), __floats2bfloat162_rn(b.z, b.w)};
+    reinterpret_cast<uint4*>(y)[i] = *reinterpret_cast<const uint4*>(o);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+cudaError_t prefill_set_attributes() {
+    cudaError_t e = cudaFuncSetAttribute(prefill_router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, RG_SMEM);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(prefill_gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, G1_SMEM);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(prefill_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, G2_SMEM);
+    return e;
+}
+
+cudaError_t launch_prefill_router(const LaunchCtx& L, const CUtensorMap& x_map, const CUtensorMap& wr_map, int T,
+                                  const float* bias, float* logits, int32_t* idx, float* w, int32_t* local_rank,
+                                  int32_t* blk_counts) {
+    RouterGemmParams rp{T, bias, logits, idx, w, local_rank, blk_counts, L.status, L.wait_limit_ns};
+    return launch_pdl(L, prefill_router_kernel, dim3((T + PF_TILE - 1) / PF_TILE), dim3(PF_THREADS), RG_SMEM, x_map,
+                      wr_map, rp);
+}
+
+cudaError_t launch_prefill_experts(const LaunchCtx& L, const CUtensorMap& xg_map, const CUtensorMap& h_map, int T,
+                                   const int32_t* offsets, const int32_t* gather, const float* w_route,
+                                   const CUtensorMap* gu_maps, const CUtensorMap* dn_maps, __nv_bfloat16* h_perm,
+                                   float* y32, __nv_bfloat16* y) {
+    GroupedParams gp{T, offsets, gather, w_route, gu_maps, dn_maps, h_perm, y32, L.status, L.wait_limit_ns};
+    cudaError_t e = launch_pdl(L, prefill_gateup_kernel, dim3(L.num_sms), dim3(PF_THREADS), G1_SMEM, xg_map, gp);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(L, prefill_down_kernel, dim3(L.num_sms), dim3(PF_THREADS), G2_SMEM, h_map, gp);
+    if (e != cudaSuccess) return e;
+    const int n8 = T * H / 8;
+    return launch_pdl(L, convert_y_kernel, dim3((n8 + 255) / 256), dim3(256), 0, (const float*)y32, y, n8);
+}
+
+}  // namespace flint

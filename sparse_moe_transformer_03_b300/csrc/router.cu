@@ -331,4 +331,14 @@ cudaError_t launch_permutation(const LaunchCtx& L, const int32_t* idx, int T, in
                       (const int32_t*)local_rank, T, (const int32_t*)blk_base, (const int32_t*)offsets, gather);
 }
 
+cudaError_t launch_perm_scan_scatter(const LaunchCtx& L, const int32_t* idx, int T, const int32_t* local_rank,
+                                     const int32_t* blk_counts, int32_t* blk_base, int32_t* offsets,
+                                     int32_t* gather) {
+    const int nblk = (T + PB_TOK - 1) / PB_TOK;
+    cudaError_t err = launch_pdl(L, perm_scan_kernel, dim3(1), dim3(E), 0, blk_counts, nblk, blk_base, offsets);
+    if (err != cudaSuccess || !gather) return err;
+    return launch_pdl(L, perm_scatter_kernel, dim3((T * TOPK + 255) / 256), dim3(256), 0, idx, local_rank, T,
+                      (const int32_t*)blk_base, (const int32_t*)offsets, gather);
+}
+
 }  // namespace flint
