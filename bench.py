@@ -37,7 +37,10 @@ WORKLOADS = {
     "decode1": {"T": 1, "x": "gauss", "x_seed": 11},
     "decode8": {"T": 8, "x": "clustered", "x_seed": 12},
     "decode32": {"T": 32, "x": "clustered", "x_seed": 13},
+    "prefill8192": {"T": 8192, "x": "gauss", "x_seed": 14, "prefill": True},
 }
+# dense flops of one layer per token: 7 experts x (gate, up, down) + router
+FLOPS_PER_TOKEN = 7 * 2 * 3 * 2048 * 512 + 2 * 256 * 2048
 
 
 def parse():
@@ -48,6 +51,7 @@ def parse():
     ap.add_argument("--impl", default="flint", choices=["flint", "reference"])
     ap.add_argument("--workload", default="decode1", choices=sorted(WORKLOADS))
     ap.add_argument("--layers", type=int, default=N_LAYERS, help=argparse.SUPPRESS)
+    ap.add_argument("--tokens", type=int, default=0, help=argparse.SUPPRESS)
     return ap.parse_args()
 
 
@@ -395,12 +399,102 @@ def run_flint(args, wl, ws, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def run_prefill(args, wl, ws, rank, local):
+    """One MoE layer (layer 0 of the stack: skewed router bias) on T = 8192
+    tokens; weights (1.6 GB) exceed L2, so each step streams them again."""
+    import numpy as np
+    import torch
+    from sparse_moe_transformer_03_b300 import flint
+    from synth import device
+
+    flint.load_library()
+    device.build()
+    T = wl["T"]
+    pk, pk_kind = peaks()
+    lw = device.LayerWeights(1, 0, True)
+    h = flint.flint_moe_create(lw.router_W, lw.router_b, list(lw.gate_up[:256]), list(lw.down[:256]),
+                               (lw.gate_up[256], lw.down[256]))
+    xb = x_bits_for(wl)
+    x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
+    y = torch.empty_like(x)
+    stream = torch.cuda.Stream()
+
+    def step():
+        flint.flint_moe_forward(h, x, T, y, stream)
+
+    def timed(fn, n):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        ev[0].record(stream)
+        for _ in range(n):
+            fn()
+        ev[1].record(stream)
+        ev[1].synchronize()
+        return ev[0].elapsed_time(ev[1]) / n
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    stream.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        with torch.cuda.stream(stream):
+            ms = timed(step, args.steps)
+    torch.cuda.synchronize()
+    clocks = clk.summary()
+
+    x_host = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).pin_memory()
+    y_host = torch.empty_like(x_host).pin_memory()
+    x_dev = torch.empty_like(x)
+
+    def step_e2e():
+        x_dev.copy_(x_host, non_blocking=True)
+        flint.flint_moe_forward(h, x_dev, T, y, stream)
+        y_host.copy_(y, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        step_e2e()
+        ms_e2e = timed(step_e2e, max(3, args.steps // 2))
+    if ws > 1:
+        t = torch.tensor([ms, ms_e2e], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms, ms_e2e = t.tolist()
+    flops = FLOPS_PER_TOKEN * T
+    achieved = flops / (ms * 1e-3) / 1e12
+    peak = float(pk["bf16_tflops"])
+    line = {
+        "metric": f"MoE-layer tokens/s, prefill T={T}", "value": ws * T / (ms * 1e-3), "unit": "tokens/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "us_per_layer": ms * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded counter-based generator; random-init weights)",
+        "config": {"workload": f"prefill: one BF16 MoE layer (H=2048, I=512, 256 routed + 1 shared, top-6 sigmoid, "
+                               f"router bias N(0,0.5)), T={T} tokens (x ~ N(0,1) RMS-normalised, seed {wl['x_seed']})",
+                   "l2": "inputs larger than L2 (1.6 GB of expert weights per step)", "parallelism": f"replicas x{ws}"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                     "traffic": None,
+                     "what": f"dense layer FLOPs (experts {7 * 6 * 2048 * 512 * T / 1e9:.1f} GFLOP + router "
+                             f"{2 * 256 * 2048 * T / 1e9:.1f}) / step time; peak = {pk_kind} bf16 burst"},
+        "gpu_launches": 7 * args.steps,
+        "clocks": clocks,
+        "e2e": {"value": ws * T / (ms_e2e * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": T * 2048 * 2,
+                "d2h_bytes_per_step": T * 2048 * 2},
+    }
+    flint.flint_moe_destroy(h)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
-    wl = WORKLOADS[args.workload]
+    wl = dict(WORKLOADS[args.workload])
+    if args.tokens:
+        wl["T"] = args.tokens
     ws, rank, local = dist_setup(args)
     if args.impl == "reference":
         run_reference(args, wl, ws, rank)
+    elif wl.get("prefill"):
+        run_prefill(args, wl, ws, rank, local)
     else:
         run_flint(args, wl, ws, rank, local)
     if ws > 1:

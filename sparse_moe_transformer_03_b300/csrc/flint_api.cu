@@ -27,7 +27,7 @@ struct flint_moe {
     CUtensorMap* gu_maps;          // [NEXP] boxes 64 x 128
     CUtensorMap* dn_maps;          // [NEXP] boxes 64 x 128
     CUtensorMap wr_map;            // boxes 64 x 256
-    CUtensorMap h_map;             // h_perm, boxes 64 x 128
+    CUtensorMap h_map;             // h_perm, boxes 64 x 256
 
     // status word in host-mapped memory
     uint32_t* status_host;
@@ -210,7 +210,7 @@ flint_status_t flint_moe_create(flint_moe_t* out, const void* router_W, const fl
                   encode_bf16_2d(&dn[e], h->host_tables.down[e], H, I, I, 128, 64);
         }
         enc = enc && encode_bf16_2d(&h->wr_map, h->router_W, E, H, H, E, 64) &&
-              encode_bf16_2d(&h->h_map, h->h_perm, (uint64_t)(TOPK + 1) * CHUNK, I, I, 128, 64);
+              encode_bf16_2d(&h->h_map, h->h_perm, (uint64_t)(TOPK + 1) * CHUNK, I, I, 256, 64);
         if (!enc) st = FLINT_ERR_CUDA;
         if (st == FLINT_OK && (cudaMalloc(&h->gu_maps, sizeof(CUtensorMap) * NEXP) != cudaSuccess ||
                                cudaMalloc(&h->dn_maps, sizeof(CUtensorMap) * NEXP) != cudaSuccess))
@@ -257,9 +257,8 @@ flint_status_t flint_moe_forward(flint_moe_t h, const void* x, int T, void* y, c
     for (int t0 = 0; t0 < T; t0 += CHUNK) {
         const int Tc = T - t0 < CHUNK ? T - t0 : CHUNK;
         const __nv_bfloat16* xc = xs + (size_t)t0 * H;
-        CUtensorMap xmap, xgmap;
-        if (!encode_bf16_2d(&xmap, xc, Tc, H, H, 128, 64) || !encode_bf16_2d(&xgmap, xc, Tc, H, H, 1, 64))
-            return FLINT_ERR_CUDA;
+        CUtensorMap xmap;
+        if (!encode_bf16_2d(&xmap, xc, Tc, H, H, 128, 64)) return FLINT_ERR_CUDA;
         cudaError_t e = cudaMemsetAsync(h->y32, 0, (size_t)Tc * H * sizeof(float), s);
         if (e == cudaSuccess)
             e = launch_prefill_router(L, xmap, h->wr_map, Tc, h->router_b, nullptr, h->idx, h->w, h->local_rank,
@@ -268,7 +267,7 @@ flint_status_t flint_moe_forward(flint_moe_t h, const void* x, int T, void* y, c
             e = launch_perm_scan_scatter(L, h->idx, Tc, h->local_rank, h->blk_counts, h->blk_base, h->offsets,
                                          h->gather);
         if (e == cudaSuccess)
-            e = launch_prefill_experts(L, xgmap, h->h_map, Tc, h->offsets, h->gather, h->w, h->gu_maps, h->dn_maps,
+            e = launch_prefill_experts(L, xc, h->h_map, Tc, h->offsets, h->gather, h->w, h->gu_maps, h->dn_maps,
                                        h->h_perm, h->y32, ys + (size_t)t0 * H);
         if (e != cudaSuccess) return FLINT_ERR_CUDA;
     }

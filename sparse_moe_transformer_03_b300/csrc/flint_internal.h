@@ -62,7 +62,7 @@ cudaError_t prefill_set_attributes();
 cudaError_t launch_prefill_router(const LaunchCtx& L, const CUtensorMap& x_map, const CUtensorMap& wr_map, int T,
                                   const float* bias, float* logits, int32_t* idx, float* w, int32_t* local_rank,
                                   int32_t* blk_counts);
-cudaError_t launch_prefill_experts(const LaunchCtx& L, const CUtensorMap& xg_map, const CUtensorMap& h_map, int T,
+cudaError_t launch_prefill_experts(const LaunchCtx& L, const __nv_bfloat16* x, const CUtensorMap& h_map, int T,
                                    const int32_t* offsets, const int32_t* gather, const float* w_route,
                                    const CUtensorMap* gu_maps, const CUtensorMap* dn_maps, __nv_bfloat16* h_perm,
                                    float* y32, __nv_bfloat16* y);

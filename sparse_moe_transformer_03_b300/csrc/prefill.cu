@@ -1,6 +1,6 @@
 // prefill.cu -- the many-token path (T > 32) on the 5th-generation tensor
 // cores: tcgen05.mma with fp32 accumulators in TMEM, operands staged in smem
-// by TMA (tiled loads, and gather4 for the routed token rows).
+// by TMA tiled loads (weights) and cp.async gathers (routed token rows).
 //
 //   prefill_router   logits[128 tokens][256 experts] per CTA (K = 2048); the
 //                    epilogue (one thread per token) adds the bias, selects the
@@ -11,22 +11,23 @@
 //   (scan, scatter)  offsets[257] and the expert-grouped pair list (router.cu)
 //   prefill_gateup   grouped GEMM, "swapped": M = 128 rows of an expert's gate
 //                    (and, in a second accumulator, the matching up) matrix,
-//                    N = up to 128 of the expert's tokens gathered from x,
+//                    N = up to 256 of the expert's tokens gathered from x by
+//                    cp.async (16-byte chunks into the swizzled tile),
 //                    K = 2048.  Epilogue: h = silu(gate) * up, bf16, into
 //                    h_perm[slot][512] (routed slots in expert order, then the
 //                    shared expert's T slots).
 //   prefill_down     grouped GEMM: M = 128 rows of the expert's down matrix,
-//                    N = up to 128 slots of h_perm, K = 512.  Epilogue: each
+//                    N = up to 256 slots of h_perm, K = 512.  Epilogue: each
 //                    result times the pair's routing weight (1 for the shared
 //                    expert) is added into y32[token][h] with fp32 reductions.
 //   convert          y = bf16(y32).
 //
 // Warp roles in every GEMM kernel: warp 0 issues TMA (one elected thread),
 // warp 1 allocates TMEM and issues MMAs (one thread), warps 2..5 drain TMEM in
-// the epilogue (warp w reads TMEM lanes 32*(w%4)..+31).  The grouped GEMMs are
-// persistent: CTA c takes units c, c + grid, ... of the list ordered by
-// (expert, row block, token tile), so CTAs working at the same time share the
-// expert's weight tiles through L2.  Every wait is bounded; a timeout sets an
+// the epilogue (warp w reads TMEM lanes 32*(w%4)..+31; the grouped GEMMs use
+// two epilogue warps per lane quarter).  The grouped GEMMs are persistent:
+// CTA c takes units c, c + grid, ... of the list ordered by (expert, row
+// block, token pass).  Every wait is bounded; a timeout sets an
 // abort flag the other roles observe, reports FLINT_ERR_DEVICE_TIMEOUT and the
 // CTA still frees its TMEM.
 //
@@ -253,6 +254,32 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
 // ===========================================================================
 // grouped expert GEMMs
 // ===========================================================================
+// A unit is (expert, row block, token pass): 128 rows of one expert matrix
+// against up to GP_N (256) of its tokens.  Most experts receive fewer than
+// 256 tokens, so each weight tile is streamed from HBM once and used for all
+// of the expert's tokens; passes of one row block are adjacent in the unit
+// order so larger experts share the tile through L2.
+
+constexpr int GP_N = 256;                        // tokens per pass (MMA N <= 256)
+constexpr int GP_EPI_WARPS = 8;                  // two per TMEM lane quarter
+constexpr int GP_GATHER_WARPS = 2;               // token-row gathers of the gate/up GEMM
+constexpr int GP_THREADS = 64 + 32 * GP_EPI_WARPS;   // producer + MMA + epilogue
+constexpr int G1_THREADS = GP_THREADS + 32;      // + a second gather warp (the last warp)
+constexpr int GP_B_BYTES = GP_N * PF_BK * 2;     // 32 KiB
+
+__device__ __forceinline__ void gp_epi_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * GP_EPI_WARPS) : "memory");
+}
+__device__ __forceinline__ bool gp_epi_all(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n barrier.cta.red.and.pred q, 1, %2, p;\n"
+        " selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"(v ? 1u : 0u), "n"(32 * GP_EPI_WARPS)
+        : "memory");
+    return r != 0;
+}
 
 struct GroupedParams {
     int T;
@@ -275,7 +302,7 @@ struct Sched {
     int upre[NEXP + 1];
 };
 
-__device__ void build_sched(Sched* S, const GroupedParams& p, int units_per_tile) {
+__device__ void build_sched(Sched* S, const GroupedParams& p, int blocks) {
     const int tid = threadIdx.x;
     for (int e = tid; e < NEXP; e += blockDim.x) {
         const int b = e < E ? p.offsets[e] : TOPK * p.T;
@@ -290,7 +317,7 @@ __device__ void build_sched(Sched* S, const GroupedParams& p, int units_per_tile
 #pragma unroll
         for (int k = 0; k < 9; ++k) {
             const int e = tid * 9 + k;
-            loc[k] = e < NEXP ? units_per_tile * ((S->cnt[e] + PF_TILE - 1) / PF_TILE) : 0;
+            loc[k] = e < NEXP ? blocks * ((S->cnt[e] + GP_N - 1) / GP_N) : 0;
             sum += loc[k];
         }
         int inc = sum;
@@ -323,20 +350,20 @@ __device__ __forceinline__ int unit_expert(const Sched* S, int u) {
 }
 
 struct Unit {
-    int e, blk, tt, base, nvalid, npad;
+    int e, blk, pass, base, nvalid, npad;
 };
 
-__device__ __forceinline__ Unit decode_unit(const Sched* S, int u, int blocks) {
+// unit order within an expert: (row block, pass)
+__device__ __forceinline__ Unit decode_unit(const Sched* S, int u) {
     Unit U;
     U.e = unit_expert(S, u);
-    const int nt = (S->cnt[U.e] + PF_TILE - 1) / PF_TILE;
+    const int np = (S->cnt[U.e] + GP_N - 1) / GP_N;
     const int r = u - S->upre[U.e];
-    U.blk = r / nt;
-    U.tt = r - U.blk * nt;
-    U.base = S->base[U.e] + U.tt * PF_TILE;
-    U.nvalid = min(PF_TILE, S->cnt[U.e] - U.tt * PF_TILE);
+    U.blk = r / np;
+    U.pass = r - U.blk * np;
+    U.base = S->base[U.e] + U.pass * GP_N;
+    U.nvalid = min(GP_N, S->cnt[U.e] - U.pass * GP_N);
     U.npad = (U.nvalid + 15) & ~15;
-    (void)blocks;
     return U;
 }
 
@@ -344,35 +371,38 @@ __device__ __forceinline__ Unit decode_unit(const Sched* S, int u, int blocks) {
 // GEMM 1: gate/up + SwiGLU
 // ---------------------------------------------------------------------------
 
-constexpr int G1_STAGES = 4;
-constexpr int G1_STAGE = 3 * PF_TILE_BYTES;    // gate tile, up tile, token tile
-constexpr int G1_BLOCKS = I / PF_TILE;         // 4 row blocks of 128
-constexpr int G1_SMEM = 1024 + G1_STAGES * G1_STAGE + 512 + PF_TILE * 4 + (int)sizeof(Sched);
+constexpr int G1_STAGES = 3;
+constexpr int G1_STAGE = 2 * PF_TILE_BYTES + GP_B_BYTES;    // gate, up, tokens: 64 KiB
+constexpr int G1_BLOCKS = I / PF_TILE;                      // 4 row blocks of 128
+constexpr int G1_SMEM = 1024 + G1_STAGES * G1_STAGE + 512 + GP_N * 4 + (int)sizeof(Sched);
 
-__global__ void __launch_bounds__(PF_THREADS, 1)
-    prefill_gateup_kernel(const __grid_constant__ CUtensorMap xg_map, GroupedParams p) {
+__global__ void __launch_bounds__(G1_THREADS, 1)
+    prefill_gateup_kernel(const __nv_bfloat16* __restrict__ x, GroupedParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + G1_STAGES * G1_STAGE);
     uint64_t* empty = full + G1_STAGES;
-    uint64_t* tfull = empty + G1_STAGES;    // [2]
-    uint64_t* tempty = tfull + 2;           // [2]
-    uint64_t* mdone = tempty + 2;
+    uint64_t* tfull = empty + G1_STAGES;
+    uint64_t* tempty = tfull + 1;
+    uint64_t* mdone = tempty + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mdone + 1);
     volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    int* tok = reinterpret_cast<int*>(smem + G1_STAGES * G1_STAGE + 512);           // [128]
-    Sched* S = reinterpret_cast<Sched*>(tok + PF_TILE);
+    int* tok = reinterpret_cast<int*>(smem + G1_STAGES * G1_STAGE + 512);           // [GP_N]
+    Sched* S = reinterpret_cast<Sched*>(tok + GP_N);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nwarps = G1_THREADS / 32;
+    // gather warps: warp 0 (which also issues the weight TMA) and the last warp
+    const bool gather_warp = warp == 0 || warp == nwarps - 1;
+    const int gw = warp == 0 ? 0 : 1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < G1_STAGES; ++s) {
-            mbar_init(&full[s], 1);
+            // one arrive.expect_tx for the weight tiles + one cp.async arrival per gather thread
+            mbar_init(&full[s], 1 + 32 * GP_GATHER_WARPS);
             mbar_init(&empty[s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&tfull[b], 1);
-            mbar_init(&tempty[b], 4);
-        }
+        mbar_init(tfull, 1);
+        mbar_init(tempty, GP_EPI_WARPS);
         mbar_init(mdone, 1);
         *abort = 0;
         fence_mbar_init();
@@ -384,7 +414,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    const uint32_t tmem = *tmem_slot;
+    const uint32_t tmem = *tmem_slot;   // gate accumulator: columns 0..255, up: 256..511
     pdl_wait();     // routing, permutation and x are complete
     pdl_trigger();
     build_sched(S, p, G1_BLOCKS);
@@ -392,60 +422,75 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     const int sixT = TOPK * p.T;
     constexpr int KC = H / PF_BK;   // 32
 
-    if (warp == 0) {
-        if (lane == 0) tc::prefetch_tensormap(&xg_map);
+    if (gather_warp) {
         int kc_all = 0;
         for (int u = blockIdx.x; u < total && !__shfl_sync(0xFFFFFFFFu, *abort, 0); u += gridDim.x) {
-            const Unit U = decode_unit(S, u, G1_BLOCKS);
-            // token rows of this tile (padding rows repeat the last valid one)
+            const Unit U = decode_unit(S, u);
+            // this warp's token rows of the pass: n = 128 * gw + 32 * k + lane
+            // (padding rows repeat the last valid token)
+            const __nv_bfloat16* src[4];
+            int nrow[4];
 #pragma unroll
-            for (int k = 0; k < PF_TILE / 32; ++k) {
-                const int n = lane + 32 * k;
+            for (int k = 0; k < 4; ++k) {
+                const int n = 128 * gw + 32 * k + lane;
                 const int slot = U.base + min(n, U.nvalid - 1);
-                tok[n] = U.e < E ? __ldg(p.gather + slot) / TOPK : slot - sixT;
+                const int t = U.e < E ? __ldg(p.gather + slot) / TOPK : slot - sixT;
+                src[k] = x + (size_t)t * H;
+                nrow[k] = n;
             }
-            __syncwarp();
-            if (lane == 0) {
-                const CUtensorMap* wm = p.gu_maps + U.e;
-                for (int kc = 0; kc < KC; ++kc, ++kc_all) {
-                    const int s = kc_all % G1_STAGES;
-                    if (!pf_wait(&empty[s], ((kc_all / G1_STAGES) & 1) ^ 1, p.limit_ns, abort)) break;
-                    uint8_t* st = smem + s * G1_STAGE;
-                    mbar_arrive_expect_tx(&full[s], 2 * PF_TILE_BYTES + U.npad * PF_BK * 2);
+            const CUtensorMap* wm = p.gu_maps + U.e;
+            for (int kc = 0; kc < KC; ++kc, ++kc_all) {
+                const int s = kc_all % G1_STAGES;
+                bool ok = true;
+                if (lane == 0) ok = pf_wait(&empty[s], ((kc_all / G1_STAGES) & 1) ^ 1, p.limit_ns, abort);
+                if (!__shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0)) break;
+                uint8_t* st = smem + s * G1_STAGE;
+                if (warp == 0 && lane == 0) {
+                    mbar_arrive_expect_tx(&full[s], 2 * PF_TILE_BYTES);
                     tc::tma_load_2d(st, wm, kc * PF_BK, U.blk * PF_TILE, &full[s]);
                     tc::tma_load_2d(st + PF_TILE_BYTES, wm, kc * PF_BK, I + U.blk * PF_TILE, &full[s]);
-                    for (int g = 0; g < U.npad / 4; ++g)
-                        tc::tma_gather4(st + 2 * PF_TILE_BYTES + g * 4 * PF_BK * 2, &xg_map, kc * PF_BK, tok[4 * g],
-                                        tok[4 * g + 1], tok[4 * g + 2], tok[4 * g + 3], &full[s]);
                 }
+                // token rows into the 128-byte-swizzled K-major tile: 16-byte
+                // chunk c of row n lands at n*128 + ((c ^ (n & 7)) * 16)
+                uint8_t* bt = st + 2 * PF_TILE_BYTES;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int n = nrow[k];
+                    if (n < U.npad) {
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            tc::cp_async16(bt + n * 128 + ((c ^ (n & 7)) << 4), src[k] + kc * PF_BK + 8 * c);
+                    }
+                }
+                tc::cp_async_arrive_noinc(&full[s]);
             }
-            __syncwarp();
         }
     } else if (warp == 1) {
         if (lane == 0) {
             int kc_all = 0, lu = 0;
             for (int u = blockIdx.x; u < total && !*abort; u += gridDim.x, ++lu) {
-                const Unit U = decode_unit(S, u, G1_BLOCKS);
-                const int b = lu & 1;
-                if (!pf_wait(&tempty[b], ((lu >> 1) & 1) ^ 1, p.limit_ns, abort)) break;
+                const Unit U = decode_unit(S, u);
+                if (!pf_wait(tempty, (lu & 1) ^ 1, p.limit_ns, abort)) break;
                 tc::fence_after_sync();
                 const uint32_t idesc = tc::idesc_bf16_f32(128, U.npad);
-                const uint32_t dg = tmem + b * 256, du = tmem + b * 256 + 128;
                 for (int kc = 0; kc < KC; ++kc, ++kc_all) {
                     const int s = kc_all % G1_STAGES;
                     if (!pf_wait(&full[s], (kc_all / G1_STAGES) & 1, p.limit_ns, abort)) break;
+                    // the token rows were written by cp.async (generic proxy); the
+                    // tensor core reads smem through the async proxy
+                    fence_proxy_async_smem();
                     tc::fence_after_sync();
                     const uint8_t* st = smem + s * G1_STAGE;
                     const uint64_t ag = tc::smem_desc_sw128(st), au = tc::smem_desc_sw128(st + PF_TILE_BYTES);
                     const uint64_t bx = tc::smem_desc_sw128(st + 2 * PF_TILE_BYTES);
 #pragma unroll
                     for (int kk = 0; kk < PF_BK / 16; ++kk) {
-                        tc::mma_bf16(dg, ag + 2 * kk, bx + 2 * kk, idesc, (kc | kk) != 0);
-                        tc::mma_bf16(du, au + 2 * kk, bx + 2 * kk, idesc, (kc | kk) != 0);
+                        tc::mma_bf16(tmem, ag + 2 * kk, bx + 2 * kk, idesc, (kc | kk) != 0);
+                        tc::mma_bf16(tmem + GP_N, au + 2 * kk, bx + 2 * kk, idesc, (kc | kk) != 0);
                     }
                     tc::mma_commit(&empty[s]);
                 }
-                tc::mma_commit(&tfull[b]);
+                tc::mma_commit(tfull);
             }
             // every MMA this thread issued has finished before TMEM is freed
             tc::mma_commit(mdone);
@@ -453,19 +498,19 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         }
         __syncwarp();
     } else {
-        const int q = warp & 3, row = 32 * q + lane;
+        const int ew = warp - 2, q = warp & 3, half = ew >> 2, row = 32 * q + lane;
         int lu = 0;
         for (int u = blockIdx.x; u < total; u += gridDim.x, ++lu) {
-            const Unit U = decode_unit(S, u, G1_BLOCKS);
-            const int b = lu & 1;
-            if (!__all_sync(0xFFFFFFFFu, pf_wait(&tfull[b], (lu >> 1) & 1, p.limit_ns, abort))) break;
+            const Unit U = decode_unit(S, u);
+            if (!__all_sync(0xFFFFFFFFu, pf_wait(tfull, lu & 1, p.limit_ns, abort))) break;
             tc::fence_after_sync();
             const int j = U.blk * PF_TILE + row;
-            const uint32_t tg = tmem + ((uint32_t)(32 * q) << 16) + b * 256;
-            for (int c0 = 0; c0 < U.npad; c0 += 32) {
+            const uint32_t tg = tmem + ((uint32_t)(32 * q) << 16);
+            // the two warps of a lane quarter take alternate 32-column chunks
+            for (int c0 = 32 * half; c0 < U.npad; c0 += 64) {
                 uint32_t g[32], up[32];
                 tc::tmem_ld32(tg + c0, g);
-                tc::tmem_ld32(tg + 128 + c0, up);
+                tc::tmem_ld32(tg + GP_N + c0, up);
                 tc::tmem_ld_wait();
 #pragma unroll
                 for (int m = 0; m < 32; ++m) {
@@ -478,7 +523,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             }
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[b]);
+            if (lane == 0) mbar_arrive(tempty);
         }
     }
     if (*abort && threadIdx.x == 0) report_status(p.status, ST_TIMEOUT);
@@ -494,12 +539,12 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
 // GEMM 2: down projection + weighted scatter-add
 // ---------------------------------------------------------------------------
 
-constexpr int G2_STAGES = 6;
-constexpr int G2_STAGE = 2 * PF_TILE_BYTES;    // down tile, activation tile
-constexpr int G2_BLOCKS = H / PF_TILE;         // 16 row blocks of 128
-constexpr int G2_SMEM = 1024 + G2_STAGES * G2_STAGE + 512 + PF_TILE * 8 + (int)sizeof(Sched);
+constexpr int G2_STAGES = 4;
+constexpr int G2_STAGE = PF_TILE_BYTES + GP_B_BYTES;   // down tile, activation tile: 48 KiB
+constexpr int G2_BLOCKS = H / PF_TILE;                 // 16 row blocks of 128
+constexpr int G2_SMEM = 1024 + G2_STAGES * G2_STAGE + 512 + GP_N * 8 + (int)sizeof(Sched);
 
-__global__ void __launch_bounds__(PF_THREADS, 1)
+__global__ void __launch_bounds__(GP_THREADS, 1)
     prefill_down_kernel(const __grid_constant__ CUtensorMap h_map, GroupedParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
@@ -510,9 +555,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     uint64_t* mdone = tempty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mdone + 1);
     volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    int* tok = reinterpret_cast<int*>(smem + G2_STAGES * G2_STAGE + 512);          // [128]
-    float* wgt = reinterpret_cast<float*>(tok + PF_TILE);                           // [128]
-    Sched* S = reinterpret_cast<Sched*>(wgt + PF_TILE);
+    int* tok = reinterpret_cast<int*>(smem + G2_STAGES * G2_STAGE + 512);          // [GP_N]
+    float* wgt = reinterpret_cast<float*>(tok + GP_N);                              // [GP_N]
+    Sched* S = reinterpret_cast<Sched*>(wgt + GP_N);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -522,20 +567,20 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
-            mbar_init(&tempty[b], 4);
+            mbar_init(&tempty[b], GP_EPI_WARPS);
         }
         mbar_init(mdone, 1);
         *abort = 0;
         fence_mbar_init();
     }
     if (warp == 1) {
-        tc::tmem_alloc(tmem_slot, 256);
+        tc::tmem_alloc(tmem_slot, 512);
         tc::tmem_relinquish();
     }
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    const uint32_t tmem = *tmem_slot;
+    const uint32_t tmem = *tmem_slot;   // two accumulators of 256 columns
     pdl_wait();     // h_perm is complete
     pdl_trigger();
     build_sched(S, p, G2_BLOCKS);
@@ -548,13 +593,13 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             tc::prefetch_tensormap(&h_map);
             int kc_all = 0;
             for (int u = blockIdx.x; u < total && !*abort; u += gridDim.x) {
-                const Unit U = decode_unit(S, u, G2_BLOCKS);
+                const Unit U = decode_unit(S, u);
                 const CUtensorMap* wm = p.dn_maps + U.e;
                 for (int kc = 0; kc < KC; ++kc, ++kc_all) {
                     const int s = kc_all % G2_STAGES;
                     if (!pf_wait(&empty[s], ((kc_all / G2_STAGES) & 1) ^ 1, p.limit_ns, abort)) break;
                     uint8_t* st = smem + s * G2_STAGE;
-                    mbar_arrive_expect_tx(&full[s], 2 * PF_TILE_BYTES);
+                    mbar_arrive_expect_tx(&full[s], PF_TILE_BYTES + GP_B_BYTES);
                     tc::tma_load_2d(st, wm, kc * PF_BK, U.blk * PF_TILE, &full[s]);
                     tc::tma_load_2d(st + PF_TILE_BYTES, &h_map, kc * PF_BK, U.base, &full[s]);
                 }
@@ -565,12 +610,12 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         if (lane == 0) {
             int kc_all = 0, lu = 0;
             for (int u = blockIdx.x; u < total && !*abort; u += gridDim.x, ++lu) {
-                const Unit U = decode_unit(S, u, G2_BLOCKS);
+                const Unit U = decode_unit(S, u);
                 const int b = lu & 1;
                 if (!pf_wait(&tempty[b], ((lu >> 1) & 1) ^ 1, p.limit_ns, abort)) break;
                 tc::fence_after_sync();
                 const uint32_t idesc = tc::idesc_bf16_f32(128, U.npad);
-                const uint32_t d = tmem + b * 128;
+                const uint32_t d = tmem + b * GP_N;
                 for (int kc = 0; kc < KC; ++kc, ++kc_all) {
                     const int s = kc_all % G2_STAGES;
                     if (!pf_wait(&full[s], (kc_all / G2_STAGES) & 1, p.limit_ns, abort)) break;
@@ -584,35 +629,35 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 }
                 tc::mma_commit(&tfull[b]);
             }
-            // every MMA this thread issued has finished before TMEM is freed
             tc::mma_commit(mdone);
             mbar_wait_bounded(mdone, 0, p.limit_ns);
         }
         __syncwarp();
     } else {
-        const int q = warp & 3, row = 32 * q + lane;
+        const int ew = warp - 2, q = warp & 3, half = ew >> 2, row = 32 * q + lane;
+        const int et = threadIdx.x - 64;   // 0 .. 255
         int lu = 0;
         for (int u = blockIdx.x; u < total; u += gridDim.x, ++lu) {
-            const Unit U = decode_unit(S, u, G2_BLOCKS);
+            const Unit U = decode_unit(S, u);
             const int b = lu & 1;
-            // token and routing weight of each column of the tile
-            if (row < U.nvalid) {
-                const int slot = U.base + row;
+            // token and routing weight of each column of the pass
+            if (et < U.nvalid) {
+                const int slot = U.base + et;
                 if (U.e < E) {
                     const int pr = __ldg(p.gather + slot);
-                    tok[row] = pr / TOPK;
-                    wgt[row] = __ldg(p.w_route + pr);
+                    tok[et] = pr / TOPK;
+                    wgt[et] = __ldg(p.w_route + pr);
                 } else {
-                    tok[row] = slot - sixT;
-                    wgt[row] = 1.f;
+                    tok[et] = slot - sixT;
+                    wgt[et] = 1.f;
                 }
             }
-            // waits for the accumulator; also publishes tok/wgt to all four warps
-            if (!epi_all(pf_wait(&tfull[b], (lu >> 1) & 1, p.limit_ns, abort))) break;
+            // waits for the accumulator; also publishes tok/wgt to every warp
+            if (!gp_epi_all(pf_wait(&tfull[b], (lu >> 1) & 1, p.limit_ns, abort))) break;
             tc::fence_after_sync();
             const int h = U.blk * PF_TILE + row;
-            const uint32_t td = tmem + ((uint32_t)(32 * q) << 16) + b * 128;
-            for (int c0 = 0; c0 < U.npad; c0 += 32) {
+            const uint32_t td = tmem + ((uint32_t)(32 * q) << 16) + b * GP_N;
+            for (int c0 = 32 * half; c0 < U.npad; c0 += 64) {
                 uint32_t v[32];
                 tc::tmem_ld32(td + c0, v);
                 tc::tmem_ld_wait();
@@ -625,7 +670,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[b]);
-            epi_sync();   // tok/wgt of this unit no longer needed
+            gp_epi_sync();   // tok/wgt of this pass no longer needed
         }
     }
     if (*abort && threadIdx.x == 0) report_status(p.status, ST_TIMEOUT);
@@ -633,7 +678,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     __syncthreads();
     if (warp == 1) {
         tc::fence_after_sync();
-        tc::tmem_dealloc(tmem, 256);
+        tc::tmem_dealloc(tmem, 512);
     }
 }
 
@@ -670,14 +715,14 @@ cudaError_t launch_prefill_router(const LaunchCtx& L, const CUtensorMap& x_map, 
                       wr_map, rp);
 }
 
-cudaError_t launch_prefill_experts(const LaunchCtx& L, const CUtensorMap& xg_map, const CUtensorMap& h_map, int T,
+cudaError_t launch_prefill_experts(const LaunchCtx& L, const __nv_bfloat16* x, const CUtensorMap& h_map, int T,
                                    const int32_t* offsets, const int32_t* gather, const float* w_route,
                                    const CUtensorMap* gu_maps, const CUtensorMap* dn_maps, __nv_bfloat16* h_perm,
                                    float* y32, __nv_bfloat16* y) {
     GroupedParams gp{T, offsets, gather, w_route, gu_maps, dn_maps, h_perm, y32, L.status, L.wait_limit_ns};
-    cudaError_t e = launch_pdl(L, prefill_gateup_kernel, dim3(L.num_sms), dim3(PF_THREADS), G1_SMEM, xg_map, gp);
+    cudaError_t e = launch_pdl(L, prefill_gateup_kernel, dim3(L.num_sms), dim3(G1_THREADS), G1_SMEM, x, gp);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(L, prefill_down_kernel, dim3(L.num_sms), dim3(PF_THREADS), G2_SMEM, h_map, gp);
+    e = launch_pdl(L, prefill_down_kernel, dim3(L.num_sms), dim3(GP_THREADS), G2_SMEM, h_map, gp);
     if (e != cudaSuccess) return e;
     const int n8 = T * H / 8;
     return launch_pdl(L, convert_y_kernel, dim3((n8 + 255) / 256), dim3(256), 0, (const float*)y32, y, n8);

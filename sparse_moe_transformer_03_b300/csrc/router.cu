@@ -251,14 +251,21 @@ __global__ void __launch_bounds__(PB_TOK) perm_local_kernel(const int32_t* idx, 
     }
 }
 
-__global__ void __launch_bounds__(E) perm_scan_kernel(const int32_t* blk_counts, int nblk, int32_t* blk_base,
-                                                     int32_t* offsets) {
+__global__ void __launch_bounds__(E) perm_scan_kernel(const int32_t* __restrict__ blk_counts, int nblk,
+                                                     int32_t* __restrict__ blk_base, int32_t* __restrict__ offsets) {
     pdl_wait();
     const int e = threadIdx.x;
     int run = 0;
-    for (int b = 0; b < nblk; ++b) {
-        blk_base[b * E + e] = run;
-        run += blk_counts[b * E + e];
+    // independent loads, 16 in flight at a time
+    for (int b0 = 0; b0 < nblk; b0 += 16) {
+        int c[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) c[k] = b0 + k < nblk ? __ldcg(blk_counts + (b0 + k) * E + e) : 0;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            if (b0 + k < nblk) blk_base[(b0 + k) * E + e] = run;
+            run += c[k];
+        }
     }
     // exclusive scan of run over the 256 experts
     __shared__ int warp_tot[E / 32];
