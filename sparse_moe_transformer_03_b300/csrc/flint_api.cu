@@ -23,10 +23,10 @@ struct flint_moe {
     ExpertTables host_tables;      // BF16 pointers (host copy)
     ExpertTables* dev_tables;      // same, in device memory
 
-    // TMA tensor maps (device arrays) of the expert matrices and the router
-    CUtensorMap* gu_maps;          // [NEXP] boxes 64 x 128
-    CUtensorMap* dn_maps;          // [NEXP] boxes 64 x 128
-    CUtensorMap wr_map;            // boxes 64 x 256
+    // owned tiled copies of the expert matrices for the tensor-core path
+    // (per expert: gate_up tiles then down tiles, see repack.cu)
+    __nv_bfloat16* tiled;
+    CUtensorMap wr_map;            // router, boxes 64 x 256
     CUtensorMap h_map;             // h_perm, boxes 64 x 256
 
     // status word in host-mapped memory
@@ -48,8 +48,9 @@ struct flint_moe {
     int32_t* blk_base;             // [CHUNK/128][E]
     int32_t* offsets;              // [E+1]
     int32_t* gather;               // [CHUNK*TOPK]
+    int32_t* pair_slot;            // [CHUNK*TOPK] slot of each (token, choice) pair
     __nv_bfloat16* h_perm;         // [(TOPK+1)*CHUNK][I]
-    float* y32;                    // [CHUNK][H]
+    __nv_bfloat16* o_perm;         // [(TOPK+1)*CHUNK][H]
 };
 
 namespace {
@@ -96,8 +97,7 @@ void free_handle(flint_moe* h) {
     if (!h) return;
     if (h->ws_base) cudaFree(h->ws_base);
     if (h->dev_tables) cudaFree(h->dev_tables);
-    if (h->gu_maps) cudaFree(h->gu_maps);
-    if (h->dn_maps) cudaFree(h->dn_maps);
+    if (h->tiled) cudaFree(h->tiled);
     if (h->status_host) cudaFreeHost(h->status_host);
     delete h;
 }
@@ -116,8 +116,9 @@ void carve_workspace(flint_moe* h, char* base, size_t* bytes_out) {
     h->blk_base = c.take<int32_t>((size_t)(CHUNK / 128) * E);
     h->offsets = c.take<int32_t>(E + 1);
     h->gather = c.take<int32_t>((size_t)CHUNK * TOPK);
+    h->pair_slot = c.take<int32_t>((size_t)CHUNK * TOPK);
     h->h_perm = c.take<__nv_bfloat16>((size_t)(TOPK + 1) * CHUNK * I);
-    h->y32 = c.take<float>((size_t)CHUNK * H);
+    h->o_perm = c.take<__nv_bfloat16>((size_t)(TOPK + 1) * CHUNK * H);
     *bytes_out = c.off;
 }
 
@@ -200,27 +201,22 @@ flint_status_t flint_moe_create(flint_moe_t* out, const void* router_W, const fl
             if (cudaMemset(h->ws_base, 0, bytes) != cudaSuccess) st = FLINT_ERR_CUDA;
         }
     }
+    const size_t expert_elems = (size_t)3 * H * I;   // gate_up + down
     if (st == FLINT_OK) {
-        // tensor maps of every expert matrix, the router and h_perm
-        CUtensorMap* gu = new (std::nothrow) CUtensorMap[NEXP];
-        CUtensorMap* dn = new (std::nothrow) CUtensorMap[NEXP];
-        bool enc = gu && dn;
-        for (int e = 0; enc && e < NEXP; ++e) {
-            enc = encode_bf16_2d(&gu[e], h->host_tables.gate_up[e], 2 * I, H, H, 128, 64) &&
-                  encode_bf16_2d(&dn[e], h->host_tables.down[e], H, I, I, 128, 64);
-        }
-        enc = enc && encode_bf16_2d(&h->wr_map, h->router_W, E, H, H, E, 64) &&
-              encode_bf16_2d(&h->h_map, h->h_perm, (uint64_t)(TOPK + 1) * CHUNK, I, I, 256, 64);
-        if (!enc) st = FLINT_ERR_CUDA;
-        if (st == FLINT_OK && (cudaMalloc(&h->gu_maps, sizeof(CUtensorMap) * NEXP) != cudaSuccess ||
-                               cudaMalloc(&h->dn_maps, sizeof(CUtensorMap) * NEXP) != cudaSuccess))
+        if (cudaMalloc(&h->tiled, (size_t)NEXP * expert_elems * sizeof(__nv_bfloat16)) != cudaSuccess)
             st = FLINT_ERR_OOM;
-        if (st == FLINT_OK &&
-            (cudaMemcpy(h->gu_maps, gu, sizeof(CUtensorMap) * NEXP, cudaMemcpyHostToDevice) != cudaSuccess ||
-             cudaMemcpy(h->dn_maps, dn, sizeof(CUtensorMap) * NEXP, cudaMemcpyHostToDevice) != cudaSuccess))
-            st = FLINT_ERR_CUDA;
-        delete[] gu;
-        delete[] dn;
+        for (int e = 0; st == FLINT_OK && e < NEXP; ++e) {
+            __nv_bfloat16* b = h->tiled + (size_t)e * expert_elems;
+            if (launch_repack_tiled(h->host_tables.gate_up[e], b, 2 * I, H, 0) != cudaSuccess ||
+                launch_repack_tiled(h->host_tables.down[e], b + (size_t)2 * I * H, H, I, 0) != cudaSuccess)
+                st = FLINT_ERR_CUDA;
+        }
+    }
+    if (st == FLINT_OK) {
+        // tensor maps of the router and of h_perm
+        const bool enc = encode_bf16_2d(&h->wr_map, h->router_W, E, H, H, E, 64) &&
+                         encode_bf16_2d(&h->h_map, h->h_perm, (uint64_t)(TOPK + 1) * CHUNK, I, I, 256, 64);
+        if (!enc) st = FLINT_ERR_CUDA;
     }
     if (st == FLINT_OK) st = from_cuda(prefill_set_attributes());
     if (st == FLINT_OK) st = from_cuda(decode_set_attributes());
@@ -259,16 +255,14 @@ flint_status_t flint_moe_forward(flint_moe_t h, const void* x, int T, void* y, c
         const __nv_bfloat16* xc = xs + (size_t)t0 * H;
         CUtensorMap xmap;
         if (!encode_bf16_2d(&xmap, xc, Tc, H, H, 128, 64)) return FLINT_ERR_CUDA;
-        cudaError_t e = cudaMemsetAsync(h->y32, 0, (size_t)Tc * H * sizeof(float), s);
-        if (e == cudaSuccess)
-            e = launch_prefill_router(L, xmap, h->wr_map, Tc, h->router_b, nullptr, h->idx, h->w, h->local_rank,
-                                      h->blk_counts);
+        cudaError_t e = launch_prefill_router(L, xmap, h->wr_map, Tc, h->router_b, nullptr, h->idx, h->w,
+                                              h->local_rank, h->blk_counts);
         if (e == cudaSuccess)
             e = launch_perm_scan_scatter(L, h->idx, Tc, h->local_rank, h->blk_counts, h->blk_base, h->offsets,
-                                         h->gather);
+                                         h->gather, h->pair_slot);
         if (e == cudaSuccess)
-            e = launch_prefill_experts(L, xc, h->h_map, Tc, h->offsets, h->gather, h->w, h->gu_maps, h->dn_maps,
-                                       h->h_perm, h->y32, ys + (size_t)t0 * H);
+            e = launch_prefill_experts(L, xc, h->h_map, Tc, h->offsets, h->gather, h->pair_slot, h->w, h->tiled,
+                                       h->h_perm, h->o_perm, ys + (size_t)t0 * H);
         if (e != cudaSuccess) return FLINT_ERR_CUDA;
     }
     return FLINT_OK;
@@ -297,7 +291,7 @@ flint_status_t flint_moe_route_only(flint_moe_t h, const void* x, float* logits,
                                       h->blk_counts);
             if (e == cudaSuccess && (offsets || gather_idx))
                 e = launch_perm_scan_scatter(L, idx, T, h->local_rank, h->blk_counts, h->blk_base,
-                                             offsets ? offsets : h->offsets, gather_idx);
+                                             offsets ? offsets : h->offsets, gather_idx, nullptr);
             if (e == cudaSuccess) e = cudaStreamSynchronize(s);
             if (e != cudaSuccess) return FLINT_ERR_CUDA;
             return take_device_status(h);

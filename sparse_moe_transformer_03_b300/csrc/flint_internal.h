@@ -51,11 +51,14 @@ cudaError_t launch_permutation(const LaunchCtx& L, const int32_t* idx, int T, in
 // scan + scatter only (block-local ranks and counts already computed)
 cudaError_t launch_perm_scan_scatter(const LaunchCtx& L, const int32_t* idx, int T, const int32_t* local_rank,
                                      const int32_t* blk_counts, int32_t* blk_base, int32_t* offsets,
-                                     int32_t* gather);
+                                     int32_t* gather, int32_t* pair_slot);
 
 // tmap.cu
 bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t pitch,
                     uint32_t box_rows, uint32_t box_cols);
+
+// repack.cu
+cudaError_t launch_repack_tiled(const __nv_bfloat16* in, __nv_bfloat16* out, int R, int K, cudaStream_t s);
 
 // prefill.cu
 cudaError_t prefill_set_attributes();
@@ -63,9 +66,9 @@ cudaError_t launch_prefill_router(const LaunchCtx& L, const CUtensorMap& x_map, 
                                   const float* bias, float* logits, int32_t* idx, float* w, int32_t* local_rank,
                                   int32_t* blk_counts);
 cudaError_t launch_prefill_experts(const LaunchCtx& L, const __nv_bfloat16* x, const CUtensorMap& h_map, int T,
-                                   const int32_t* offsets, const int32_t* gather, const float* w_route,
-                                   const CUtensorMap* gu_maps, const CUtensorMap* dn_maps, __nv_bfloat16* h_perm,
-                                   float* y32, __nv_bfloat16* y);
+                                   const int32_t* offsets, const int32_t* gather, const int32_t* pair_slot,
+                                   const float* w_route, const __nv_bfloat16* tiled, __nv_bfloat16* h_perm,
+                                   __nv_bfloat16* o_perm, __nv_bfloat16* y);
 
 // decode.cu
 cudaError_t decode_set_attributes();

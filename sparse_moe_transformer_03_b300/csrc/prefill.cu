@@ -1,6 +1,6 @@
 // prefill.cu -- the many-token path (T > 32) on the 5th-generation tensor
 // cores: tcgen05.mma with fp32 accumulators in TMEM, operands staged in smem
-// by TMA tiled loads (weights) and cp.async gathers (routed token rows).
+// by bulk copies of pre-tiled weights, TMA tiled loads and cp.async gathers.
 //
 //   prefill_router   logits[128 tokens][256 experts] per CTA (K = 2048); the
 //                    epilogue (one thread per token) adds the bias, selects the
@@ -17,10 +17,10 @@
 //                    h_perm[slot][512] (routed slots in expert order, then the
 //                    shared expert's T slots).
 //   prefill_down     grouped GEMM: M = 128 rows of the expert's down matrix,
-//                    N = up to 256 slots of h_perm, K = 512.  Epilogue: each
-//                    result times the pair's routing weight (1 for the shared
-//                    expert) is added into y32[token][h] with fp32 reductions.
-//   convert          y = bf16(y32).
+//                    N = up to 256 slots of h_perm, K = 512.  Epilogue: the
+//                    expert output of every slot, bf16, into o_perm[slot][2048].
+//   combine          y[t] = sum of the token's six routed slots times their
+//                    routing weights plus its shared slot, fp32, fixed order.
 //
 // Warp roles in every GEMM kernel: warp 0 issues TMA (one elected thread),
 // warp 1 allocates TMEM and issues MMAs (one thread), warps 2..5 drain TMEM in
@@ -43,9 +43,14 @@ constexpr int PF_THREADS = 192;
 constexpr int PF_TILE = 128;                 // rows of every operand tile
 constexpr int PF_BK = 64;                    // K per stage: 128 bytes of bf16
 constexpr int PF_TILE_BYTES = PF_TILE * PF_BK * 2;   // 16 KiB
+constexpr size_t EXPERT_ELEMS = (size_t)3 * H * I;   // one expert's gate_up + down
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ uint8_t* align16(uint8_t* p) {
+    return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 15) & ~uintptr_t(15));
 }
 
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
@@ -281,15 +286,41 @@ __device__ __forceinline__ bool gp_epi_all(bool v) {
     return r != 0;
 }
 
+// Epilogue staging: each epilogue warp holds a 32 (tokens) x 32 (rows) bf16
+// tile, written column-wise from TMEM lanes and read back row-wise so every
+// lane stores 64 contiguous bytes of one token row (rows padded to 80 bytes
+// so both phases are free of bank conflicts).
+constexpr int STG_ROW = 80;                       // bytes per staged token row
+constexpr int STG_WARP = 32 * STG_ROW;            // 2.5 KiB per epilogue warp
+
+// lane = row r of a 32-row block holding 32 token values v[n] (fp32): stage
+// them as bf16 and let lane n write its 64-byte token row to dst(n).
+template <typename DstFn>
+__device__ __forceinline__ void stage_store_32x32(uint8_t* stg, int lane, const float (&v)[32], int nvalid_here,
+                                                  DstFn dst) {
+#pragma unroll
+    for (int m = 0; m < 32; ++m)
+        *reinterpret_cast<__nv_bfloat16*>(stg + m * STG_ROW + 2 * lane) = __float2bfloat16_rn(v[m]);
+    __syncwarp();
+    if (lane < nvalid_here) {
+        const uint4* src = reinterpret_cast<const uint4*>(stg + lane * STG_ROW);
+        uint4* d = reinterpret_cast<uint4*>(dst(lane));
+        d[0] = src[0];
+        d[1] = src[1];
+        d[2] = src[2];
+        d[3] = src[3];
+    }
+    __syncwarp();
+}
+
 struct GroupedParams {
     int T;
     const int32_t* offsets;      // [E+1] slot base of each routed expert (6T total)
     const int32_t* gather;       // [6T] pair ids t*6+j grouped by expert
     const float* w_route;        // [T][6]
-    const CUtensorMap* gu_maps;  // [NEXP] gate_up matrices, boxes 64 x 128
-    const CUtensorMap* dn_maps;  // [NEXP] down matrices, boxes 64 x 128
+    const __nv_bfloat16* tiled;  // [NEXP] x (gate_up tiles, down tiles), 16 KiB tiles (repack.cu)
     __nv_bfloat16* h_perm;       // [7T][I]
-    float* y32;                  // [T][H]
+    __nv_bfloat16* o_perm;       // [7T][H] per-slot expert outputs
     uint32_t* status;
     uint64_t limit_ns;
 };
@@ -374,7 +405,7 @@ __device__ __forceinline__ Unit decode_unit(const Sched* S, int u) {
 constexpr int G1_STAGES = 3;
 constexpr int G1_STAGE = 2 * PF_TILE_BYTES + GP_B_BYTES;    // gate, up, tokens: 64 KiB
 constexpr int G1_BLOCKS = I / PF_TILE;                      // 4 row blocks of 128
-constexpr int G1_SMEM = 1024 + G1_STAGES * G1_STAGE + 512 + GP_N * 4 + (int)sizeof(Sched);
+constexpr int G1_SMEM = 1024 + G1_STAGES * G1_STAGE + 512 + GP_N * 4 + (int)sizeof(Sched) + 16 + GP_EPI_WARPS * STG_WARP;
 
 __global__ void __launch_bounds__(G1_THREADS, 1)
     prefill_gateup_kernel(const __nv_bfloat16* __restrict__ x, GroupedParams p) {
@@ -389,6 +420,7 @@ __global__ void __launch_bounds__(G1_THREADS, 1)
     volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int* tok = reinterpret_cast<int*>(smem + G1_STAGES * G1_STAGE + 512);           // [GP_N]
     Sched* S = reinterpret_cast<Sched*>(tok + GP_N);
+    uint8_t* stg_all = align16(reinterpret_cast<uint8_t*>(S + 1));                            // [8][STG_WARP]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nwarps = G1_THREADS / 32;
     // gather warps: warp 0 (which also issues the weight TMA) and the last warp
@@ -438,7 +470,8 @@ __global__ void __launch_bounds__(G1_THREADS, 1)
                 src[k] = x + (size_t)t * H;
                 nrow[k] = n;
             }
-            const CUtensorMap* wm = p.gu_maps + U.e;
+            // gate tiles of row block blk, up tiles of row block 4 + blk
+            const uint8_t* wt = reinterpret_cast<const uint8_t*>(p.tiled + (size_t)U.e * EXPERT_ELEMS);
             for (int kc = 0; kc < KC; ++kc, ++kc_all) {
                 const int s = kc_all % G1_STAGES;
                 bool ok = true;
@@ -447,8 +480,9 @@ __global__ void __launch_bounds__(G1_THREADS, 1)
                 uint8_t* st = smem + s * G1_STAGE;
                 if (warp == 0 && lane == 0) {
                     mbar_arrive_expect_tx(&full[s], 2 * PF_TILE_BYTES);
-                    tc::tma_load_2d(st, wm, kc * PF_BK, U.blk * PF_TILE, &full[s]);
-                    tc::tma_load_2d(st + PF_TILE_BYTES, wm, kc * PF_BK, I + U.blk * PF_TILE, &full[s]);
+                    bulk_g2s(st, wt + (size_t)(U.blk * KC + kc) * PF_TILE_BYTES, PF_TILE_BYTES, &full[s]);
+                    bulk_g2s(st + PF_TILE_BYTES, wt + (size_t)((I / PF_TILE + U.blk) * KC + kc) * PF_TILE_BYTES,
+                             PF_TILE_BYTES, &full[s]);
                 }
                 // token rows into the 128-byte-swizzled K-major tile: 16-byte
                 // chunk c of row n lands at n*128 + ((c ^ (n & 7)) * 16)
@@ -498,13 +532,14 @@ __global__ void __launch_bounds__(G1_THREADS, 1)
         }
         __syncwarp();
     } else {
-        const int ew = warp - 2, q = warp & 3, half = ew >> 2, row = 32 * q + lane;
+        const int ew = warp - 2, q = warp & 3, half = ew >> 2;
+        uint8_t* stg = stg_all + ew * STG_WARP;
         int lu = 0;
         for (int u = blockIdx.x; u < total; u += gridDim.x, ++lu) {
             const Unit U = decode_unit(S, u);
             if (!__all_sync(0xFFFFFFFFu, pf_wait(tfull, lu & 1, p.limit_ns, abort))) break;
             tc::fence_after_sync();
-            const int j = U.blk * PF_TILE + row;
+            const int j0 = U.blk * PF_TILE + 32 * q;   // this warp's 32 rows of h
             const uint32_t tg = tmem + ((uint32_t)(32 * q) << 16);
             // the two warps of a lane quarter take alternate 32-column chunks
             for (int c0 = 32 * half; c0 < U.npad; c0 += 64) {
@@ -512,14 +547,12 @@ __global__ void __launch_bounds__(G1_THREADS, 1)
                 tc::tmem_ld32(tg + c0, g);
                 tc::tmem_ld32(tg + GP_N + c0, up);
                 tc::tmem_ld_wait();
+                float h[32];
 #pragma unroll
-                for (int m = 0; m < 32; ++m) {
-                    const int n = c0 + m;
-                    if (n < U.nvalid) {
-                        const float h = silu_f(__uint_as_float(g[m])) * __uint_as_float(up[m]);
-                        p.h_perm[(size_t)(U.base + n) * I + j] = __float2bfloat16_rn(h);
-                    }
-                }
+                for (int m = 0; m < 32; ++m) h[m] = silu_f(__uint_as_float(g[m])) * __uint_as_float(up[m]);
+                stage_store_32x32(stg, lane, h, U.nvalid - c0, [&](int n) {
+                    return p.h_perm + (size_t)(U.base + c0 + n) * I + j0;
+                });
             }
             tc::fence_before_sync();
             __syncwarp();
@@ -542,7 +575,7 @@ __global__ void __launch_bounds__(G1_THREADS, 1)
 constexpr int G2_STAGES = 4;
 constexpr int G2_STAGE = PF_TILE_BYTES + GP_B_BYTES;   // down tile, activation tile: 48 KiB
 constexpr int G2_BLOCKS = H / PF_TILE;                 // 16 row blocks of 128
-constexpr int G2_SMEM = 1024 + G2_STAGES * G2_STAGE + 512 + GP_N * 8 + (int)sizeof(Sched);
+constexpr int G2_SMEM = 1024 + G2_STAGES * G2_STAGE + 512 + (int)sizeof(Sched) + 16 + GP_EPI_WARPS * STG_WARP;
 
 __global__ void __launch_bounds__(GP_THREADS, 1)
     prefill_down_kernel(const __grid_constant__ CUtensorMap h_map, GroupedParams p) {
@@ -555,9 +588,8 @@ __global__ void __launch_bounds__(GP_THREADS, 1)
     uint64_t* mdone = tempty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mdone + 1);
     volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    int* tok = reinterpret_cast<int*>(smem + G2_STAGES * G2_STAGE + 512);          // [GP_N]
-    float* wgt = reinterpret_cast<float*>(tok + GP_N);                              // [GP_N]
-    Sched* S = reinterpret_cast<Sched*>(wgt + GP_N);
+    Sched* S = reinterpret_cast<Sched*>(smem + G2_STAGES * G2_STAGE + 512);
+    uint8_t* stg_all = align16(reinterpret_cast<uint8_t*>(S + 1));                           // [8][STG_WARP]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -594,13 +626,14 @@ __global__ void __launch_bounds__(GP_THREADS, 1)
             int kc_all = 0;
             for (int u = blockIdx.x; u < total && !*abort; u += gridDim.x) {
                 const Unit U = decode_unit(S, u);
-                const CUtensorMap* wm = p.dn_maps + U.e;
+                const uint8_t* wt = reinterpret_cast<const uint8_t*>(p.tiled + (size_t)U.e * EXPERT_ELEMS +
+                                                                     (size_t)2 * I * H);
                 for (int kc = 0; kc < KC; ++kc, ++kc_all) {
                     const int s = kc_all % G2_STAGES;
                     if (!pf_wait(&empty[s], ((kc_all / G2_STAGES) & 1) ^ 1, p.limit_ns, abort)) break;
                     uint8_t* st = smem + s * G2_STAGE;
                     mbar_arrive_expect_tx(&full[s], PF_TILE_BYTES + GP_B_BYTES);
-                    tc::tma_load_2d(st, wm, kc * PF_BK, U.blk * PF_TILE, &full[s]);
+                    bulk_g2s(st, wt + (size_t)(U.blk * KC + kc) * PF_TILE_BYTES, PF_TILE_BYTES, &full[s]);
                     tc::tma_load_2d(st + PF_TILE_BYTES, &h_map, kc * PF_BK, U.base, &full[s]);
                 }
             }
@@ -634,43 +667,30 @@ __global__ void __launch_bounds__(GP_THREADS, 1)
         }
         __syncwarp();
     } else {
-        const int ew = warp - 2, q = warp & 3, half = ew >> 2, row = 32 * q + lane;
-        const int et = threadIdx.x - 64;   // 0 .. 255
+        const int ew = warp - 2, q = warp & 3, half = ew >> 2;
+        uint8_t* stg = stg_all + ew * STG_WARP;
         int lu = 0;
         for (int u = blockIdx.x; u < total; u += gridDim.x, ++lu) {
             const Unit U = decode_unit(S, u);
             const int b = lu & 1;
-            // token and routing weight of each column of the pass
-            if (et < U.nvalid) {
-                const int slot = U.base + et;
-                if (U.e < E) {
-                    const int pr = __ldg(p.gather + slot);
-                    tok[et] = pr / TOPK;
-                    wgt[et] = __ldg(p.w_route + pr);
-                } else {
-                    tok[et] = slot - sixT;
-                    wgt[et] = 1.f;
-                }
-            }
-            // waits for the accumulator; also publishes tok/wgt to every warp
-            if (!gp_epi_all(pf_wait(&tfull[b], (lu >> 1) & 1, p.limit_ns, abort))) break;
+            if (!__all_sync(0xFFFFFFFFu, pf_wait(&tfull[b], (lu >> 1) & 1, p.limit_ns, abort))) break;
             tc::fence_after_sync();
-            const int h = U.blk * PF_TILE + row;
+            const int h0 = U.blk * PF_TILE + 32 * q;   // this warp's 32 rows of the output
             const uint32_t td = tmem + ((uint32_t)(32 * q) << 16) + b * GP_N;
             for (int c0 = 32 * half; c0 < U.npad; c0 += 64) {
                 uint32_t v[32];
                 tc::tmem_ld32(td + c0, v);
                 tc::tmem_ld_wait();
+                float o[32];
 #pragma unroll
-                for (int m = 0; m < 32; ++m) {
-                    const int n = c0 + m;
-                    if (n < U.nvalid) atomicAdd(p.y32 + (size_t)tok[n] * H + h, wgt[n] * __uint_as_float(v[m]));
-                }
+                for (int m = 0; m < 32; ++m) o[m] = __uint_as_float(v[m]);
+                stage_store_32x32(stg, lane, o, U.nvalid - c0, [&](int n) {
+                    return p.o_perm + (size_t)(U.base + c0 + n) * H + h0;
+                });
             }
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[b]);
-            gp_epi_sync();   // tok/wgt of this pass no longer needed
         }
     }
     if (*abort && threadIdx.x == 0) report_status(p.status, ST_TIMEOUT);
@@ -682,16 +702,41 @@ __global__ void __launch_bounds__(GP_THREADS, 1)
     }
 }
 
-__global__ void __launch_bounds__(256) convert_y_kernel(const float* y32, __nv_bfloat16* y, int n8) {
+// y[t] = sum_j w[t][j] * o_perm[slot(t, j)] + o_perm[6T + t], summed in fp32 in
+// slot order (the six routed experts by decreasing logit, then the shared
+// expert): deterministic.  One thread per 8 output columns of a token.
+__global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __restrict__ o_perm,
+                                                     const int32_t* __restrict__ pair_slot,
+                                                     const float* __restrict__ w_route, int T,
+                                                     __nv_bfloat16* __restrict__ y) {
     pdl_wait();
     pdl_trigger();
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= n8) return;
-    const float4 a = __ldcg(reinterpret_cast<const float4*>(y32) + 2 * i);
-    const float4 b = __ldcg(reinterpret_cast<const float4*>(y32) + 2 * i + 1);
-    __nv_bfloat162 o[4] = {__floats2bfloat162_rn(a.x, a.y), __floats2bfloat162_rn(a.z, a.w),
-                           __floats2bfloat162_rn(b.x, b.y), __floats2bfloat162_rn(b.z, b.w)};
-    reinterpret_cast<uint4*>(y)[i] = *reinterpret_cast<const uint4*>(o);
+    if (i >= T * (H / 8)) return;
+    const int t = i / (H / 8), c = (i % (H / 8)) * 8;
+    float acc[8];
+    {
+        const uint4 v = __ldcg(reinterpret_cast<const uint4*>(o_perm + ((size_t)TOPK * T + t) * H + c));
+        acc[0] = bf_lo(v.x); acc[1] = bf_hi(v.x); acc[2] = bf_lo(v.y); acc[3] = bf_hi(v.y);
+        acc[4] = bf_lo(v.z); acc[5] = bf_hi(v.z); acc[6] = bf_lo(v.w); acc[7] = bf_hi(v.w);
+    }
+    float r[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) r[k] = 0.f;
+#pragma unroll
+    for (int j = 0; j < TOPK; ++j) {
+        const int slot = __ldg(pair_slot + t * TOPK + j);
+        const float wj = __ldg(w_route + t * TOPK + j);
+        const uint4 v = __ldcg(reinterpret_cast<const uint4*>(o_perm + (size_t)slot * H + c));
+        r[0] = fmaf(wj, bf_lo(v.x), r[0]); r[1] = fmaf(wj, bf_hi(v.x), r[1]);
+        r[2] = fmaf(wj, bf_lo(v.y), r[2]); r[3] = fmaf(wj, bf_hi(v.y), r[3]);
+        r[4] = fmaf(wj, bf_lo(v.z), r[4]); r[5] = fmaf(wj, bf_hi(v.z), r[5]);
+        r[6] = fmaf(wj, bf_lo(v.w), r[6]); r[7] = fmaf(wj, bf_hi(v.w), r[7]);
+    }
+    __nv_bfloat162 out[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) out[k] = __floats2bfloat162_rn(r[2 * k] + acc[2 * k], r[2 * k + 1] + acc[2 * k + 1]);
+    *reinterpret_cast<uint4*>(y + (size_t)t * H + c) = *reinterpret_cast<const uint4*>(out);
 }
 
 // ---------------------------------------------------------------------------
@@ -716,16 +761,17 @@ cudaError_t launch_prefill_router(const LaunchCtx& L, const CUtensorMap& x_map, 
 }
 
 cudaError_t launch_prefill_experts(const LaunchCtx& L, const __nv_bfloat16* x, const CUtensorMap& h_map, int T,
-                                   const int32_t* offsets, const int32_t* gather, const float* w_route,
-                                   const CUtensorMap* gu_maps, const CUtensorMap* dn_maps, __nv_bfloat16* h_perm,
-                                   float* y32, __nv_bfloat16* y) {
-    GroupedParams gp{T, offsets, gather, w_route, gu_maps, dn_maps, h_perm, y32, L.status, L.wait_limit_ns};
+                                   const int32_t* offsets, const int32_t* gather, const int32_t* pair_slot,
+                                   const float* w_route, const __nv_bfloat16* tiled, __nv_bfloat16* h_perm,
+                                   __nv_bfloat16* o_perm, __nv_bfloat16* y) {
+    GroupedParams gp{T, offsets, gather, w_route, tiled, h_perm, o_perm, L.status, L.wait_limit_ns};
     cudaError_t e = launch_pdl(L, prefill_gateup_kernel, dim3(L.num_sms), dim3(G1_THREADS), G1_SMEM, x, gp);
     if (e != cudaSuccess) return e;
     e = launch_pdl(L, prefill_down_kernel, dim3(L.num_sms), dim3(GP_THREADS), G2_SMEM, h_map, gp);
     if (e != cudaSuccess) return e;
-    const int n8 = T * H / 8;
-    return launch_pdl(L, convert_y_kernel, dim3((n8 + 255) / 256), dim3(256), 0, (const float*)y32, y, n8);
+    const int n8 = T * (H / 8);
+    return launch_pdl(L, combine_kernel, dim3((n8 + 255) / 256), dim3(256), 0, (const __nv_bfloat16*)o_perm,
+                      pair_slot, w_route, T, y);
 }
 
 }  // namespace flint

@@ -286,7 +286,7 @@ __global__ void __launch_bounds__(E) perm_scan_kernel(const int32_t* __restrict_
 
 __global__ void __launch_bounds__(256) perm_scatter_kernel(const int32_t* idx, const int32_t* local_rank, int T,
                                                           const int32_t* blk_base, const int32_t* offsets,
-                                                          int32_t* gather) {
+                                                          int32_t* gather, int32_t* pair_slot) {
     pdl_wait();
     const int p = blockIdx.x * blockDim.x + threadIdx.x;
     if (p >= T * TOPK) return;
@@ -294,7 +294,9 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(const int32_t* idx, c
     const int b = t / PB_TOK;
     const int e = idx[p];
     if (e < 0 || e >= E) return;
-    gather[offsets[e] + blk_base[b * E + e] + local_rank[p]] = p;
+    const int slot = offsets[e] + blk_base[b * E + e] + local_rank[p];
+    gather[slot] = p;
+    if (pair_slot) pair_slot[p] = slot;
 }
 
 // ---------------------------------------------------------------------------
@@ -335,17 +337,18 @@ cudaError_t launch_permutation(const LaunchCtx& L, const int32_t* idx, int T, in
     if (err != cudaSuccess) return err;
     if (!gather) return cudaSuccess;
     return launch_pdl(L, perm_scatter_kernel, dim3((T * TOPK + 255) / 256), dim3(256), 0, idx,
-                      (const int32_t*)local_rank, T, (const int32_t*)blk_base, (const int32_t*)offsets, gather);
+                      (const int32_t*)local_rank, T, (const int32_t*)blk_base, (const int32_t*)offsets, gather,
+                      (int32_t*)nullptr);
 }
 
 cudaError_t launch_perm_scan_scatter(const LaunchCtx& L, const int32_t* idx, int T, const int32_t* local_rank,
                                      const int32_t* blk_counts, int32_t* blk_base, int32_t* offsets,
-                                     int32_t* gather) {
+                                     int32_t* gather, int32_t* pair_slot) {
     const int nblk = (T + PB_TOK - 1) / PB_TOK;
     cudaError_t err = launch_pdl(L, perm_scan_kernel, dim3(1), dim3(E), 0, blk_counts, nblk, blk_base, offsets);
     if (err != cudaSuccess || !gather) return err;
     return launch_pdl(L, perm_scatter_kernel, dim3((T * TOPK + 255) / 256), dim3(256), 0, idx, local_rank, T,
-                      (const int32_t*)blk_base, (const int32_t*)offsets, gather);
+                      (const int32_t*)blk_base, (const int32_t*)offsets, gather, pair_slot);
 }
 
 }  // namespace flint

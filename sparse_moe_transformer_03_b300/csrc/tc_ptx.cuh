@@ -1,6 +1,6 @@
 // tc_ptx.cuh -- inline-PTX wrappers for the 5th-generation tensor cores
 // (tcgen05: TMEM allocation, MMA, commit, TMEM loads) and for TMA tensor
-// copies (tiled and gather4), plus the shared-memory / instruction
+// copies (2-D and 4-D tiles), cp.async gathers, plus the shared-memory / instruction
 // descriptors the MMA consumes.  sm_100-family (sm_103a) only.
 #pragma once
 
@@ -26,14 +26,13 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
-// Four rows r0..r3 (each one box of one row high, starting at column c0)
-// gathered into consecutive row slots of smem.
-__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, int c0, int r0, int r1, int r2, int r3,
+// 4-D tiled load of the box at coordinates (c0, c1, c2, c3), innermost first.
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
                                             uint64_t* bar) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
-        "%3, %4, %5, %6}], [%7];" ::"r"(smem_addr(dst)),
-        "l"(map), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_addr(bar))
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+        "%5}], [%6];" ::"r"(smem_addr(dst)),
+        "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_addr(bar))
         : "memory");
 }
 
