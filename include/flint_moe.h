@@ -138,6 +138,26 @@ FLINT_API flint_status_t flint_moe_destroy(flint_moe_t h);
 /* Human-readable name of a status code (static storage). */
 FLINT_API const char* flint_status_string(flint_status_t st);
 
+/* The expert permutation of flint_moe_route_only (offsets and gather_idx,
+ * same definitions and results) computed from a given routing, without a
+ * layer handle and without allocating any device memory.  The pages define
+ * no such call: it exists for callers that must not allocate at routing time
+ * (allocator-free serving loops, external memory pools).
+ *   idx        int32 [T][6] expert ids in 0..255 (device).
+ *   offsets    int32 [257] (device), as in flint_moe_route_only.
+ *   gather_idx int32 [6T] (device), as in flint_moe_route_only.
+ *   T          1 <= T <= FLINT_CHUNK; a larger T is rejected with
+ *              FLINT_ERR_INVALID_ARG, because the scratch is a fixed device
+ *              array sized for FLINT_CHUNK tokens (327,936 bytes).
+ * The scratch is one array per device shared by every call: calls that
+ * overlap in time (two streams, two host threads) race on it and must be
+ * serialised by the caller.  The first call on a device looks up the array's
+ * address; make that first call before capturing s into a graph.
+ * Synchronises s.  Errors: INVALID_ARG, CUDA, DEVICE_BADINDEX (an id in idx
+ * outside 0..255; outputs are then unspecified). */
+FLINT_API flint_status_t flint_permute_static(const int32_t* idx, int T, int32_t* offsets,
+                                              int32_t* gather_idx, cudaStream_t s);
+
 /* Test hook: launch one kernel that waits on a device flag nothing sets,
  * with a wait limit of timeout_ns nanoseconds of %globaltimer; returns
  * FLINT_ERR_DEVICE_TIMEOUT when the bounded wait gives up as designed.

@@ -38,6 +38,7 @@ cudaError_t launch_pdl(const LaunchCtx& L, void (*kern)(KArgs...), dim3 grid, di
 }
 
 // router.cu
+constexpr int PERM_BLOCK_TOKENS = 128;   // tokens per block of the permutation's counting sort
 cudaError_t launch_router_decode(const LaunchCtx& L, const __nv_bfloat16* x, int T, const __nv_bfloat16* Wr,
                                  const float* bias, float* logits, float* x_f32, int32_t* idx, float* w,
                                  DecodeTables* tables, unsigned* ticket);

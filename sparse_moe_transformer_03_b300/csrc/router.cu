@@ -209,7 +209,7 @@ __global__ void __launch_bounds__(128) select_kernel(const float* logits, int T,
 // perm_scan: offsets[e] and each block's base per expert.  perm_scatter:
 // gather[offsets[e] + base[b][e] + rank] = pair id.
 
-constexpr int PB_TOK = 128;
+constexpr int PB_TOK = PERM_BLOCK_TOKENS;
 
 __global__ void __launch_bounds__(PB_TOK) perm_local_kernel(const int32_t* idx, int T, int32_t* local_rank,
                                                            int32_t* blk_counts, uint32_t* status) {

@@ -64,6 +64,8 @@ def load_library():
     lib.flint_moe_destroy.argtypes = [P]
     lib.flint_status_string.restype = ctypes.c_char_p
     lib.flint_status_string.argtypes = [I32]
+    lib.flint_permute_static.restype = I32
+    lib.flint_permute_static.argtypes = [P, I32, P, P, P]
     lib.flint_debug_bounded_wait.restype = I32
     lib.flint_debug_bounded_wait.argtypes = [ctypes.c_uint64, P]
     _lib = lib
@@ -142,6 +144,11 @@ def flint_moe_route_only(h, x, logits, T, idx, w, offsets=None, gather_idx=None,
     _check("flint_moe_route_only",
            load_library().flint_moe_route_only(ctypes.c_void_p(h), _ptr(x), _ptr(logits), int(T), _ptr(idx), _ptr(w),
                                                _ptr(offsets), _ptr(gather_idx), _stream(stream)))
+
+
+def flint_permute_static(idx, T, offsets, gather_idx, stream=None):
+    _check("flint_permute_static",
+           load_library().flint_permute_static(_ptr(idx), int(T), _ptr(offsets), _ptr(gather_idx), _stream(stream)))
 
 
 def flint_moe_destroy(h):
