@@ -78,6 +78,15 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
 __device__ __forceinline__ float sigmoid_f(float z) { return 1.0f / (1.0f + expf(-z)); }
+// silu through the hardware base-2 exponential and reciprocal approximations:
+// exp(-z) = 2^(-z log2(e)).  Relative error a few 1e-7 (far below bf16
+// rounding); z -> -inf gives 2^+inf = inf, 1/inf = 0 and the result -0.
+__device__ __forceinline__ float silu_fast(float z) {
+    float e, r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(z * -1.4426950408889634f));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
+    return z * r;
+}
 
 // ---------------------------------------------------------------------------
 // programmatic dependent launch

@@ -455,20 +455,22 @@ __global__ void __launch_bounds__(G1_THREADS, 1)
     constexpr int KC = H / PF_BK;   // 32
 
     if (gather_warp) {
+        // Thread g of the 64 gather threads copies 16-byte chunk c = g % 8 of
+        // token rows n = g / 8 + 8 i: eight lanes cover one 128-byte row, so a
+        // warp-wide copy reads four whole rows.
+        const int g = 32 * gw + lane, c = g & 7, r0 = g >> 3;
+        const uint32_t dst_off = (uint32_t)r0 * 128u + ((uint32_t)(c ^ r0) << 4);   // n & 7 == r0
         int kc_all = 0;
         for (int u = blockIdx.x; u < total && !__shfl_sync(0xFFFFFFFFu, *abort, 0); u += gridDim.x) {
             const Unit U = decode_unit(S, u);
-            // this warp's token rows of the pass: n = 128 * gw + 32 * k + lane
-            // (padding rows repeat the last valid token)
-            const __nv_bfloat16* src[4];
-            int nrow[4];
+            // token of each of this thread's rows (padding rows repeat the last
+            // valid token); npad is a multiple of 16, so rows i < npad / 8 are in
+            const int nrows = U.npad >> 3;
+            int tk[GP_N / 8];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int n = 128 * gw + 32 * k + lane;
-                const int slot = U.base + min(n, U.nvalid - 1);
-                const int t = U.e < E ? __ldg(p.gather + slot) / TOPK : slot - sixT;
-                src[k] = x + (size_t)t * H;
-                nrow[k] = n;
+            for (int i = 0; i < GP_N / 8; ++i) {
+                const int slot = U.base + min(r0 + 8 * i, U.nvalid - 1);
+                tk[i] = i < nrows ? (U.e < E ? __ldg(p.gather + slot) / TOPK : slot - sixT) : 0;
             }
             // gate tiles of row block blk, up tiles of row block 4 + blk
             const uint8_t* wt = reinterpret_cast<const uint8_t*>(p.tiled + (size_t)U.e * EXPERT_ELEMS);
@@ -486,16 +488,11 @@ __global__ void __launch_bounds__(G1_THREADS, 1)
                 }
                 // token rows into the 128-byte-swizzled K-major tile: 16-byte
                 // chunk c of row n lands at n*128 + ((c ^ (n & 7)) * 16)
-                uint8_t* bt = st + 2 * PF_TILE_BYTES;
+                uint8_t* bt = st + 2 * PF_TILE_BYTES + dst_off;
+                const __nv_bfloat16* xk = x + kc * PF_BK + 8 * c;
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int n = nrow[k];
-                    if (n < U.npad) {
-#pragma unroll
-                        for (int c = 0; c < 8; ++c)
-                            tc::cp_async16(bt + n * 128 + ((c ^ (n & 7)) << 4), src[k] + kc * PF_BK + 8 * c);
-                    }
-                }
+                for (int i = 0; i < GP_N / 8; ++i)
+                    if (i < nrows) tc::cp_async16(bt + i * 1024, xk + (size_t)tk[i] * H);
                 tc::cp_async_arrive_noinc(&full[s]);
             }
         }
@@ -549,7 +546,7 @@ __global__ void __launch_bounds__(G1_THREADS, 1)
                 tc::tmem_ld_wait();
                 float h[32];
 #pragma unroll
-                for (int m = 0; m < 32; ++m) h[m] = silu_f(__uint_as_float(g[m])) * __uint_as_float(up[m]);
+                for (int m = 0; m < 32; ++m) h[m] = silu_fast(__uint_as_float(g[m])) * __uint_as_float(up[m]);
                 stage_store_32x32(stg, lane, h, U.nvalid - c0, [&](int n) {
                     return p.h_perm + (size_t)(U.base + c0 + n) * I + j0;
                 });
