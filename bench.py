@@ -41,6 +41,17 @@ WORKLOADS = {
 }
 # dense flops of one layer per token: 7 experts x (gate, up, down) + router
 FLOPS_PER_TOKEN = 7 * 2 * 3 * 2048 * 512 + 2 * 256 * 2048
+GATE_UP_BYTES = 2 * 512 * 2048 * 2            # one expert's gate and up matrices, bf16
+DOWN_BYTES = 2048 * 512 * 2                   # one expert's down matrix, bf16
+# kernel ids of flint_moe_set_kernel_events (include/flint_moe.h)
+K_ROUTER, K_GATE_UP, K_DOWN, K_COMBINE = 0, 1, 2, 3
+# the source files each timed kernel is built from (for the ncu traffic record)
+KERNEL_SOURCES = {
+    "gateup_decode_kernel": ["decode.cu", "routing.cuh", "flint_common.cuh"],
+    "down_decode_kernel": ["decode.cu", "flint_common.cuh"],
+    "prefill_gateup_kernel": ["prefill.cu", "tc_ptx.cuh", "flint_common.cuh"],
+    "prefill_down_kernel": ["prefill.cu", "tc_ptx.cuh", "flint_common.cuh"],
+}
 
 
 def parse():
@@ -192,6 +203,71 @@ def dist_setup(args):
     return ws, rank, local
 
 
+def max_over_ranks(values, device="cuda"):
+    """Element-wise maximum of this rank's timings over all ranks (the
+    slowest rank sets the job's time); the values themselves at N = 1."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_rate(units_per_rank, ws, ms):
+    """Units per second of the whole job: every rank processed units_per_rank
+    in at most ms milliseconds."""
+    return ws * units_per_rank / (ms * 1e-3)
+
+
+def sources_digest(kernel):
+    """sha1 of the sources `kernel` is compiled from."""
+    import hashlib
+    h = hashlib.sha1()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "sparse_moe_transformer_03_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profiles(kernel, workload):
+    """DRAM bytes (read + write) per launch of `kernel` on `workload` from
+    the ncu record in profiles/dram_traffic.md, or None when there is none or
+    the kernel's sources changed since it was taken."""
+    try:
+        lines = open(os.path.join(ROOT, "profiles", "dram_traffic.md")).read().splitlines()
+    except OSError:
+        return None
+    digest = sources_digest(kernel)
+    for ln in lines:
+        f = [c.strip() for c in ln.strip().strip("|").split("|")]
+        if len(f) >= 4 and f[0] == kernel and f[1] == workload and f[3] == digest:
+            try:
+                return float(f[2])
+            except ValueError:
+                return None
+    return None
+
+
+def kernel_durations(flint, torch, stream, calls, kid, nsteps):
+    """Device durations (ms) of kernel `kid` in every forward of `calls`
+    (a list of (handle, x, T, y)), over nsteps passes launched directly: the
+    library records a CUDA event pair on `stream` immediately around that
+    kernel's launch (flint_moe_set_kernel_events)."""
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in calls]
+           for _ in range(nsteps)]
+    with torch.cuda.stream(stream):
+        for st in range(nsteps):
+            for (h, x, T, y), (e0, e1) in zip(calls, evs[st]):
+                flint.flint_moe_set_kernel_events(h, kid, e0, e1)
+                flint.flint_moe_forward(h, x, T, y, stream)
+    stream.synchronize()
+    for (h, _, _, _) in calls:
+        flint.flint_moe_set_kernel_events(h, -1)
+    return [[e0.elapsed_time(e1) for (e0, e1) in row] for row in evs]
+
+
 def x_bits_for(wl):
     from synth import gen
     if wl["x"] == "gauss":
@@ -204,7 +280,9 @@ def x_bits_for(wl):
 # ---------------------------------------------------------------------------
 
 def run_reference(args, wl, ws, rank):
-    import numpy as np
+    """The oracle as it stands on the host cores: each step a bounded sample
+    of the workload (two layers of the decode stack, or the first
+    PREFILL_SAMPLE tokens of the prefill input on its one layer)."""
     from oracle.reference import LayerOracle
     from synth import device
 
@@ -213,12 +291,14 @@ def run_reference(args, wl, ws, rank):
     device.build()
     T = wl["T"]
     xb = x_bits_for(wl)
-    n_sample = 2   # layers per step: each step is a bounded sample of the stack
+    prefill = bool(wl.get("prefill"))
+    n_layers = 1 if prefill else 2
+    xs = xb[:PREFILL_SAMPLE] if prefill else xb
     orcs = []
-    for l in range(n_sample):
+    for l in range(n_layers):
         lw = device.LayerWeights(1, l, True)
         orc = LayerOracle.from_bf16_layer(lw)
-        orc.forward(xb)    # copies the touched experts to the host (untimed)
+        orc.forward(xs)    # copies the touched experts to the host (untimed)
         orcs.append(orc)
         del lw
     cores = os.cpu_count() or 1
@@ -226,22 +306,33 @@ def run_reference(args, wl, ws, rank):
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
         for orc in orcs:
-            orc.forward(xb)
+            orc.forward(xs)
         dt = time.perf_counter() - t0
         if i >= args.warmup:
             times.append(dt)
     step = sum(times) / len(times)
-    value = n_sample * T / step
-    line = {"metric": f"MoE-layer tokens/s, decode stack T={T}", "value": value, "unit": "layer-tokens/s",
+    if prefill:
+        value, unit = len(xs) / step, "tokens/s"
+        metric = f"MoE-layer tokens/s, prefill T={T}"
+        workload = (f"prefill: one BF16 MoE layer (H=2048, I=512, 256 routed + 1 shared, top-6 sigmoid, router bias "
+                    f"N(0,0.5)), T={T} tokens (x ~ N(0,1) RMS-normalised, seed {wl['x_seed']}); "
+                    f"sample of the first {len(xs)} tokens per step")
+        sample = f"first {len(xs)} of the {T} prefill tokens, one layer, touched experts on the host"
+        us_layer = step * 1e6 * T / len(xs)
+    else:
+        value, unit = n_layers * T / step, "layer-tokens/s"
+        metric = f"MoE-layer tokens/s, decode stack T={T}"
+        workload = f"decode stack, {N_LAYERS} BF16 MoE layers, T={T}, sample of {n_layers} layers per step"
+        sample = f"{n_layers} layers of the stack at T={T}, touched experts on the host"
+        us_layer = step * 1e6 / n_layers
+    line = {"metric": metric, "value": value, "unit": unit,
             "impl": "reference", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": step * 1e3, "higher_is_better": True, "scaling": "weak",
-            "us_per_layer": step * 1e6 / n_sample, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": f"decode stack, {N_LAYERS} BF16 MoE layers, T={T}, sample of {n_sample} layers per step",
-                       "H": 2048, "I": 512, "experts": 257, "top_k": 6},
+            "us_per_layer": us_layer, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload, "H": 2048, "I": 512, "experts": 257, "top_k": 6},
             "vs_baseline": None,
-            "cpu_baseline": {"value": value, "unit": "layer-tokens/s", "cores": cores, "kind": "oracle",
-                             "sample": f"{n_sample} layers of the stack at T={T}, touched experts on the host"},
-            "e2e": {"value": value, "unit": "layer-tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
@@ -269,6 +360,28 @@ def cpu_baseline(wl, stack_layers, cores_hint=None):
     dt = (time.perf_counter() - t0) / reps
     return {"value": n * T / dt, "unit": "layer-tokens/s", "cores": os.cpu_count() or 1, "kind": "oracle",
             "sample": f"{n} layers of the decode stack at T={T} (touched experts copied to host, copy untimed), {reps} reps"}
+
+
+PREFILL_SAMPLE = 256   # tokens of the prefill input the oracle runs per step
+
+
+def cpu_baseline_prefill(wl, lw, xb):
+    """The oracle, as it stands, on the first PREFILL_SAMPLE tokens of the prefill input."""
+    from oracle.reference import LayerOracle
+    orc = LayerOracle.from_bf16_layer(lw)
+    xs = xb[:PREFILL_SAMPLE]
+    orc.forward(xs)                    # host copies of touched experts (untimed)
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        orc.forward(xs)
+        reps += 1
+        if time.perf_counter() - t0 > 10.0 or reps >= 20:
+            break
+    dt = (time.perf_counter() - t0) / reps
+    return {"value": PREFILL_SAMPLE / dt, "unit": "tokens/s", "cores": os.cpu_count() or 1, "kind": "oracle",
+            "sample": f"first {PREFILL_SAMPLE} of the {wl['T']} prefill tokens, one layer "
+                      f"(touched experts copied to host, copy untimed), {reps} reps"}
 
 
 def run_flint(args, wl, ws, rank, local):
@@ -360,13 +473,23 @@ def run_flint(args, wl, ws, rank, local):
         ms_e2e = timed(step_e2e, max(3, args.steps // 2))
     stream.synchronize()
 
-    if ws > 1:
-        t = torch.tensor([ms, ms_e2e], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms, ms_e2e = t.tolist()
+    ms, ms_e2e = max_over_ranks([ms, ms_e2e])
+
+    # the dominant kernel, timed on its own (events around its launch, every layer)
+    calls = [(handles[l], x, T, ys[l]) for l in range(L)]
+    ksteps = max(3, min(args.steps, 10))
+    kern = {}
+    for name, kid, per_expert in (("gateup_decode_kernel", K_GATE_UP, GATE_UP_BYTES),
+                                  ("down_decode_kernel", K_DOWN, DOWN_BYTES)):
+        d = kernel_durations(flint, torch, stream, calls, kid, ksteps)
+        tot_ms = sum(sum(r) for r in d)
+        tot_bytes = ksteps * sum((u + 1) * per_expert for u in uniq)
+        kern[name] = {"us_per_launch": tot_ms * 1e3 / (ksteps * L), "bytes_per_launch": tot_bytes / (ksteps * L),
+                      "gbs": tot_bytes / (tot_ms * 1e-3) / 1e9, "launches_timed": ksteps * L}
+    dom = max(kern, key=lambda k: kern[k]["us_per_launch"])
 
     us_layer = ms * 1e3 / L
-    value = ws * L * T / (ms * 1e-3)
+    value = whole_job_rate(L * T, ws, ms)
     achieved = bytes_per_step / (ms * 1e-3) / 1e9
     peak_hbm = float(pk["hbm_gbs"])
     line = {
@@ -381,13 +504,22 @@ def run_flint(args, wl, ws, rank, local):
                    "l2": "inputs larger than L2 (each layer's weights are read once per step)",
                    "parallelism": f"replicas x{ws}", "graph": True},
         "unique_experts_per_layer": {"mean": float(np.mean(uniq)), "min": int(min(uniq)), "max": int(max(uniq))},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak_hbm, "unit": "GB/s",
-                     "frac": achieved / peak_hbm, "traffic": None,
-                     "what": "unique touched expert-weight bytes per layer / us per layer (router+gate_up+down "
-                             f"kernels, overlapped by PDL); peak = {pk_kind} HBM copy bandwidth"},
+        "roofline": {"bound": "hbm", "achieved": kern[dom]["gbs"], "peak": peak_hbm, "unit": "GB/s",
+                     "frac": kern[dom]["gbs"] / peak_hbm,
+                     "traffic": traffic_from_profiles(dom, args.workload),
+                     "kernel": dom, "bytes_per_launch": kern[dom]["bytes_per_launch"],
+                     "us_per_launch": kern[dom]["us_per_launch"],
+                     "what": "algorithmic bytes per launch (unique touched experts incl. the shared one x the "
+                             "matrices this kernel reads) / its device duration (CUDA events around its launch in "
+                             f"every layer of {ksteps} extra direct steps); peak = {pk_kind} HBM copy bandwidth "
+                             "(burst)"},
+        "kernels": kern,
+        "layer_hbm": {"achieved": achieved, "peak": peak_hbm, "unit": "GB/s", "frac": achieved / peak_hbm,
+                      "what": "unique touched expert-weight bytes per layer / us per layer in the timed graph "
+                              "(router, gate/up and down kernels chained by programmatic launch)"},
         "gpu_launches": 3 * L * args.steps,
         "clocks": clocks,
-        "e2e": {"value": ws * L * T / (ms_e2e * 1e-3), "unit": "layer-tokens/s",
+        "e2e": {"value": whole_job_rate(L * T, ws, ms_e2e), "unit": "layer-tokens/s",
                 "h2d_bytes_per_step": T * 2048 * 2, "d2h_bytes_per_step": L * T * 2048 * 2},
         "gen_seconds": round(t_gen, 2),
     }
@@ -456,30 +588,63 @@ def run_prefill(args, wl, ws, rank, local):
     with torch.cuda.stream(stream):
         step_e2e()
         ms_e2e = timed(step_e2e, max(3, args.steps // 2))
-    if ws > 1:
-        t = torch.tensor([ms, ms_e2e], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms, ms_e2e = t.tolist()
+    ms, ms_e2e = max_over_ranks([ms, ms_e2e])
+    # the dominant kernels timed on their own (events around each launch)
+    ksteps = max(3, min(args.steps, 10))
+    calls = [(h, x, T, y)]
+    slots = 7 * T
+    gu_flops, dn_flops = 2.0 * slots * 2048 * 1024, 2.0 * slots * 512 * 2048
+    # algorithmic bytes: every expert's matrices once (all 257 are touched at this T), the activations
+    # the kernel reads once and the outputs it writes once
+    gu_bytes = 257 * GATE_UP_BYTES + T * 2048 * 2 + slots * 512 * 2
+    dn_bytes = 257 * DOWN_BYTES + slots * 512 * 2 + slots * 2048 * 2
+    kern = {}
+    for name, kid, fl, by in (("prefill_gateup_kernel", K_GATE_UP, gu_flops, gu_bytes),
+                              ("prefill_down_kernel", K_DOWN, dn_flops, dn_bytes)):
+        d = kernel_durations(flint, torch, stream, calls, kid, ksteps)
+        us = sum(r[0] for r in d) * 1e3 / ksteps
+        kern[name] = {"us_per_launch": us, "flops_per_launch": fl, "bytes_per_launch": by,
+                      "tflops": fl / (us * 1e-6) / 1e12, "gbs": by / (us * 1e-6) / 1e9, "launches_timed": ksteps}
+    dom = max(kern, key=lambda k: kern[k]["us_per_launch"])
+    peak_hbm = float(pk["hbm_gbs"])
+    peak_tc = float(pk["bf16_tflops"])
+    kd = kern[dom]
+    # the binding resource of the kernel's own roofline: the larger of bytes / bandwidth and flops / peak
+    hbm_bound = kd["bytes_per_launch"] / peak_hbm / 1e9 >= kd["flops_per_launch"] / peak_tc / 1e12
+    if hbm_bound:
+        roof = {"bound": "hbm", "achieved": kd["gbs"], "peak": peak_hbm, "unit": "GB/s", "frac": kd["gbs"] / peak_hbm}
+    else:
+        roof = {"bound": "tensor", "achieved": kd["tflops"], "peak": peak_tc, "unit": "TFLOP/s",
+                "frac": kd["tflops"] / peak_tc}
+    roof.update({"traffic": traffic_from_profiles(dom, args.workload), "kernel": dom,
+                 "us_per_launch": kd["us_per_launch"], "bytes_per_launch": kd["bytes_per_launch"],
+                 "flops_per_launch": kd["flops_per_launch"], "tensor_frac": kd["tflops"] / peak_tc,
+                 "what": f"algorithmic bytes and flops per launch / its device duration (CUDA events around its "
+                         f"launch, {ksteps} extra direct steps); peaks = {pk_kind} HBM copy bandwidth and bf16 "
+                         "burst; bound = the larger of bytes/bandwidth and flops/peak"})
     flops = FLOPS_PER_TOKEN * T
     achieved = flops / (ms * 1e-3) / 1e12
     peak = float(pk["bf16_tflops"])
     line = {
-        "metric": f"MoE-layer tokens/s, prefill T={T}", "value": ws * T / (ms * 1e-3), "unit": "tokens/s",
+        "metric": f"MoE-layer tokens/s, prefill T={T}", "value": whole_job_rate(T, ws, ms), "unit": "tokens/s",
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "us_per_layer": ms * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded counter-based generator; random-init weights)",
         "config": {"workload": f"prefill: one BF16 MoE layer (H=2048, I=512, 256 routed + 1 shared, top-6 sigmoid, "
                                f"router bias N(0,0.5)), T={T} tokens (x ~ N(0,1) RMS-normalised, seed {wl['x_seed']})",
                    "l2": "inputs larger than L2 (1.6 GB of expert weights per step)", "parallelism": f"replicas x{ws}"},
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                     "traffic": None,
-                     "what": f"dense layer FLOPs (experts {7 * 6 * 2048 * 512 * T / 1e9:.1f} GFLOP + router "
-                             f"{2 * 256 * 2048 * T / 1e9:.1f}) / step time; peak = {pk_kind} bf16 burst"},
-        "gpu_launches": 7 * args.steps,
+        "roofline": roof,
+        "kernels": kern,
+        "layer_tensor": {"achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                         "what": f"dense layer FLOPs (experts {7 * 6 * 2048 * 512 * T / 1e9:.1f} GFLOP + router "
+                                 f"{2 * 256 * 2048 * T / 1e9:.1f}) / step time; peak = {pk_kind} bf16 burst"},
+        "gpu_launches": 6 * args.steps,
         "clocks": clocks,
-        "e2e": {"value": ws * T / (ms_e2e * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": T * 2048 * 2,
+        "e2e": {"value": whole_job_rate(T, ws, ms_e2e), "unit": "tokens/s", "h2d_bytes_per_step": T * 2048 * 2,
                 "d2h_bytes_per_step": T * 2048 * 2},
     }
+    if rank == 0 and ws == 1:
+        line["cpu_baseline"] = cpu_baseline_prefill(wl, lw, xb)
     flint.flint_moe_destroy(h)
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -94,10 +94,14 @@ typedef struct {
  *   shared_W   host array {gate_up, down} of the shared expert, same rules.
  *   dtype      FLINT_BF16 or FLINT_NVFP4 (the router stays bf16 either way).
  * Ownership: bf16 weights are borrowed (the caller keeps them alive and
- * unchanged until destroy).  NVFP4 weights are copied into a layout the handle
- * owns; the caller may free its buffers on return.  The handle also owns its
- * pointer tables and a workspace for FLINT_CHUNK tokens.  Synchronises the
- * device.  Errors: INVALID_ARG, OOM, CUDA, UNSUPPORTED (device is not sm_103). */
+ * unchanged until destroy: the decode kernels stream them in place).  The
+ * handle additionally owns a copy of every expert matrix cut into 16 KiB
+ * tensor-core operand tiles for the many-token path (1.6 GB per layer), its
+ * pointer tables and a workspace for FLINT_CHUNK tokens (about 310 MB).
+ * NVFP4 weights are copied into a layout the handle owns; the caller may
+ * free its buffers on return (not available yet: FLINT_NVFP4 returns
+ * FLINT_ERR_UNSUPPORTED).  Synchronises the device.
+ * Errors: INVALID_ARG, OOM, CUDA, UNSUPPORTED (device is not sm_103). */
 FLINT_API flint_status_t flint_moe_create(flint_moe_t* out, const void* router_W, const float* router_b,
                                 const void* const* gate_up_W, const void* const* down_W,
                                 const void* const* shared_W, flint_dtype_t dtype);
@@ -134,6 +138,28 @@ FLINT_API flint_status_t flint_moe_route_only(flint_moe_t h, const void* x, floa
 /* Synchronise the device, release everything the handle owns and return the
  * last device status.  NULL is accepted (returns FLINT_OK). */
 FLINT_API flint_status_t flint_moe_destroy(flint_moe_t h);
+
+/* Kernels of one forward that flint_moe_set_kernel_events can time. */
+typedef enum {
+    FLINT_KERNEL_ROUTER = 0,   /* router logits (T <= 32) / router GEMM + top-6 (T > 32) */
+    FLINT_KERNEL_GATE_UP = 1,  /* expert gate/up projections + SwiGLU                  */
+    FLINT_KERNEL_DOWN = 2,     /* expert down projections (T <= 32: with the combine)  */
+    FLINT_KERNEL_COMBINE = 3   /* weighted combine (T > 32 only)                       */
+} flint_kernel_t;
+
+/* Profiling hook: while set, every flint_moe_forward on h records `start`
+ * on its stream immediately before launching the kernel `kernel`
+ * (a flint_kernel_t) and `stop` immediately after it, so that
+ * cudaEventElapsedTime(start, stop) is that kernel's duration (for a forward
+ * of several FLINT_CHUNK chunks: the last chunk's).  The events (created by
+ * the caller, timing enabled) must outlive the setting.  An event recorded
+ * between two kernels removes their programmatic-launch overlap, so a hooked
+ * forward is slower than an unhooked one: for measurement only.  Not for
+ * use during stream capture (the records would not become graph nodes).
+ * kernel = -1 clears the hook (events may then be NULL).
+ * Errors: INVALID_ARG (null handle, unknown kernel, null event). */
+FLINT_API flint_status_t flint_moe_set_kernel_events(flint_moe_t h, int kernel, cudaEvent_t start,
+                                                     cudaEvent_t stop);
 
 /* Human-readable name of a status code (static storage). */
 FLINT_API const char* flint_status_string(flint_status_t st);

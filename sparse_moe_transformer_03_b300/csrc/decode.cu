@@ -32,6 +32,7 @@
 // experts, top-6 sigmoid routing plus a shared expert); SwiGLU experts with
 // H = 2048, I = 512 are this library's reading (the pages name neither).
 #include "flint_common.cuh"
+#include "../../include/flint_moe.h"
 #include "flint_internal.h"
 #include "routing.cuh"
 
@@ -403,12 +404,12 @@ cudaError_t launch_decode_experts(const LaunchCtx& L, const ExpertTables* expert
                                   float* a_buf, __nv_bfloat16* y) {
     const int Gd = down_grid(L.num_sms);
     GateUpParams gp{experts, logits, x, T, tables, idx, w, a_buf, L.status, L.wait_limit_ns};
-    cudaError_t e = launch_pdl(L, gateup_decode_kernel, dim3(L.num_sms), dim3(GU_WARPS * 32), GU_SMEM, gp);
+    cudaError_t e = launch_hooked(L, FLINT_KERNEL_GATE_UP, gateup_decode_kernel, dim3(L.num_sms), dim3(GU_WARPS * 32), GU_SMEM, gp);
     if (e != cudaSuccess) return e;
     const int rows_max = (H + Gd - 1) / Gd;
     const int apairs = (TOPK + 1) * T < DN_APAIRS ? (TOPK + 1) * T : DN_APAIRS;
     DownParams dp{experts, tables, a_buf, y, rows_max, apairs, L.status, L.wait_limit_ns};
-    return launch_pdl(L, down_decode_kernel, dim3(Gd), dim3(DN_WARPS * 32), down_smem_bytes(T, rows_max, apairs),
+    return launch_hooked(L, FLINT_KERNEL_DOWN, down_decode_kernel, dim3(Gd), dim3(DN_WARPS * 32), down_smem_bytes(T, rows_max, apairs),
                       dp);
 }
 

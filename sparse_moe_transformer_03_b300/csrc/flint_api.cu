@@ -16,6 +16,8 @@ struct flint_moe {
     int device;
     int num_sms;
     uint64_t wait_limit_ns;
+    int prof_kernel;               // profiling hook (flint_moe_set_kernel_events), -1 when unset
+    cudaEvent_t prof_start, prof_stop;
 
     // weights
     const __nv_bfloat16* router_W;
@@ -77,6 +79,9 @@ LaunchCtx ctx_of(const flint_moe* h, cudaStream_t s) {
     L.wait_limit_ns = h->wait_limit_ns;
     L.num_sms = h->num_sms;
     L.pdl = true;
+    L.prof_kernel = h->prof_kernel;
+    L.prof_start = h->prof_start;
+    L.prof_stop = h->prof_stop;
     return L;
 }
 
@@ -168,6 +173,7 @@ flint_status_t flint_moe_create(flint_moe_t* out, const void* router_W, const fl
     h->device = dev;
     h->num_sms = prop.multiProcessorCount;
     h->wait_limit_ns = 1000000000ull;   // one second
+    h->prof_kernel = -1;
     h->router_W = static_cast<const __nv_bfloat16*>(router_W);
     h->router_b = router_b;
     for (int e = 0; e < NEXP; ++e) {
@@ -306,6 +312,21 @@ flint_status_t flint_moe_route_only(flint_moe_t h, const void* x, float* logits,
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return FLINT_ERR_CUDA;
     return take_device_status(h);
+}
+
+flint_status_t flint_moe_set_kernel_events(flint_moe_t h, int kernel, cudaEvent_t start, cudaEvent_t stop) {
+    if (!h) return FLINT_ERR_INVALID_ARG;
+    if (kernel == -1) {
+        h->prof_kernel = -1;
+        h->prof_start = h->prof_stop = nullptr;
+        return FLINT_OK;
+    }
+    if (kernel < FLINT_KERNEL_ROUTER || kernel > FLINT_KERNEL_COMBINE || !start || !stop)
+        return FLINT_ERR_INVALID_ARG;
+    h->prof_kernel = kernel;
+    h->prof_start = start;
+    h->prof_stop = stop;
+    return FLINT_OK;
 }
 
 flint_status_t flint_moe_destroy(flint_moe_t h) {

@@ -17,6 +17,8 @@ struct LaunchCtx {
     uint64_t wait_limit_ns;
     int num_sms;
     bool pdl;              // launch kernels as programmatic dependents
+    int prof_kernel;       // flint_kernel_t whose launch is bracketed by the events below, or -1
+    cudaEvent_t prof_start, prof_stop;
 };
 
 // Launch `kern` on L.stream, as a programmatic dependent of the previous
@@ -35,6 +37,21 @@ cudaError_t launch_pdl(const LaunchCtx& L, void (*kern)(KArgs...), dim3 grid, di
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
+// launch_pdl, with the launch bracketed by L's profiling events when `kid`
+// is the kernel the caller asked to time.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_hooked(const LaunchCtx& L, int kid, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          Args... args) {
+    const bool hook = L.prof_kernel == kid;
+    if (hook) {
+        const cudaError_t e = cudaEventRecord(L.prof_start, L.stream);
+        if (e != cudaSuccess) return e;
+    }
+    const cudaError_t e = launch_pdl(L, kern, grid, block, smem, args...);
+    if (e != cudaSuccess || !hook) return e;
+    return cudaEventRecord(L.prof_stop, L.stream);
 }
 
 // router.cu

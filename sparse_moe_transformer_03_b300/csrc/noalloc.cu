@@ -76,6 +76,8 @@ extern "C" flint_status_t flint_permute_static(const int32_t* idx, int T, int32_
     L.wait_limit_ns = 1000000000ull;
     L.num_sms = 0;
     L.pdl = true;
+    L.prof_kernel = -1;
+    L.prof_start = L.prof_stop = nullptr;
     cudaError_t e = launch_permutation(L, idx, T, reinterpret_cast<int32_t*>(base + NA_RANK),
                                        reinterpret_cast<int32_t*>(base + NA_COUNTS),
                                        reinterpret_cast<int32_t*>(base + NA_BASE), offsets, gather_idx);

@@ -33,6 +33,7 @@
 //
 // Layer definition: RecursiveSI/flint (vLLM recipe page), "Overview"; SwiGLU
 // experts with H = 2048, I = 512 are this library's reading.
+#include "../../include/flint_moe.h"
 #include "flint_common.cuh"
 #include "flint_internal.h"
 #include "tc_ptx.cuh"
@@ -614,7 +615,6 @@ __global__ void __launch_bounds__(GP_THREADS, 1)
     pdl_trigger();
     build_sched(S, p, G2_BLOCKS);
     const int total = S->upre[NEXP];
-    const int sixT = TOPK * p.T;
     constexpr int KC = I / PF_BK;   // 8
 
     if (warp == 0) {
@@ -753,7 +753,7 @@ cudaError_t launch_prefill_router(const LaunchCtx& L, const CUtensorMap& x_map, 
                                   const float* bias, float* logits, int32_t* idx, float* w, int32_t* local_rank,
                                   int32_t* blk_counts) {
     RouterGemmParams rp{T, bias, logits, idx, w, local_rank, blk_counts, L.status, L.wait_limit_ns};
-    return launch_pdl(L, prefill_router_kernel, dim3((T + PF_TILE - 1) / PF_TILE), dim3(PF_THREADS), RG_SMEM, x_map,
+    return launch_hooked(L, FLINT_KERNEL_ROUTER, prefill_router_kernel, dim3((T + PF_TILE - 1) / PF_TILE), dim3(PF_THREADS), RG_SMEM, x_map,
                       wr_map, rp);
 }
 
@@ -762,12 +762,12 @@ cudaError_t launch_prefill_experts(const LaunchCtx& L, const __nv_bfloat16* x, c
                                    const float* w_route, const __nv_bfloat16* tiled, __nv_bfloat16* h_perm,
                                    __nv_bfloat16* o_perm, __nv_bfloat16* y) {
     GroupedParams gp{T, offsets, gather, w_route, tiled, h_perm, o_perm, L.status, L.wait_limit_ns};
-    cudaError_t e = launch_pdl(L, prefill_gateup_kernel, dim3(L.num_sms), dim3(G1_THREADS), G1_SMEM, x, gp);
+    cudaError_t e = launch_hooked(L, FLINT_KERNEL_GATE_UP, prefill_gateup_kernel, dim3(L.num_sms), dim3(G1_THREADS), G1_SMEM, x, gp);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(L, prefill_down_kernel, dim3(L.num_sms), dim3(GP_THREADS), G2_SMEM, h_map, gp);
+    e = launch_hooked(L, FLINT_KERNEL_DOWN, prefill_down_kernel, dim3(L.num_sms), dim3(GP_THREADS), G2_SMEM, h_map, gp);
     if (e != cudaSuccess) return e;
     const int n8 = T * (H / 8);
-    return launch_pdl(L, combine_kernel, dim3((n8 + 255) / 256), dim3(256), 0, (const __nv_bfloat16*)o_perm,
+    return launch_hooked(L, FLINT_KERNEL_COMBINE, combine_kernel, dim3((n8 + 255) / 256), dim3(256), 0, (const __nv_bfloat16*)o_perm,
                       pair_slot, w_route, T, y);
 }
 

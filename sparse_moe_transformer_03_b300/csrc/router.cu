@@ -7,6 +7,7 @@
 // without its fp32 saturation), keeps the lower expert index on equal logits,
 // and renormalises the six sigmoid scores to sum to one.
 #include "flint_common.cuh"
+#include "../../include/flint_moe.h"
 #include "flint_internal.h"
 #include "routing.cuh"
 
@@ -312,7 +313,7 @@ cudaError_t launch_router_decode(const LaunchCtx& L, const __nv_bfloat16* x, int
 
 cudaError_t launch_router_logits_decode(const LaunchCtx& L, const __nv_bfloat16* x, int T,
                                         const __nv_bfloat16* Wr, const float* bias, float* logits) {
-    return launch_pdl(L, router_logits_decode_kernel, dim3(RT_CTAS), dim3(RT_WARPS * 32), 0, x, T, Wr, bias,
+    return launch_hooked(L, FLINT_KERNEL_ROUTER, router_logits_decode_kernel, dim3(RT_CTAS), dim3(RT_WARPS * 32), 0, x, T, Wr, bias,
                       logits);
 }
 

@@ -64,6 +64,8 @@ def load_library():
     lib.flint_moe_destroy.argtypes = [P]
     lib.flint_status_string.restype = ctypes.c_char_p
     lib.flint_status_string.argtypes = [I32]
+    lib.flint_moe_set_kernel_events.restype = I32
+    lib.flint_moe_set_kernel_events.argtypes = [P, I32, P, P]
     lib.flint_permute_static.restype = I32
     lib.flint_permute_static.argtypes = [P, I32, P, P, P]
     lib.flint_debug_bounded_wait.restype = I32
@@ -144,6 +146,23 @@ def flint_moe_route_only(h, x, logits, T, idx, w, offsets=None, gather_idx=None,
     _check("flint_moe_route_only",
            load_library().flint_moe_route_only(ctypes.c_void_p(h), _ptr(x), _ptr(logits), int(T), _ptr(idx), _ptr(w),
                                                _ptr(offsets), _ptr(gather_idx), _stream(stream)))
+
+
+FLINT_KERNEL_ROUTER, FLINT_KERNEL_GATE_UP, FLINT_KERNEL_DOWN, FLINT_KERNEL_COMBINE = 0, 1, 2, 3
+
+
+def flint_moe_set_kernel_events(h, kernel, start=None, stop=None):
+    """start/stop: torch.cuda.Event(enable_timing=True) (or raw cudaEvent_t), None to clear."""
+    def ev(e):
+        if e is None:
+            return None
+        if hasattr(e, "cuda_event"):
+            if not e.cuda_event:
+                e.record()        # torch creates the CUDA event on its first record
+            return ctypes.c_void_p(e.cuda_event)
+        return ctypes.c_void_p(int(e))
+    _check("flint_moe_set_kernel_events",
+           load_library().flint_moe_set_kernel_events(ctypes.c_void_p(h), int(kernel), ev(start), ev(stop)))
 
 
 def flint_permute_static(idx, T, offsets, gather_idx, stream=None):

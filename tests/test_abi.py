@@ -60,3 +60,10 @@ def test_host_argument_checks(lib):
     arr[3] = 4096 * 4 + 8
     assert lib.flint_moe_create(ctypes.byref(h), P(256), None, arr, arr, sh, 0) == 1  # misaligned expert
     assert lib.flint_debug_bounded_wait(0, None) == 1
+
+
+def test_kernel_event_hook_rejects_bad_arguments():
+    """Argument checks of the profiling hook run on the host (no GPU needed)."""
+    from sparse_moe_transformer_03_b300 import flint
+    lib = flint.load_library()
+    assert lib.flint_moe_set_kernel_events(None, 1, None, None) == 1       # null handle
