@@ -38,16 +38,24 @@ WORKLOADS = {
     "decode8": {"T": 8, "x": "clustered", "x_seed": 12},
     "decode32": {"T": 32, "x": "clustered", "x_seed": 13},
     "prefill8192": {"T": 8192, "x": "gauss", "x_seed": 14, "prefill": True},
+    "nvfp4_decode1": {"T": 1, "x": "gauss", "x_seed": 11, "nvfp4": True},
+    "nvfp4_decode8": {"T": 8, "x": "clustered", "x_seed": 12, "nvfp4": True},
+    "nvfp4_decode32": {"T": 32, "x": "clustered", "x_seed": 13, "nvfp4": True},
 }
 # dense flops of one layer per token: 7 experts x (gate, up, down) + router
 FLOPS_PER_TOKEN = 7 * 2 * 3 * 2048 * 512 + 2 * 256 * 2048
 GATE_UP_BYTES = 2 * 512 * 2048 * 2            # one expert's gate and up matrices, bf16
 DOWN_BYTES = 2048 * 512 * 2                   # one expert's down matrix, bf16
+# NVFP4: E2M1 codes (half a byte per weight) + one E4M3 scale per 16 weights + an fp32 scale per matrix
+NV_GATE_UP_BYTES = 2 * 512 * 2048 // 2 + 2 * 512 * 2048 // 16 + 4     # 1,179,652
+NV_DOWN_BYTES = 2048 * 512 // 2 + 2048 * 512 // 16 + 4                  # 589,828
 # kernel ids of flint_moe_set_kernel_events (include/flint_moe.h)
 K_ROUTER, K_GATE_UP, K_DOWN, K_COMBINE = 0, 1, 2, 3
 # the source files each timed kernel is built from (for the ncu traffic record)
 KERNEL_SOURCES = {
     "gateup_decode_kernel": ["decode.cu", "routing.cuh", "flint_common.cuh"],
+    "gateup_nvfp4_kernel": ["decode_nvfp4.cu", "routing.cuh", "flint_common.cuh"],
+    "down_nvfp4_kernel": ["decode_nvfp4.cu", "flint_common.cuh"],
     "down_decode_kernel": ["decode.cu", "flint_common.cuh"],
     "prefill_gateup_kernel": ["prefill.cu", "tc_ptx.cuh", "flint_common.cuh"],
     "prefill_down_kernel": ["prefill.cu", "tc_ptx.cuh", "flint_common.cuh"],
@@ -283,7 +291,6 @@ def run_reference(args, wl, ws, rank):
     """The oracle as it stands on the host cores: each step a bounded sample
     of the workload (two layers of the decode stack, or the first
     PREFILL_SAMPLE tokens of the prefill input on its one layer)."""
-    from oracle.reference import LayerOracle
     from synth import device
 
     if rank != 0:
@@ -297,7 +304,7 @@ def run_reference(args, wl, ws, rank):
     orcs = []
     for l in range(n_layers):
         lw = device.LayerWeights(1, l, True)
-        orc = LayerOracle.from_bf16_layer(lw)
+        orc = layer_oracle(lw, device.LayerNVFP4(lw) if wl.get("nvfp4") else None)
         orc.forward(xs)    # copies the touched experts to the host (untimed)
         orcs.append(orc)
         del lw
@@ -321,8 +328,9 @@ def run_reference(args, wl, ws, rank):
         us_layer = step * 1e6 * T / len(xs)
     else:
         value, unit = n_layers * T / step, "layer-tokens/s"
-        metric = f"MoE-layer tokens/s, decode stack T={T}"
-        workload = f"decode stack, {N_LAYERS} BF16 MoE layers, T={T}, sample of {n_layers} layers per step"
+        kind = "NVFP4" if wl.get("nvfp4") else "BF16"
+        metric = f"MoE-layer tokens/s, {'NVFP4 ' if wl.get('nvfp4') else ''}decode stack T={T}"
+        workload = f"decode stack, {N_LAYERS} {kind} MoE layers, T={T}, sample of {n_layers} layers per step"
         sample = f"{n_layers} layers of the stack at T={T}, touched experts on the host"
         us_layer = step * 1e6 / n_layers
     line = {"metric": metric, "value": value, "unit": unit,
@@ -340,13 +348,28 @@ def run_reference(args, wl, ws, rank):
 # flint arm
 # ---------------------------------------------------------------------------
 
-def cpu_baseline(wl, stack_layers, cores_hint=None):
-    """The oracle, as it stands, on one decode step of a 2-layer sample."""
+def layer_oracle(lw, q=None):
+    """The oracle of a device layer: bf16 experts, or the NVFP4 encoding q of them."""
+    import oracle
     from oracle.reference import LayerOracle
+    if q is None:
+        return LayerOracle.from_bf16_layer(lw)
+
+    def mats(e):
+        (pg, sg, tg), (pd, sd, td) = q.expert_parts(e)
+        return (oracle.Mat(packed=pg, scales=sg, tensor_scale=tg),
+                oracle.Mat(packed=pd, scales=sd, tensor_scale=td))
+    return LayerOracle(lw.router_bits(), lw.bias_host(), mats, mats(lw.E), lw.E)
+
+
+def cpu_baseline(wl, stack_layers, cores_hint=None):
+    """The oracle, as it stands, on one decode step of a 2-layer sample
+    (stack_layers: bf16 layers, or (bf16 layer, NVFP4 encoding) pairs)."""
     T = wl["T"]
     xb = x_bits_for(wl)
     n = 2
-    orcs = [LayerOracle.from_bf16_layer(stack_layers[l]) for l in range(n)]
+    orcs = [layer_oracle(*(stack_layers[l] if isinstance(stack_layers[l], tuple) else (stack_layers[l],)))
+            for l in range(n)]
     for o in orcs:
         o.forward(xb)                  # host copies of touched experts (untimed)
     t0 = time.perf_counter()
@@ -396,12 +419,33 @@ def run_flint(args, wl, ws, rank, local):
     L = args.layers
     pk, pk_kind = peaks()
 
+    nv = bool(wl.get("nvfp4"))
     t_gen = time.perf_counter()
-    layers = [device.LayerWeights(1, l, True) for l in range(L)]
+    layers, handles, routers = [], [], []
+    resident = 0
+    for l in range(L):
+        lw = device.LayerWeights(1, l, True)
+        if nv:
+            # encode the experts to NVFP4; the handle repacks them into memory it owns, so the
+            # bf16 experts and the encoding are dropped (kept for the two layers the oracle samples)
+            q = device.LayerNVFP4(lw)
+            gu, dn, sh = q.create_args()
+            handles.append(flint.flint_moe_create(lw.router_W, lw.router_b, gu, dn, sh, dtype=flint.FLINT_NVFP4))
+            routers.append((lw.router_W, lw.router_b))
+            if l < 2:
+                layers.append((lw, q))
+            else:
+                del q, gu, dn, sh
+                lw.gate_up = lw.down = None
+            resident += 257 * (NV_GATE_UP_BYTES + NV_DOWN_BYTES)
+        else:
+            layers.append(lw)
+            handles.append(flint.flint_moe_create(lw.router_W, lw.router_b, list(lw.gate_up[:256]),
+                                                  list(lw.down[:256]), (lw.gate_up[256], lw.down[256])))
+            resident += lw.gate_up.numel() * 2 + lw.down.numel() * 2
+        del lw
     torch.cuda.synchronize()
     t_gen = time.perf_counter() - t_gen
-    handles = [flint.flint_moe_create(lw.router_W, lw.router_b, list(lw.gate_up[:256]), list(lw.down[:256]),
-                                      (lw.gate_up[256], lw.down[256])) for lw in layers]
     xb = x_bits_for(wl)
     x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
     ys = [torch.empty_like(x) for _ in range(L)]
@@ -413,7 +457,8 @@ def run_flint(args, wl, ws, rank, local):
         w = torch.empty((T, 6), dtype=torch.float32, device="cuda")
         flint.flint_moe_route_only(h, x, None, T, idx, w)
         uniq.append(len(set(idx.cpu().numpy().ravel().tolist())))
-    bytes_per_step = sum((u + 1) * EXPERT_BYTES_BF16 for u in uniq)
+    per_expert = NV_GATE_UP_BYTES + NV_DOWN_BYTES if nv else EXPERT_BYTES_BF16
+    bytes_per_step = sum((u + 1) * per_expert for u in uniq)
 
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()
@@ -479,8 +524,10 @@ def run_flint(args, wl, ws, rank, local):
     calls = [(handles[l], x, T, ys[l]) for l in range(L)]
     ksteps = max(3, min(args.steps, 10))
     kern = {}
-    for name, kid, per_expert in (("gateup_decode_kernel", K_GATE_UP, GATE_UP_BYTES),
-                                  ("down_decode_kernel", K_DOWN, DOWN_BYTES)):
+    kernels = ((("gateup_nvfp4_kernel", K_GATE_UP, NV_GATE_UP_BYTES), ("down_nvfp4_kernel", K_DOWN, NV_DOWN_BYTES))
+               if nv else (("gateup_decode_kernel", K_GATE_UP, GATE_UP_BYTES),
+                           ("down_decode_kernel", K_DOWN, DOWN_BYTES)))
+    for name, kid, per_expert in kernels:
         d = kernel_durations(flint, torch, stream, calls, kid, ksteps)
         tot_ms = sum(sum(r) for r in d)
         tot_bytes = ksteps * sum((u + 1) * per_expert for u in uniq)
@@ -493,14 +540,16 @@ def run_flint(args, wl, ws, rank, local):
     achieved = bytes_per_step / (ms * 1e-3) / 1e9
     peak_hbm = float(pk["hbm_gbs"])
     line = {
-        "metric": f"MoE-layer tokens/s, decode stack T={T}",
+        "metric": f"MoE-layer tokens/s, {'NVFP4 ' if nv else ''}decode stack T={T}",
         "value": value, "unit": "layer-tokens/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic (seeded counter-based generator; random-init weights)",
+        "dtype": "nvfp4 weights (e2m1 + e4m3 block scales), bf16 activations, f32 accumulation" if nv else "bf16",
+        "data": "synthetic (seeded counter-based generator; random-init weights)",
         "us_per_layer": us_layer, "us_per_layer_no_graph": ms_direct * 1e3 / L,
-        "config": {"workload": f"decode stack: {L} distinct BF16 MoE layers (H=2048, I=512, 256 routed + 1 shared, "
-                               f"top-6 sigmoid, router bias N(0,0.5)), T={T} tokens ({wl['x']} x, seed {wl['x_seed']})",
-                   "weights_resident_gb": round(sum(l.gate_up.numel() * 2 + l.down.numel() * 2 for l in layers) / 1e9, 2),
+        "config": {"workload": f"decode stack: {L} distinct {'NVFP4 (W4A16)' if nv else 'BF16'} MoE layers (H=2048, "
+                               f"I=512, 256 routed + 1 shared, top-6 sigmoid, router bias N(0,0.5)), T={T} tokens "
+                               f"({wl['x']} x, seed {wl['x_seed']})",
+                   "weights_resident_gb": round(resident / 1e9, 2),
                    "l2": "inputs larger than L2 (each layer's weights are read once per step)",
                    "parallelism": f"replicas x{ws}", "graph": True},
         "unique_experts_per_layer": {"mean": float(np.mean(uniq)), "min": int(min(uniq)), "max": int(max(uniq))},

@@ -94,13 +94,14 @@ typedef struct {
  *   shared_W   host array {gate_up, down} of the shared expert, same rules.
  *   dtype      FLINT_BF16 or FLINT_NVFP4 (the router stays bf16 either way).
  * Ownership: bf16 weights are borrowed (the caller keeps them alive and
- * unchanged until destroy: the decode kernels stream them in place).  The
- * handle additionally owns a copy of every expert matrix cut into 16 KiB
- * tensor-core operand tiles for the many-token path (1.6 GB per layer), its
+ * unchanged until destroy: the decode kernels stream them in place).  For
+ * FLINT_BF16 the handle additionally owns a copy of every expert matrix cut
+ * into 16 KiB tensor-core operand tiles for the many-token path (1.6 GB per
+ * layer).  The router (bf16, both dtypes) is borrowed.  The handle owns its
  * pointer tables and a workspace for FLINT_CHUNK tokens (about 310 MB).
- * NVFP4 weights are copied into a layout the handle owns; the caller may
- * free its buffers on return (not available yet: FLINT_NVFP4 returns
- * FLINT_ERR_UNSUPPORTED).  Synchronises the device.
+ * NVFP4 weights are repacked into a layout the handle owns (1.77 MB per
+ * expert, no bf16 copy); the caller may free its buffers on return.
+ * Synchronises the device.
  * Errors: INVALID_ARG, OOM, CUDA, UNSUPPORTED (device is not sm_103). */
 FLINT_API flint_status_t flint_moe_create(flint_moe_t* out, const void* router_W, const float* router_b,
                                 const void* const* gate_up_W, const void* const* down_W,
@@ -109,9 +110,11 @@ FLINT_API flint_status_t flint_moe_create(flint_moe_t* out, const void* router_W
 /* y = layer(x) for T >= 1 tokens.
  *   x  bf16 [T][2048], y bf16 [T][2048] (fully overwritten); x and y must not
  *   overlap.  Runs asynchronously on stream s; allocates nothing; capturable in
- *   a CUDA graph.  T <= 32 takes the weight-streaming decode kernels, larger T
- *   the grouped tensor-core path, in chunks of FLINT_CHUNK tokens.  One handle
- *   serves one stream at a time (the workspace is per handle).
+ *   a CUDA graph.  FLINT_BF16: T <= 32 takes the weight-streaming decode
+ *   kernels, larger T the grouped tensor-core path, in chunks of FLINT_CHUNK
+ *   tokens.  FLINT_NVFP4: the W4A16 weight-streaming kernels, in pieces of up
+ *   to 32 tokens.  One handle serves one stream at a time (the workspace is
+ *   per handle).
  * Errors: INVALID_ARG (null, misaligned, T < 1), CUDA (launch failed), or a
  * device status left by an earlier call. */
 FLINT_API flint_status_t flint_moe_forward(flint_moe_t h, const void* x, int T, void* y, cudaStream_t s);

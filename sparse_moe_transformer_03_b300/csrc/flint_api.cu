@@ -26,8 +26,11 @@ struct flint_moe {
     ExpertTables* dev_tables;      // same, in device memory
 
     // owned tiled copies of the expert matrices for the tensor-core path
-    // (per expert: gate_up tiles then down tiles, see repack.cu)
+    // (per expert: gate_up tiles then down tiles, see repack.cu); bf16 only
     __nv_bfloat16* tiled;
+    // NVFP4: owned repacked experts (NV_EXPERT_BYTES each) and tensor scales [NEXP][2]
+    uint8_t* nv;
+    float* nv_ts;
     CUtensorMap wr_map;            // router, boxes 64 x 256
     CUtensorMap h_map;             // h_perm, boxes 64 x 256
 
@@ -103,6 +106,8 @@ void free_handle(flint_moe* h) {
     if (h->ws_base) cudaFree(h->ws_base);
     if (h->dev_tables) cudaFree(h->dev_tables);
     if (h->tiled) cudaFree(h->tiled);
+    if (h->nv) cudaFree(h->nv);
+    if (h->nv_ts) cudaFree(h->nv_ts);
     if (h->status_host) cudaFreeHost(h->status_host);
     delete h;
 }
@@ -157,8 +162,12 @@ flint_status_t flint_moe_create(flint_moe_t* out, const void* router_W, const fl
         const void* dn = e < E ? down_W[e] : shared_W[1];
         if (!gu || !dn) return FLINT_ERR_INVALID_ARG;
         if (dtype == FLINT_BF16 && (!aligned16(gu) || !aligned16(dn))) return FLINT_ERR_INVALID_ARG;
+        if (dtype == FLINT_NVFP4) {
+            const flint_nvfp4_t* mg = static_cast<const flint_nvfp4_t*>(gu);
+            const flint_nvfp4_t* md = static_cast<const flint_nvfp4_t*>(dn);
+            if (!mg->packed || !mg->block_scales || !md->packed || !md->block_scales) return FLINT_ERR_INVALID_ARG;
+        }
     }
-    if (dtype == FLINT_NVFP4) return FLINT_ERR_UNSUPPORTED;
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return FLINT_ERR_CUDA;
@@ -176,7 +185,7 @@ flint_status_t flint_moe_create(flint_moe_t* out, const void* router_W, const fl
     h->prof_kernel = -1;
     h->router_W = static_cast<const __nv_bfloat16*>(router_W);
     h->router_b = router_b;
-    for (int e = 0; e < NEXP; ++e) {
+    for (int e = 0; dtype == FLINT_BF16 && e < NEXP; ++e) {
         h->host_tables.gate_up[e] = static_cast<const __nv_bfloat16*>(e < E ? gate_up_W[e] : shared_W[0]);
         h->host_tables.down[e] = static_cast<const __nv_bfloat16*>(e < E ? down_W[e] : shared_W[1]);
     }
@@ -208,7 +217,26 @@ flint_status_t flint_moe_create(flint_moe_t* out, const void* router_W, const fl
         }
     }
     const size_t expert_elems = (size_t)3 * H * I;   // gate_up + down
-    if (st == FLINT_OK) {
+    if (st == FLINT_OK && dtype == FLINT_NVFP4) {
+        // repack every expert into the owned chunk layout; keep the tensor scales
+        float ts[NEXP * 2];
+        if (cudaMalloc(&h->nv, (size_t)NEXP * NV_EXPERT_BYTES) != cudaSuccess ||
+            cudaMalloc(&h->nv_ts, sizeof ts) != cudaSuccess)
+            st = FLINT_ERR_OOM;
+        for (int e = 0; st == FLINT_OK && e < NEXP; ++e) {
+            const flint_nvfp4_t* mg = static_cast<const flint_nvfp4_t*>(e < E ? gate_up_W[e] : shared_W[0]);
+            const flint_nvfp4_t* md = static_cast<const flint_nvfp4_t*>(e < E ? down_W[e] : shared_W[1]);
+            ts[2 * e] = mg->tensor_scale;
+            ts[2 * e + 1] = md->tensor_scale;
+            uint8_t* b = h->nv + (size_t)e * NV_EXPERT_BYTES;
+            if (launch_repack_nvfp4(mg->packed, mg->block_scales, 0, b, 0) != cudaSuccess ||
+                launch_repack_nvfp4(md->packed, md->block_scales, 1, b + NV_GU_BYTES, 0) != cudaSuccess)
+                st = FLINT_ERR_CUDA;
+        }
+        if (st == FLINT_OK && cudaMemcpy(h->nv_ts, ts, sizeof ts, cudaMemcpyHostToDevice) != cudaSuccess)
+            st = FLINT_ERR_CUDA;
+    }
+    if (st == FLINT_OK && dtype == FLINT_BF16) {
         if (cudaMalloc(&h->tiled, (size_t)NEXP * expert_elems * sizeof(__nv_bfloat16)) != cudaSuccess)
             st = FLINT_ERR_OOM;
         for (int e = 0; st == FLINT_OK && e < NEXP; ++e) {
@@ -226,6 +254,7 @@ flint_status_t flint_moe_create(flint_moe_t* out, const void* router_W, const fl
     }
     if (st == FLINT_OK) st = from_cuda(prefill_set_attributes());
     if (st == FLINT_OK) st = from_cuda(decode_set_attributes());
+    if (st == FLINT_OK) st = from_cuda(decode_nvfp4_set_attributes());
     if (st == FLINT_OK) st = from_cuda(cudaDeviceSynchronize());
     if (st != FLINT_OK) {
         cudaGetLastError();
@@ -249,6 +278,19 @@ flint_status_t flint_moe_forward(flint_moe_t h, const void* x, int T, void* y, c
     const LaunchCtx L = ctx_of(h, s);
     const __nv_bfloat16* xs = static_cast<const __nv_bfloat16*>(x);
     __nv_bfloat16* ys = static_cast<__nv_bfloat16*>(y);
+    if (h->dtype == FLINT_NVFP4) {
+        // weight-streaming kernels, in pieces of up to FLINT_DECODE_MAX_T tokens
+        for (int t0 = 0; t0 < T; t0 += DEC_T) {
+            const int Tc = T - t0 < DEC_T ? T - t0 : DEC_T;
+            cudaError_t e = launch_router_logits_decode(L, xs + (size_t)t0 * H, Tc, h->router_W, h->router_b,
+                                                        h->logits);
+            if (e == cudaSuccess)
+                e = launch_decode_experts_nvfp4(L, h->nv, h->nv_ts, h->logits, xs + (size_t)t0 * H, Tc,
+                                                h->dec_tables, h->idx, h->w, h->a_dec, ys + (size_t)t0 * H);
+            if (e != cudaSuccess) return FLINT_ERR_CUDA;
+        }
+        return FLINT_OK;
+    }
     if (T <= DEC_T) {
         cudaError_t e = launch_router_logits_decode(L, xs, T, h->router_W, h->router_b, h->logits);
         if (e == cudaSuccess)

@@ -88,6 +88,29 @@ cudaError_t launch_prefill_experts(const LaunchCtx& L, const __nv_bfloat16* x, c
                                    const float* w_route, const __nv_bfloat16* tiled, __nv_bfloat16* h_perm,
                                    __nv_bfloat16* o_perm, __nv_bfloat16* y);
 
+// decode_nvfp4.cu -- owned NVFP4 expert layout.  A chunk holds 16 matrix
+// rows x 512 columns (32 blocks of 16 columns): 32 x 128 bytes of E2M1 codes
+// in mma.sync A-fragment order, then 32 x 16 bytes of E4M3 block scales.
+// Per expert: 64 gate/up units (gate rows 8u..8u+7 and up rows 8u..8u+7) of
+// 4 chunks each (K = 2048), then 128 down units (rows 16v..16v+15) of one
+// chunk (K = 512).
+constexpr int NV_CHUNK_KB = 32;                          // 16-column blocks per chunk
+constexpr int NV_CODES = NV_CHUNK_KB * 128;              // 4096
+constexpr int NV_CHUNK = NV_CODES + NV_CHUNK_KB * 16;    // 4608
+constexpr int NV_GU_UNITS = I / 8;                       // 64
+constexpr int NV_GU_CHUNKS = H / (16 * NV_CHUNK_KB);     // 4
+constexpr int NV_DN_UNITS = H / 16;                      // 128
+constexpr size_t NV_GU_BYTES = (size_t)NV_GU_UNITS * NV_GU_CHUNKS * NV_CHUNK;   // 1,179,648
+constexpr size_t NV_DN_BYTES = (size_t)NV_DN_UNITS * NV_CHUNK;                 // 589,824
+constexpr size_t NV_EXPERT_BYTES = NV_GU_BYTES + NV_DN_BYTES;                  // 1,769,472
+
+cudaError_t launch_repack_nvfp4(const uint8_t* packed, const uint8_t* scales, int kind, uint8_t* out,
+                                cudaStream_t s);
+cudaError_t decode_nvfp4_set_attributes();
+cudaError_t launch_decode_experts_nvfp4(const LaunchCtx& L, const uint8_t* nv, const float* nv_ts,
+                                        const float* logits, const __nv_bfloat16* x, int T, DecodeTables* tables,
+                                        int32_t* idx, float* w, float* a_buf, __nv_bfloat16* y);
+
 // decode.cu
 cudaError_t decode_set_attributes();
 cudaError_t launch_decode_experts(const LaunchCtx& L, const ExpertTables* experts, const float* logits,

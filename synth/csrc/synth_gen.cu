@@ -91,6 +91,107 @@ __global__ void fill_normal_f32_kernel(float* dst, uint64_t n, uint64_t key, dou
     }
 }
 
+// ---------------------------------------------------------------------------
+// NVFP4 encoding of bf16 matrices (the same steps, in the same fp32
+// operations, as synth/gen.py nvfp4_quantize)
+// ---------------------------------------------------------------------------
+
+// max |w| of each matrix, as the bits of a non-negative float (which order
+// like unsigned integers)
+__global__ void amax_kernel(const uint16_t* w, uint64_t per_mat, uint32_t* amax_bits) {
+    const uint32_t m = blockIdx.y;
+    const uint16_t* src = w + uint64_t(m) * per_mat;
+    uint32_t mx = 0;
+    for (uint64_t i = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; i < per_mat;
+         i += (uint64_t)gridDim.x * blockDim.x)
+        mx = max(mx, uint32_t(src[i] & 0x7FFFu) << 16);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+    __shared__ uint32_t part[32];
+    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int k = 1; k < (int)(blockDim.x >> 5); ++k) mx = max(mx, part[k]);
+        atomicMax(&amax_bits[m], mx);
+    }
+}
+
+// non-negative float -> E4M3 code, round to nearest even, saturating at 448
+__device__ uint8_t e4m3_encode_rn_sat(float v) {
+    if (!(v > 0.f)) return 0;
+    int ex;
+    (void)frexpf(v, &ex);                 // v = mant * 2^ex, mant in [0.5, 1)
+    const int ue = ex - 1;
+    const int step = ue < -6 ? -9 : ue - 3;
+    const float q = rintf(ldexpf(v, -step));
+    int code;
+    if (ue < -6) {
+        code = int(q);
+    } else {
+        int m = int(q) - 8, e = ue + 7;
+        if (q >= 16.f) {
+            e += 1;
+            m = 0;
+        }
+        code = (e << 3) | m;
+    }
+    return uint8_t(min(code, 0x7E));
+}
+
+__device__ float e4m3_decode_f32(uint8_t c) {
+    const int e = (c >> 3) & 15, m = c & 7;
+    const float v = e == 0 ? ldexpf(float(m) / 8.f, -6) : ldexpf(1.f + float(m) / 8.f, e - 7);
+    return (c & 0x80) ? -v : v;
+}
+
+// float -> E2M1 code: magnitude index into {0, .5, 1, 1.5, 2, 3, 4, 6}, round
+// to nearest with ties to even, clamped at 6; bit 3 = sign (none for zero)
+__device__ uint8_t e2m1_encode_rn(float v) {
+    const float a = fabsf(v);
+    uint8_t i = 7;
+    if (a <= 5.0f) i = 6;
+    if (a < 3.5f) i = 5;
+    if (a <= 2.5f) i = 4;
+    if (a < 1.75f) i = 3;
+    if (a <= 1.25f) i = 2;
+    if (a < 0.75f) i = 1;
+    if (a <= 0.25f) i = 0;
+    return uint8_t(i | ((v < 0.f && i > 0) ? 8 : 0));
+}
+
+// one thread per block of 16 consecutive elements of a row
+__global__ void nvfp4_quant_kernel(const uint16_t* w, uint32_t n_mat, uint32_t R, uint32_t K,
+                                   const uint32_t* amax_bits, uint8_t* packed, uint8_t* scales, float* tscale) {
+    const uint64_t per = uint64_t(R) * (K / 16);
+    for (uint64_t b = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; b < per * n_mat;
+         b += (uint64_t)gridDim.x * blockDim.x) {
+        const uint32_t m = uint32_t(b / per);
+        const uint64_t bi = b - uint64_t(m) * per;
+        const float amax = __uint_as_float(amax_bits[m]);
+        const float s_t = amax == 0.f ? 1.f : __fdiv_rn(amax, 2688.0f);
+        if (bi == 0) tscale[m] = s_t;
+        const uint16_t* src = w + uint64_t(m) * R * K + bi * 16;
+        float v[16], amax_b = 0.f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            v[k] = __uint_as_float(uint32_t(src[k]) << 16);
+            amax_b = fmaxf(amax_b, fabsf(v[k]));
+        }
+        const float denom = __fmul_rn(6.0f, s_t);
+        const uint8_t sb = e4m3_encode_rn_sat(__fdiv_rn(amax_b, denom));
+        const float scale = __fmul_rn(e4m3_decode_f32(sb), s_t);
+        const float safe = scale > 0.f ? scale : 1.f;
+        uint8_t* pk = packed + uint64_t(m) * R * (K / 2) + bi * 8;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint8_t q0 = scale > 0.f ? e2m1_encode_rn(__fdiv_rn(v[2 * k], safe)) : 0;
+            const uint8_t q1 = scale > 0.f ? e2m1_encode_rn(__fdiv_rn(v[2 * k + 1], safe)) : 0;
+            pk[k] = uint8_t(q0 | (q1 << 4));
+        }
+        scales[uint64_t(m) * per + bi] = sb;
+    }
+}
+
 int grid_for(uint64_t items) {
     uint64_t g = (items + 255) / 256;
     if (g > 148ull * 64) g = 148ull * 64;
@@ -126,5 +227,20 @@ SYNTH_API int synth_fill_normal_f32(float* dst, uint64_t n, uint32_t seed, uint3
                                     double std_, cudaStream_t s) {
     if (!dst || n == 0) return 1;
     fill_normal_f32_kernel<<<grid_for((n + 1) / 2), 256, 0, s>>>(dst, n, stream_key(seed, layer, tensor), std_);
+    return cudaGetLastError() == cudaSuccess ? 0 : 2;
+}
+
+// NVFP4 encoding of n_mat bf16 matrices [R][K] stored one after another:
+// packed [n_mat][R][K/2], scales [n_mat][R][K/16], tscale [n_mat].
+// amax_scratch: n_mat uint32 of device memory (overwritten).
+SYNTH_API int synth_nvfp4_quantize(const void* w, uint32_t n_mat, uint32_t R, uint32_t K, void* packed,
+                                   void* scales, float* tscale, uint32_t* amax_scratch, cudaStream_t s) {
+    if (!w || !packed || !scales || !tscale || !amax_scratch || n_mat == 0 || R == 0 || K % 16) return 1;
+    if (cudaMemsetAsync(amax_scratch, 0, n_mat * sizeof(uint32_t), s) != cudaSuccess) return 2;
+    amax_kernel<<<dim3(64, n_mat), 256, 0, s>>>(static_cast<const uint16_t*>(w), uint64_t(R) * K, amax_scratch);
+    const uint64_t blocks = uint64_t(n_mat) * R * (K / 16);
+    nvfp4_quant_kernel<<<grid_for(blocks), 256, 0, s>>>(static_cast<const uint16_t*>(w), n_mat, R, K, amax_scratch,
+                                                         static_cast<uint8_t*>(packed),
+                                                         static_cast<uint8_t*>(scales), tscale);
     return cudaGetLastError() == cudaSuccess ? 0 : 2;
 }

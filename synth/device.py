@@ -44,6 +44,10 @@ def _load():
         lib.synth_fill_normal_f32.restype = ctypes.c_int
         lib.synth_fill_normal_f32.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32,
                                               ctypes.c_uint32, ctypes.c_double, ctypes.c_void_p]
+        lib.synth_nvfp4_quantize.restype = ctypes.c_int
+        lib.synth_nvfp4_quantize.argtypes = [ctypes.c_void_p, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32,
+                                             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                             ctypes.c_void_p]
         _lib = lib
     return _lib
 
@@ -123,3 +127,50 @@ class LayerWeights:
 
     def bias_host(self):
         return None if self.router_b is None else self.router_b.cpu().numpy()
+
+
+def nvfp4_quantize(w, stream=None):
+    """NVFP4 encoding (as synth.gen.nvfp4_quantize) of a bf16 CUDA tensor
+    [n][R][K] (or [R][K]): returns (packed uint8 [n][R][K/2], scales uint8
+    [n][R][K/16], tensor scales float32 [n]) as CUDA tensors."""
+    import torch
+    assert w.is_cuda and w.dtype == torch.bfloat16 and w.is_contiguous()
+    w3 = w if w.dim() == 3 else w.unsqueeze(0)
+    n, R, K = w3.shape
+    packed = torch.empty((n, R, K // 2), dtype=torch.uint8, device=w.device)
+    scales = torch.empty((n, R, K // 16), dtype=torch.uint8, device=w.device)
+    ts = torch.empty((n,), dtype=torch.float32, device=w.device)
+    scratch = torch.empty((n,), dtype=torch.int32, device=w.device)
+    rc = _load().synth_nvfp4_quantize(ctypes.c_void_p(w3.data_ptr()), n, R, K, ctypes.c_void_p(packed.data_ptr()),
+                                      ctypes.c_void_p(scales.data_ptr()), ctypes.c_void_p(ts.data_ptr()),
+                                      ctypes.c_void_p(scratch.data_ptr()), _stream_ptr(stream))
+    if rc != 0:
+        raise RuntimeError(f"synth_nvfp4_quantize failed ({rc})")
+    return packed, scales, ts
+
+
+class LayerNVFP4:
+    """A layer's expert weights in NVFP4, quantised on the device from a
+    bf16 layer (synth.device.LayerWeights); the router stays bf16 (borrowed
+    from the bf16 layer, which must stay alive while this object is used
+    for the router)."""
+
+    def __init__(self, lw):
+        self.E = lw.E
+        self.router_W, self.router_b = lw.router_W, lw.router_b
+        self._router_bits, self._bias = None, None
+        self.gu = nvfp4_quantize(lw.gate_up)     # ([257][1024][1024], [257][1024][128], [257])
+        self.dn = nvfp4_quantize(lw.down)        # ([257][2048][256], [257][2048][32], [257])
+        self.ts_gu = self.gu[2].cpu().numpy()
+        self.ts_dn = self.dn[2].cpu().numpy()
+
+    def create_args(self):
+        """(gate_up entries, down entries, shared entries) for flint_moe_create(dtype=FLINT_NVFP4)."""
+        gu = [(self.gu[0][e], self.gu[1][e], float(self.ts_gu[e])) for e in range(self.E + 1)]
+        dn = [(self.dn[0][e], self.dn[1][e], float(self.ts_dn[e])) for e in range(self.E + 1)]
+        return gu[:self.E], dn[:self.E], (gu[self.E], dn[self.E])
+
+    def expert_parts(self, e: int):
+        """Host copies ((packed, scales, ts) of gate_up, same of down) of expert e."""
+        return ((self.gu[0][e].cpu().numpy(), self.gu[1][e].cpu().numpy(), self.ts_gu[e]),
+                (self.dn[0][e].cpu().numpy(), self.dn[1][e].cpu().numpy(), self.ts_dn[e]))

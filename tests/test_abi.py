@@ -67,3 +67,17 @@ def test_kernel_event_hook_rejects_bad_arguments():
     from sparse_moe_transformer_03_b300 import flint
     lib = flint.load_library()
     assert lib.flint_moe_set_kernel_events(None, 1, None, None) == 1       # null handle
+
+
+def test_nvfp4_create_rejects_null_parts():
+    """NVFP4 entries with a null code or scale pointer are rejected before any device call."""
+    import ctypes
+    from sparse_moe_transformer_03_b300 import flint
+    lib = flint.load_library()
+    bad = flint.flint_nvfp4_t(None, None, 1.0)
+    ok = flint.flint_nvfp4_t(16, 16, 1.0)       # non-null placeholders, never dereferenced on the device
+    entries = (ctypes.c_void_p * 256)(*([ctypes.addressof(ok)] * 255 + [ctypes.addressof(bad)]))
+    shared = (ctypes.c_void_p * 2)(ctypes.addressof(ok), ctypes.addressof(ok))
+    h = ctypes.c_void_p()
+    rc = lib.flint_moe_create(ctypes.byref(h), ctypes.c_void_p(16), None, entries, entries, shared, 1)
+    assert rc == 1 and not h.value
