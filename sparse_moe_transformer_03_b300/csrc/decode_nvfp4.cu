@@ -368,7 +368,7 @@ constexpr int DV_AROW = I * 2 + 16;    // bytes per staged row (+16: conflict-fr
 struct DownNvParams {
     const uint8_t* nv;
     const float* ts;
-    const DecodeTables* tables;
+    const float* logits;          // [T][E] router logits (final before this kernel starts)
     const __nv_bfloat16* a;       // [pairs][I] bf16
     __nv_bfloat16* y;             // [T][H]
     int ns;                       // ring chunks per warp
@@ -383,7 +383,8 @@ __host__ __device__ inline bool dv_staged(int T) { return (TOPK + 1) * T <= DV_A
 
 static inline size_t dv_smem_bytes(int T) {
     return (size_t)DV_WARPS * dv_ns(T) * NV_CHUNK + (dv_staged(T) ? (size_t)(TOPK + 1) * T * DV_AROW : 0) +
-           (size_t)DV_WARPS * T * 16 * 4 + (DV_WARPS * dv_ns(T) + 1) * 8 + sizeof(DecodeTables);
+           (size_t)DV_WARPS * T * 16 * 4 + (DV_WARPS * dv_ns(T) + 1) * 8 + sizeof(DecodeTables) +
+           DEC_T * TOPK * 8 + 2 * E * 4;
 }
 
 __global__ void __launch_bounds__(DV_WARPS * 32, 1) down_nvfp4_kernel(DownNvParams p) {
@@ -399,46 +400,59 @@ __global__ void __launch_bounds__(DV_WARPS * 32, 1) down_nvfp4_kernel(DownNvPara
     uint64_t* bar = bars + warp * NS;
     uint64_t* abar = bars + DV_WARPS * NS;
     DecodeTables* tab = reinterpret_cast<DecodeTables*>(abar + 1);
+    int* sel_e = reinterpret_cast<int*>(tab + 1);
+    float* sel_w = reinterpret_cast<float*>(sel_e + DEC_T * TOPK);
+    uint32_t* tmask = reinterpret_cast<uint32_t*>(sel_w + DEC_T * TOPK);
+    int* pair0 = reinterpret_cast<int*>(tmask + E);
 
     if (lane == 0) {
         for (int s = 0; s < NS; ++s) mbar_init(&bar[s], 1);
         if (warp == 0) mbar_init(abar, 1);
         fence_mbar_init();
     }
-    __syncthreads();
     auto issue = [&](int i, int expert) {
         const int s = i % NS;
         const uint8_t* src = p.nv + (size_t)expert * NV_EXPERT_BYTES + NV_GU_BYTES + (size_t)c * NV_CHUNK;
         mbar_arrive_expect_tx(&bar[s], NV_CHUNK);
         bulk_g2s(ring + (size_t)s * NV_CHUNK, src, NV_CHUNK, &bar[s]);
     };
-    // slot 0 (the shared expert) belongs to warp 0 and does not depend on the routing
-    int issued = 0;
-    if (warp == 0 && lane == 0) {
-        issue(0, SHARED);
-        issued = 1;
-    }
-    pdl_wait();     // the gate/up kernel is complete: tables and activations are visible
-    pdl_trigger();
-    {
-        const int* src = reinterpret_cast<const int*>(p.tables);
-        int* dst = reinterpret_cast<int*>(tab);
-        for (int k = threadIdx.x; k < (int)(sizeof(DecodeTables) / 4); k += blockDim.x) dst[k] = __ldcg(src + k);
+    // Every gate/up CTA triggers this launch only after its own dependency
+    // wait, which returns once the router grid has completed: the logits are
+    // final here although the gate/up kernel may still be running.  Select
+    // each token's experts and build the same tables the gate/up kernel
+    // builds, and start the weight chunks of this warp's first slots now, so
+    // they stream while the gate/up kernel runs.
+    for (int t = warp; t < Tk; t += DV_WARPS) {
+        float v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = __ldcg(p.logits + (size_t)t * E + lane + 32 * k);
+        int sel[TOPK];
+        float wt[TOPK];
+        warp_top6(v, lane, sel, wt);
+        if (lane < TOPK) {
+            sel_e[t * TOPK + lane] = pick6(sel, lane);
+            sel_w[t * TOPK + lane] = pick6(wt, lane);
+        }
     }
     for (int k = threadIdx.x; k < DV_WARPS * Tk * 16; k += blockDim.x) yw_all[k] = 0.f;
     __syncthreads();
+    if (warp == 0) build_decode_tables_warp(Tk, sel_e, sel_w, tmask, pair0, tab, lane);
+    __syncthreads();
     const int n_slots = tab->n_slots, n_pairs = tab->n_pairs;
+    const int my_slots = n_slots > warp ? (n_slots - warp + DV_WARPS - 1) / DV_WARPS : 0;
+    int issued = 0;
+    if (lane == 0) {
+        for (int i = 0; i < NS && i < my_slots; ++i) {
+            issue(i, tab->slot_expert[warp + DV_WARPS * i]);
+            issued = i + 1;
+        }
+    }
+    pdl_wait();     // the gate/up kernel is complete: activations are visible
+    pdl_trigger();
     if (staged && threadIdx.x == 0) {
         // every activation row, one bulk copy per row (padded rows in smem)
         mbar_arrive_expect_tx(abar, n_pairs * I * 2);
         for (int pr = 0; pr < n_pairs; ++pr) bulk_g2s(astage + (size_t)pr * DV_AROW, p.a + (size_t)pr * I, I * 2, abar);
-    }
-    const int my_slots = n_slots > warp ? (n_slots - warp + DV_WARPS - 1) / DV_WARPS : 0;
-    if (lane == 0) {
-        for (int i = issued; i < NS && i < my_slots; ++i) {
-            issue(i, tab->slot_expert[warp + DV_WARPS * i]);
-            issued = i + 1;
-        }
     }
     bool ok = true;
     if (staged && my_slots > 0) ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(abar, 0, p.limit_ns));
@@ -559,7 +573,7 @@ cudaError_t launch_decode_experts_nvfp4(const LaunchCtx& L, const uint8_t* nv, c
     cudaError_t e = launch_hooked(L, FLINT_KERNEL_GATE_UP, gateup_nvfp4_kernel, dim3(L.num_sms),
                                   dim3(GN_WARPS * 32), gn_smem_bytes(T), gp);
     if (e != cudaSuccess) return e;
-    DownNvParams dp{nv, nv_ts, tables, a16, y, dv_ns(T), T, L.status, L.wait_limit_ns};
+    DownNvParams dp{nv, nv_ts, logits, a16, y, dv_ns(T), T, L.status, L.wait_limit_ns};
     return launch_hooked(L, FLINT_KERNEL_DOWN, down_nvfp4_kernel, dim3(DV_CTAS), dim3(DV_WARPS * 32),
                          dv_smem_bytes(T), dp);
 }
