@@ -1,0 +1,496 @@
+// decode_mma.cu -- bf16 weight-streaming decode kernels on the warp-level
+// tensor core (mma.sync m16n8k16), for batches where the CUDA-core kernels of
+// decode.cu turn compute-bound (each weight meets several tokens: every
+// token multiplies the shared expert, and tokens of one cluster share
+// routed experts).
+//
+// They read the handle's tiled copy of the experts (repack.cu): tiles of 128
+// rows x 64 columns in the 128-byte-swizzled layout.  Eight consecutive rows
+// of a tile are 1 KiB of contiguous bytes, so a unit's operands arrive by
+// cp.async.bulk in 1 KiB (gate/up) or 2 KiB (down) pieces, and ldmatrix
+// reads them without bank conflicts (the swizzle spreads the eight rows of an
+// 8x8 matrix over all banks).
+//
+//   gateup_mma   Unit = 8 gate rows + the 8 matching up rows of one expert
+//                (the MMA's 16 rows), K = 2048 in 8 chunks of 256 columns
+//                (8 KiB) streamed into a per-warp ring; the expert's tokens
+//                are the N columns (tiles of 8), x is bf16 staged in smem.
+//                Each lane ends with
+//                gate and up of the same (row, token): a = silu(g) * u is
+//                formed in registers and written as bf16.
+//   down_mma     CTA c owns output rows 16c .. 16c + 15 (one M tile); warp w
+//                takes expert slots w, w + 8, ..., each 2 chunks of 256
+//                columns (4 pieces of 2 KiB); the activations are staged in
+//                smem when the batch has at most 64 (token, expert) pairs; w *
+//                D accumulates per (token, row) in the warp's own buffer and
+//                the eight buffers are summed in warp order: deterministic.
+//
+// Routing and tables are those of decode.cu; like the NVFP4 down kernel, the
+// down kernel routes for itself and starts its weight chunks before waiting
+// on the gate/up kernel.
+#include "flint_common.cuh"
+#include "../../include/flint_moe.h"
+#include "flint_internal.h"
+#include "mma_sync.cuh"
+#include "routing.cuh"
+
+namespace flint {
+
+constexpr size_t MM_TILE = 16384;                         // one 128 x 64 bf16 tile
+constexpr size_t MM_EXPERT_BYTES = (size_t)3 * H * I * 2; // one expert in the tiled copy
+constexpr size_t MM_DOWN_OFF = (size_t)2 * I * H * 2;     // its down tiles follow the gate/up tiles
+constexpr int MM_GU_KT = H / 64;                          // 32 column tiles per gate/up row block
+constexpr int MM_DN_KT = I / 64;                          // 8 column tiles per down row block
+constexpr int MM_CHUNK = 8192;
+constexpr int MM_WARPS = 8;
+
+// ---------------------------------------------------------------------------
+// gate/up + SwiGLU
+// ---------------------------------------------------------------------------
+
+constexpr int MG_UNITS = I / 8;          // 64 units per expert
+constexpr int MG_CHUNKS = H / 256;       // 8 chunks per unit
+constexpr int MG_XROW = H + 8;           // bf16 per staged x row (+8: conflict-free B loads)
+constexpr int MG_XSMEM_T = 32;           // x is staged in smem up to this many tokens
+
+struct GateUpMmaParams {
+    const uint8_t* tiled;         // the handle's tiled experts
+    const float* logits;
+    const __nv_bfloat16* x;
+    int T;
+    int ns;
+    DecodeTables* tables_out;
+    int32_t* idx_out;
+    float* w_out;
+    __nv_bfloat16* a;             // [pairs][I]
+    uint32_t* status;
+    uint64_t limit_ns;
+};
+
+static inline int mg_ns(int T) { return T <= 16 ? 2 : 1; }
+static inline size_t mg_smem_bytes(int T) {
+    return (size_t)MM_WARPS * mg_ns(T) * MM_CHUNK + (T <= MG_XSMEM_T ? (size_t)T * MG_XROW * 2 : 0) +
+           (size_t)MM_WARPS * mg_ns(T) * 8 + sizeof(DecodeTables) + DEC_T * TOPK * 8 + 2 * E * 4;
+}
+
+__global__ void __launch_bounds__(MM_WARPS * 32, 1) gateup_mma_kernel(GateUpMmaParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int NS = p.ns, T = p.T, G = gridDim.x, c = blockIdx.x;
+    const bool xs_on = T <= MG_XSMEM_T;
+    uint8_t* ring = smem + (size_t)warp * NS * MM_CHUNK;
+    __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(smem + (size_t)MM_WARPS * NS * MM_CHUNK);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(xs) +
+                                                 (xs_on ? (size_t)T * MG_XROW * 2 : 0));
+    uint64_t* bar = bars + warp * NS;
+    DecodeTables* tab = reinterpret_cast<DecodeTables*>(bars + MM_WARPS * NS);
+    int* sel_e = reinterpret_cast<int*>(tab + 1);
+    float* sel_w = reinterpret_cast<float*>(sel_e + DEC_T * TOPK);
+    uint32_t* tmask = reinterpret_cast<uint32_t*>(sel_w + DEC_T * TOPK);
+    int* pair0 = reinterpret_cast<int*>(tmask + E);
+
+    if (lane == 0) {
+        for (int s = 0; s < NS; ++s) mbar_init(&bar[s], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    auto unit_of = [&](int i) { return c + G * (warp + MM_WARPS * i); };
+    // chunk ci of the warp: unit ci / 8, columns 256 (ci % 8) .. + 255
+    auto issue = [&](int ci, int expert) {
+        const int q = unit_of(ci >> 3), r = q & (MG_UNITS - 1), s = ci % NS;
+        const uint8_t* base = p.tiled + (size_t)expert * MM_EXPERT_BYTES + (size_t)(r & 15) * 1024;
+        const int rbg = r >> 4, kc0 = (ci & (MG_CHUNKS - 1)) * 4;
+        uint8_t* dst = ring + (size_t)s * MM_CHUNK;
+        mbar_arrive_expect_tx(&bar[s], MM_CHUNK);
+#pragma unroll
+        for (int kt = 0; kt < 4; ++kt) {
+            bulk_g2s(dst + (2 * kt) * 1024, base + ((size_t)rbg * MM_GU_KT + kc0 + kt) * MM_TILE, 1024, &bar[s]);
+            bulk_g2s(dst + (2 * kt + 1) * 1024, base + ((size_t)(4 + rbg) * MM_GU_KT + kc0 + kt) * MM_TILE, 1024,
+                     &bar[s]);
+        }
+    };
+
+    // ---- before the router has finished: the shared expert's chunks ----
+    int issued = 0;
+    if (lane == 0) {
+        for (int ci = 0; ci < NS && unit_of(ci >> 3) < MG_UNITS; ++ci) {
+            issue(ci, SHARED);
+            issued = ci + 1;
+        }
+    }
+    pdl_wait();     // router logits are complete (and x is ready)
+    pdl_trigger();
+
+    if (xs_on) {
+        for (int k = threadIdx.x; k < T * (H / 8); k += blockDim.x) {
+            const int t = k / (H / 8), col = (k % (H / 8)) * 8;
+            *reinterpret_cast<uint4*>(xs + (size_t)t * MG_XROW + col) = ldg16(p.x + (size_t)t * H + col);
+        }
+    }
+
+    // ---- top-6 of every token, then the (slot, token) tables ----
+    for (int t = warp; t < T; t += MM_WARPS) {
+        float v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = __ldcg(p.logits + (size_t)t * E + lane + 32 * k);
+        int sel[TOPK];
+        float wt[TOPK];
+        warp_top6(v, lane, sel, wt);
+        if (lane < TOPK) {
+            const int se = pick6(sel, lane);
+            const float sw = pick6(wt, lane);
+            sel_e[t * TOPK + lane] = se;
+            sel_w[t * TOPK + lane] = sw;
+            if (c == 0) {
+                p.idx_out[t * TOPK + lane] = se;
+                p.w_out[t * TOPK + lane] = sw;
+            }
+        }
+    }
+    __syncthreads();
+    if (warp == 0) build_decode_tables_warp(T, sel_e, sel_w, tmask, pair0, tab, lane);
+    __syncthreads();
+    if (c == 0) {
+        const int* src = reinterpret_cast<const int*>(tab);
+        int* dst = reinterpret_cast<int*>(p.tables_out);
+        for (int k = threadIdx.x; k < (int)(sizeof(DecodeTables) / 4); k += blockDim.x) dst[k] = src[k];
+    }
+    const int total_units = tab->n_slots * MG_UNITS;
+    int my_units = 0;
+    while (unit_of(my_units) < total_units) ++my_units;
+    const int total_chunks = my_units * MG_CHUNKS;
+    if (lane == 0) {
+        for (int ci = issued; ci < NS && ci < total_chunks; ++ci) {
+            issue(ci, tab->slot_expert[unit_of(ci >> 3) / MG_UNITS]);
+            issued = ci + 1;
+        }
+    }
+
+    // this lane's ldmatrix row: matrix mi = lane / 8 (bit 0: gate / up piece,
+    // bit 1: columns 0-7 / 8-15 of the block), row i = lane % 8
+    const int mi = lane >> 3, li = lane & 7;
+    const uint32_t lrow = (uint32_t)((mi & 1) * 1024 + li * 128);
+    const int lkh = mi >> 1;
+    const int g = lane >> 2, cq = lane & 3;
+    bool ok = true;
+    int ci = 0;
+    for (int i = 0; ok && i < my_units; ++i) {
+        const int q = unit_of(i), u = q / MG_UNITS, r = q & (MG_UNITS - 1);
+        const int pb = tab->slot_pair0[u], np = tab->slot_pair0[u + 1] - pb;   // 1..32 tokens
+        const int ntile = (np + 7) >> 3;
+        const __nv_bfloat16* xb[4];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+            const int n = nt * 8 + g;
+            const int t = tab->pair_token[pb + (n < np ? n : np - 1)];
+            xb[nt] = (xs_on ? xs + (size_t)t * MG_XROW : p.x + (size_t)t * H) + 2 * cq;
+        }
+        float acc[4][4], acc2[4][4];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) acc[nt][k] = acc2[nt][k] = 0.f;
+        for (int qq = 0; qq < MG_CHUNKS; ++qq, ++ci) {
+            const int s = ci % NS;
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(&bar[s], (ci / NS) & 1, p.limit_ns))) {
+                ok = false;
+                break;
+            }
+            const uint8_t* buf = ring + (size_t)s * MM_CHUNK;
+#pragma unroll 2
+            for (int kb = 0; kb < 16; kb += 2) {
+                // K block kb: column tile kb / 4, 16-byte chunks 2 (kb % 4) + {0, 1}
+                uint32_t a[4], a2[4];
+                const int kt = kb >> 2, j0 = 2 * (kb & 3) + lkh;
+                ldmatrix_x4(a, buf + kt * 2048 + lrow + ((j0 ^ li) << 4));
+                ldmatrix_x4(a2, buf + kt * 2048 + lrow + (((j0 + 2) ^ li) << 4));
+                const int kx = qq * 256 + kb * 16;
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt) {
+                    if (nt < ntile) {
+                        const __nv_bfloat16* xp = xb[nt] + kx;
+                        uint32_t b0, b1, b2, b3;
+                        if (xs_on) {
+                            b0 = *reinterpret_cast<const uint32_t*>(xp);
+                            b1 = *reinterpret_cast<const uint32_t*>(xp + 8);
+                            b2 = *reinterpret_cast<const uint32_t*>(xp + 16);
+                            b3 = *reinterpret_cast<const uint32_t*>(xp + 24);
+                        } else {
+                            b0 = __ldg(reinterpret_cast<const unsigned int*>(xp));
+                            b1 = __ldg(reinterpret_cast<const unsigned int*>(xp + 8));
+                            b2 = __ldg(reinterpret_cast<const unsigned int*>(xp + 16));
+                            b3 = __ldg(reinterpret_cast<const unsigned int*>(xp + 24));
+                        }
+                        mma_bf16_16816(acc[nt], a, b0, b1);
+                        mma_bf16_16816(acc2[nt], a2, b2, b3);
+                    }
+                }
+            }
+            __syncwarp();   // every lane is done reading slot s
+            if (lane == 0 && ci + NS < total_chunks) {
+                fence_proxy_async_smem();
+                issue(ci + NS, tab->slot_expert[unit_of((ci + NS) >> 3) / MG_UNITS]);
+                issued = ci + NS + 1;
+            }
+        }
+        if (!ok) break;
+        const int j = 8 * r + g;
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int n = nt * 8 + 2 * cq + hh;
+                if (nt < ntile && n < np) {
+                    const float gv = acc[nt][hh] + acc2[nt][hh], uv = acc[nt][2 + hh] + acc2[nt][2 + hh];
+                    p.a[(size_t)(pb + n) * I + j] = __float2bfloat16_rn(silu_f(gv) * uv);
+                }
+            }
+        }
+    }
+    if (!ok) {
+        if (lane == 0) {
+            report_status(p.status, ST_TIMEOUT);
+            for (int k = ci; k < issued; ++k) mbar_wait_bounded(&bar[k % NS], (k / NS) & 1, p.limit_ns);
+        }
+        __syncwarp();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// down projection + weighted combine
+// ---------------------------------------------------------------------------
+
+constexpr int MD_CTAS = H / 16;          // 128
+constexpr int MD_APAIRS = 64;            // activation rows staged in smem up to this many pairs
+constexpr int MD_AROW = I * 2 + 16;      // bytes per staged row
+
+struct DownMmaParams {
+    const uint8_t* tiled;
+    const float* logits;          // [T][E] (final before this kernel starts)
+    const __nv_bfloat16* a;       // [pairs][I]
+    __nv_bfloat16* y;
+    int ns;
+    int T;
+    uint32_t* status;
+    uint64_t limit_ns;
+};
+
+static inline int md_ns(int T) { return T <= 9 ? 2 : 3; }
+__host__ __device__ inline bool md_staged(int T) { return (TOPK + 1) * T <= MD_APAIRS; }
+static inline size_t md_smem_bytes(int T) {
+    return (size_t)MM_WARPS * md_ns(T) * MM_CHUNK + (md_staged(T) ? (size_t)(TOPK + 1) * T * MD_AROW : 0) +
+           (size_t)MM_WARPS * T * 16 * 4 + (MM_WARPS * md_ns(T) + 1) * 8 + sizeof(DecodeTables) +
+           DEC_T * TOPK * 8 + 2 * E * 4;
+}
+
+__global__ void __launch_bounds__(MM_WARPS * 32, 1) down_mma_kernel(DownMmaParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c = blockIdx.x, NS = p.ns, Tk = p.T;
+    const bool staged = md_staged(Tk);
+    uint8_t* ring = smem + (size_t)warp * NS * MM_CHUNK;
+    uint8_t* astage = smem + (size_t)MM_WARPS * NS * MM_CHUNK;
+    float* yw_all = reinterpret_cast<float*>(astage + (staged ? (size_t)(TOPK + 1) * Tk * MD_AROW : 0));
+    float* yw = yw_all + warp * Tk * 16;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(yw_all + MM_WARPS * Tk * 16);
+    uint64_t* bar = bars + warp * NS;
+    uint64_t* abar = bars + MM_WARPS * NS;
+    DecodeTables* tab = reinterpret_cast<DecodeTables*>(abar + 1);
+    int* sel_e = reinterpret_cast<int*>(tab + 1);
+    float* sel_w = reinterpret_cast<float*>(sel_e + DEC_T * TOPK);
+    uint32_t* tmask = reinterpret_cast<uint32_t*>(sel_w + DEC_T * TOPK);
+    int* pair0 = reinterpret_cast<int*>(tmask + E);
+
+    if (lane == 0) {
+        for (int s = 0; s < NS; ++s) mbar_init(&bar[s], 1);
+        if (warp == 0) mbar_init(abar, 1);
+        fence_mbar_init();
+    }
+    // chunk ci of the warp: slot ci / 2, columns 256 (ci % 2) .. + 255 of rows 16c .. 16c + 15
+    auto issue = [&](int ci, int expert) {
+        const int s = ci % NS;
+        const uint8_t* base = p.tiled + (size_t)expert * MM_EXPERT_BYTES + MM_DOWN_OFF + (size_t)(c & 7) * 2048;
+        const int rb = c >> 3, kc0 = (ci & 1) * 4;
+        uint8_t* dst = ring + (size_t)s * MM_CHUNK;
+        mbar_arrive_expect_tx(&bar[s], MM_CHUNK);
+#pragma unroll
+        for (int kt = 0; kt < 4; ++kt)
+            bulk_g2s(dst + kt * 2048, base + ((size_t)rb * MM_DN_KT + kc0 + kt) * MM_TILE, 2048, &bar[s]);
+    };
+    // The router grid completed before any gate/up CTA passed its dependency
+    // wait, and this launch is triggered only after those waits: the logits
+    // are final here.  Route for ourselves and start the weight chunks while
+    // the gate/up kernel still runs.
+    for (int t = warp; t < Tk; t += MM_WARPS) {
+        float v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = __ldcg(p.logits + (size_t)t * E + lane + 32 * k);
+        int sel[TOPK];
+        float wt[TOPK];
+        warp_top6(v, lane, sel, wt);
+        if (lane < TOPK) {
+            sel_e[t * TOPK + lane] = pick6(sel, lane);
+            sel_w[t * TOPK + lane] = pick6(wt, lane);
+        }
+    }
+    for (int k = threadIdx.x; k < MM_WARPS * Tk * 16; k += blockDim.x) yw_all[k] = 0.f;
+    __syncthreads();
+    if (warp == 0) build_decode_tables_warp(Tk, sel_e, sel_w, tmask, pair0, tab, lane);
+    __syncthreads();
+    const int n_slots = tab->n_slots, n_pairs = tab->n_pairs;
+    const int my_slots = n_slots > warp ? (n_slots - warp + MM_WARPS - 1) / MM_WARPS : 0;
+    const int total_chunks = 2 * my_slots;
+    int issued = 0;
+    if (lane == 0) {
+        for (int ci = 0; ci < NS && ci < total_chunks; ++ci) {
+            issue(ci, tab->slot_expert[warp + MM_WARPS * (ci >> 1)]);
+            issued = ci + 1;
+        }
+    }
+    pdl_wait();     // the gate/up kernel is complete: activations are visible
+    pdl_trigger();
+    if (staged && threadIdx.x == 0) {
+        mbar_arrive_expect_tx(abar, n_pairs * I * 2);
+        for (int pr = 0; pr < n_pairs; ++pr) bulk_g2s(astage + (size_t)pr * MD_AROW, p.a + (size_t)pr * I, I * 2, abar);
+    }
+    bool ok = true;
+    if (staged && my_slots > 0) ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(abar, 0, p.limit_ns));
+
+    const int mi = lane >> 3, li = lane & 7;
+    const int lr = (mi & 1) * 8 + li;               // row 0..15 of the M tile
+    const uint32_t lrow = (uint32_t)lr * 128;
+    const int lkh = mi >> 1;
+    const int g = lane >> 2, cq = lane & 3;
+    int ci = 0, i = 0;
+    for (; ok && i < my_slots; ++i) {
+        const int u = warp + MM_WARPS * i;
+        const int pb = tab->slot_pair0[u], np = tab->slot_pair0[u + 1] - pb;
+        const int ntile = (np + 7) >> 3;
+        int prow[4];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+            const int n = nt * 8 + g;
+            prow[nt] = pb + (n < np ? n : np - 1);
+        }
+        float acc[4][4];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+        for (int hk = 0; hk < 2; ++hk, ++ci) {
+            const int s = ci % NS;
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(&bar[s], (ci / NS) & 1, p.limit_ns))) {
+                ok = false;
+                break;
+            }
+            const uint8_t* buf = ring + (size_t)s * MM_CHUNK;
+            if (staged) {
+#pragma unroll 4
+                for (int kb = 0; kb < 16; ++kb) {
+                    uint32_t a[4];
+                    const int kt = kb >> 2, j = 2 * (kb & 3) + lkh;
+                    ldmatrix_x4(a, buf + kt * 2048 + lrow + ((j ^ li) << 4));
+                    const int kx = hk * 256 + kb * 16 + 2 * cq;
+#pragma unroll
+                    for (int nt = 0; nt < 4; ++nt) {
+                        if (nt < ntile) {
+                            const uint8_t* ar = astage + (size_t)prow[nt] * MD_AROW + kx * 2;
+                            mma_bf16_16816(acc[nt], a, *reinterpret_cast<const uint32_t*>(ar),
+                                           *reinterpret_cast<const uint32_t*>(ar + 16));
+                        }
+                    }
+                }
+            } else {
+                // activations through L1 (read-only here; written by the previous
+                // grid): the first N tile's operands for the whole chunk are
+                // requested at once, the other tiles' four blocks at a time
+                uint32_t bq[16][2];
+                const unsigned int* a0 =
+                    reinterpret_cast<const unsigned int*>(p.a + (size_t)prow[0] * I + hk * 256 + 2 * cq);
+#pragma unroll
+                for (int kb = 0; kb < 16; ++kb) {
+                    bq[kb][0] = __ldg(a0 + kb * 8);
+                    bq[kb][1] = __ldg(a0 + kb * 8 + 4);
+                }
+#pragma unroll
+                for (int kb = 0; kb < 16; ++kb) {
+                    uint32_t a[4];
+                    const int kt = kb >> 2, j = 2 * (kb & 3) + lkh;
+                    ldmatrix_x4(a, buf + kt * 2048 + lrow + ((j ^ li) << 4));
+                    mma_bf16_16816(acc[0], a, bq[kb][0], bq[kb][1]);
+                    const int kx = hk * 256 + kb * 16 + 2 * cq;
+#pragma unroll
+                    for (int nt = 1; nt < 4; ++nt) {
+                        if (nt < ntile) {
+                            const unsigned int* ar =
+                                reinterpret_cast<const unsigned int*>(p.a + (size_t)prow[nt] * I + kx);
+                            mma_bf16_16816(acc[nt], a, __ldg(ar), __ldg(ar + 4));
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0 && ci + NS < total_chunks) {
+                fence_proxy_async_smem();
+                issue(ci + NS, tab->slot_expert[warp + MM_WARPS * ((ci + NS) >> 1)]);
+                issued = ci + NS + 1;
+            }
+        }
+        if (!ok) break;
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int n = nt * 8 + 2 * cq + hh;
+                if (nt < ntile && n < np) {
+                    const int pr = pb + n, t = tab->pair_token[pr];
+                    const float wgt = tab->pair_weight[pr];
+                    yw[t * 16 + g] = fmaf(wgt, acc[nt][hh], yw[t * 16 + g]);
+                    yw[t * 16 + g + 8] = fmaf(wgt, acc[nt][2 + hh], yw[t * 16 + g + 8]);
+                }
+            }
+        }
+    }
+    if (!ok && lane == 0) {
+        report_status(p.status, ST_TIMEOUT);
+        for (int k = ci; k < issued; ++k) mbar_wait_bounded(&bar[k % NS], (k / NS) & 1, p.limit_ns);
+        if (staged && warp == 0) mbar_wait_bounded(abar, 0, p.limit_ns);
+    }
+    __syncthreads();
+    for (int k = threadIdx.x; k < Tk * 16; k += blockDim.x) {
+        const int t = k >> 4, rr = k & 15;
+        float sum = 0.f;
+#pragma unroll
+        for (int w = 0; w < MM_WARPS; ++w) sum += yw_all[w * Tk * 16 + t * 16 + rr];
+        p.y[(size_t)t * H + 16 * c + rr] = __float2bfloat16_rn(sum);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+cudaError_t decode_mma_set_attributes() {
+    size_t gmax = 0, dmax = 0;
+    for (int T = 1; T <= DEC_T; ++T) {
+        gmax = mg_smem_bytes(T) > gmax ? mg_smem_bytes(T) : gmax;
+        dmax = md_smem_bytes(T) > dmax ? md_smem_bytes(T) : dmax;
+    }
+    cudaError_t e = cudaFuncSetAttribute(gateup_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gmax);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(down_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dmax);
+}
+
+cudaError_t launch_decode_experts_mma(const LaunchCtx& L, const uint8_t* tiled, const float* logits,
+                                      const __nv_bfloat16* x, int T, DecodeTables* tables, int32_t* idx, float* w,
+                                      float* a_buf, __nv_bfloat16* y) {
+    __nv_bfloat16* a16 = reinterpret_cast<__nv_bfloat16*>(a_buf);
+    GateUpMmaParams gp{tiled, logits, x, T, mg_ns(T), tables, idx, w, a16, L.status, L.wait_limit_ns};
+    cudaError_t e = launch_hooked(L, FLINT_KERNEL_GATE_UP, gateup_mma_kernel, dim3(L.num_sms), dim3(MM_WARPS * 32),
+                                  mg_smem_bytes(T), gp);
+    if (e != cudaSuccess) return e;
+    DownMmaParams dp{tiled, logits, a16, y, md_ns(T), T, L.status, L.wait_limit_ns};
+    return launch_hooked(L, FLINT_KERNEL_DOWN, down_mma_kernel, dim3(MD_CTAS), dim3(MM_WARPS * 32),
+                         md_smem_bytes(T), dp);
+}
+
+}  // namespace flint

@@ -39,6 +39,7 @@
 #include "flint_common.cuh"
 #include "../../include/flint_moe.h"
 #include "flint_internal.h"
+#include "mma_sync.cuh"
 #include "routing.cuh"
 
 namespace flint {
@@ -108,20 +109,6 @@ __device__ __forceinline__ void nv_a_frag(uint32_t codes, uint16_t sc2, uint32_t
         const __half2 r = __hmul2(q, (k & 1) ? s8 : sg);
         a[k] = *reinterpret_cast<const uint32_t*>(&r);
     }
-}
-
-__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 __device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t v) {

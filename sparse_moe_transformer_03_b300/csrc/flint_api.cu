@@ -255,6 +255,7 @@ flint_status_t flint_moe_create(flint_moe_t* out, const void* router_W, const fl
     if (st == FLINT_OK) st = from_cuda(prefill_set_attributes());
     if (st == FLINT_OK) st = from_cuda(decode_set_attributes());
     if (st == FLINT_OK) st = from_cuda(decode_nvfp4_set_attributes());
+    if (st == FLINT_OK) st = from_cuda(decode_mma_set_attributes());
     if (st == FLINT_OK) st = from_cuda(cudaDeviceSynchronize());
     if (st != FLINT_OK) {
         cudaGetLastError();
@@ -293,8 +294,14 @@ flint_status_t flint_moe_forward(flint_moe_t h, const void* x, int T, void* y, c
     }
     if (T <= DEC_T) {
         cudaError_t e = launch_router_logits_decode(L, xs, T, h->router_W, h->router_b, h->logits);
-        if (e == cudaSuccess)
-            e = launch_decode_experts(L, h->dev_tables, h->logits, xs, T, h->dec_tables, h->idx, h->w, h->a_dec, ys);
+        if (e == cudaSuccess) {
+            if (T >= DEC_MMA_MIN_T)
+                e = launch_decode_experts_mma(L, reinterpret_cast<const uint8_t*>(h->tiled), h->logits, xs, T,
+                                              h->dec_tables, h->idx, h->w, h->a_dec, ys);
+            else
+                e = launch_decode_experts(L, h->dev_tables, h->logits, xs, T, h->dec_tables, h->idx, h->w, h->a_dec,
+                                          ys);
+        }
         return from_cuda(e);
     }
     // grouped tensor-core path, chunks of CHUNK tokens

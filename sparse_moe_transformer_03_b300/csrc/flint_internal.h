@@ -111,6 +111,13 @@ cudaError_t launch_decode_experts_nvfp4(const LaunchCtx& L, const uint8_t* nv, c
                                         const float* logits, const __nv_bfloat16* x, int T, DecodeTables* tables,
                                         int32_t* idx, float* w, float* a_buf, __nv_bfloat16* y);
 
+// decode_mma.cu -- bf16 decode on mma.sync, from the tiled copy (T >= DEC_MMA_MIN_T)
+constexpr int DEC_MMA_MIN_T = 5;
+cudaError_t decode_mma_set_attributes();
+cudaError_t launch_decode_experts_mma(const LaunchCtx& L, const uint8_t* tiled, const float* logits,
+                                      const __nv_bfloat16* x, int T, DecodeTables* tables, int32_t* idx, float* w,
+                                      float* a_buf, __nv_bfloat16* y);
+
 // decode.cu
 cudaError_t decode_set_attributes();
 cudaError_t launch_decode_experts(const LaunchCtx& L, const ExpertTables* experts, const float* logits,
