@@ -52,6 +52,7 @@ constexpr int MG_UNITS = I / 8;          // 64 units per expert
 constexpr int MG_CHUNKS = H / 256;       // 8 chunks per unit
 constexpr int MG_XROW = H + 8;           // bf16 per staged x row (+8: conflict-free B loads)
 constexpr int MG_XSMEM_T = 32;           // x is staged in smem up to this many tokens
+constexpr int MG_PF_AHEAD = 3;           // one-chunk ring: chunks up to ci + 3 are prefetched into L2
 
 struct GateUpMmaParams {
     const uint8_t* tiled;         // the handle's tiled experts
@@ -97,17 +98,29 @@ __global__ void __launch_bounds__(MM_WARPS * 32, 1) gateup_mma_kernel(GateUpMmaP
 
     auto unit_of = [&](int i) { return c + G * (warp + MM_WARPS * i); };
     // chunk ci of the warp: unit ci / 8, columns 256 (ci % 8) .. + 255
+    auto chunk_src = [&](int ci, int expert, int kt, int half) {
+        const int q = unit_of(ci >> 3), r = q & (MG_UNITS - 1);
+        const int rb = (r >> 4) + 4 * half, kc = (ci & (MG_CHUNKS - 1)) * 4 + kt;
+        return p.tiled + (size_t)expert * MM_EXPERT_BYTES + ((size_t)rb * MM_GU_KT + kc) * MM_TILE +
+               (size_t)(r & 15) * 1024;
+    };
     auto issue = [&](int ci, int expert) {
-        const int q = unit_of(ci >> 3), r = q & (MG_UNITS - 1), s = ci % NS;
-        const uint8_t* base = p.tiled + (size_t)expert * MM_EXPERT_BYTES + (size_t)(r & 15) * 1024;
-        const int rbg = r >> 4, kc0 = (ci & (MG_CHUNKS - 1)) * 4;
+        const int s = ci % NS;
         uint8_t* dst = ring + (size_t)s * MM_CHUNK;
         mbar_arrive_expect_tx(&bar[s], MM_CHUNK);
 #pragma unroll
         for (int kt = 0; kt < 4; ++kt) {
-            bulk_g2s(dst + (2 * kt) * 1024, base + ((size_t)rbg * MM_GU_KT + kc0 + kt) * MM_TILE, 1024, &bar[s]);
-            bulk_g2s(dst + (2 * kt + 1) * 1024, base + ((size_t)(4 + rbg) * MM_GU_KT + kc0 + kt) * MM_TILE, 1024,
-                     &bar[s]);
+            bulk_g2s(dst + (2 * kt) * 1024, chunk_src(ci, expert, kt, 0), 1024, &bar[s]);
+            bulk_g2s(dst + (2 * kt + 1) * 1024, chunk_src(ci, expert, kt, 1), 1024, &bar[s]);
+        }
+    };
+    // with a one-chunk ring (large batches: x fills the shared memory) the
+    // next chunks are pulled into L2 ahead of their copy, keeping HBM busy
+    auto prefetch = [&](int ci, int expert) {
+#pragma unroll
+        for (int kt = 0; kt < 4; ++kt) {
+            bulk_prefetch_l2(chunk_src(ci, expert, kt, 0), 1024);
+            bulk_prefetch_l2(chunk_src(ci, expert, kt, 1), 1024);
         }
     };
 
@@ -232,6 +245,10 @@ __global__ void __launch_bounds__(MM_WARPS * 32, 1) gateup_mma_kernel(GateUpMmaP
                 fence_proxy_async_smem();
                 issue(ci + NS, tab->slot_expert[unit_of((ci + NS) >> 3) / MG_UNITS]);
                 issued = ci + NS + 1;
+            }
+            if (lane == 0 && NS == 1) {
+                for (int k = ci + 2; k <= ci + MG_PF_AHEAD && k < total_chunks; ++k)
+                    if (k == ci + MG_PF_AHEAD || ci == 0) prefetch(k, tab->slot_expert[unit_of(k >> 3) / MG_UNITS]);
             }
         }
         if (!ok) break;

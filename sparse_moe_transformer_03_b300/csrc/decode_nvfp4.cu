@@ -272,12 +272,15 @@ __global__ void __launch_bounds__(GN_WARPS * 32, 1) gateup_nvfp4_kernel(GateUpNv
             const int n = nt * 8 + g;
             xo[nt] = tab->pair_token[pb + (n < np ? n : np - 1)] * GN_XROW + 2 * cq;
         }
-        // two accumulators per N tile (even and odd K blocks): two independent MMA chains
-        float acc[4][4], acc2[4][4];
+        // four accumulators per N tile (K block kb goes to chain kb % 4): four
+        // independent MMA chains, and four blocks dequantised per step
+        float acc[4][4][4];
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
+        for (int ch = 0; ch < 4; ++ch)
 #pragma unroll
-            for (int k = 0; k < 4; ++k) acc[nt][k] = acc2[nt][k] = 0.f;
+            for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) acc[ch][nt][k] = 0.f;
         for (int qq = 0; qq < NV_GU_CHUNKS; ++qq, ++ci) {
             const int s = ci % NS;
             if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(&bar[s], (ci / NS) & 1, p.limit_ns))) {
@@ -287,20 +290,20 @@ __global__ void __launch_bounds__(GN_WARPS * 32, 1) gateup_nvfp4_kernel(GateUpNv
             const uint8_t* buf = ring + (size_t)s * NV_CHUNK;
             const __half* xk = xh + qq * NV_CHUNK_KB * 16;
 #pragma unroll 2
-            for (int kb = 0; kb < NV_CHUNK_KB; kb += 2) {
-                uint32_t a[4], a2[4];
-                nv_a_frag(*reinterpret_cast<const uint32_t*>(buf + kb * 128 + 4 * lane),
-                          *reinterpret_cast<const uint16_t*>(buf + NV_CODES + kb * 16 + 2 * g), a);
-                nv_a_frag(*reinterpret_cast<const uint32_t*>(buf + (kb + 1) * 128 + 4 * lane),
-                          *reinterpret_cast<const uint16_t*>(buf + NV_CODES + (kb + 1) * 16 + 2 * g), a2);
+            for (int kb = 0; kb < NV_CHUNK_KB; kb += 4) {
+                uint32_t a[4][4];
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch)
+                    nv_a_frag(*reinterpret_cast<const uint32_t*>(buf + (kb + ch) * 128 + 4 * lane),
+                              *reinterpret_cast<const uint16_t*>(buf + NV_CODES + (kb + ch) * 16 + 2 * g), a[ch]);
 #pragma unroll
                 for (int nt = 0; nt < 4; ++nt) {
                     if (nt < ntile) {
                         const __half* xb = xk + xo[nt] + kb * 16;
-                        mma_f16_16816(acc[nt], a, *reinterpret_cast<const uint32_t*>(xb),
-                                      *reinterpret_cast<const uint32_t*>(xb + 8));
-                        mma_f16_16816(acc2[nt], a2, *reinterpret_cast<const uint32_t*>(xb + 16),
-                                      *reinterpret_cast<const uint32_t*>(xb + 24));
+#pragma unroll
+                        for (int ch = 0; ch < 4; ++ch)
+                            mma_f16_16816(acc[ch][nt], a[ch], *reinterpret_cast<const uint32_t*>(xb + 16 * ch),
+                                          *reinterpret_cast<const uint32_t*>(xb + 16 * ch + 8));
                     }
                 }
             }
@@ -315,8 +318,8 @@ __global__ void __launch_bounds__(GN_WARPS * 32, 1) gateup_nvfp4_kernel(GateUpNv
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-            for (int k = 0; k < 4; ++k) acc[nt][k] += acc2[nt][k];
-        // lane (g, cq) holds gate (acc[.][0..1]) and up (acc[.][2..3]) of row
+            for (int k = 0; k < 4; ++k) acc[0][nt][k] += acc[1][nt][k] + (acc[2][nt][k] + acc[3][nt][k]);
+        // lane (g, cq) holds gate (acc[0][.][0..1]) and up (acc[0][.][2..3]) of row
         // j = 8r + g for tile columns 2cq, 2cq + 1
         const float tsg = __ldg(p.ts + 2 * tab->slot_expert[u]);
         const int j = 8 * r + g;
@@ -328,7 +331,7 @@ __global__ void __launch_bounds__(GN_WARPS * 32, 1) gateup_nvfp4_kernel(GateUpNv
                 if (nt < ntile && n < np) {
                     const int pr = pb + n;
                     const float f = tsg * xinv[tab->pair_token[pr]];
-                    p.a[(size_t)pr * I + j] = __float2bfloat16_rn(silu_f(acc[nt][hh] * f) * (acc[nt][2 + hh] * f));
+                    p.a[(size_t)pr * I + j] = __float2bfloat16_rn(silu_f(acc[0][nt][hh] * f) * (acc[0][nt][2 + hh] * f));
                 }
             }
         }
@@ -482,19 +485,34 @@ __global__ void __launch_bounds__(DV_WARPS * 32, 1) down_nvfp4_kernel(DownNvPara
                 }
             }
         } else {
-#pragma unroll 8
-            for (int kb = 0; kb < NV_CHUNK_KB; ++kb) {
-                uint32_t a[4];
-                nv_a_frag(*reinterpret_cast<const uint32_t*>(buf + kb * 128 + 4 * lane),
-                          *reinterpret_cast<const uint16_t*>(buf + NV_CODES + kb * 16 + 2 * g), a);
+            // activations through L1 (read-only here; written by the previous
+            // grid): the first N tile's operands for 16 blocks are requested
+            // at once, the other tiles' as they are used
+#pragma unroll 1
+            for (int kh = 0; kh < NV_CHUNK_KB; kh += 16) {
+                uint32_t bq[16][2];
+                const unsigned int* a0 =
+                    reinterpret_cast<const unsigned int*>(p.a + (size_t)prow[0] * I + kh * 16 + 2 * cq);
 #pragma unroll
-                for (int k = 0; k < 4; ++k) a[k] = f16x2_to_bf16x2(a[k]);
+                for (int kb = 0; kb < 16; ++kb) {
+                    bq[kb][0] = __ldg(a0 + kb * 8);
+                    bq[kb][1] = __ldg(a0 + kb * 8 + 4);
+                }
 #pragma unroll
-                for (int nt = 0; nt < 4; ++nt) {
-                    if (nt < ntile) {
-                        const unsigned int* ar =
-                            reinterpret_cast<const unsigned int*>(p.a + (size_t)prow[nt] * I + kb * 16 + 2 * cq);
-                        mma_bf16_16816(acc[nt], a, __ldcg(ar), __ldcg(ar + 4));
+                for (int kb = 0; kb < 16; ++kb) {
+                    uint32_t a[4];
+                    nv_a_frag(*reinterpret_cast<const uint32_t*>(buf + (kh + kb) * 128 + 4 * lane),
+                              *reinterpret_cast<const uint16_t*>(buf + NV_CODES + (kh + kb) * 16 + 2 * g), a);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) a[k] = f16x2_to_bf16x2(a[k]);
+                    mma_bf16_16816(acc[0], a, bq[kb][0], bq[kb][1]);
+#pragma unroll
+                    for (int nt = 1; nt < 4; ++nt) {
+                        if (nt < ntile) {
+                            const unsigned int* ar = reinterpret_cast<const unsigned int*>(
+                                p.a + (size_t)prow[nt] * I + (kh + kb) * 16 + 2 * cq);
+                            mma_bf16_16816(acc[nt], a, __ldg(ar), __ldg(ar + 4));
+                        }
                     }
                 }
             }
