@@ -12,12 +12,12 @@
 // 8x8 matrix over all banks).
 //
 //   gateup_mma   Unit = 8 gate rows + the 8 matching up rows of one expert
-//                (the MMA's 16 rows), K = 2048 in 8 chunks of 256 columns
-//                (8 KiB) streamed into a per-warp ring; the expert's tokens
-//                are the N columns (tiles of 8), x is bf16 staged in smem.
-//                Each lane ends with
-//                gate and up of the same (row, token): a = silu(g) * u is
-//                formed in registers and written as bf16.
+//                (the MMA's 16 rows) against the expert's tokens (the N
+//                columns, tiles of 8; x staged in smem as bf16).  The CTA
+//                takes one unit at a time: warp w streams columns 256w ..
+//                256w + 255 (8 KiB) into its ring and multiplies them; the
+//                eight partial sums are added in warp order in smem, then
+//                a = silu(g) * u is written as bf16.
 //   down_mma     CTA c owns output rows 16c .. 16c + 15 (one M tile); warp w
 //                takes expert slots w, w + 8, ..., each 2 chunks of 256
 //                columns (4 pieces of 2 KiB); the activations are staged in
@@ -49,10 +49,8 @@ constexpr int MM_WARPS = 8;
 // ---------------------------------------------------------------------------
 
 constexpr int MG_UNITS = I / 8;          // 64 units per expert
-constexpr int MG_CHUNKS = H / 256;       // 8 chunks per unit
 constexpr int MG_XROW = H + 8;           // bf16 per staged x row (+8: conflict-free B loads)
-constexpr int MG_XSMEM_T = 32;           // x is staged in smem up to this many tokens
-constexpr int MG_PF_AHEAD = 3;           // one-chunk ring: chunks up to ci + 3 are prefetched into L2
+constexpr int MG_PART = MM_WARPS * 4 * 32 * 4;   // per-warp partial sums: [warp][N tile][lane][4]
 
 struct GateUpMmaParams {
     const uint8_t* tiled;         // the handle's tiled experts
@@ -68,21 +66,26 @@ struct GateUpMmaParams {
     uint64_t limit_ns;
 };
 
+// ring chunks per warp: two (the next unit's chunk in flight) while x is
+// small, one when x fills the shared memory (the next chunk then goes to L2)
 static inline int mg_ns(int T) { return T <= 16 ? 2 : 1; }
 static inline size_t mg_smem_bytes(int T) {
-    return (size_t)MM_WARPS * mg_ns(T) * MM_CHUNK + (T <= MG_XSMEM_T ? (size_t)T * MG_XROW * 2 : 0) +
+    return (size_t)MM_WARPS * mg_ns(T) * MM_CHUNK + (size_t)T * MG_XROW * 2 + (size_t)MG_PART * 4 +
            (size_t)MM_WARPS * mg_ns(T) * 8 + sizeof(DecodeTables) + DEC_T * TOPK * 8 + 2 * E * 4;
 }
 
+// The CTA works on one unit at a time: warp w streams and multiplies the
+// unit's columns 256w .. 256w + 255, the eight partial sums meet in shared
+// memory and are added in warp order.  Units per CTA then differ by at most
+// one across the grid (whole units per warp would differ by a factor of two).
 __global__ void __launch_bounds__(MM_WARPS * 32, 1) gateup_mma_kernel(GateUpMmaParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int NS = p.ns, T = p.T, G = gridDim.x, c = blockIdx.x;
-    const bool xs_on = T <= MG_XSMEM_T;
     uint8_t* ring = smem + (size_t)warp * NS * MM_CHUNK;
     __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(smem + (size_t)MM_WARPS * NS * MM_CHUNK);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(xs) +
-                                                 (xs_on ? (size_t)T * MG_XROW * 2 : 0));
+    float* part = reinterpret_cast<float*>(xs + (size_t)T * MG_XROW);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(part + MG_PART);
     uint64_t* bar = bars + warp * NS;
     DecodeTables* tab = reinterpret_cast<DecodeTables*>(bars + MM_WARPS * NS);
     int* sel_e = reinterpret_cast<int*>(tab + 1);
@@ -96,50 +99,46 @@ __global__ void __launch_bounds__(MM_WARPS * 32, 1) gateup_mma_kernel(GateUpMmaP
     }
     __syncthreads();
 
-    auto unit_of = [&](int i) { return c + G * (warp + MM_WARPS * i); };
-    // chunk ci of the warp: unit ci / 8, columns 256 (ci % 8) .. + 255
-    auto chunk_src = [&](int ci, int expert, int kt, int half) {
-        const int q = unit_of(ci >> 3), r = q & (MG_UNITS - 1);
-        const int rb = (r >> 4) + 4 * half, kc = (ci & (MG_CHUNKS - 1)) * 4 + kt;
+    // the CTA's i-th unit; this warp's piece of it: column tiles 4w .. 4w + 3
+    auto unit_of = [&](int i) { return c + G * i; };
+    auto piece = [&](int i, int expert, int kt, int half) {
+        const int r = unit_of(i) & (MG_UNITS - 1);
+        const int rb = (r >> 4) + 4 * half, kc = warp * 4 + kt;
         return p.tiled + (size_t)expert * MM_EXPERT_BYTES + ((size_t)rb * MM_GU_KT + kc) * MM_TILE +
                (size_t)(r & 15) * 1024;
     };
-    auto issue = [&](int ci, int expert) {
-        const int s = ci % NS;
+    auto issue = [&](int i, int expert) {
+        const int s = i % NS;
         uint8_t* dst = ring + (size_t)s * MM_CHUNK;
         mbar_arrive_expect_tx(&bar[s], MM_CHUNK);
 #pragma unroll
         for (int kt = 0; kt < 4; ++kt) {
-            bulk_g2s(dst + (2 * kt) * 1024, chunk_src(ci, expert, kt, 0), 1024, &bar[s]);
-            bulk_g2s(dst + (2 * kt + 1) * 1024, chunk_src(ci, expert, kt, 1), 1024, &bar[s]);
+            bulk_g2s(dst + (2 * kt) * 1024, piece(i, expert, kt, 0), 1024, &bar[s]);
+            bulk_g2s(dst + (2 * kt + 1) * 1024, piece(i, expert, kt, 1), 1024, &bar[s]);
         }
     };
-    // with a one-chunk ring (large batches: x fills the shared memory) the
-    // next chunks are pulled into L2 ahead of their copy, keeping HBM busy
-    auto prefetch = [&](int ci, int expert) {
+    auto prefetch = [&](int i, int expert) {
 #pragma unroll
         for (int kt = 0; kt < 4; ++kt) {
-            bulk_prefetch_l2(chunk_src(ci, expert, kt, 0), 1024);
-            bulk_prefetch_l2(chunk_src(ci, expert, kt, 1), 1024);
+            bulk_prefetch_l2(piece(i, expert, kt, 0), 1024);
+            bulk_prefetch_l2(piece(i, expert, kt, 1), 1024);
         }
     };
 
-    // ---- before the router has finished: the shared expert's chunks ----
+    // ---- before the router has finished: the shared expert's pieces ----
     int issued = 0;
     if (lane == 0) {
-        for (int ci = 0; ci < NS && unit_of(ci >> 3) < MG_UNITS; ++ci) {
-            issue(ci, SHARED);
-            issued = ci + 1;
+        for (int i = 0; i < NS && unit_of(i) < MG_UNITS; ++i) {
+            issue(i, SHARED);
+            issued = i + 1;
         }
     }
     pdl_wait();     // router logits are complete (and x is ready)
     pdl_trigger();
 
-    if (xs_on) {
-        for (int k = threadIdx.x; k < T * (H / 8); k += blockDim.x) {
-            const int t = k / (H / 8), col = (k % (H / 8)) * 8;
-            *reinterpret_cast<uint4*>(xs + (size_t)t * MG_XROW + col) = ldg16(p.x + (size_t)t * H + col);
-        }
+    for (int k = threadIdx.x; k < T * (H / 8); k += blockDim.x) {
+        const int t = k / (H / 8), col = (k % (H / 8)) * 8;
+        *reinterpret_cast<uint4*>(xs + (size_t)t * MG_XROW + col) = ldg16(p.x + (size_t)t * H + col);
     }
 
     // ---- top-6 of every token, then the (slot, token) tables ----
@@ -170,14 +169,14 @@ __global__ void __launch_bounds__(MM_WARPS * 32, 1) gateup_mma_kernel(GateUpMmaP
         for (int k = threadIdx.x; k < (int)(sizeof(DecodeTables) / 4); k += blockDim.x) dst[k] = src[k];
     }
     const int total_units = tab->n_slots * MG_UNITS;
-    int my_units = 0;
-    while (unit_of(my_units) < total_units) ++my_units;
-    const int total_chunks = my_units * MG_CHUNKS;
+    const int my_units = c < total_units ? (total_units - c + G - 1) / G : 0;
+    auto expert_of = [&](int i) { return tab->slot_expert[unit_of(i) / MG_UNITS]; };
     if (lane == 0) {
-        for (int ci = issued; ci < NS && ci < total_chunks; ++ci) {
-            issue(ci, tab->slot_expert[unit_of(ci >> 3) / MG_UNITS]);
-            issued = ci + 1;
+        for (int i = issued; i < NS && i < my_units; ++i) {
+            issue(i, expert_of(i));
+            issued = i + 1;
         }
+        if (NS == 1 && my_units > 1) prefetch(1, expert_of(1));
     }
 
     // this lane's ldmatrix row: matrix mi = lane / 8 (bit 0: gate / up piece,
@@ -187,8 +186,8 @@ __global__ void __launch_bounds__(MM_WARPS * 32, 1) gateup_mma_kernel(GateUpMmaP
     const int lkh = mi >> 1;
     const int g = lane >> 2, cq = lane & 3;
     bool ok = true;
-    int ci = 0;
-    for (int i = 0; ok && i < my_units; ++i) {
+    int i = 0;
+    for (; i < my_units; ++i) {
         const int q = unit_of(i), u = q / MG_UNITS, r = q & (MG_UNITS - 1);
         const int pb = tab->slot_pair0[u], np = tab->slot_pair0[u + 1] - pb;   // 1..32 tokens
         const int ntile = (np + 7) >> 3;
@@ -196,79 +195,77 @@ __global__ void __launch_bounds__(MM_WARPS * 32, 1) gateup_mma_kernel(GateUpMmaP
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt) {
             const int n = nt * 8 + g;
-            const int t = tab->pair_token[pb + (n < np ? n : np - 1)];
-            xb[nt] = (xs_on ? xs + (size_t)t * MG_XROW : p.x + (size_t)t * H) + 2 * cq;
+            xb[nt] = xs + (size_t)tab->pair_token[pb + (n < np ? n : np - 1)] * MG_XROW + warp * 256 + 2 * cq;
         }
         float acc[4][4], acc2[4][4];
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
             for (int k = 0; k < 4; ++k) acc[nt][k] = acc2[nt][k] = 0.f;
-        for (int qq = 0; qq < MG_CHUNKS; ++qq, ++ci) {
-            const int s = ci % NS;
-            if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(&bar[s], (ci / NS) & 1, p.limit_ns))) {
-                ok = false;
-                break;
-            }
+        const int s = i % NS;
+        const bool got = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(&bar[s], (i / NS) & 1, p.limit_ns));
+        if (got) {
             const uint8_t* buf = ring + (size_t)s * MM_CHUNK;
 #pragma unroll 2
             for (int kb = 0; kb < 16; kb += 2) {
-                // K block kb: column tile kb / 4, 16-byte chunks 2 (kb % 4) + {0, 1}
                 uint32_t a[4], a2[4];
                 const int kt = kb >> 2, j0 = 2 * (kb & 3) + lkh;
                 ldmatrix_x4(a, buf + kt * 2048 + lrow + ((j0 ^ li) << 4));
                 ldmatrix_x4(a2, buf + kt * 2048 + lrow + (((j0 + 2) ^ li) << 4));
-                const int kx = qq * 256 + kb * 16;
 #pragma unroll
                 for (int nt = 0; nt < 4; ++nt) {
                     if (nt < ntile) {
-                        const __nv_bfloat16* xp = xb[nt] + kx;
-                        uint32_t b0, b1, b2, b3;
-                        if (xs_on) {
-                            b0 = *reinterpret_cast<const uint32_t*>(xp);
-                            b1 = *reinterpret_cast<const uint32_t*>(xp + 8);
-                            b2 = *reinterpret_cast<const uint32_t*>(xp + 16);
-                            b3 = *reinterpret_cast<const uint32_t*>(xp + 24);
-                        } else {
-                            b0 = __ldg(reinterpret_cast<const unsigned int*>(xp));
-                            b1 = __ldg(reinterpret_cast<const unsigned int*>(xp + 8));
-                            b2 = __ldg(reinterpret_cast<const unsigned int*>(xp + 16));
-                            b3 = __ldg(reinterpret_cast<const unsigned int*>(xp + 24));
-                        }
-                        mma_bf16_16816(acc[nt], a, b0, b1);
-                        mma_bf16_16816(acc2[nt], a2, b2, b3);
+                        const __nv_bfloat16* xp = xb[nt] + kb * 16;
+                        mma_bf16_16816(acc[nt], a, *reinterpret_cast<const uint32_t*>(xp),
+                                       *reinterpret_cast<const uint32_t*>(xp + 8));
+                        mma_bf16_16816(acc2[nt], a2, *reinterpret_cast<const uint32_t*>(xp + 16),
+                                       *reinterpret_cast<const uint32_t*>(xp + 24));
                     }
                 }
             }
             __syncwarp();   // every lane is done reading slot s
-            if (lane == 0 && ci + NS < total_chunks) {
-                fence_proxy_async_smem();
-                issue(ci + NS, tab->slot_expert[unit_of((ci + NS) >> 3) / MG_UNITS]);
-                issued = ci + NS + 1;
-            }
-            if (lane == 0 && NS == 1) {
-                for (int k = ci + 2; k <= ci + MG_PF_AHEAD && k < total_chunks; ++k)
-                    if (k == ci + MG_PF_AHEAD || ci == 0) prefetch(k, tab->slot_expert[unit_of(k >> 3) / MG_UNITS]);
-            }
-        }
-        if (!ok) break;
-        const int j = 8 * r + g;
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int n = nt * 8 + 2 * cq + hh;
-                if (nt < ntile && n < np) {
-                    const float gv = acc[nt][hh] + acc2[nt][hh], uv = acc[nt][2 + hh] + acc2[nt][2 + hh];
-                    p.a[(size_t)(pb + n) * I + j] = __float2bfloat16_rn(silu_f(gv) * uv);
+            if (lane == 0) {
+                if (i + NS < my_units) {
+                    fence_proxy_async_smem();
+                    issue(i + NS, expert_of(i + NS));
+                    issued = i + NS + 1;
                 }
+                if (NS == 1 && i + 2 < my_units) prefetch(i + 2, expert_of(i + 2));
             }
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt)
+                if (nt < ntile)
+                    *reinterpret_cast<float4*>(part + ((warp * 4 + nt) * 32 + lane) * 4) =
+                        make_float4(acc[nt][0] + acc2[nt][0], acc[nt][1] + acc2[nt][1], acc[nt][2] + acc2[nt][2],
+                                    acc[nt][3] + acc2[nt][3]);
         }
+        // the decision to go on is taken by the whole CTA
+        if (!__syncthreads_and(got)) {
+            ok = false;
+            break;
+        }
+        // warp nt adds tile nt's eight partial sums in warp order; lane (g, cq)
+        // then holds gate (0, 1) and up (2, 3) of row j = 8r + g, columns 2cq, 2cq + 1
+        if (warp < ntile) {
+            float4 sum = *reinterpret_cast<const float4*>(part + (warp * 32 + lane) * 4);
+#pragma unroll
+            for (int w = 1; w < MM_WARPS; ++w) {
+                const float4 v = *reinterpret_cast<const float4*>(part + ((w * 4 + warp) * 32 + lane) * 4);
+                sum.x += v.x;
+                sum.y += v.y;
+                sum.z += v.z;
+                sum.w += v.w;
+            }
+            const int j = 8 * r + g, n0 = warp * 8 + 2 * cq;
+            if (n0 < np) p.a[(size_t)(pb + n0) * I + j] = __float2bfloat16_rn(silu_f(sum.x) * sum.z);
+            if (n0 + 1 < np) p.a[(size_t)(pb + n0 + 1) * I + j] = __float2bfloat16_rn(silu_f(sum.y) * sum.w);
+        }
+        __syncthreads();   // the partial sums are read before the next unit writes them
     }
     if (!ok) {
         if (lane == 0) {
             report_status(p.status, ST_TIMEOUT);
-            for (int k = ci; k < issued; ++k) mbar_wait_bounded(&bar[k % NS], (k / NS) & 1, p.limit_ns);
+            for (int k = i; k < issued; ++k) mbar_wait_bounded(&bar[k % NS], (k / NS) & 1, p.limit_ns);
         }
         __syncwarp();
     }
