@@ -112,37 +112,55 @@ __global__ void __launch_bounds__(RT_WARPS * 32) router_decode_kernel(RouterDeco
     if (p.tables && warp == 0) build_decode_tables_warp(T, sel_e, sel_w, tmask, pair0, p.tables, lane);
 }
 
-// Logits only (the forward path: the expert kernel selects per CTA).
+// Logits only (the forward path: the expert kernels select for themselves).
+// Grid: (64 expert groups of 4, token groups of RL_TOK).  Each warp keeps its
+// expert's 4 KiB router row in registers (loaded before the dependency wait);
+// the CTA stages its tokens' x rows in smem with one bulk copy, so a token
+// costs shared-memory reads instead of an L2 round trip.
+constexpr int RL_TOK = 8;
+
 __global__ void __launch_bounds__(RT_WARPS * 32) router_logits_decode_kernel(const __nv_bfloat16* x, int T,
                                                                            const __nv_bfloat16* Wr,
                                                                            const float* bias, float* logits) {
+    __shared__ __align__(128) __nv_bfloat16 xs[RL_TOK * H];   // 32 KiB
+    __shared__ __align__(8) uint64_t xbar;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e = blockIdx.x * RT_WARPS + warp;
+    const int t0 = blockIdx.y * RL_TOK, nt = min(RL_TOK, T - t0);
     uint4 wr[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) wr[i] = ldg16(Wr + (size_t)e * H + 8 * (lane + 32 * i));
     const float b = bias ? __ldg(bias + e) : 0.f;
+    if (threadIdx.x == 0) {
+        mbar_init(&xbar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
     pdl_trigger();
     pdl_wait();
-    for (int t = 0; t < T; ++t) {
-        const __nv_bfloat16* xr = x + (size_t)t * H;
-        uint4 xv[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) xv[i] = ldg16(xr + 8 * (lane + 32 * i));
+    if (threadIdx.x == 0) {
+        mbar_arrive_expect_tx(&xbar, nt * H * 2);
+        bulk_g2s(xs, x + (size_t)t0 * H, nt * H * 2, &xbar);
+    }
+    const bool ok = __syncthreads_and(mbar_wait_bounded(&xbar, 0, 1000000000ull));
+    if (!ok) return;   // the copy never completed (cannot happen for valid pointers); logits stay stale
+    for (int t = 0; t < nt; ++t) {
+        const __nv_bfloat16* xr = xs + t * H;
         float acc = 0.f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            acc = fmaf(bf_lo(wr[i].x), bf_lo(xv[i].x), acc);
-            acc = fmaf(bf_hi(wr[i].x), bf_hi(xv[i].x), acc);
-            acc = fmaf(bf_lo(wr[i].y), bf_lo(xv[i].y), acc);
-            acc = fmaf(bf_hi(wr[i].y), bf_hi(xv[i].y), acc);
-            acc = fmaf(bf_lo(wr[i].z), bf_lo(xv[i].z), acc);
-            acc = fmaf(bf_hi(wr[i].z), bf_hi(xv[i].z), acc);
-            acc = fmaf(bf_lo(wr[i].w), bf_lo(xv[i].w), acc);
-            acc = fmaf(bf_hi(wr[i].w), bf_hi(xv[i].w), acc);
+            const uint4 xv = *reinterpret_cast<const uint4*>(xr + 8 * (lane + 32 * i));
+            acc = fmaf(bf_lo(wr[i].x), bf_lo(xv.x), acc);
+            acc = fmaf(bf_hi(wr[i].x), bf_hi(xv.x), acc);
+            acc = fmaf(bf_lo(wr[i].y), bf_lo(xv.y), acc);
+            acc = fmaf(bf_hi(wr[i].y), bf_hi(xv.y), acc);
+            acc = fmaf(bf_lo(wr[i].z), bf_lo(xv.z), acc);
+            acc = fmaf(bf_hi(wr[i].z), bf_hi(xv.z), acc);
+            acc = fmaf(bf_lo(wr[i].w), bf_lo(xv.w), acc);
+            acc = fmaf(bf_hi(wr[i].w), bf_hi(xv.w), acc);
         }
         acc = warp_sum(acc);
-        if (lane == 0) logits[(size_t)t * E + e] = acc + b;
+        if (lane == 0) logits[(size_t)(t0 + t) * E + e] = acc + b;
     }
 }
 
@@ -313,8 +331,8 @@ cudaError_t launch_router_decode(const LaunchCtx& L, const __nv_bfloat16* x, int
 
 cudaError_t launch_router_logits_decode(const LaunchCtx& L, const __nv_bfloat16* x, int T,
                                         const __nv_bfloat16* Wr, const float* bias, float* logits) {
-    return launch_hooked(L, FLINT_KERNEL_ROUTER, router_logits_decode_kernel, dim3(RT_CTAS), dim3(RT_WARPS * 32), 0, x, T, Wr, bias,
-                      logits);
+    return launch_hooked(L, FLINT_KERNEL_ROUTER, router_logits_decode_kernel,
+                         dim3(RT_CTAS, (T + RL_TOK - 1) / RL_TOK), dim3(RT_WARPS * 32), 0, x, T, Wr, bias, logits);
 }
 
 cudaError_t launch_router_logits_general(const LaunchCtx& L, const __nv_bfloat16* x, int T,
