@@ -15,9 +15,11 @@
 // weight block and token.
 //
 //   gateup_nvfp4  Unit = 8 gate rows + the 8 matching up rows of one expert
-//                 (the MMA's 16 rows), K = 2048 in 4 chunks of 4608 bytes
-//                 streamed by cp.async.bulk into a per-warp ring.  The
-//                 tokens are the N columns (tiles of 8).  x is staged in
+//                 (the MMA's 16 rows), K = 2048 in 4 chunks of 4608 bytes;
+//                 a quad of warps takes a unit, each warp streaming one
+//                 chunk by cp.async.bulk into its ring, and the four partial
+//                 sums are added in warp order.  The tokens are the N
+//                 columns (tiles of 8).  x is staged in
 //                 shared memory as f16 times a power of two per token
 //                 (chosen so the token's largest |x| lies in [2^14, 2^15):
 //                 exact for every bf16 value not 28 binades below it); the
@@ -139,21 +141,45 @@ struct GateUpNvParams {
     uint64_t limit_ns;
 };
 
-static inline int gn_ns(int T) { return T <= 8 ? 4 : 2; }
+constexpr int GN_QUADS = GN_WARPS / 4;                 // a quad of warps works on one unit
+constexpr int GN_PART = GN_QUADS * 4 * 4 * 32 * 4;      // partial sums [quad][warp][N tile][lane][4]
+
+// ring chunks per warp (one chunk = the warp's quarter of a unit): deep while
+// x is small; one when x fills the shared memory (the next chunk then goes to L2)
+static inline int gn_ns(int T) { return T <= 8 ? 4 : (T <= 24 ? 2 : 1); }
 
 static inline size_t gn_smem_bytes(int T) {
-    return (size_t)GN_WARPS * gn_ns(T) * NV_CHUNK + (size_t)T * GN_XROW * 2 + DEC_T * 4 +
+    return (size_t)GN_WARPS * gn_ns(T) * NV_CHUNK + (size_t)T * GN_XROW * 2 + DEC_T * 4 + (size_t)GN_PART * 4 +
            (size_t)GN_WARPS * gn_ns(T) * 8 + sizeof(DecodeTables) + DEC_T * TOPK * 8 + 2 * E * 4;
 }
 
+// barrier (and AND of a predicate) of the 128 threads of quad q
+__device__ __forceinline__ bool quad_all(int q, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, t;\n setp.ne.u32 p, %1, 0;\n barrier.cta.red.and.pred t, %2, 128, p;\n"
+        " selp.u32 %0, 1, 0, t;\n}\n"
+        : "=r"(r)
+        : "r"(v ? 1u : 0u), "r"(1 + q)
+        : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ void quad_sync(int q) { asm volatile("bar.sync %0, 128;" ::"r"(1 + q) : "memory"); }
+
+// Quad q of CTA c takes units c + G q, c + G (q + 2), ...; warp k of the quad
+// streams and multiplies chunk k (columns 512k .. 512k + 511) of each, and the
+// four partial sums are added in warp order.  A unit then costs each warp a
+// quarter of the dequantise -> MMA chain it used to cost one warp.
 __global__ void __launch_bounds__(GN_WARPS * 32, 1) gateup_nvfp4_kernel(GateUpNvParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int quad = warp >> 2, wq = warp & 3;
     const int NS = p.ns, T = p.T, G = gridDim.x, c = blockIdx.x;
     uint8_t* ring = smem + (size_t)warp * NS * NV_CHUNK;
     __half* xh = reinterpret_cast<__half*>(smem + (size_t)GN_WARPS * NS * NV_CHUNK);
     float* xinv = reinterpret_cast<float*>(xh + (size_t)T * GN_XROW);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(xinv + DEC_T);
+    float* part = xinv + DEC_T;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(part + GN_PART);
     uint64_t* bar = bars + warp * NS;
     DecodeTables* tab = reinterpret_cast<DecodeTables*>(bars + GN_WARPS * NS);
     int* sel_e = reinterpret_cast<int*>(tab + 1);
@@ -167,22 +193,24 @@ __global__ void __launch_bounds__(GN_WARPS * 32, 1) gateup_nvfp4_kernel(GateUpNv
     }
     __syncthreads();
 
-    // the warp's i-th unit; its chunks are ci = 4i .. 4i + 3
-    auto unit_of = [&](int i) { return c + G * (warp + GN_WARPS * i); };
-    auto issue = [&](int ci, int expert) {
-        const int q = unit_of(ci >> 2), r = q & (NV_GU_UNITS - 1), s = ci % NS;
-        const uint8_t* src = p.nv + (size_t)expert * NV_EXPERT_BYTES +
-                             ((size_t)r * NV_GU_CHUNKS + (ci & (NV_GU_CHUNKS - 1))) * NV_CHUNK;
+    // the quad's i-th unit; this warp's chunk of it is chunk wq
+    auto unit_of = [&](int i) { return c + G * (quad + GN_QUADS * i); };
+    auto chunk_ptr = [&](int i, int expert) {
+        const int r = unit_of(i) & (NV_GU_UNITS - 1);
+        return p.nv + (size_t)expert * NV_EXPERT_BYTES + ((size_t)r * NV_GU_CHUNKS + wq) * NV_CHUNK;
+    };
+    auto issue = [&](int i, int expert) {
+        const int s = i % NS;
         mbar_arrive_expect_tx(&bar[s], NV_CHUNK);
-        bulk_g2s(ring + (size_t)s * NV_CHUNK, src, NV_CHUNK, &bar[s]);
+        bulk_g2s(ring + (size_t)s * NV_CHUNK, chunk_ptr(i, expert), NV_CHUNK, &bar[s]);
     };
 
     // ---- before the router has finished: the shared expert's chunks ----
     int issued = 0;
     if (lane == 0) {
-        for (int ci = 0; ci < NS && unit_of(ci >> 2) < NV_GU_UNITS; ++ci) {
-            issue(ci, SHARED);
-            issued = ci + 1;
+        for (int i = 0; i < NS && unit_of(i) < NV_GU_UNITS; ++i) {
+            issue(i, SHARED);
+            issued = i + 1;
         }
     }
     pdl_wait();     // router logits are complete (and x is ready)
@@ -251,18 +279,20 @@ __global__ void __launch_bounds__(GN_WARPS * 32, 1) gateup_nvfp4_kernel(GateUpNv
     const int total_units = tab->n_slots * NV_GU_UNITS;
     int my_units = 0;
     while (unit_of(my_units) < total_units) ++my_units;
-    const int total_chunks = my_units * NV_GU_CHUNKS;
+    auto expert_of = [&](int i) { return tab->slot_expert[unit_of(i) / NV_GU_UNITS]; };
     if (lane == 0) {
-        for (int ci = issued; ci < NS && ci < total_chunks; ++ci) {
-            issue(ci, tab->slot_expert[unit_of(ci >> 2) / NV_GU_UNITS]);
-            issued = ci + 1;
+        for (int i = issued; i < NS && i < my_units; ++i) {
+            issue(i, expert_of(i));
+            issued = i + 1;
         }
+        if (NS == 1 && my_units > 1) bulk_prefetch_l2(chunk_ptr(1, expert_of(1)), NV_CHUNK);
     }
 
     const int g = lane >> 2, cq = lane & 3;
+    float* qpart = part + quad * (4 * 4 * 32 * 4);
     bool ok = true;
-    int ci = 0;
-    for (int i = 0; ok && i < my_units; ++i) {
+    int i = 0;
+    for (; i < my_units; ++i) {
         const int q = unit_of(i), u = q / NV_GU_UNITS, r = q & (NV_GU_UNITS - 1);
         const int pb = tab->slot_pair0[u], np = tab->slot_pair0[u + 1] - pb;   // 1..32 tokens
         const int ntile = (np + 7) >> 3;
@@ -270,25 +300,20 @@ __global__ void __launch_bounds__(GN_WARPS * 32, 1) gateup_nvfp4_kernel(GateUpNv
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt) {
             const int n = nt * 8 + g;
-            xo[nt] = tab->pair_token[pb + (n < np ? n : np - 1)] * GN_XROW + 2 * cq;
+            xo[nt] = tab->pair_token[pb + (n < np ? n : np - 1)] * GN_XROW + 2 * cq + wq * 512;
         }
-        // four accumulators per N tile (K block kb goes to chain kb % 4): four
-        // independent MMA chains, and four blocks dequantised per step
-        float acc[4][4][4];
+        const int s = i % NS;
+        const bool got = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(&bar[s], (i / NS) & 1, p.limit_ns));
+        if (got) {
+            // four accumulators per N tile (K block kb goes to chain kb % 4)
+            float acc[4][4][4];
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch)
+            for (int ch = 0; ch < 4; ++ch)
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt)
+                for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-                for (int k = 0; k < 4; ++k) acc[ch][nt][k] = 0.f;
-        for (int qq = 0; qq < NV_GU_CHUNKS; ++qq, ++ci) {
-            const int s = ci % NS;
-            if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(&bar[s], (ci / NS) & 1, p.limit_ns))) {
-                ok = false;
-                break;
-            }
+                    for (int k = 0; k < 4; ++k) acc[ch][nt][k] = 0.f;
             const uint8_t* buf = ring + (size_t)s * NV_CHUNK;
-            const __half* xk = xh + qq * NV_CHUNK_KB * 16;
 #pragma unroll 2
             for (int kb = 0; kb < NV_CHUNK_KB; kb += 4) {
                 uint32_t a[4][4];
@@ -299,7 +324,7 @@ __global__ void __launch_bounds__(GN_WARPS * 32, 1) gateup_nvfp4_kernel(GateUpNv
 #pragma unroll
                 for (int nt = 0; nt < 4; ++nt) {
                     if (nt < ntile) {
-                        const __half* xb = xk + xo[nt] + kb * 16;
+                        const __half* xb = xh + xo[nt] + kb * 16;
 #pragma unroll
                         for (int ch = 0; ch < 4; ++ch)
                             mma_f16_16816(acc[ch][nt], a[ch], *reinterpret_cast<const uint32_t*>(xb + 16 * ch),
@@ -308,39 +333,58 @@ __global__ void __launch_bounds__(GN_WARPS * 32, 1) gateup_nvfp4_kernel(GateUpNv
                 }
             }
             __syncwarp();   // every lane is done reading slot s
-            if (lane == 0 && ci + NS < total_chunks) {
-                fence_proxy_async_smem();
-                issue(ci + NS, tab->slot_expert[unit_of((ci + NS) >> 2) / NV_GU_UNITS]);
-                issued = ci + NS + 1;
-            }
-        }
-        if (!ok) break;
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) acc[0][nt][k] += acc[1][nt][k] + (acc[2][nt][k] + acc[3][nt][k]);
-        // lane (g, cq) holds gate (acc[0][.][0..1]) and up (acc[0][.][2..3]) of row
-        // j = 8r + g for tile columns 2cq, 2cq + 1
-        const float tsg = __ldg(p.ts + 2 * tab->slot_expert[u]);
-        const int j = 8 * r + g;
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int n = nt * 8 + 2 * cq + hh;
-                if (nt < ntile && n < np) {
-                    const int pr = pb + n;
-                    const float f = tsg * xinv[tab->pair_token[pr]];
-                    p.a[(size_t)pr * I + j] = __float2bfloat16_rn(silu_f(acc[0][nt][hh] * f) * (acc[0][nt][2 + hh] * f));
+            if (lane == 0) {
+                if (i + NS < my_units) {
+                    fence_proxy_async_smem();
+                    issue(i + NS, expert_of(i + NS));
+                    issued = i + NS + 1;
                 }
+                if (NS == 1 && i + 2 < my_units) bulk_prefetch_l2(chunk_ptr(i + 2, expert_of(i + 2)), NV_CHUNK);
+            }
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt)
+                if (nt < ntile)
+                    *reinterpret_cast<float4*>(qpart + ((wq * 4 + nt) * 32 + lane) * 4) = make_float4(
+                        acc[0][nt][0] + acc[1][nt][0] + (acc[2][nt][0] + acc[3][nt][0]),
+                        acc[0][nt][1] + acc[1][nt][1] + (acc[2][nt][1] + acc[3][nt][1]),
+                        acc[0][nt][2] + acc[1][nt][2] + (acc[2][nt][2] + acc[3][nt][2]),
+                        acc[0][nt][3] + acc[1][nt][3] + (acc[2][nt][3] + acc[3][nt][3]));
+        }
+        // the decision to go on is taken by the whole quad
+        if (!quad_all(quad, got)) {
+            ok = false;
+            break;
+        }
+        // warp nt of the quad adds tile nt's four partial sums in warp order;
+        // lane (g, cq) then holds gate (0, 1) and up (2, 3) of row j = 8r + g
+        if (wq < ntile) {
+            float4 sum = *reinterpret_cast<const float4*>(qpart + (wq * 32 + lane) * 4);
+#pragma unroll
+            for (int w = 1; w < 4; ++w) {
+                const float4 v = *reinterpret_cast<const float4*>(qpart + ((w * 4 + wq) * 32 + lane) * 4);
+                sum.x += v.x;
+                sum.y += v.y;
+                sum.z += v.z;
+                sum.w += v.w;
+            }
+            const float tsg = __ldg(p.ts + 2 * tab->slot_expert[u]);
+            const int j = 8 * r + g, n0 = wq * 8 + 2 * cq;
+            if (n0 < np) {
+                const float f = tsg * xinv[tab->pair_token[pb + n0]];
+                p.a[(size_t)(pb + n0) * I + j] = __float2bfloat16_rn(silu_f(sum.x * f) * (sum.z * f));
+            }
+            if (n0 + 1 < np) {
+                const float f = tsg * xinv[tab->pair_token[pb + n0 + 1]];
+                p.a[(size_t)(pb + n0 + 1) * I + j] = __float2bfloat16_rn(silu_f(sum.y * f) * (sum.w * f));
             }
         }
+        quad_sync(quad);   // the partial sums are read before the next unit writes them
     }
     if (!ok) {
         if (lane == 0) {
             report_status(p.status, ST_TIMEOUT);
             // drain copies still in flight into this warp's ring (bounded)
-            for (int k = ci; k < issued; ++k) mbar_wait_bounded(&bar[k % NS], (k / NS) & 1, p.limit_ns);
+            for (int k = i; k < issued; ++k) mbar_wait_bounded(&bar[k % NS], (k / NS) & 1, p.limit_ns);
         }
         __syncwarp();
     }
