@@ -61,8 +61,6 @@ cudaError_t launch_router_decode(const LaunchCtx& L, const __nv_bfloat16* x, int
                                  DecodeTables* tables, unsigned* ticket);
 cudaError_t launch_router_logits_decode(const LaunchCtx& L, const __nv_bfloat16* x, int T,
                                         const __nv_bfloat16* Wr, const float* bias, float* logits);
-cudaError_t launch_router_logits_general(const LaunchCtx& L, const __nv_bfloat16* x, int T,
-                                         const __nv_bfloat16* Wr, const float* bias, float* logits);
 cudaError_t launch_select(const LaunchCtx& L, const float* logits, int T, int32_t* idx, float* w);
 cudaError_t launch_permutation(const LaunchCtx& L, const int32_t* idx, int T, int32_t* local_rank,
                                int32_t* blk_counts, int32_t* blk_base, int32_t* offsets, int32_t* gather);

@@ -165,43 +165,10 @@ __global__ void __launch_bounds__(RT_WARPS * 32) router_logits_decode_kernel(con
 }
 
 // ---------------------------------------------------------------------------
-// general-T router logits (CUDA cores; used by route-only for T > 32)
+// selection from given fp32 logits (route-only fed with logits): one warp per
+// token, the same warp top-6 as the forward path
 // ---------------------------------------------------------------------------
 
-constexpr int RG_TOK = 8;   // tokens per CTA row of the grid
-
-__global__ void __launch_bounds__(RT_WARPS * 32) router_logits_general_kernel(const __nv_bfloat16* x, int T,
-                                                                            const __nv_bfloat16* Wr,
-                                                                            const float* bias, float* logits) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int e = blockIdx.x * RT_WARPS + warp;
-    uint4 wr[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) wr[i] = ldg16(Wr + (size_t)e * H + 8 * (lane + 32 * i));
-    const float b = bias ? __ldg(bias + e) : 0.f;
-    pdl_wait();
-    const int t0 = blockIdx.y * RG_TOK;
-    for (int t = t0; t < min(T, t0 + RG_TOK); ++t) {
-        const __nv_bfloat16* xr = x + (size_t)t * H;
-        float acc = 0.f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint4 xv = ldg16(xr + 8 * (lane + 32 * i));
-            acc = fmaf(bf_lo(wr[i].x), bf_lo(xv.x), acc);
-            acc = fmaf(bf_hi(wr[i].x), bf_hi(xv.x), acc);
-            acc = fmaf(bf_lo(wr[i].y), bf_lo(xv.y), acc);
-            acc = fmaf(bf_hi(wr[i].y), bf_hi(xv.y), acc);
-            acc = fmaf(bf_lo(wr[i].z), bf_lo(xv.z), acc);
-            acc = fmaf(bf_hi(wr[i].z), bf_hi(xv.z), acc);
-            acc = fmaf(bf_lo(wr[i].w), bf_lo(xv.w), acc);
-            acc = fmaf(bf_hi(wr[i].w), bf_hi(xv.w), acc);
-        }
-        acc = warp_sum(acc);
-        if (lane == 0) logits[(size_t)t * E + e] = acc + b;
-    }
-}
-
-// one warp per token: selection from fp32 logits
 __global__ void __launch_bounds__(128) select_kernel(const float* logits, int T, int32_t* idx, float* w) {
     pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -333,12 +300,6 @@ cudaError_t launch_router_logits_decode(const LaunchCtx& L, const __nv_bfloat16*
                                         const __nv_bfloat16* Wr, const float* bias, float* logits) {
     return launch_hooked(L, FLINT_KERNEL_ROUTER, router_logits_decode_kernel,
                          dim3(RT_CTAS, (T + RL_TOK - 1) / RL_TOK), dim3(RT_WARPS * 32), 0, x, T, Wr, bias, logits);
-}
-
-cudaError_t launch_router_logits_general(const LaunchCtx& L, const __nv_bfloat16* x, int T,
-                                         const __nv_bfloat16* Wr, const float* bias, float* logits) {
-    return launch_pdl(L, router_logits_general_kernel, dim3(RT_CTAS, (T + RG_TOK - 1) / RG_TOK),
-                      dim3(RT_WARPS * 32), 0, x, T, Wr, bias, logits);
 }
 
 cudaError_t launch_select(const LaunchCtx& L, const float* logits, int T, int32_t* idx, float* w) {
