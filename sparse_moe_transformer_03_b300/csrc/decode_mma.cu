@@ -18,12 +18,16 @@
 //                256w + 255 (8 KiB) into its ring and multiplies them; the
 //                eight partial sums are added in warp order in smem, then
 //                a = silu(g) * u is written as bf16.
-//   down_mma     CTA c owns output rows 16c .. 16c + 15 (one M tile); warp w
-//                takes expert slots w, w + 8, ..., each 2 chunks of 256
-//                columns (4 pieces of 2 KiB); the activations are staged in
-//                smem when the batch has at most 64 (token, expert) pairs; w *
-//                D accumulates per (token, row) in the warp's own buffer and
-//                the eight buffers are summed in warp order: deterministic.
+//   down_mma     CTA c owns output rows 16c .. 16c + 15 (one M tile).  Its
+//                work items are (slot, column half, tile of 8 tokens): 256
+//                columns of the slot's 16 rows (4 pieces of 2 KiB) against up
+//                to 8 of its tokens; item j goes to warp j % 8, so the shared
+//                slot's tiles and halves spread over the warps.  The
+//                activations are staged in smem when the batch has at most 64
+//                (token, expert) pairs, else each item's B fragments are
+//                fetched into registers while the item before it computes.
+//                w * D accumulates per (token, row) in the warp's own buffer
+//                and the eight buffers are summed in warp order: deterministic.
 //
 // Routing and tables are those of decode.cu; like the NVFP4 down kernel, the
 // down kernel routes for itself and starts its weight chunks before waiting
@@ -71,7 +75,7 @@ struct GateUpMmaParams {
 static inline int mg_ns(int T) { return T <= 16 ? 2 : 1; }
 static inline size_t mg_smem_bytes(int T) {
     return (size_t)MM_WARPS * mg_ns(T) * MM_CHUNK + (size_t)T * MG_XROW * 2 + (size_t)MG_PART * 4 +
-           (size_t)MM_WARPS * mg_ns(T) * 8 + sizeof(DecodeTables) + DEC_T * TOPK * 8 + 2 * E * 4;
+           (size_t)(MM_WARPS * mg_ns(T) + 1) * 8 + sizeof(DecodeTables) + DEC_T * TOPK * 8 + 2 * E * 4;
 }
 
 // The CTA works on one unit at a time: warp w streams and multiplies the
@@ -87,7 +91,8 @@ __global__ void __launch_bounds__(MM_WARPS * 32, 1) gateup_mma_kernel(GateUpMmaP
     float* part = reinterpret_cast<float*>(xs + (size_t)T * MG_XROW);
     uint64_t* bars = reinterpret_cast<uint64_t*>(part + MG_PART);
     uint64_t* bar = bars + warp * NS;
-    DecodeTables* tab = reinterpret_cast<DecodeTables*>(bars + MM_WARPS * NS);
+    uint64_t* xbar = bars + MM_WARPS * NS;   // the staged x rows
+    DecodeTables* tab = reinterpret_cast<DecodeTables*>(xbar + 1);
     int* sel_e = reinterpret_cast<int*>(tab + 1);
     float* sel_w = reinterpret_cast<float*>(sel_e + DEC_T * TOPK);
     uint32_t* tmask = reinterpret_cast<uint32_t*>(sel_w + DEC_T * TOPK);
@@ -95,6 +100,7 @@ __global__ void __launch_bounds__(MM_WARPS * 32, 1) gateup_mma_kernel(GateUpMmaP
 
     if (lane == 0) {
         for (int s = 0; s < NS; ++s) mbar_init(&bar[s], 1);
+        if (warp == 0) mbar_init(xbar, 1);
         fence_mbar_init();
     }
     __syncthreads();
@@ -136,9 +142,12 @@ __global__ void __launch_bounds__(MM_WARPS * 32, 1) gateup_mma_kernel(GateUpMmaP
     pdl_wait();     // router logits are complete (and x is ready)
     pdl_trigger();
 
-    for (int k = threadIdx.x; k < T * (H / 8); k += blockDim.x) {
-        const int t = k / (H / 8), col = (k % (H / 8)) * 8;
-        *reinterpret_cast<uint4*>(xs + (size_t)t * MG_XROW + col) = ldg16(p.x + (size_t)t * H + col);
+    // x rows by bulk copy (lane t of warp 0 copies token t; T <= 32), landing
+    // while the CTA ranks the experts
+    if (warp == 0) {
+        if (lane == 0) mbar_arrive_expect_tx(xbar, (uint32_t)T * H * 2);
+        __syncwarp();
+        if (lane < T) bulk_g2s(xs + (size_t)lane * MG_XROW, p.x + (size_t)lane * H, H * 2, xbar);
     }
 
     // ---- top-6 of every token, then the (slot, token) tables ----
@@ -185,9 +194,9 @@ __global__ void __launch_bounds__(MM_WARPS * 32, 1) gateup_mma_kernel(GateUpMmaP
     const uint32_t lrow = (uint32_t)((mi & 1) * 1024 + li * 128);
     const int lkh = mi >> 1;
     const int g = lane >> 2, cq = lane & 3;
-    bool ok = true;
+    bool ok = __syncthreads_and(mbar_wait_bounded(xbar, 0, p.limit_ns));
     int i = 0;
-    for (; i < my_units; ++i) {
+    for (; ok && i < my_units; ++i) {
         const int q = unit_of(i), u = q / MG_UNITS, r = q & (MG_UNITS - 1);
         const int pb = tab->slot_pair0[u], np = tab->slot_pair0[u + 1] - pb;   // 1..32 tokens
         const int ntile = (np + 7) >> 3;
@@ -266,6 +275,7 @@ __global__ void __launch_bounds__(MM_WARPS * 32, 1) gateup_mma_kernel(GateUpMmaP
         if (lane == 0) {
             report_status(p.status, ST_TIMEOUT);
             for (int k = i; k < issued; ++k) mbar_wait_bounded(&bar[k % NS], (k / NS) & 1, p.limit_ns);
+            if (warp == 0) mbar_wait_bounded(xbar, 0, p.limit_ns);
         }
         __syncwarp();
     }
@@ -278,6 +288,9 @@ __global__ void __launch_bounds__(MM_WARPS * 32, 1) gateup_mma_kernel(GateUpMmaP
 constexpr int MD_CTAS = H / 16;          // 128
 constexpr int MD_APAIRS = 64;            // activation rows staged in smem up to this many pairs
 constexpr int MD_AROW = I * 2 + 16;      // bytes per staged row
+// items: 2 column halves x the N tiles of every slot (sum of ceil(np / 8) over
+// the slots is below slots + pairs / 8)
+constexpr int MD_MAX_ITEMS = 2 * (NEXP + DEC_PAIRS / 8);
 
 struct DownMmaParams {
     const uint8_t* tiled;
@@ -295,7 +308,30 @@ __host__ __device__ inline bool md_staged(int T) { return (TOPK + 1) * T <= MD_A
 static inline size_t md_smem_bytes(int T) {
     return (size_t)MM_WARPS * md_ns(T) * MM_CHUNK + (md_staged(T) ? (size_t)(TOPK + 1) * T * MD_AROW : 0) +
            (size_t)MM_WARPS * T * 16 * 4 + (MM_WARPS * md_ns(T) + 1) * 8 + sizeof(DecodeTables) +
-           DEC_T * TOPK * 8 + 2 * E * 4;
+           DEC_T * TOPK * 8 + 2 * E * 4 + (MD_MAX_ITEMS + 1) * 4;
+}
+
+// Lists the down kernel's work items in slot order, each slot's first column
+// half before its second and the N tiles in order within a half; packed as
+// slot << 3 | half << 2 | tile.  One warp; returns the count on every lane.
+__device__ __forceinline__ int build_down_items_warp(const DecodeTables* tab, int* items, int lane) {
+    int base = 0;
+    for (int u0 = 0; u0 < tab->n_slots; u0 += 32) {
+        const int u = u0 + lane;
+        const int nt = u < tab->n_slots ? (tab->slot_pair0[u + 1] - tab->slot_pair0[u] + 7) >> 3 : 0;
+        int inc = nt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+            if (lane >= o) inc += v;
+        }
+        const int off = base + 2 * (inc - nt);
+        for (int hk = 0; hk < 2; ++hk)
+            for (int t = 0; t < nt; ++t) items[off + hk * nt + t] = (u << 3) | (hk << 2) | t;
+        base += 2 * __shfl_sync(0xFFFFFFFFu, inc, 31);
+    }
+    __syncwarp();
+    return base;
 }
 
 __global__ void __launch_bounds__(MM_WARPS * 32, 1) down_mma_kernel(DownMmaParams p) {
@@ -315,17 +351,22 @@ __global__ void __launch_bounds__(MM_WARPS * 32, 1) down_mma_kernel(DownMmaParam
     float* sel_w = reinterpret_cast<float*>(sel_e + DEC_T * TOPK);
     uint32_t* tmask = reinterpret_cast<uint32_t*>(sel_w + DEC_T * TOPK);
     int* pair0 = reinterpret_cast<int*>(tmask + E);
+    int* items = pair0 + E;
+    int* n_items_s = items + MD_MAX_ITEMS;
 
     if (lane == 0) {
         for (int s = 0; s < NS; ++s) mbar_init(&bar[s], 1);
         if (warp == 0) mbar_init(abar, 1);
         fence_mbar_init();
     }
-    // chunk ci of the warp: slot ci / 2, columns 256 (ci % 2) .. + 255 of rows 16c .. 16c + 15
-    auto issue = [&](int ci, int expert) {
-        const int s = ci % NS;
+    // the warp's k-th item is items[warp + 8k]; its weights: columns 256 half
+    // .. + 255 of rows 16c .. 16c + 15 of the slot's expert
+    auto item_of = [&](int k) { return items[warp + MM_WARPS * k]; };
+    auto issue = [&](int k) {
+        const int it = item_of(k), s = k % NS;
+        const int expert = tab->slot_expert[it >> 3];
         const uint8_t* base = p.tiled + (size_t)expert * MM_EXPERT_BYTES + MM_DOWN_OFF + (size_t)(c & 7) * 2048;
-        const int rb = c >> 3, kc0 = (ci & 1) * 4;
+        const int rb = c >> 3, kc0 = ((it >> 2) & 1) * 4;
         uint8_t* dst = ring + (size_t)s * MM_CHUNK;
         mbar_arrive_expect_tx(&bar[s], MM_CHUNK);
 #pragma unroll
@@ -350,16 +391,19 @@ __global__ void __launch_bounds__(MM_WARPS * 32, 1) down_mma_kernel(DownMmaParam
     }
     for (int k = threadIdx.x; k < MM_WARPS * Tk * 16; k += blockDim.x) yw_all[k] = 0.f;
     __syncthreads();
-    if (warp == 0) build_decode_tables_warp(Tk, sel_e, sel_w, tmask, pair0, tab, lane);
+    if (warp == 0) {
+        build_decode_tables_warp(Tk, sel_e, sel_w, tmask, pair0, tab, lane);
+        const int n = build_down_items_warp(tab, items, lane);
+        if (lane == 0) *n_items_s = n;
+    }
     __syncthreads();
-    const int n_slots = tab->n_slots, n_pairs = tab->n_pairs;
-    const int my_slots = n_slots > warp ? (n_slots - warp + MM_WARPS - 1) / MM_WARPS : 0;
-    const int total_chunks = 2 * my_slots;
+    const int n_items = *n_items_s, n_pairs = tab->n_pairs;
+    const int my_items = n_items > warp ? (n_items - warp + MM_WARPS - 1) / MM_WARPS : 0;
     int issued = 0;
     if (lane == 0) {
-        for (int ci = 0; ci < NS && ci < total_chunks; ++ci) {
-            issue(ci, tab->slot_expert[warp + MM_WARPS * (ci >> 1)]);
-            issued = ci + 1;
+        for (int k = 0; k < NS && k < my_items; ++k) {
+            issue(k);
+            issued = k + 1;
         }
     }
     pdl_wait();     // the gate/up kernel is complete: activations are visible
@@ -369,109 +413,98 @@ __global__ void __launch_bounds__(MM_WARPS * 32, 1) down_mma_kernel(DownMmaParam
         for (int pr = 0; pr < n_pairs; ++pr) bulk_g2s(astage + (size_t)pr * MD_AROW, p.a + (size_t)pr * I, I * 2, abar);
     }
     bool ok = true;
-    if (staged && my_slots > 0) ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(abar, 0, p.limit_ns));
+    if (staged && my_items > 0) ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(abar, 0, p.limit_ns));
 
     const int mi = lane >> 3, li = lane & 7;
     const int lr = (mi & 1) * 8 + li;               // row 0..15 of the M tile
     const uint32_t lrow = (uint32_t)lr * 128;
     const int lkh = mi >> 1;
     const int g = lane >> 2, cq = lane & 3;
-    int ci = 0, i = 0;
-    for (; ok && i < my_slots; ++i) {
-        const int u = warp + MM_WARPS * i;
+    // this lane's B row of item k: pair pb + 8 tile + g (the last pair past np)
+    auto b_row = [&](int it) {
+        const int u = it >> 3, pb = tab->slot_pair0[u], np = tab->slot_pair0[u + 1] - pb;
+        const int n = (it & 3) * 8 + g;
+        return pb + (n < np ? n : np - 1);
+    };
+    // B fragments of the warp's k-th item from the activations in global
+    // memory (read-only here; written by the previous grid)
+    auto load_b = [&](int k, uint32_t (&b)[16][2]) {
+        const int it = item_of(k);
+        const unsigned int* a0 = reinterpret_cast<const unsigned int*>(p.a + (size_t)b_row(it) * I +
+                                                                       ((it >> 2) & 1) * 256 + 2 * cq);
+#pragma unroll
+        for (int kb = 0; kb < 16; ++kb) {
+            b[kb][0] = __ldg(a0 + kb * 8);
+            b[kb][1] = __ldg(a0 + kb * 8 + 4);
+        }
+    };
+    uint32_t bq[16][2];
+    if (!staged && my_items > 0) load_b(0, bq);
+    int k = 0;
+    for (; ok && k < my_items; ++k) {
+        const int it = item_of(k), u = it >> 3, hk = (it >> 2) & 1, nt = it & 3;
         const int pb = tab->slot_pair0[u], np = tab->slot_pair0[u + 1] - pb;
-        const int ntile = (np + 7) >> 3;
-        int prow[4];
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-            const int n = nt * 8 + g;
-            prow[nt] = pb + (n < np ? n : np - 1);
+        uint32_t bn[16][2];
+        if (!staged && k + 1 < my_items) load_b(k + 1, bn);
+        const int s = k % NS;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(&bar[s], (k / NS) & 1, p.limit_ns))) {
+            ok = false;
+            break;
         }
-        float acc[4][4];
+        const uint8_t* buf = ring + (size_t)s * MM_CHUNK;
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        if (staged) {
+            const uint8_t* ar = astage + (size_t)b_row(it) * MD_AROW + (hk * 256 + 2 * cq) * 2;
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-        for (int hk = 0; hk < 2; ++hk, ++ci) {
-            const int s = ci % NS;
-            if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(&bar[s], (ci / NS) & 1, p.limit_ns))) {
-                ok = false;
-                break;
+            for (int kb = 0; kb < 16; ++kb) {
+                uint32_t a[4];
+                const int kt = kb >> 2, j = 2 * (kb & 3) + lkh;
+                ldmatrix_x4(a, buf + kt * 2048 + lrow + ((j ^ li) << 4));
+                mma_bf16_16816(acc[kb & 1], a, *reinterpret_cast<const uint32_t*>(ar + kb * 32),
+                               *reinterpret_cast<const uint32_t*>(ar + kb * 32 + 16));
             }
-            const uint8_t* buf = ring + (size_t)s * MM_CHUNK;
-            if (staged) {
-#pragma unroll 4
-                for (int kb = 0; kb < 16; ++kb) {
-                    uint32_t a[4];
-                    const int kt = kb >> 2, j = 2 * (kb & 3) + lkh;
-                    ldmatrix_x4(a, buf + kt * 2048 + lrow + ((j ^ li) << 4));
-                    const int kx = hk * 256 + kb * 16 + 2 * cq;
+        } else {
 #pragma unroll
-                    for (int nt = 0; nt < 4; ++nt) {
-                        if (nt < ntile) {
-                            const uint8_t* ar = astage + (size_t)prow[nt] * MD_AROW + kx * 2;
-                            mma_bf16_16816(acc[nt], a, *reinterpret_cast<const uint32_t*>(ar),
-                                           *reinterpret_cast<const uint32_t*>(ar + 16));
-                        }
-                    }
-                }
-            } else {
-                // activations through L1 (read-only here; written by the previous
-                // grid): the first N tile's operands for the whole chunk are
-                // requested at once, the other tiles' four blocks at a time
-                uint32_t bq[16][2];
-                const unsigned int* a0 =
-                    reinterpret_cast<const unsigned int*>(p.a + (size_t)prow[0] * I + hk * 256 + 2 * cq);
-#pragma unroll
-                for (int kb = 0; kb < 16; ++kb) {
-                    bq[kb][0] = __ldg(a0 + kb * 8);
-                    bq[kb][1] = __ldg(a0 + kb * 8 + 4);
-                }
-#pragma unroll
-                for (int kb = 0; kb < 16; ++kb) {
-                    uint32_t a[4];
-                    const int kt = kb >> 2, j = 2 * (kb & 3) + lkh;
-                    ldmatrix_x4(a, buf + kt * 2048 + lrow + ((j ^ li) << 4));
-                    mma_bf16_16816(acc[0], a, bq[kb][0], bq[kb][1]);
-                    const int kx = hk * 256 + kb * 16 + 2 * cq;
-#pragma unroll
-                    for (int nt = 1; nt < 4; ++nt) {
-                        if (nt < ntile) {
-                            const unsigned int* ar =
-                                reinterpret_cast<const unsigned int*>(p.a + (size_t)prow[nt] * I + kx);
-                            mma_bf16_16816(acc[nt], a, __ldg(ar), __ldg(ar + 4));
-                        }
-                    }
-                }
-            }
-            __syncwarp();
-            if (lane == 0 && ci + NS < total_chunks) {
-                fence_proxy_async_smem();
-                issue(ci + NS, tab->slot_expert[warp + MM_WARPS * ((ci + NS) >> 1)]);
-                issued = ci + NS + 1;
+            for (int kb = 0; kb < 16; ++kb) {
+                uint32_t a[4];
+                const int kt = kb >> 2, j = 2 * (kb & 3) + lkh;
+                ldmatrix_x4(a, buf + kt * 2048 + lrow + ((j ^ li) << 4));
+                mma_bf16_16816(acc[kb & 1], a, bq[kb][0], bq[kb][1]);
             }
         }
-        if (!ok) break;
+        __syncwarp();
+        if (lane == 0 && k + NS < my_items) {
+            fence_proxy_async_smem();
+            issue(k + NS);
+            issued = k + NS + 1;
+        }
+        // lane (g, cq) holds rows g, g + 8 of tokens 2cq, 2cq + 1 of the tile
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
+        for (int hh = 0; hh < 2; ++hh) {
+            const int n = nt * 8 + 2 * cq + hh;
+            if (n < np) {
+                const int pr = pb + n, t = tab->pair_token[pr];
+                const float wgt = tab->pair_weight[pr];
+                yw[t * 16 + g] = fmaf(wgt, acc[0][hh] + acc[1][hh], yw[t * 16 + g]);
+                yw[t * 16 + g + 8] = fmaf(wgt, acc[0][2 + hh] + acc[1][2 + hh], yw[t * 16 + g + 8]);
+            }
+        }
+        if (!staged) {
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int n = nt * 8 + 2 * cq + hh;
-                if (nt < ntile && n < np) {
-                    const int pr = pb + n, t = tab->pair_token[pr];
-                    const float wgt = tab->pair_weight[pr];
-                    yw[t * 16 + g] = fmaf(wgt, acc[nt][hh], yw[t * 16 + g]);
-                    yw[t * 16 + g + 8] = fmaf(wgt, acc[nt][2 + hh], yw[t * 16 + g + 8]);
-                }
+            for (int kb = 0; kb < 16; ++kb) {
+                bq[kb][0] = bn[kb][0];
+                bq[kb][1] = bn[kb][1];
             }
         }
     }
     if (!ok && lane == 0) {
         report_status(p.status, ST_TIMEOUT);
-        for (int k = ci; k < issued; ++k) mbar_wait_bounded(&bar[k % NS], (k / NS) & 1, p.limit_ns);
+        for (int q = k; q < issued; ++q) mbar_wait_bounded(&bar[q % NS], (q / NS) & 1, p.limit_ns);
         if (staged && warp == 0) mbar_wait_bounded(abar, 0, p.limit_ns);
     }
     __syncthreads();
-    for (int k = threadIdx.x; k < Tk * 16; k += blockDim.x) {
-        const int t = k >> 4, rr = k & 15;
+    for (int q = threadIdx.x; q < Tk * 16; q += blockDim.x) {
+        const int t = q >> 4, rr = q & 15;
         float sum = 0.f;
 #pragma unroll
         for (int w = 0; w < MM_WARPS; ++w) sum += yw_all[w * Tk * 16 + t * 16 + rr];
@@ -497,6 +530,7 @@ cudaError_t decode_mma_set_attributes() {
 cudaError_t launch_decode_experts_mma(const LaunchCtx& L, const uint8_t* tiled, const float* logits,
                                       const __nv_bfloat16* x, int T, DecodeTables* tables, int32_t* idx, float* w,
                                       float* a_buf, __nv_bfloat16* y) {
+    if (T < 1 || T > DEC_T) return cudaErrorInvalidValue;   // x rows are copied one per lane of a warp
     __nv_bfloat16* a16 = reinterpret_cast<__nv_bfloat16*>(a_buf);
     GateUpMmaParams gp{tiled, logits, x, T, mg_ns(T), tables, idx, w, a16, L.status, L.wait_limit_ns};
     cudaError_t e = launch_hooked(L, FLINT_KERNEL_GATE_UP, gateup_mma_kernel, dim3(L.num_sms), dim3(MM_WARPS * 32),
