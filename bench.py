@@ -49,17 +49,14 @@ DOWN_BYTES = 2048 * 512 * 2                   # one expert's down matrix, bf16
 # NVFP4: E2M1 codes (half a byte per weight) + one E4M3 scale per 16 weights + an fp32 scale per matrix
 NV_GATE_UP_BYTES = 2 * 512 * 2048 // 2 + 2 * 512 * 2048 // 16 + 4     # 1,179,652
 NV_DOWN_BYTES = 2048 * 512 // 2 + 2048 * 512 // 16 + 4                  # 589,828
-DECODE_MMA_MIN_T = 5          # the library's threshold (csrc/flint_internal.h DEC_MMA_MIN_T)
 # kernel ids of flint_moe_set_kernel_events (include/flint_moe.h)
 K_ROUTER, K_GATE_UP, K_DOWN, K_COMBINE = 0, 1, 2, 3
 # the source files each timed kernel is built from (for the ncu traffic record)
 KERNEL_SOURCES = {
-    "gateup_decode_kernel": ["decode.cu", "routing.cuh", "flint_common.cuh"],
     "gateup_nvfp4_kernel": ["decode_nvfp4.cu", "routing.cuh", "flint_common.cuh"],
     "gateup_mma_kernel": ["decode_mma.cu", "mma_sync.cuh", "routing.cuh", "flint_common.cuh"],
     "down_mma_kernel": ["decode_mma.cu", "mma_sync.cuh", "routing.cuh", "flint_common.cuh"],
     "down_nvfp4_kernel": ["decode_nvfp4.cu", "flint_common.cuh"],
-    "down_decode_kernel": ["decode.cu", "flint_common.cuh"],
     "prefill_gateup_kernel": ["prefill.cu", "tc_ptx.cuh", "flint_common.cuh"],
     "prefill_down_kernel": ["prefill.cu", "tc_ptx.cuh", "flint_common.cuh"],
 }
@@ -527,11 +524,8 @@ def run_flint(args, wl, ws, rank, local):
     calls = [(handles[l], x, T, ys[l]) for l in range(L)]
     ksteps = max(3, min(args.steps, 10))
     kern = {}
-    # bf16 batches of DECODE_MMA_MIN_T tokens or more run on the mma.sync kernels (decode_mma.cu)
-    bf16_names = ("gateup_mma_kernel", "down_mma_kernel") if T >= DECODE_MMA_MIN_T else \
-        ("gateup_decode_kernel", "down_decode_kernel")
     kernels = ((("gateup_nvfp4_kernel", K_GATE_UP, NV_GATE_UP_BYTES), ("down_nvfp4_kernel", K_DOWN, NV_DOWN_BYTES))
-               if nv else ((bf16_names[0], K_GATE_UP, GATE_UP_BYTES), (bf16_names[1], K_DOWN, DOWN_BYTES)))
+               if nv else (("gateup_mma_kernel", K_GATE_UP, GATE_UP_BYTES), ("down_mma_kernel", K_DOWN, DOWN_BYTES)))
     for name, kid, per_expert in kernels:
         d = kernel_durations(flint, torch, stream, calls, kid, ksteps)
         tot_ms = sum(sum(r) for r in d)

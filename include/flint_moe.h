@@ -56,7 +56,7 @@ extern "C" {
 typedef struct flint_moe* flint_moe_t;
 
 typedef enum {
-    FLINT_BF16 = 0,   /* bf16 weights, borrowed from the caller            */
+    FLINT_BF16 = 0,   /* bf16 expert weights, copied into an owned layout  */
     FLINT_NVFP4 = 1   /* NVFP4 (W4A16) expert weights, repacked and owned   */
 } flint_dtype_t;
 
@@ -93,13 +93,13 @@ typedef struct {
  *   down_W     host array of 256 entries: bf16 [2048][512], or flint_nvfp4_t*.
  *   shared_W   host array {gate_up, down} of the shared expert, same rules.
  *   dtype      FLINT_BF16 or FLINT_NVFP4 (the router stays bf16 either way).
- * Ownership: bf16 weights are borrowed (the caller keeps them alive and
- * unchanged until destroy: the decode kernels stream them in place).  For
- * FLINT_BF16 the handle additionally owns a copy of every expert matrix cut
- * into 16 KiB tensor-core operand tiles for the many-token path (1.6 GB per
- * layer).  The router (bf16, both dtypes) is borrowed.  The handle owns its
- * pointer tables and a workspace for FLINT_CHUNK tokens (about 310 MB).
- * NVFP4 weights are repacked into a layout the handle owns (1.77 MB per
+ * Ownership: bf16 expert weights are read during create only: the handle
+ * owns a copy of every expert matrix cut into 16 KiB tensor-core operand
+ * tiles (1.6 GB per layer), which both the decode and the many-token path
+ * read, and the caller may free its buffers on return.  The router (bf16,
+ * both dtypes) is borrowed: it stays alive and unchanged until destroy.  The
+ * handle owns a workspace for FLINT_CHUNK tokens (about 310 MB).  NVFP4
+ * weights are repacked into a layout the handle owns (1.77 MB per
  * expert, no bf16 copy); the caller may free its buffers on return.
  * Synchronises the device.
  * Errors: INVALID_ARG, OOM, CUDA, UNSUPPORTED (device is not sm_103). */

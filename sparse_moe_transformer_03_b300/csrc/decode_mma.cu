@@ -1,8 +1,23 @@
-// decode_mma.cu -- bf16 weight-streaming decode kernels on the warp-level
-// tensor core (mma.sync m16n8k16), for batches where the CUDA-core kernels of
-// decode.cu turn compute-bound (each weight meets several tokens: every
-// token multiplies the shared expert, and tokens of one cluster share
-// routed experts).
+// decode_mma.cu -- bf16 weight-streaming decode kernels (T <= 32) on the
+// warp-level tensor core (mma.sync m16n8k16).
+//
+// Layer definition: RecursiveSI/flint (vLLM recipe page), "Overview" (256
+// experts, top-6 sigmoid routing plus a shared expert); SwiGLU experts with
+// H = 2048, I = 512 are this library's reading (the pages name neither).
+//
+// At decode sizes each expert weight meets only a few tokens, so the layer is
+// bound by reading the touched experts' weights from HBM once: (U + 1)
+// experts x 6 MiB, U = distinct routed experts of the batch.  The expert
+// matrices are dotted with the tokens on the tensor core all the same: one
+// MMA instruction does 2048 multiply-adds for the warp, so the kernels keep
+// pace with HBM when every weight meets 8 or more tokens (the shared expert
+// meets all of them), and at one token they measured faster than CUDA-core
+// dot products as well.  After the router kernel has written the
+// fp32 logits, two kernels run, chained with programmatic dependent launch;
+// each ranks the experts of every token from the logits and builds the
+// (expert slot, token) tables in its own shared memory (slot 0 = the shared
+// expert), and the shared expert's first weights are requested before the
+// kernel waits on the router.
 //
 // They read the handle's tiled copy of the experts (repack.cu): tiles of 128
 // rows x 64 columns in the 128-byte-swizzled layout.  Eight consecutive rows
@@ -12,11 +27,12 @@
 // 8x8 matrix over all banks).
 //
 //   gateup_mma   Unit = 8 gate rows + the 8 matching up rows of one expert
-//                (the MMA's 16 rows) against the expert's tokens (the N
-//                columns, tiles of 8; x staged in smem as bf16).  The CTA
-//                takes one unit at a time: warp w streams columns 256w ..
-//                256w + 255 (8 KiB) into its ring and multiplies them; the
-//                eight partial sums are added in warp order in smem, then
+//                (the MMA's 16 rows); item = a unit against one tile of up
+//                to 8 of the expert's tokens (the N columns).  The CTA takes
+//                one item at a time: warp w streams columns 256w .. 256w +
+//                255 (8 KiB) into its ring and multiplies them by x
+//                fragments it fetched into registers during the item before;
+//                the eight partial sums are added in warp order in smem, then
 //                a = silu(g) * u is written as bf16.
 //   down_mma     CTA c owns output rows 16c .. 16c + 15 (one M tile).  Its
 //                work items are (slot, column half, tile of 8 tokens): 256
@@ -29,9 +45,8 @@
 //                w * D accumulates per (token, row) in the warp's own buffer
 //                and the eight buffers are summed in warp order: deterministic.
 //
-// Routing and tables are those of decode.cu; like the NVFP4 down kernel, the
-// down kernel routes for itself and starts its weight chunks before waiting
-// on the gate/up kernel.
+// The down kernel routes for itself, like the NVFP4 one, and starts its
+// weight chunks before waiting on the gate/up kernel.
 #include "flint_common.cuh"
 #include "../../include/flint_moe.h"
 #include "flint_internal.h"
@@ -53,15 +68,12 @@ constexpr int MM_WARPS = 8;
 // ---------------------------------------------------------------------------
 
 constexpr int MG_UNITS = I / 8;          // 64 units per expert
-constexpr int MG_XROW = H + 8;           // bf16 per staged x row (+8: conflict-free B loads)
-constexpr int MG_PART = MM_WARPS * 4 * 32 * 4;   // per-warp partial sums: [warp][N tile][lane][4]
 
 struct GateUpMmaParams {
     const uint8_t* tiled;         // the handle's tiled experts
     const float* logits;
     const __nv_bfloat16* x;
     int T;
-    int ns;
     DecodeTables* tables_out;
     int32_t* idx_out;
     float* w_out;
@@ -70,85 +82,71 @@ struct GateUpMmaParams {
     uint64_t limit_ns;
 };
 
-// ring chunks per warp: two (the next unit's chunk in flight) while x is
-// small, one when x fills the shared memory (the next chunk then goes to L2)
-static inline int mg_ns(int T) { return T <= 16 ? 2 : 1; }
-static inline size_t mg_smem_bytes(int T) {
-    return (size_t)MM_WARPS * mg_ns(T) * MM_CHUNK + (size_t)T * MG_XROW * 2 + (size_t)MG_PART * 4 +
-           (size_t)(MM_WARPS * mg_ns(T) + 1) * 8 + sizeof(DecodeTables) + DEC_T * TOPK * 8 + 2 * E * 4;
+// Work item = (slot u, unit r, tile nt of 8 tokens), packed u << 8 | r << 2 |
+// nt; item j of the grid goes to CTA j % G.  Each warp fetches its B
+// fragments (x rows of the tile's tokens, its 256 columns) into registers
+// while the item before runs, so x needs no shared memory and the weight ring
+// holds three chunks per warp.  A unit with several token tiles (the shared
+// expert's for T > 8) reads its weights once per tile; the repeats hit L2.
+
+constexpr int MI_NS = 3;                            // ring chunks per warp
+constexpr int MI_MAX_CTA_ITEMS = 256;               // items of one CTA (grid >= 72 CTAs)
+constexpr int MI_PART = 2 * MM_WARPS * 32 * 4;      // partial sums: [item parity][warp][lane][4]
+
+static inline size_t mi_smem_bytes() {
+    return (size_t)MM_WARPS * MI_NS * MM_CHUNK + (size_t)MI_PART * 4 + (size_t)MM_WARPS * MI_NS * 8 +
+           sizeof(DecodeTables) + DEC_T * TOPK * 8 + 2 * E * 4 + (NEXP + 1) * 4 + MI_MAX_CTA_ITEMS * 4;
 }
 
-// The CTA works on one unit at a time: warp w streams and multiplies the
-// unit's columns 256w .. 256w + 255, the eight partial sums meet in shared
-// memory and are added in warp order.  Units per CTA then differ by at most
-// one across the grid (whole units per warp would differ by a factor of two).
 __global__ void __launch_bounds__(MM_WARPS * 32, 1) gateup_mma_kernel(GateUpMmaParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int NS = p.ns, T = p.T, G = gridDim.x, c = blockIdx.x;
-    uint8_t* ring = smem + (size_t)warp * NS * MM_CHUNK;
-    __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(smem + (size_t)MM_WARPS * NS * MM_CHUNK);
-    float* part = reinterpret_cast<float*>(xs + (size_t)T * MG_XROW);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(part + MG_PART);
-    uint64_t* bar = bars + warp * NS;
-    uint64_t* xbar = bars + MM_WARPS * NS;   // the staged x rows
-    DecodeTables* tab = reinterpret_cast<DecodeTables*>(xbar + 1);
+    const int T = p.T, G = gridDim.x, c = blockIdx.x;
+    uint8_t* ring = smem + (size_t)warp * MI_NS * MM_CHUNK;
+    float* part = reinterpret_cast<float*>(smem + (size_t)MM_WARPS * MI_NS * MM_CHUNK);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(part + MI_PART) + warp * MI_NS;
+    DecodeTables* tab = reinterpret_cast<DecodeTables*>(reinterpret_cast<uint64_t*>(part + MI_PART) + MM_WARPS * MI_NS);
     int* sel_e = reinterpret_cast<int*>(tab + 1);
     float* sel_w = reinterpret_cast<float*>(sel_e + DEC_T * TOPK);
     uint32_t* tmask = reinterpret_cast<uint32_t*>(sel_w + DEC_T * TOPK);
     int* pair0 = reinterpret_cast<int*>(tmask + E);
+    int* slot_item0 = pair0 + E;                     // first item of each slot (+ the total)
+    int* list = slot_item0 + NEXP + 1;               // this CTA's items c, c + G, ...
 
     if (lane == 0) {
-        for (int s = 0; s < NS; ++s) mbar_init(&bar[s], 1);
-        if (warp == 0) mbar_init(xbar, 1);
+        for (int s = 0; s < MI_NS; ++s) mbar_init(&bar[s], 1);
         fence_mbar_init();
     }
     __syncthreads();
 
-    // the CTA's i-th unit; this warp's piece of it: column tiles 4w .. 4w + 3
-    auto unit_of = [&](int i) { return c + G * i; };
-    auto piece = [&](int i, int expert, int kt, int half) {
-        const int r = unit_of(i) & (MG_UNITS - 1);
-        const int rb = (r >> 4) + 4 * half, kc = warp * 4 + kt;
-        return p.tiled + (size_t)expert * MM_EXPERT_BYTES + ((size_t)rb * MM_GU_KT + kc) * MM_TILE +
-               (size_t)(r & 15) * 1024;
-    };
-    auto issue = [&](int i, int expert) {
-        const int s = i % NS;
+    const int nt0 = (T + 7) >> 3;                    // token tiles of the shared slot (slot 0)
+    // this warp's chunk of an item: 4 column tiles x (gate piece, up piece)
+    auto issue = [&](int i, int it, int expert) {
+        const int s = i % MI_NS, r = (it >> 2) & (MG_UNITS - 1);
         uint8_t* dst = ring + (size_t)s * MM_CHUNK;
+        const uint8_t* src = p.tiled + (size_t)expert * MM_EXPERT_BYTES + (size_t)(r & 15) * 1024;
         mbar_arrive_expect_tx(&bar[s], MM_CHUNK);
 #pragma unroll
         for (int kt = 0; kt < 4; ++kt) {
-            bulk_g2s(dst + (2 * kt) * 1024, piece(i, expert, kt, 0), 1024, &bar[s]);
-            bulk_g2s(dst + (2 * kt + 1) * 1024, piece(i, expert, kt, 1), 1024, &bar[s]);
-        }
-    };
-    auto prefetch = [&](int i, int expert) {
-#pragma unroll
-        for (int kt = 0; kt < 4; ++kt) {
-            bulk_prefetch_l2(piece(i, expert, kt, 0), 1024);
-            bulk_prefetch_l2(piece(i, expert, kt, 1), 1024);
+            const int kc = warp * 4 + kt;
+            bulk_g2s(dst + (2 * kt) * 1024, src + ((size_t)(r >> 4) * MM_GU_KT + kc) * MM_TILE, 1024, &bar[s]);
+            bulk_g2s(dst + (2 * kt + 1) * 1024, src + ((size_t)((r >> 4) + 4) * MM_GU_KT + kc) * MM_TILE, 1024,
+                     &bar[s]);
         }
     };
 
-    // ---- before the router has finished: the shared expert's pieces ----
+    // ---- before the router has finished: the shared slot's items (their
+    // tile count is ceil(T / 8) whatever the routing) ----
     int issued = 0;
     if (lane == 0) {
-        for (int i = 0; i < NS && unit_of(i) < MG_UNITS; ++i) {
-            issue(i, SHARED);
+        for (int i = 0; i < MI_NS && c + G * i < MG_UNITS * nt0; ++i) {
+            const int j = c + G * i;
+            issue(i, ((j / nt0) << 2) | (j % nt0), SHARED);
             issued = i + 1;
         }
     }
     pdl_wait();     // router logits are complete (and x is ready)
     pdl_trigger();
-
-    // x rows by bulk copy (lane t of warp 0 copies token t; T <= 32), landing
-    // while the CTA ranks the experts
-    if (warp == 0) {
-        if (lane == 0) mbar_arrive_expect_tx(xbar, (uint32_t)T * H * 2);
-        __syncwarp();
-        if (lane < T) bulk_g2s(xs + (size_t)lane * MG_XROW, p.x + (size_t)lane * H, H * 2, xbar);
-    }
 
     // ---- top-6 of every token, then the (slot, token) tables ----
     for (int t = warp; t < T; t += MM_WARPS) {
@@ -170,112 +168,141 @@ __global__ void __launch_bounds__(MM_WARPS * 32, 1) gateup_mma_kernel(GateUpMmaP
         }
     }
     __syncthreads();
-    if (warp == 0) build_decode_tables_warp(T, sel_e, sel_w, tmask, pair0, tab, lane);
+    if (warp == 0) {
+        build_decode_tables_warp(T, sel_e, sel_w, tmask, pair0, tab, lane);
+        // slot_item0: exclusive prefix of 64 * ceil(np / 8) over the slots
+        int base = 0;
+        for (int u0 = 0; u0 < tab->n_slots; u0 += 32) {
+            const int u = u0 + lane;
+            const int n = u < tab->n_slots ? MG_UNITS * ((tab->slot_pair0[u + 1] - tab->slot_pair0[u] + 7) >> 3) : 0;
+            int inc = n;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+                if (lane >= o) inc += v;
+            }
+            if (u < tab->n_slots) slot_item0[u] = base + inc - n;
+            base += __shfl_sync(0xFFFFFFFFu, inc, 31);
+        }
+        if (lane == 0) slot_item0[tab->n_slots] = base;
+    }
     __syncthreads();
     if (c == 0) {
         const int* src = reinterpret_cast<const int*>(tab);
         int* dst = reinterpret_cast<int*>(p.tables_out);
         for (int k = threadIdx.x; k < (int)(sizeof(DecodeTables) / 4); k += blockDim.x) dst[k] = src[k];
     }
-    const int total_units = tab->n_slots * MG_UNITS;
-    const int my_units = c < total_units ? (total_units - c + G - 1) / G : 0;
-    auto expert_of = [&](int i) { return tab->slot_expert[unit_of(i) / MG_UNITS]; };
+    const int n_slots = tab->n_slots, total = slot_item0[n_slots];
+    int my_items = c < total ? (total - c + G - 1) / G : 0;
+    if (my_items > MI_MAX_CTA_ITEMS) {   // the launcher sizes the grid so that this cannot happen
+        if (threadIdx.x == 0) report_status(p.status, ST_BADINDEX);
+        my_items = 0;
+    }
+    for (int i = threadIdx.x; i < my_items; i += blockDim.x) {
+        const int j = c + G * i;
+        int lo = 0, hi = n_slots - 1;     // the last slot u with slot_item0[u] <= j
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (slot_item0[mid] <= j) lo = mid;
+            else hi = mid - 1;
+        }
+        const int l = j - slot_item0[lo];
+        const int ntu = (tab->slot_pair0[lo + 1] - tab->slot_pair0[lo] + 7) >> 3;
+        list[i] = (lo << 8) | ((l / ntu) << 2) | (l % ntu);
+    }
+    __syncthreads();
     if (lane == 0) {
-        for (int i = issued; i < NS && i < my_units; ++i) {
-            issue(i, expert_of(i));
+        for (int i = issued; i < MI_NS && i < my_items; ++i) {
+            issue(i, list[i], tab->slot_expert[list[i] >> 8]);
             issued = i + 1;
         }
-        if (NS == 1 && my_units > 1) prefetch(1, expert_of(1));
     }
 
-    // this lane's ldmatrix row: matrix mi = lane / 8 (bit 0: gate / up piece,
-    // bit 1: columns 0-7 / 8-15 of the block), row i = lane % 8
     const int mi = lane >> 3, li = lane & 7;
     const uint32_t lrow = (uint32_t)((mi & 1) * 1024 + li * 128);
     const int lkh = mi >> 1;
     const int g = lane >> 2, cq = lane & 3;
-    bool ok = __syncthreads_and(mbar_wait_bounded(xbar, 0, p.limit_ns));
-    int i = 0;
-    for (; ok && i < my_units; ++i) {
-        const int q = unit_of(i), u = q / MG_UNITS, r = q & (MG_UNITS - 1);
-        const int pb = tab->slot_pair0[u], np = tab->slot_pair0[u + 1] - pb;   // 1..32 tokens
-        const int ntile = (np + 7) >> 3;
-        const __nv_bfloat16* xb[4];
+    // B fragments of an item: x row of the tile's token g (the last token past
+    // the slot's end), this warp's columns
+    auto load_b = [&](int it, uint32_t (&b)[16][2]) {
+        const int u = it >> 8, pb = tab->slot_pair0[u], np = tab->slot_pair0[u + 1] - pb;
+        const int n = (it & 3) * 8 + g;
+        const int tok = tab->pair_token[pb + (n < np ? n : np - 1)];
+        const unsigned int* x0 = reinterpret_cast<const unsigned int*>(p.x + (size_t)tok * H + warp * 256 + 2 * cq);
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-            const int n = nt * 8 + g;
-            xb[nt] = xs + (size_t)tab->pair_token[pb + (n < np ? n : np - 1)] * MG_XROW + warp * 256 + 2 * cq;
+        for (int kb = 0; kb < 16; ++kb) {
+            b[kb][0] = __ldg(x0 + kb * 8);
+            b[kb][1] = __ldg(x0 + kb * 8 + 4);
         }
-        float acc[4][4], acc2[4][4];
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) acc[nt][k] = acc2[nt][k] = 0.f;
-        const int s = i % NS;
-        const bool got = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(&bar[s], (i / NS) & 1, p.limit_ns));
+    };
+    uint32_t bq[16][2];
+    if (my_items > 0) load_b(list[0], bq);
+    bool ok = true;
+    int i = 0;
+    for (; i < my_items; ++i) {
+        const int it = list[i];
+        uint32_t bn[16][2];
+        if (i + 1 < my_items) load_b(list[i + 1], bn);
+        const int s = i % MI_NS;
+        const bool got = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(&bar[s], (i / MI_NS) & 1, p.limit_ns));
+        float* pw = part + (((i & 1) * MM_WARPS + warp) * 32 + lane) * 4;
         if (got) {
             const uint8_t* buf = ring + (size_t)s * MM_CHUNK;
-#pragma unroll 2
+            float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
             for (int kb = 0; kb < 16; kb += 2) {
                 uint32_t a[4], a2[4];
                 const int kt = kb >> 2, j0 = 2 * (kb & 3) + lkh;
                 ldmatrix_x4(a, buf + kt * 2048 + lrow + ((j0 ^ li) << 4));
                 ldmatrix_x4(a2, buf + kt * 2048 + lrow + (((j0 + 2) ^ li) << 4));
-#pragma unroll
-                for (int nt = 0; nt < 4; ++nt) {
-                    if (nt < ntile) {
-                        const __nv_bfloat16* xp = xb[nt] + kb * 16;
-                        mma_bf16_16816(acc[nt], a, *reinterpret_cast<const uint32_t*>(xp),
-                                       *reinterpret_cast<const uint32_t*>(xp + 8));
-                        mma_bf16_16816(acc2[nt], a2, *reinterpret_cast<const uint32_t*>(xp + 16),
-                                       *reinterpret_cast<const uint32_t*>(xp + 24));
-                    }
-                }
+                mma_bf16_16816(acc, a, bq[kb][0], bq[kb][1]);
+                mma_bf16_16816(acc2, a2, bq[kb + 1][0], bq[kb + 1][1]);
             }
             __syncwarp();   // every lane is done reading slot s
-            if (lane == 0) {
-                if (i + NS < my_units) {
-                    fence_proxy_async_smem();
-                    issue(i + NS, expert_of(i + NS));
-                    issued = i + NS + 1;
-                }
-                if (NS == 1 && i + 2 < my_units) prefetch(i + 2, expert_of(i + 2));
+            if (lane == 0 && i + MI_NS < my_items) {
+                fence_proxy_async_smem();
+                issue(i + MI_NS, list[i + MI_NS], tab->slot_expert[list[i + MI_NS] >> 8]);
+                issued = i + MI_NS + 1;
             }
-#pragma unroll
-            for (int nt = 0; nt < 4; ++nt)
-                if (nt < ntile)
-                    *reinterpret_cast<float4*>(part + ((warp * 4 + nt) * 32 + lane) * 4) =
-                        make_float4(acc[nt][0] + acc2[nt][0], acc[nt][1] + acc2[nt][1], acc[nt][2] + acc2[nt][2],
-                                    acc[nt][3] + acc2[nt][3]);
+            *reinterpret_cast<float4*>(pw) = make_float4(acc[0] + acc2[0], acc[1] + acc2[1], acc[2] + acc2[2],
+                                                         acc[3] + acc2[3]);
         }
-        // the decision to go on is taken by the whole CTA
         if (!__syncthreads_and(got)) {
             ok = false;
             break;
         }
-        // warp nt adds tile nt's eight partial sums in warp order; lane (g, cq)
-        // then holds gate (0, 1) and up (2, 3) of row j = 8r + g, columns 2cq, 2cq + 1
-        if (warp < ntile) {
-            float4 sum = *reinterpret_cast<const float4*>(part + (warp * 32 + lane) * 4);
+        // warp i % 8 adds the item's eight partial sums in warp order; lane
+        // (g, cq) then holds gate (x, y) and up (z, w) of row 8r + g for
+        // tokens 2cq, 2cq + 1 of the tile.  The buffer of parity i & 1 is
+        // next written after the barrier of item i + 1, which this warp
+        // reaches only after the sum.
+        if (warp == (i & (MM_WARPS - 1))) {
+            const float* pb0 = part + ((i & 1) * MM_WARPS * 32 + lane) * 4;
+            float4 sum = *reinterpret_cast<const float4*>(pb0);
 #pragma unroll
             for (int w = 1; w < MM_WARPS; ++w) {
-                const float4 v = *reinterpret_cast<const float4*>(part + ((w * 4 + warp) * 32 + lane) * 4);
+                const float4 v = *reinterpret_cast<const float4*>(pb0 + w * 32 * 4);
                 sum.x += v.x;
                 sum.y += v.y;
                 sum.z += v.z;
                 sum.w += v.w;
             }
-            const int j = 8 * r + g, n0 = warp * 8 + 2 * cq;
+            const int u = it >> 8, r = (it >> 2) & (MG_UNITS - 1);
+            const int pb = tab->slot_pair0[u], np = tab->slot_pair0[u + 1] - pb;
+            const int j = 8 * r + g, n0 = (it & 3) * 8 + 2 * cq;
             if (n0 < np) p.a[(size_t)(pb + n0) * I + j] = __float2bfloat16_rn(silu_f(sum.x) * sum.z);
             if (n0 + 1 < np) p.a[(size_t)(pb + n0 + 1) * I + j] = __float2bfloat16_rn(silu_f(sum.y) * sum.w);
         }
-        __syncthreads();   // the partial sums are read before the next unit writes them
+#pragma unroll
+        for (int kb = 0; kb < 16; ++kb) {
+            bq[kb][0] = bn[kb][0];
+            bq[kb][1] = bn[kb][1];
+        }
     }
     if (!ok) {
         if (lane == 0) {
             report_status(p.status, ST_TIMEOUT);
-            for (int k = i; k < issued; ++k) mbar_wait_bounded(&bar[k % NS], (k / NS) & 1, p.limit_ns);
-            if (warp == 0) mbar_wait_bounded(xbar, 0, p.limit_ns);
+            for (int k = i; k < issued; ++k) mbar_wait_bounded(&bar[k % MI_NS], (k / MI_NS) & 1, p.limit_ns);
         }
         __syncwarp();
     }
@@ -517,12 +544,10 @@ __global__ void __launch_bounds__(MM_WARPS * 32, 1) down_mma_kernel(DownMmaParam
 // ---------------------------------------------------------------------------
 
 cudaError_t decode_mma_set_attributes() {
-    size_t gmax = 0, dmax = 0;
-    for (int T = 1; T <= DEC_T; ++T) {
-        gmax = mg_smem_bytes(T) > gmax ? mg_smem_bytes(T) : gmax;
-        dmax = md_smem_bytes(T) > dmax ? md_smem_bytes(T) : dmax;
-    }
-    cudaError_t e = cudaFuncSetAttribute(gateup_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gmax);
+    size_t dmax = 0;
+    for (int T = 1; T <= DEC_T; ++T) dmax = md_smem_bytes(T) > dmax ? md_smem_bytes(T) : dmax;
+    cudaError_t e =
+        cudaFuncSetAttribute(gateup_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mi_smem_bytes());
     if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(down_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dmax);
 }
@@ -530,11 +555,14 @@ cudaError_t decode_mma_set_attributes() {
 cudaError_t launch_decode_experts_mma(const LaunchCtx& L, const uint8_t* tiled, const float* logits,
                                       const __nv_bfloat16* x, int T, DecodeTables* tables, int32_t* idx, float* w,
                                       float* a_buf, __nv_bfloat16* y) {
-    if (T < 1 || T > DEC_T) return cudaErrorInvalidValue;   // x rows are copied one per lane of a warp
+    if (T < 1 || T > DEC_T) return cudaErrorInvalidValue;
     __nv_bfloat16* a16 = reinterpret_cast<__nv_bfloat16*>(a_buf);
-    GateUpMmaParams gp{tiled, logits, x, T, mg_ns(T), tables, idx, w, a16, L.status, L.wait_limit_ns};
-    cudaError_t e = launch_hooked(L, FLINT_KERNEL_GATE_UP, gateup_mma_kernel, dim3(L.num_sms), dim3(MM_WARPS * 32),
-                                  mg_smem_bytes(T), gp);
+    GateUpMmaParams gp{tiled, logits, x, T, tables, idx, w, a16, L.status, L.wait_limit_ns};
+    // at most 64 x (257 + 28) items over the grid: 72 CTAs or more keep every
+    // CTA's list within its 256 entries
+    const int gi = L.num_sms >= 72 ? L.num_sms : 72;
+    cudaError_t e = launch_hooked(L, FLINT_KERNEL_GATE_UP, gateup_mma_kernel, dim3(gi), dim3(MM_WARPS * 32),
+                                  mi_smem_bytes(), gp);
     if (e != cudaSuccess) return e;
     DownMmaParams dp{tiled, logits, a16, y, md_ns(T), T, L.status, L.wait_limit_ns};
     return launch_hooked(L, FLINT_KERNEL_DOWN, down_mma_kernel, dim3(MD_CTAS), dim3(MM_WARPS * 32),

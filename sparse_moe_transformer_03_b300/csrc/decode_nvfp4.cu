@@ -35,7 +35,7 @@
 //                 the eight buffers are summed in warp order: deterministic.
 //
 // Routing, tables and the shared-expert prefetch are those of the bf16
-// decode kernels (decode.cu).
+// decode kernels (decode_mma.cu).
 #include <cuda_fp16.h>
 
 #include "flint_common.cuh"

@@ -22,9 +22,6 @@ struct flint_moe {
     // weights
     const __nv_bfloat16* router_W;
     const float* router_b;
-    ExpertTables host_tables;      // BF16 pointers (host copy)
-    ExpertTables* dev_tables;      // same, in device memory
-
     // owned tiled copies of the expert matrices for the tensor-core path
     // (per expert: gate_up tiles then down tiles, see repack.cu); bf16 only
     __nv_bfloat16* tiled;
@@ -42,12 +39,10 @@ struct flint_moe {
     void* ws_base;
     size_t ws_bytes;
     float* logits;                 // [CHUNK][E]
-    float* x_f32;                  // [DEC_T][H]
     int32_t* idx;                  // [CHUNK][TOPK]
     float* w;                      // [CHUNK][TOPK]
     DecodeTables* dec_tables;
     float* a_dec;                  // [DEC_PAIRS][I]
-    unsigned* ticket;              // router last-CTA ticket
     int32_t* local_rank;           // [CHUNK][TOPK]
     int32_t* blk_counts;           // [CHUNK/128][E]
     int32_t* blk_base;             // [CHUNK/128][E]
@@ -104,7 +99,6 @@ struct Carve {
 void free_handle(flint_moe* h) {
     if (!h) return;
     if (h->ws_base) cudaFree(h->ws_base);
-    if (h->dev_tables) cudaFree(h->dev_tables);
     if (h->tiled) cudaFree(h->tiled);
     if (h->nv) cudaFree(h->nv);
     if (h->nv_ts) cudaFree(h->nv_ts);
@@ -115,12 +109,10 @@ void free_handle(flint_moe* h) {
 void carve_workspace(flint_moe* h, char* base, size_t* bytes_out) {
     Carve c{base, 0};
     h->logits = c.take<float>((size_t)CHUNK * E);
-    h->x_f32 = c.take<float>((size_t)DEC_T * H);
     h->idx = c.take<int32_t>((size_t)CHUNK * TOPK);
     h->w = c.take<float>((size_t)CHUNK * TOPK);
     h->dec_tables = c.take<DecodeTables>(1);
     h->a_dec = c.take<float>((size_t)DEC_PAIRS * I);
-    h->ticket = c.take<unsigned>(64);
     h->local_rank = c.take<int32_t>((size_t)CHUNK * TOPK);
     h->blk_counts = c.take<int32_t>((size_t)(CHUNK / 128) * E);
     h->blk_base = c.take<int32_t>((size_t)(CHUNK / 128) * E);
@@ -185,17 +177,9 @@ flint_status_t flint_moe_create(flint_moe_t* out, const void* router_W, const fl
     h->prof_kernel = -1;
     h->router_W = static_cast<const __nv_bfloat16*>(router_W);
     h->router_b = router_b;
-    for (int e = 0; dtype == FLINT_BF16 && e < NEXP; ++e) {
-        h->host_tables.gate_up[e] = static_cast<const __nv_bfloat16*>(e < E ? gate_up_W[e] : shared_W[0]);
-        h->host_tables.down[e] = static_cast<const __nv_bfloat16*>(e < E ? down_W[e] : shared_W[1]);
-    }
 
     flint_status_t st = FLINT_OK;
-    if (cudaMalloc(&h->dev_tables, sizeof(ExpertTables)) != cudaSuccess) st = FLINT_ERR_OOM;
-    if (st == FLINT_OK &&
-        cudaMemcpy(h->dev_tables, &h->host_tables, sizeof(ExpertTables), cudaMemcpyHostToDevice) != cudaSuccess)
-        st = FLINT_ERR_CUDA;
-    if (st == FLINT_OK) {
+    {
         if (cudaHostAlloc(reinterpret_cast<void**>(&h->status_host), 64, cudaHostAllocMapped) != cudaSuccess)
             st = FLINT_ERR_OOM;
         else {
@@ -239,10 +223,13 @@ flint_status_t flint_moe_create(flint_moe_t* out, const void* router_W, const fl
     if (st == FLINT_OK && dtype == FLINT_BF16) {
         if (cudaMalloc(&h->tiled, (size_t)NEXP * expert_elems * sizeof(__nv_bfloat16)) != cudaSuccess)
             st = FLINT_ERR_OOM;
+        // the caller's matrices are read here only
         for (int e = 0; st == FLINT_OK && e < NEXP; ++e) {
             __nv_bfloat16* b = h->tiled + (size_t)e * expert_elems;
-            if (launch_repack_tiled(h->host_tables.gate_up[e], b, 2 * I, H, 0) != cudaSuccess ||
-                launch_repack_tiled(h->host_tables.down[e], b + (size_t)2 * I * H, H, I, 0) != cudaSuccess)
+            const auto* gu = static_cast<const __nv_bfloat16*>(e < E ? gate_up_W[e] : shared_W[0]);
+            const auto* dn = static_cast<const __nv_bfloat16*>(e < E ? down_W[e] : shared_W[1]);
+            if (launch_repack_tiled(gu, b, 2 * I, H, 0) != cudaSuccess ||
+                launch_repack_tiled(dn, b + (size_t)2 * I * H, H, I, 0) != cudaSuccess)
                 st = FLINT_ERR_CUDA;
         }
     }
@@ -253,7 +240,6 @@ flint_status_t flint_moe_create(flint_moe_t* out, const void* router_W, const fl
         if (!enc) st = FLINT_ERR_CUDA;
     }
     if (st == FLINT_OK) st = from_cuda(prefill_set_attributes());
-    if (st == FLINT_OK) st = from_cuda(decode_set_attributes());
     if (st == FLINT_OK) st = from_cuda(decode_nvfp4_set_attributes());
     if (st == FLINT_OK) st = from_cuda(decode_mma_set_attributes());
     if (st == FLINT_OK) st = from_cuda(cudaDeviceSynchronize());
@@ -294,14 +280,9 @@ flint_status_t flint_moe_forward(flint_moe_t h, const void* x, int T, void* y, c
     }
     if (T <= DEC_T) {
         cudaError_t e = launch_router_logits_decode(L, xs, T, h->router_W, h->router_b, h->logits);
-        if (e == cudaSuccess) {
-            if (T >= DEC_MMA_MIN_T)
-                e = launch_decode_experts_mma(L, reinterpret_cast<const uint8_t*>(h->tiled), h->logits, xs, T,
-                                              h->dec_tables, h->idx, h->w, h->a_dec, ys);
-            else
-                e = launch_decode_experts(L, h->dev_tables, h->logits, xs, T, h->dec_tables, h->idx, h->w, h->a_dec,
-                                          ys);
-        }
+        if (e == cudaSuccess)
+            e = launch_decode_experts_mma(L, reinterpret_cast<const uint8_t*>(h->tiled), h->logits, xs, T,
+                                          h->dec_tables, h->idx, h->w, h->a_dec, ys);
         return from_cuda(e);
     }
     // grouped tensor-core path, chunks of CHUNK tokens
@@ -337,8 +318,8 @@ flint_status_t flint_moe_route_only(flint_moe_t h, const void* x, float* logits,
         float* lg = logits ? logits : h->logits;
         const __nv_bfloat16* xs = static_cast<const __nv_bfloat16*>(x);
         if (T <= DEC_T) {
-            e = launch_router_decode(L, xs, T, h->router_W, h->router_b, lg, nullptr, idx, w, nullptr,
-                                     h->ticket);
+            e = launch_router_logits_decode(L, xs, T, h->router_W, h->router_b, lg);
+            if (e == cudaSuccess) e = launch_select(L, lg, T, idx, w);
         } else {
             CUtensorMap xmap;
             if (!encode_bf16_2d(&xmap, xs, T, H, H, 128, 64)) return FLINT_ERR_CUDA;

@@ -37,12 +37,6 @@ struct DecodeTables {
     float pair_weight[DEC_PAIRS]; // routing weight of each pair (shared: 1)
 };
 
-// Device-side pointer tables of one layer.
-struct ExpertTables {
-    const __nv_bfloat16* gate_up[NEXP];   // [2I][H]
-    const __nv_bfloat16* down[NEXP];      // [H][I]
-};
-
 // ---------------------------------------------------------------------------
 // small helpers
 // ---------------------------------------------------------------------------

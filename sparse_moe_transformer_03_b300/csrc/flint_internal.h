@@ -56,9 +56,6 @@ cudaError_t launch_hooked(const LaunchCtx& L, int kid, void (*kern)(KArgs...), d
 
 // router.cu
 constexpr int PERM_BLOCK_TOKENS = 128;   // tokens per block of the permutation's counting sort
-cudaError_t launch_router_decode(const LaunchCtx& L, const __nv_bfloat16* x, int T, const __nv_bfloat16* Wr,
-                                 const float* bias, float* logits, float* x_f32, int32_t* idx, float* w,
-                                 DecodeTables* tables, unsigned* ticket);
 cudaError_t launch_router_logits_decode(const LaunchCtx& L, const __nv_bfloat16* x, int T,
                                         const __nv_bfloat16* Wr, const float* bias, float* logits);
 cudaError_t launch_select(const LaunchCtx& L, const float* logits, int T, int32_t* idx, float* w);
@@ -109,17 +106,10 @@ cudaError_t launch_decode_experts_nvfp4(const LaunchCtx& L, const uint8_t* nv, c
                                         const float* logits, const __nv_bfloat16* x, int T, DecodeTables* tables,
                                         int32_t* idx, float* w, float* a_buf, __nv_bfloat16* y);
 
-// decode_mma.cu -- bf16 decode on mma.sync, from the tiled copy (T >= DEC_MMA_MIN_T)
-constexpr int DEC_MMA_MIN_T = 5;
+// decode_mma.cu -- bf16 decode (T <= DEC_T) on mma.sync, from the tiled copy
 cudaError_t decode_mma_set_attributes();
 cudaError_t launch_decode_experts_mma(const LaunchCtx& L, const uint8_t* tiled, const float* logits,
                                       const __nv_bfloat16* x, int T, DecodeTables* tables, int32_t* idx, float* w,
                                       float* a_buf, __nv_bfloat16* y);
-
-// decode.cu
-cudaError_t decode_set_attributes();
-cudaError_t launch_decode_experts(const LaunchCtx& L, const ExpertTables* experts, const float* logits,
-                                  const __nv_bfloat16* x, int T, DecodeTables* tables, int32_t* idx, float* w,
-                                  float* a_buf, __nv_bfloat16* y);
 
 }  // namespace flint

@@ -14,105 +14,13 @@
 namespace flint {
 
 // ---------------------------------------------------------------------------
-// decode router: logits for T <= 32, then (last CTA) selection + tables
+// decode router: logits for T <= 32
 // ---------------------------------------------------------------------------
 
 constexpr int RT_WARPS = 4;                    // one expert per warp
 constexpr int RT_CTAS = E / RT_WARPS;          // 64
 
-struct RouterDecodeParams {
-    const __nv_bfloat16* x;  // [T][H]
-    int T;
-    const __nv_bfloat16* Wr; // [E][H]
-    const float* bias;       // [E] or null
-    float* logits;           // [T][E] out (workspace or caller)
-    float* x_f32;            // [T][H] out (fp32 copy of x for the expert kernels) or null
-    int32_t* idx;            // [T][6]
-    float* w;                // [T][6]
-    DecodeTables* tables;    // or null
-    unsigned* ticket;
-};
-
-__global__ void __launch_bounds__(RT_WARPS * 32) router_decode_kernel(RouterDecodeParams p) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int e = blockIdx.x * RT_WARPS + warp;
-    // weights are immutable: load the row before waiting on the producer of x
-    uint4 wr[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) wr[i] = ldg16(p.Wr + (size_t)e * H + 8 * (lane + 32 * i));
-    const float b = p.bias ? __ldg(p.bias + e) : 0.f;
-    pdl_trigger();
-    pdl_wait();
-
-    const int T = p.T;
-    for (int t = 0; t < T; ++t) {
-        const __nv_bfloat16* xr = p.x + (size_t)t * H;
-        float acc = 0.f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint4 xv = ldg16(xr + 8 * (lane + 32 * i));
-            acc = fmaf(bf_lo(wr[i].x), bf_lo(xv.x), acc);
-            acc = fmaf(bf_hi(wr[i].x), bf_hi(xv.x), acc);
-            acc = fmaf(bf_lo(wr[i].y), bf_lo(xv.y), acc);
-            acc = fmaf(bf_hi(wr[i].y), bf_hi(xv.y), acc);
-            acc = fmaf(bf_lo(wr[i].z), bf_lo(xv.z), acc);
-            acc = fmaf(bf_hi(wr[i].z), bf_hi(xv.z), acc);
-            acc = fmaf(bf_lo(wr[i].w), bf_lo(xv.w), acc);
-            acc = fmaf(bf_hi(wr[i].w), bf_hi(xv.w), acc);
-        }
-        acc = warp_sum(acc);
-        if (lane == 0) p.logits[(size_t)t * E + e] = acc + b;
-    }
-    // fp32 copy of x for the expert kernels (each CTA converts a share)
-    if (p.x_f32) {
-        const int n8 = T * H / 8;
-        for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += gridDim.x * blockDim.x) {
-            const uint4 xv = ldg16(p.x + 8 * (size_t)i);
-            float4 a = make_float4(bf_lo(xv.x), bf_hi(xv.x), bf_lo(xv.y), bf_hi(xv.y));
-            float4 c = make_float4(bf_lo(xv.z), bf_hi(xv.z), bf_lo(xv.w), bf_hi(xv.w));
-            reinterpret_cast<float4*>(p.x_f32)[2 * i] = a;
-            reinterpret_cast<float4*>(p.x_f32)[2 * i + 1] = c;
-        }
-    }
-
-    // the last CTA to finish selects and builds the tables
-    __shared__ int s_last;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        const unsigned done = atomicAdd(p.ticket, 1u);
-        s_last = (done == gridDim.x - 1);
-    }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-
-    __shared__ int sel_e[DEC_T * TOPK];
-    __shared__ float sel_w[DEC_T * TOPK];
-    __shared__ uint32_t tmask[E];
-    __shared__ int pair0[E];
-    for (int t = warp; t < T; t += RT_WARPS) {
-        float v[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = __ldcg(p.logits + (size_t)t * E + lane + 32 * i);
-        int sel[TOPK];
-        float wt[TOPK];
-        warp_top6(v, lane, sel, wt);
-        if (lane < TOPK) {
-            const int se = pick6(sel, lane);
-            const float sw = pick6(wt, lane);
-            p.idx[t * TOPK + lane] = se;
-            p.w[t * TOPK + lane] = sw;
-            sel_e[t * TOPK + lane] = se;
-            sel_w[t * TOPK + lane] = sw;
-        }
-    }
-    if (threadIdx.x == 0) *p.ticket = 0;  // ready for the next call
-    __syncthreads();
-    if (p.tables && warp == 0) build_decode_tables_warp(T, sel_e, sel_w, tmask, pair0, p.tables, lane);
-}
-
-// Logits only (the forward path: the expert kernels select for themselves).
+// Logits only (the expert kernels of the forward select for themselves).
 // Grid: (64 expert groups of 4, token groups of RL_TOK).  Each warp keeps its
 // expert's 4 KiB router row in registers (loaded before the dependency wait);
 // the CTA stages its tokens' x rows in smem with one bulk copy, so a token
@@ -288,13 +196,6 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(const int32_t* idx, c
 // ---------------------------------------------------------------------------
 // host launchers
 // ---------------------------------------------------------------------------
-
-cudaError_t launch_router_decode(const LaunchCtx& L, const __nv_bfloat16* x, int T, const __nv_bfloat16* Wr,
-                                 const float* bias, float* logits, float* x_f32, int32_t* idx, float* w,
-                                 DecodeTables* tables, unsigned* ticket) {
-    RouterDecodeParams p{x, T, Wr, bias, logits, x_f32, idx, w, tables, ticket};
-    return launch_pdl(L, router_decode_kernel, dim3(RT_CTAS), dim3(RT_WARPS * 32), 0, p);
-}
 
 cudaError_t launch_router_logits_decode(const LaunchCtx& L, const __nv_bfloat16* x, int T,
                                         const __nv_bfloat16* Wr, const float* bias, float* logits) {

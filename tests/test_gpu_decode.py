@@ -66,3 +66,28 @@ def test_bounded_wait_gives_up_with_status():
     # a wait on a barrier nothing arrives on returns FLINT_ERR_DEVICE_TIMEOUT
     assert flint.flint_debug_bounded_wait(2_000_000) == 4
     torch.cuda.synchronize()
+
+
+def test_bf16_expert_buffers_are_not_read_after_create():
+    """The handle's tiled copy is the only expert storage both paths read: the
+    caller's bf16 expert buffers, overwritten with NaN right after create,
+    change nothing (decode sizes and the many-token path)."""
+    device.build()
+    own = device.LayerWeights(0, 0, False)
+    h = handle_for(own)
+    try:
+        own.gate_up.fill_(float("nan"))
+        own.down.fill_(float("nan"))
+        torch.cuda.synchronize()
+        orc = LayerOracle.from_bf16_layer(layer(0, 0, False))
+        for T in (1, 8, 32, 40):
+            xb = x_for("clustered", 500 + T, T)
+            y = forward(h, xb)
+            assert np.isfinite(y).all(), T
+            ref, alt = orc.forward_with_alternatives(xb)
+            res = compare(y, ref, alt)
+            assert res["ok"], (T, res)
+    finally:
+        flint.flint_moe_destroy(h)
+        del own
+        torch.cuda.empty_cache()
