@@ -38,12 +38,12 @@
 //                work items are (slot, column half, tile of 8 tokens): 256
 //                columns of the slot's 16 rows (4 pieces of 2 KiB) against up
 //                to 8 of its tokens; item j goes to warp j % 8, so the shared
-//                slot's tiles and halves spread over the warps.  The
-//                activations are staged in smem when the batch has at most 64
-//                (token, expert) pairs, else each item's B fragments are
-//                fetched into registers while the item before it computes.
-//                w * D accumulates per (token, row) in the warp's own buffer
-//                and the eight buffers are summed in warp order: deterministic.
+//                slot's tiles and halves spread over the warps.  An item's
+//                activations (8 pairs x 256 columns, contiguous in the
+//                act_index layout the gate/up kernel writes) arrive in the
+//                same ring slot as its weights, by one more bulk copy.  w * D
+//                accumulates per (token, row) in the warp's own buffer and
+//                the eight buffers are summed in warp order: deterministic.
 //
 // The down kernel routes for itself, like the NVFP4 one, and starts its
 // weight chunks before waiting on the gate/up kernel.
@@ -67,7 +67,7 @@ constexpr int MM_WARPS = 8;
 // gate/up + SwiGLU
 // ---------------------------------------------------------------------------
 
-constexpr int MG_UNITS = I / 8;          // 64 units per expert
+constexpr int MG_UNITS = DEC_UNITS;      // 64 units per expert
 
 struct GateUpMmaParams {
     const uint8_t* tiled;         // the handle's tiled experts
@@ -77,7 +77,7 @@ struct GateUpMmaParams {
     DecodeTables* tables_out;
     int32_t* idx_out;
     float* w_out;
-    __nv_bfloat16* a;             // [pairs][I]
+    __nv_bfloat16* a;             // activations, act_index layout
     uint32_t* status;
     uint64_t limit_ns;
 };
@@ -90,12 +90,11 @@ struct GateUpMmaParams {
 // expert's for T > 8) reads its weights once per tile; the repeats hit L2.
 
 constexpr int MI_NS = 3;                            // ring chunks per warp
-constexpr int MI_MAX_CTA_ITEMS = 256;               // items of one CTA (grid >= 72 CTAs)
 constexpr int MI_PART = 2 * MM_WARPS * 32 * 4;      // partial sums: [item parity][warp][lane][4]
 
 static inline size_t mi_smem_bytes() {
     return (size_t)MM_WARPS * MI_NS * MM_CHUNK + (size_t)MI_PART * 4 + (size_t)MM_WARPS * MI_NS * 8 +
-           sizeof(DecodeTables) + DEC_T * TOPK * 8 + 2 * E * 4 + (NEXP + 1) * 4 + MI_MAX_CTA_ITEMS * 4;
+           sizeof(DecodeTables) + DEC_T * TOPK * 8 + 2 * E * 4 + (NEXP + 1) * 4 + DEC_MAX_CTA_ITEMS * 4;
 }
 
 __global__ void __launch_bounds__(MM_WARPS * 32, 1) gateup_mma_kernel(GateUpMmaParams p) {
@@ -170,21 +169,7 @@ __global__ void __launch_bounds__(MM_WARPS * 32, 1) gateup_mma_kernel(GateUpMmaP
     __syncthreads();
     if (warp == 0) {
         build_decode_tables_warp(T, sel_e, sel_w, tmask, pair0, tab, lane);
-        // slot_item0: exclusive prefix of 64 * ceil(np / 8) over the slots
-        int base = 0;
-        for (int u0 = 0; u0 < tab->n_slots; u0 += 32) {
-            const int u = u0 + lane;
-            const int n = u < tab->n_slots ? MG_UNITS * ((tab->slot_pair0[u + 1] - tab->slot_pair0[u] + 7) >> 3) : 0;
-            int inc = n;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int v = __shfl_up_sync(0xFFFFFFFFu, inc, o);
-                if (lane >= o) inc += v;
-            }
-            if (u < tab->n_slots) slot_item0[u] = base + inc - n;
-            base += __shfl_sync(0xFFFFFFFFu, inc, 31);
-        }
-        if (lane == 0) slot_item0[tab->n_slots] = base;
+        build_gateup_item_starts_warp(tab, slot_item0, lane);
     }
     __syncthreads();
     if (c == 0) {
@@ -192,23 +177,10 @@ __global__ void __launch_bounds__(MM_WARPS * 32, 1) gateup_mma_kernel(GateUpMmaP
         int* dst = reinterpret_cast<int*>(p.tables_out);
         for (int k = threadIdx.x; k < (int)(sizeof(DecodeTables) / 4); k += blockDim.x) dst[k] = src[k];
     }
-    const int n_slots = tab->n_slots, total = slot_item0[n_slots];
-    int my_items = c < total ? (total - c + G - 1) / G : 0;
-    if (my_items > MI_MAX_CTA_ITEMS) {   // the launcher sizes the grid so that this cannot happen
+    int my_items = list_gateup_items(tab, slot_item0, c, G, list);
+    if (my_items < 0) {   // the launcher sizes the grid so that this cannot happen
         if (threadIdx.x == 0) report_status(p.status, ST_BADINDEX);
         my_items = 0;
-    }
-    for (int i = threadIdx.x; i < my_items; i += blockDim.x) {
-        const int j = c + G * i;
-        int lo = 0, hi = n_slots - 1;     // the last slot u with slot_item0[u] <= j
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (slot_item0[mid] <= j) lo = mid;
-            else hi = mid - 1;
-        }
-        const int l = j - slot_item0[lo];
-        const int ntu = (tab->slot_pair0[lo + 1] - tab->slot_pair0[lo] + 7) >> 3;
-        list[i] = (lo << 8) | ((l / ntu) << 2) | (l % ntu);
     }
     __syncthreads();
     if (lane == 0) {
@@ -290,8 +262,8 @@ __global__ void __launch_bounds__(MM_WARPS * 32, 1) gateup_mma_kernel(GateUpMmaP
             const int u = it >> 8, r = (it >> 2) & (MG_UNITS - 1);
             const int pb = tab->slot_pair0[u], np = tab->slot_pair0[u + 1] - pb;
             const int j = 8 * r + g, n0 = (it & 3) * 8 + 2 * cq;
-            if (n0 < np) p.a[(size_t)(pb + n0) * I + j] = __float2bfloat16_rn(silu_f(sum.x) * sum.z);
-            if (n0 + 1 < np) p.a[(size_t)(pb + n0 + 1) * I + j] = __float2bfloat16_rn(silu_f(sum.y) * sum.w);
+            if (n0 < np) p.a[act_index(pb + n0, j)] = __float2bfloat16_rn(silu_f(sum.x) * sum.z);
+            if (n0 + 1 < np) p.a[act_index(pb + n0 + 1, j)] = __float2bfloat16_rn(silu_f(sum.y) * sum.w);
         }
 #pragma unroll
         for (int kb = 0; kb < 16; ++kb) {
@@ -313,92 +285,66 @@ __global__ void __launch_bounds__(MM_WARPS * 32, 1) gateup_mma_kernel(GateUpMmaP
 // ---------------------------------------------------------------------------
 
 constexpr int MD_CTAS = H / 16;          // 128
-constexpr int MD_APAIRS = 64;            // activation rows staged in smem up to this many pairs
-constexpr int MD_AROW = I * 2 + 16;      // bytes per staged row
-// items: 2 column halves x the N tiles of every slot (sum of ceil(np / 8) over
-// the slots is below slots + pairs / 8)
-constexpr int MD_MAX_ITEMS = 2 * (NEXP + DEC_PAIRS / 8);
+constexpr int MD_NS = 2;                 // ring slots per warp
+constexpr int MD_ACT = 8 * 256 * 2;      // an item's activation tile: 8 pairs x 256 columns, bf16
+constexpr int MD_SLOT = MM_CHUNK + MD_ACT;
 
 struct DownMmaParams {
     const uint8_t* tiled;
     const float* logits;          // [T][E] (final before this kernel starts)
-    const __nv_bfloat16* a;       // [pairs][I]
+    const __nv_bfloat16* a;       // activations, act_index layout
     __nv_bfloat16* y;
-    int ns;
     int T;
     uint32_t* status;
     uint64_t limit_ns;
 };
 
-static inline int md_ns(int T) { return T <= 9 ? 2 : 3; }
-__host__ __device__ inline bool md_staged(int T) { return (TOPK + 1) * T <= MD_APAIRS; }
 static inline size_t md_smem_bytes(int T) {
-    return (size_t)MM_WARPS * md_ns(T) * MM_CHUNK + (md_staged(T) ? (size_t)(TOPK + 1) * T * MD_AROW : 0) +
-           (size_t)MM_WARPS * T * 16 * 4 + (MM_WARPS * md_ns(T) + 1) * 8 + sizeof(DecodeTables) +
-           DEC_T * TOPK * 8 + 2 * E * 4 + (MD_MAX_ITEMS + 1) * 4;
-}
-
-// Lists the down kernel's work items in slot order, each slot's first column
-// half before its second and the N tiles in order within a half; packed as
-// slot << 3 | half << 2 | tile.  One warp; returns the count on every lane.
-__device__ __forceinline__ int build_down_items_warp(const DecodeTables* tab, int* items, int lane) {
-    int base = 0;
-    for (int u0 = 0; u0 < tab->n_slots; u0 += 32) {
-        const int u = u0 + lane;
-        const int nt = u < tab->n_slots ? (tab->slot_pair0[u + 1] - tab->slot_pair0[u] + 7) >> 3 : 0;
-        int inc = nt;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(0xFFFFFFFFu, inc, o);
-            if (lane >= o) inc += v;
-        }
-        const int off = base + 2 * (inc - nt);
-        for (int hk = 0; hk < 2; ++hk)
-            for (int t = 0; t < nt; ++t) items[off + hk * nt + t] = (u << 3) | (hk << 2) | t;
-        base += 2 * __shfl_sync(0xFFFFFFFFu, inc, 31);
-    }
-    __syncwarp();
-    return base;
+    return (size_t)MM_WARPS * MD_NS * (MD_SLOT + 8) + (size_t)MM_WARPS * T * 16 * 4 + sizeof(DecodeTables) +
+           DEC_T * TOPK * 8 + 2 * E * 4 + (DEC_MAX_DOWN_ITEMS + 1) * 4;
 }
 
 __global__ void __launch_bounds__(MM_WARPS * 32, 1) down_mma_kernel(DownMmaParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int c = blockIdx.x, NS = p.ns, Tk = p.T;
-    const bool staged = md_staged(Tk);
-    uint8_t* ring = smem + (size_t)warp * NS * MM_CHUNK;
-    uint8_t* astage = smem + (size_t)MM_WARPS * NS * MM_CHUNK;
-    float* yw_all = reinterpret_cast<float*>(astage + (staged ? (size_t)(TOPK + 1) * Tk * MD_AROW : 0));
+    const int c = blockIdx.x, Tk = p.T;
+    uint8_t* ring = smem + (size_t)warp * MD_NS * MD_SLOT;
+    float* yw_all = reinterpret_cast<float*>(smem + (size_t)MM_WARPS * MD_NS * MD_SLOT);
     float* yw = yw_all + warp * Tk * 16;
     uint64_t* bars = reinterpret_cast<uint64_t*>(yw_all + MM_WARPS * Tk * 16);
-    uint64_t* bar = bars + warp * NS;
-    uint64_t* abar = bars + MM_WARPS * NS;
-    DecodeTables* tab = reinterpret_cast<DecodeTables*>(abar + 1);
+    uint64_t* bar = bars + warp * MD_NS;
+    DecodeTables* tab = reinterpret_cast<DecodeTables*>(bars + MM_WARPS * MD_NS);
     int* sel_e = reinterpret_cast<int*>(tab + 1);
     float* sel_w = reinterpret_cast<float*>(sel_e + DEC_T * TOPK);
     uint32_t* tmask = reinterpret_cast<uint32_t*>(sel_w + DEC_T * TOPK);
     int* pair0 = reinterpret_cast<int*>(tmask + E);
     int* items = pair0 + E;
-    int* n_items_s = items + MD_MAX_ITEMS;
+    int* n_items_s = items + DEC_MAX_DOWN_ITEMS;
 
     if (lane == 0) {
-        for (int s = 0; s < NS; ++s) mbar_init(&bar[s], 1);
-        if (warp == 0) mbar_init(abar, 1);
+        for (int s = 0; s < MD_NS; ++s) mbar_init(&bar[s], 1);
         fence_mbar_init();
     }
     // the warp's k-th item is items[warp + 8k]; its weights: columns 256 half
-    // .. + 255 of rows 16c .. 16c + 15 of the slot's expert
+    // .. + 255 of rows 16c .. 16c + 15 of the slot's expert; its activations:
+    // the tile's 8 pairs in that half (pairs past the slot's end come along
+    // and are not used)
     auto item_of = [&](int k) { return items[warp + MM_WARPS * k]; };
-    auto issue = [&](int k) {
-        const int it = item_of(k), s = k % NS;
+    auto copy_w = [&](int k) {
+        const int it = item_of(k), s = k % MD_NS;
         const int expert = tab->slot_expert[it >> 3];
         const uint8_t* base = p.tiled + (size_t)expert * MM_EXPERT_BYTES + MM_DOWN_OFF + (size_t)(c & 7) * 2048;
         const int rb = c >> 3, kc0 = ((it >> 2) & 1) * 4;
-        uint8_t* dst = ring + (size_t)s * MM_CHUNK;
-        mbar_arrive_expect_tx(&bar[s], MM_CHUNK);
+        uint8_t* dst = ring + (size_t)s * MD_SLOT;
 #pragma unroll
         for (int kt = 0; kt < 4; ++kt)
             bulk_g2s(dst + kt * 2048, base + ((size_t)rb * MM_DN_KT + kc0 + kt) * MM_TILE, 2048, &bar[s]);
+    };
+    auto copy_a = [&](int k) {
+        const int it = item_of(k), s = k % MD_NS;
+        const int p0 = tab->slot_pair0[it >> 3] + (it & 3) * 8;
+        bulk_g2s(ring + (size_t)s * MD_SLOT + MM_CHUNK, p.a + ((size_t)((it >> 2) & 1) * DEC_ACT_ROWS + p0) * 256,
+                 MD_ACT, &bar[s]);
     };
     // The router grid completed before any gate/up CTA passed its dependency
     // wait, and this launch is triggered only after those waits: the logits
@@ -424,86 +370,62 @@ __global__ void __launch_bounds__(MM_WARPS * 32, 1) down_mma_kernel(DownMmaParam
         if (lane == 0) *n_items_s = n;
     }
     __syncthreads();
-    const int n_items = *n_items_s, n_pairs = tab->n_pairs;
+    const int n_items = *n_items_s;
     const int my_items = n_items > warp ? (n_items - warp + MM_WARPS - 1) / MM_WARPS : 0;
+    // weights of the first items now (the phase waits for its arrival, which
+    // comes with the activations after the dependency wait)
     int issued = 0;
     if (lane == 0) {
-        for (int k = 0; k < NS && k < my_items; ++k) {
-            issue(k);
+        for (int k = 0; k < MD_NS && k < my_items; ++k) {
+            mbar_expect_tx(&bar[k], MM_CHUNK);
+            copy_w(k);
             issued = k + 1;
         }
     }
     pdl_wait();     // the gate/up kernel is complete: activations are visible
     pdl_trigger();
-    if (staged && threadIdx.x == 0) {
-        mbar_arrive_expect_tx(abar, n_pairs * I * 2);
-        for (int pr = 0; pr < n_pairs; ++pr) bulk_g2s(astage + (size_t)pr * MD_AROW, p.a + (size_t)pr * I, I * 2, abar);
+    if (lane == 0) {
+        for (int k = 0; k < issued; ++k) {
+            mbar_arrive_expect_tx(&bar[k], MD_ACT);
+            copy_a(k);
+        }
     }
-    bool ok = true;
-    if (staged && my_items > 0) ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(abar, 0, p.limit_ns));
 
     const int mi = lane >> 3, li = lane & 7;
     const int lr = (mi & 1) * 8 + li;               // row 0..15 of the M tile
     const uint32_t lrow = (uint32_t)lr * 128;
     const int lkh = mi >> 1;
     const int g = lane >> 2, cq = lane & 3;
-    // this lane's B row of item k: pair pb + 8 tile + g (the last pair past np)
-    auto b_row = [&](int it) {
-        const int u = it >> 3, pb = tab->slot_pair0[u], np = tab->slot_pair0[u + 1] - pb;
-        const int n = (it & 3) * 8 + g;
-        return pb + (n < np ? n : np - 1);
-    };
-    // B fragments of the warp's k-th item from the activations in global
-    // memory (read-only here; written by the previous grid)
-    auto load_b = [&](int k, uint32_t (&b)[16][2]) {
-        const int it = item_of(k);
-        const unsigned int* a0 = reinterpret_cast<const unsigned int*>(p.a + (size_t)b_row(it) * I +
-                                                                       ((it >> 2) & 1) * 256 + 2 * cq);
-#pragma unroll
-        for (int kb = 0; kb < 16; ++kb) {
-            b[kb][0] = __ldg(a0 + kb * 8);
-            b[kb][1] = __ldg(a0 + kb * 8 + 4);
-        }
-    };
-    uint32_t bq[16][2];
-    if (!staged && my_items > 0) load_b(0, bq);
+    bool ok = true;
     int k = 0;
-    for (; ok && k < my_items; ++k) {
-        const int it = item_of(k), u = it >> 3, hk = (it >> 2) & 1, nt = it & 3;
+    for (; k < my_items; ++k) {
+        const int it = item_of(k), u = it >> 3, nt = it & 3;
         const int pb = tab->slot_pair0[u], np = tab->slot_pair0[u + 1] - pb;
-        uint32_t bn[16][2];
-        if (!staged && k + 1 < my_items) load_b(k + 1, bn);
-        const int s = k % NS;
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(&bar[s], (k / NS) & 1, p.limit_ns))) {
+        const int s = k % MD_NS;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(&bar[s], (k / MD_NS) & 1, p.limit_ns))) {
             ok = false;
             break;
         }
-        const uint8_t* buf = ring + (size_t)s * MM_CHUNK;
+        const uint8_t* buf = ring + (size_t)s * MD_SLOT;
+        // row g of the activation tile; chunk q of it sits at q ^ (pair % 8)
+        const uint8_t* ar = buf + MM_CHUNK + g * 512 + 4 * cq;
+        const int sw = (pb + nt * 8 + g) & 7;
         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        if (staged) {
-            const uint8_t* ar = astage + (size_t)b_row(it) * MD_AROW + (hk * 256 + 2 * cq) * 2;
 #pragma unroll
-            for (int kb = 0; kb < 16; ++kb) {
-                uint32_t a[4];
-                const int kt = kb >> 2, j = 2 * (kb & 3) + lkh;
-                ldmatrix_x4(a, buf + kt * 2048 + lrow + ((j ^ li) << 4));
-                mma_bf16_16816(acc[kb & 1], a, *reinterpret_cast<const uint32_t*>(ar + kb * 32),
-                               *reinterpret_cast<const uint32_t*>(ar + kb * 32 + 16));
-            }
-        } else {
-#pragma unroll
-            for (int kb = 0; kb < 16; ++kb) {
-                uint32_t a[4];
-                const int kt = kb >> 2, j = 2 * (kb & 3) + lkh;
-                ldmatrix_x4(a, buf + kt * 2048 + lrow + ((j ^ li) << 4));
-                mma_bf16_16816(acc[kb & 1], a, bq[kb][0], bq[kb][1]);
-            }
+        for (int kb = 0; kb < 16; ++kb) {
+            uint32_t a[4];
+            const int kt = kb >> 2, j = 2 * (kb & 3) + lkh;
+            ldmatrix_x4(a, buf + kt * 2048 + lrow + ((j ^ li) << 4));
+            mma_bf16_16816(acc[kb & 1], a, *reinterpret_cast<const uint32_t*>(ar + (((2 * kb) ^ sw) << 4)),
+                           *reinterpret_cast<const uint32_t*>(ar + (((2 * kb + 1) ^ sw) << 4)));
         }
         __syncwarp();
-        if (lane == 0 && k + NS < my_items) {
+        if (lane == 0 && k + MD_NS < my_items) {
             fence_proxy_async_smem();
-            issue(k + NS);
-            issued = k + NS + 1;
+            mbar_arrive_expect_tx(&bar[s], MM_CHUNK + MD_ACT);
+            copy_w(k + MD_NS);
+            copy_a(k + MD_NS);
+            issued = k + MD_NS + 1;
         }
         // lane (g, cq) holds rows g, g + 8 of tokens 2cq, 2cq + 1 of the tile
 #pragma unroll
@@ -516,18 +438,10 @@ __global__ void __launch_bounds__(MM_WARPS * 32, 1) down_mma_kernel(DownMmaParam
                 yw[t * 16 + g + 8] = fmaf(wgt, acc[0][2 + hh] + acc[1][2 + hh], yw[t * 16 + g + 8]);
             }
         }
-        if (!staged) {
-#pragma unroll
-            for (int kb = 0; kb < 16; ++kb) {
-                bq[kb][0] = bn[kb][0];
-                bq[kb][1] = bn[kb][1];
-            }
-        }
     }
     if (!ok && lane == 0) {
         report_status(p.status, ST_TIMEOUT);
-        for (int q = k; q < issued; ++q) mbar_wait_bounded(&bar[q % NS], (q / NS) & 1, p.limit_ns);
-        if (staged && warp == 0) mbar_wait_bounded(abar, 0, p.limit_ns);
+        for (int q = k; q < issued; ++q) mbar_wait_bounded(&bar[q % MD_NS], (q / MD_NS) & 1, p.limit_ns);
     }
     __syncthreads();
     for (int q = threadIdx.x; q < Tk * 16; q += blockDim.x) {
@@ -554,9 +468,9 @@ cudaError_t decode_mma_set_attributes() {
 
 cudaError_t launch_decode_experts_mma(const LaunchCtx& L, const uint8_t* tiled, const float* logits,
                                       const __nv_bfloat16* x, int T, DecodeTables* tables, int32_t* idx, float* w,
-                                      float* a_buf, __nv_bfloat16* y) {
+                                      __nv_bfloat16* a_buf, __nv_bfloat16* y) {
     if (T < 1 || T > DEC_T) return cudaErrorInvalidValue;
-    __nv_bfloat16* a16 = reinterpret_cast<__nv_bfloat16*>(a_buf);
+    __nv_bfloat16* a16 = a_buf;
     GateUpMmaParams gp{tiled, logits, x, T, tables, idx, w, a16, L.status, L.wait_limit_ns};
     // at most 64 x (257 + 28) items over the grid: 72 CTAs or more keep every
     // CTA's list within its 256 entries
@@ -564,7 +478,7 @@ cudaError_t launch_decode_experts_mma(const LaunchCtx& L, const uint8_t* tiled, 
     cudaError_t e = launch_hooked(L, FLINT_KERNEL_GATE_UP, gateup_mma_kernel, dim3(gi), dim3(MM_WARPS * 32),
                                   mi_smem_bytes(), gp);
     if (e != cudaSuccess) return e;
-    DownMmaParams dp{tiled, logits, a16, y, md_ns(T), T, L.status, L.wait_limit_ns};
+    DownMmaParams dp{tiled, logits, a16, y, T, L.status, L.wait_limit_ns};
     return launch_hooked(L, FLINT_KERNEL_DOWN, down_mma_kernel, dim3(MD_CTAS), dim3(MM_WARPS * 32),
                          md_smem_bytes(T), dp);
 }

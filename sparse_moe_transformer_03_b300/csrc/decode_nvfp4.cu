@@ -16,23 +16,27 @@
 //
 //   gateup_nvfp4  Unit = 8 gate rows + the 8 matching up rows of one expert
 //                 (the MMA's 16 rows), K = 2048 in 4 chunks of 4608 bytes;
-//                 a quad of warps takes a unit, each warp streaming one
-//                 chunk by cp.async.bulk into its ring, and the four partial
-//                 sums are added in warp order.  The tokens are the N
-//                 columns (tiles of 8).  x is staged in
-//                 shared memory as f16 times a power of two per token
-//                 (chosen so the token's largest |x| lies in [2^14, 2^15):
-//                 exact for every bf16 value not 28 binades below it); the
-//                 factor is divided out of the result.  Each lane ends with
-//                 gate and up of the same (row, token), so a = silu(g) * u is
-//                 formed in registers and written as bf16.
-//   down_nvfp4    CTA c owns output rows 16c..16c+15 (one MMA M tile).  Warp
-//                 w takes expert slots w, w + 8, ... (one 4608-byte chunk
-//                 each); the activations arrive as bf16 (written so by the
-//                 gate/up kernel; bf16 has fp32's range) for a bf16 MMA,
-//                 staged in smem when the batch is small; w * s_tensor * D is
-//                 accumulated per (token, row) in the warp's own buffer and
-//                 the eight buffers are summed in warp order: deterministic.
+//                 item = a unit against one tile of up to 8 of the expert's
+//                 tokens (the N columns).  The CTA takes one item at a time:
+//                 warp w streams half of chunk w / 2 (16 K blocks: 2 KiB of
+//                 codes, 256 bytes of scales) by cp.async.bulk into its ring,
+//                 and the eight partial sums are added in warp order.  x is
+//                 staged in shared memory as f16 times a power of two per
+//                 token (chosen so the token's largest |x| lies in [2^14,
+//                 2^15): exact for every bf16 value not 28 binades below it);
+//                 the factor is divided out of the result.  The lane that
+//                 adds the partial sums holds gate and up of the same (row,
+//                 token), so a = silu(g) * u is formed in registers and
+//                 written as bf16.
+//   down_nvfp4    CTA c owns output rows 16c..16c+15 (one MMA M tile).  Its
+//                 items are (slot, column half, tile of 8 tokens), item j to
+//                 warp j % 8, each half of the slot's 4608-byte chunk; the
+//                 activations arrive as bf16 (written so by the gate/up
+//                 kernel; bf16 has fp32's range) for a bf16 MMA, in the same
+//                 ring slot as the weights (one 4 KiB bulk copy per item);
+//                 w * s_tensor * D is accumulated per (token, row) in the
+//                 warp's own buffer and the eight buffers are summed in warp
+//                 order: deterministic.
 //
 // Routing, tables and the shared-expert prefetch are those of the bf16
 // decode kernels (decode_mma.cu).
@@ -124,7 +128,12 @@ __device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t v) {
 // ---------------------------------------------------------------------------
 
 constexpr int GN_WARPS = 8;
-constexpr int GN_XROW = H + 8;   // f16 per staged token row (+8: conflict-free B loads)
+constexpr int GN_XROW = H + 8;                   // f16 per staged token row (+8: conflict-free B loads)
+constexpr int NV_PIECE = NV_CHUNK / 2;           // half a chunk: 16 K blocks of codes, then their scales
+constexpr int NV_PIECE_CODES = NV_CODES / 2;     // 2048
+constexpr int NV_SMEM_BUDGET = 227 * 1024;       // dynamic shared memory of one CTA
+constexpr int GN_PART = 2 * GN_WARPS * 32 * 4;   // partial sums [item parity][warp][lane][4]
+static_assert(NV_PIECE % 16 == 0 && NV_PIECE_CODES % 16 == 0, "bulk copies want 16-byte pieces");
 
 struct GateUpNvParams {
     const uint8_t* nv;            // owned experts, NV_EXPERT_BYTES each
@@ -132,60 +141,50 @@ struct GateUpNvParams {
     const float* logits;          // [T][E]
     const __nv_bfloat16* x;       // [T][H]
     int T;
-    int ns;                       // ring chunks per warp
+    int ns;                       // ring pieces per warp
     DecodeTables* tables_out;
     int32_t* idx_out;
     float* w_out;
-    __nv_bfloat16* a;             // [pairs][I] bf16 (the down kernel's MMA operand)
+    __nv_bfloat16* a;             // activations, act_index layout (the down kernel's MMA operand)
     uint32_t* status;
     uint64_t limit_ns;
 };
 
-constexpr int GN_QUADS = GN_WARPS / 4;                 // a quad of warps works on one unit
-constexpr int GN_PART = GN_QUADS * 4 * 4 * 32 * 4;      // partial sums [quad][warp][N tile][lane][4]
-
-// ring chunks per warp (one chunk = the warp's quarter of a unit): deep while
-// x is small; one when x fills the shared memory (the next chunk then goes to L2)
-static inline int gn_ns(int T) { return T <= 8 ? 4 : (T <= 24 ? 2 : 1); }
-
+static inline size_t gn_fixed_bytes(int T) {
+    return (size_t)T * GN_XROW * 2 + DEC_T * 4 + (size_t)GN_PART * 4 + sizeof(DecodeTables) + DEC_T * TOPK * 8 +
+           2 * E * 4 + (NEXP + 1) * 4 + DEC_MAX_CTA_ITEMS * 4;
+}
+// ring pieces per warp: what the shared memory left beside x holds, at most 8
+// (4 for one or two tokens, whose CTAs have about three items each)
+static inline int gn_ns(int T) {
+    const int room = (int)(((size_t)NV_SMEM_BUDGET - gn_fixed_bytes(T)) / ((size_t)GN_WARPS * (NV_PIECE + 8)));
+    const int cap = T <= 2 ? 4 : 8;
+    return room < cap ? room : cap;
+}
 static inline size_t gn_smem_bytes(int T) {
-    return (size_t)GN_WARPS * gn_ns(T) * NV_CHUNK + (size_t)T * GN_XROW * 2 + DEC_T * 4 + (size_t)GN_PART * 4 +
-           (size_t)GN_WARPS * gn_ns(T) * 8 + sizeof(DecodeTables) + DEC_T * TOPK * 8 + 2 * E * 4;
+    return (size_t)GN_WARPS * gn_ns(T) * (NV_PIECE + 8) + gn_fixed_bytes(T);
 }
 
-// barrier (and AND of a predicate) of the 128 threads of quad q
-__device__ __forceinline__ bool quad_all(int q, bool v) {
-    uint32_t r;
-    asm volatile(
-        "{\n .reg .pred p, t;\n setp.ne.u32 p, %1, 0;\n barrier.cta.red.and.pred t, %2, 128, p;\n"
-        " selp.u32 %0, 1, 0, t;\n}\n"
-        : "=r"(r)
-        : "r"(v ? 1u : 0u), "r"(1 + q)
-        : "memory");
-    return r != 0;
-}
-__device__ __forceinline__ void quad_sync(int q) { asm volatile("bar.sync %0, 128;" ::"r"(1 + q) : "memory"); }
-
-// Quad q of CTA c takes units c + G q, c + G (q + 2), ...; warp k of the quad
-// streams and multiplies chunk k (columns 512k .. 512k + 511) of each, and the
-// four partial sums are added in warp order.  A unit then costs each warp a
-// quarter of the dequantise -> MMA chain it used to cost one warp.
+// Work items as in the bf16 kernel: (slot, unit of 8 gate + 8 up rows, tile of
+// up to 8 tokens), one at a time per CTA.  Warp w takes K blocks 16w .. 16w +
+// 15 (half of chunk w / 2 of the unit: 2 KiB of codes and 256 bytes of
+// scales); the eight partial sums are added in warp order.
 __global__ void __launch_bounds__(GN_WARPS * 32, 1) gateup_nvfp4_kernel(GateUpNvParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int quad = warp >> 2, wq = warp & 3;
     const int NS = p.ns, T = p.T, G = gridDim.x, c = blockIdx.x;
-    uint8_t* ring = smem + (size_t)warp * NS * NV_CHUNK;
-    __half* xh = reinterpret_cast<__half*>(smem + (size_t)GN_WARPS * NS * NV_CHUNK);
+    uint8_t* ring = smem + (size_t)warp * NS * NV_PIECE;
+    __half* xh = reinterpret_cast<__half*>(smem + (size_t)GN_WARPS * NS * NV_PIECE);
     float* xinv = reinterpret_cast<float*>(xh + (size_t)T * GN_XROW);
     float* part = xinv + DEC_T;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(part + GN_PART);
-    uint64_t* bar = bars + warp * NS;
-    DecodeTables* tab = reinterpret_cast<DecodeTables*>(bars + GN_WARPS * NS);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(part + GN_PART) + warp * NS;
+    DecodeTables* tab = reinterpret_cast<DecodeTables*>(reinterpret_cast<uint64_t*>(part + GN_PART) + GN_WARPS * NS);
     int* sel_e = reinterpret_cast<int*>(tab + 1);
     float* sel_w = reinterpret_cast<float*>(sel_e + DEC_T * TOPK);
     uint32_t* tmask = reinterpret_cast<uint32_t*>(sel_w + DEC_T * TOPK);
     int* pair0 = reinterpret_cast<int*>(tmask + E);
+    int* slot_item0 = pair0 + E;
+    int* list = slot_item0 + NEXP + 1;
 
     if (lane == 0) {
         for (int s = 0; s < NS; ++s) mbar_init(&bar[s], 1);
@@ -193,23 +192,24 @@ __global__ void __launch_bounds__(GN_WARPS * 32, 1) gateup_nvfp4_kernel(GateUpNv
     }
     __syncthreads();
 
-    // the quad's i-th unit; this warp's chunk of it is chunk wq
-    auto unit_of = [&](int i) { return c + G * (quad + GN_QUADS * i); };
-    auto chunk_ptr = [&](int i, int expert) {
-        const int r = unit_of(i) & (NV_GU_UNITS - 1);
-        return p.nv + (size_t)expert * NV_EXPERT_BYTES + ((size_t)r * NV_GU_CHUNKS + wq) * NV_CHUNK;
-    };
-    auto issue = [&](int i, int expert) {
-        const int s = i % NS;
-        mbar_arrive_expect_tx(&bar[s], NV_CHUNK);
-        bulk_g2s(ring + (size_t)s * NV_CHUNK, chunk_ptr(i, expert), NV_CHUNK, &bar[s]);
+    const int nt0 = (T + 7) >> 3;                    // token tiles of the shared slot (slot 0)
+    auto issue = [&](int i, int it, int expert) {
+        const int s = i % NS, r = (it >> 2) & (NV_GU_UNITS - 1);
+        const uint8_t* chunk =
+            p.nv + (size_t)expert * NV_EXPERT_BYTES + ((size_t)r * NV_GU_CHUNKS + (warp >> 1)) * NV_CHUNK;
+        uint8_t* dst = ring + (size_t)s * NV_PIECE;
+        mbar_arrive_expect_tx(&bar[s], NV_PIECE);
+        bulk_g2s(dst, chunk + (warp & 1) * NV_PIECE_CODES, NV_PIECE_CODES, &bar[s]);
+        bulk_g2s(dst + NV_PIECE_CODES, chunk + NV_CODES + (warp & 1) * (NV_PIECE - NV_PIECE_CODES),
+                 NV_PIECE - NV_PIECE_CODES, &bar[s]);
     };
 
-    // ---- before the router has finished: the shared expert's chunks ----
+    // ---- before the router has finished: the shared slot's items ----
     int issued = 0;
     if (lane == 0) {
-        for (int i = 0; i < NS && unit_of(i) < NV_GU_UNITS; ++i) {
-            issue(i, SHARED);
+        for (int i = 0; i < NS && c + G * i < NV_GU_UNITS * nt0; ++i) {
+            const int j = c + G * i;
+            issue(i, ((j / nt0) << 2) | (j % nt0), SHARED);
             issued = i + 1;
         }
     }
@@ -249,7 +249,7 @@ __global__ void __launch_bounds__(GN_WARPS * 32, 1) gateup_nvfp4_kernel(GateUpNv
         }
     }
 
-    // ---- top-6 of every token, then the (slot, token) tables ----
+    // ---- top-6 of every token, then the (slot, token) tables and the items ----
     for (int t = warp; t < T; t += GN_WARPS) {
         float v[8];
 #pragma unroll
@@ -269,116 +269,101 @@ __global__ void __launch_bounds__(GN_WARPS * 32, 1) gateup_nvfp4_kernel(GateUpNv
         }
     }
     __syncthreads();
-    if (warp == 0) build_decode_tables_warp(T, sel_e, sel_w, tmask, pair0, tab, lane);
+    if (warp == 0) {
+        build_decode_tables_warp(T, sel_e, sel_w, tmask, pair0, tab, lane);
+        build_gateup_item_starts_warp(tab, slot_item0, lane);
+    }
     __syncthreads();
     if (c == 0) {
         const int* src = reinterpret_cast<const int*>(tab);
         int* dst = reinterpret_cast<int*>(p.tables_out);
         for (int k = threadIdx.x; k < (int)(sizeof(DecodeTables) / 4); k += blockDim.x) dst[k] = src[k];
     }
-    const int total_units = tab->n_slots * NV_GU_UNITS;
-    int my_units = 0;
-    while (unit_of(my_units) < total_units) ++my_units;
-    auto expert_of = [&](int i) { return tab->slot_expert[unit_of(i) / NV_GU_UNITS]; };
+    int my_items = list_gateup_items(tab, slot_item0, c, G, list);
+    if (my_items < 0) {   // the launcher sizes the grid so that this cannot happen
+        if (threadIdx.x == 0) report_status(p.status, ST_BADINDEX);
+        my_items = 0;
+    }
+    __syncthreads();
     if (lane == 0) {
-        for (int i = issued; i < NS && i < my_units; ++i) {
-            issue(i, expert_of(i));
+        for (int i = issued; i < NS && i < my_items; ++i) {
+            issue(i, list[i], tab->slot_expert[list[i] >> 8]);
             issued = i + 1;
         }
-        if (NS == 1 && my_units > 1) bulk_prefetch_l2(chunk_ptr(1, expert_of(1)), NV_CHUNK);
     }
 
     const int g = lane >> 2, cq = lane & 3;
-    float* qpart = part + quad * (4 * 4 * 32 * 4);
     bool ok = true;
     int i = 0;
-    for (; i < my_units; ++i) {
-        const int q = unit_of(i), u = q / NV_GU_UNITS, r = q & (NV_GU_UNITS - 1);
-        const int pb = tab->slot_pair0[u], np = tab->slot_pair0[u + 1] - pb;   // 1..32 tokens
-        const int ntile = (np + 7) >> 3;
-        int xo[4];
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-            const int n = nt * 8 + g;
-            xo[nt] = tab->pair_token[pb + (n < np ? n : np - 1)] * GN_XROW + 2 * cq + wq * 512;
-        }
+    for (; i < my_items; ++i) {
+        const int it = list[i], u = it >> 8;
+        const int pb = tab->slot_pair0[u], np = tab->slot_pair0[u + 1] - pb;
+        const int n = (it & 3) * 8 + g;
+        const __half* xb = xh + tab->pair_token[pb + (n < np ? n : np - 1)] * GN_XROW + warp * 256 + 2 * cq;
         const int s = i % NS;
         const bool got = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(&bar[s], (i / NS) & 1, p.limit_ns));
+        float* pw = part + (((i & 1) * GN_WARPS + warp) * 32 + lane) * 4;
         if (got) {
-            // four accumulators per N tile (K block kb goes to chain kb % 4)
-            float acc[4][4][4];
+            // four accumulators (K block kb goes to chain kb % 4)
+            float acc[4][4];
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch)
+            for (int ch = 0; ch < 4; ++ch) acc[ch][0] = acc[ch][1] = acc[ch][2] = acc[ch][3] = 0.f;
+            const uint8_t* buf = ring + (size_t)s * NV_PIECE;
 #pragma unroll
-                for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) acc[ch][nt][k] = 0.f;
-            const uint8_t* buf = ring + (size_t)s * NV_CHUNK;
-#pragma unroll 2
-            for (int kb = 0; kb < NV_CHUNK_KB; kb += 4) {
+            for (int kb = 0; kb < 16; kb += 4) {
                 uint32_t a[4][4];
 #pragma unroll
                 for (int ch = 0; ch < 4; ++ch)
                     nv_a_frag(*reinterpret_cast<const uint32_t*>(buf + (kb + ch) * 128 + 4 * lane),
-                              *reinterpret_cast<const uint16_t*>(buf + NV_CODES + (kb + ch) * 16 + 2 * g), a[ch]);
+                              *reinterpret_cast<const uint16_t*>(buf + NV_PIECE_CODES + (kb + ch) * 16 + 2 * g),
+                              a[ch]);
 #pragma unroll
-                for (int nt = 0; nt < 4; ++nt) {
-                    if (nt < ntile) {
-                        const __half* xb = xh + xo[nt] + kb * 16;
-#pragma unroll
-                        for (int ch = 0; ch < 4; ++ch)
-                            mma_f16_16816(acc[ch][nt], a[ch], *reinterpret_cast<const uint32_t*>(xb + 16 * ch),
-                                          *reinterpret_cast<const uint32_t*>(xb + 16 * ch + 8));
-                    }
-                }
+                for (int ch = 0; ch < 4; ++ch)
+                    mma_f16_16816(acc[ch], a[ch], *reinterpret_cast<const uint32_t*>(xb + (kb + ch) * 16),
+                                  *reinterpret_cast<const uint32_t*>(xb + (kb + ch) * 16 + 8));
             }
             __syncwarp();   // every lane is done reading slot s
-            if (lane == 0) {
-                if (i + NS < my_units) {
-                    fence_proxy_async_smem();
-                    issue(i + NS, expert_of(i + NS));
-                    issued = i + NS + 1;
-                }
-                if (NS == 1 && i + 2 < my_units) bulk_prefetch_l2(chunk_ptr(i + 2, expert_of(i + 2)), NV_CHUNK);
+            if (lane == 0 && i + NS < my_items) {
+                fence_proxy_async_smem();
+                issue(i + NS, list[i + NS], tab->slot_expert[list[i + NS] >> 8]);
+                issued = i + NS + 1;
             }
-#pragma unroll
-            for (int nt = 0; nt < 4; ++nt)
-                if (nt < ntile)
-                    *reinterpret_cast<float4*>(qpart + ((wq * 4 + nt) * 32 + lane) * 4) = make_float4(
-                        acc[0][nt][0] + acc[1][nt][0] + (acc[2][nt][0] + acc[3][nt][0]),
-                        acc[0][nt][1] + acc[1][nt][1] + (acc[2][nt][1] + acc[3][nt][1]),
-                        acc[0][nt][2] + acc[1][nt][2] + (acc[2][nt][2] + acc[3][nt][2]),
-                        acc[0][nt][3] + acc[1][nt][3] + (acc[2][nt][3] + acc[3][nt][3]));
+            *reinterpret_cast<float4*>(pw) = make_float4(acc[0][0] + acc[1][0] + (acc[2][0] + acc[3][0]),
+                                                         acc[0][1] + acc[1][1] + (acc[2][1] + acc[3][1]),
+                                                         acc[0][2] + acc[1][2] + (acc[2][2] + acc[3][2]),
+                                                         acc[0][3] + acc[1][3] + (acc[2][3] + acc[3][3]));
         }
-        // the decision to go on is taken by the whole quad
-        if (!quad_all(quad, got)) {
+        if (!__syncthreads_and(got)) {
             ok = false;
             break;
         }
-        // warp nt of the quad adds tile nt's four partial sums in warp order;
-        // lane (g, cq) then holds gate (0, 1) and up (2, 3) of row j = 8r + g
-        if (wq < ntile) {
-            float4 sum = *reinterpret_cast<const float4*>(qpart + (wq * 32 + lane) * 4);
+        // warp i % 8 adds the item's eight partial sums in warp order; lane
+        // (g, cq) then holds gate (x, y) and up (z, w) of row 8r + g for tokens
+        // 2cq, 2cq + 1 of the tile.  The buffer of parity i & 1 is next written
+        // after the barrier of item i + 1, which this warp reaches only after
+        // the sum.
+        if (warp == (i & (GN_WARPS - 1))) {
+            const float* pb0 = part + ((i & 1) * GN_WARPS * 32 + lane) * 4;
+            float4 sum = *reinterpret_cast<const float4*>(pb0);
 #pragma unroll
-            for (int w = 1; w < 4; ++w) {
-                const float4 v = *reinterpret_cast<const float4*>(qpart + ((w * 4 + wq) * 32 + lane) * 4);
+            for (int w = 1; w < GN_WARPS; ++w) {
+                const float4 v = *reinterpret_cast<const float4*>(pb0 + w * 32 * 4);
                 sum.x += v.x;
                 sum.y += v.y;
                 sum.z += v.z;
                 sum.w += v.w;
             }
             const float tsg = __ldg(p.ts + 2 * tab->slot_expert[u]);
-            const int j = 8 * r + g, n0 = wq * 8 + 2 * cq;
+            const int j = 8 * ((it >> 2) & (NV_GU_UNITS - 1)) + g, n0 = (it & 3) * 8 + 2 * cq;
             if (n0 < np) {
                 const float f = tsg * xinv[tab->pair_token[pb + n0]];
-                p.a[(size_t)(pb + n0) * I + j] = __float2bfloat16_rn(silu_f(sum.x * f) * (sum.z * f));
+                p.a[act_index(pb + n0, j)] = __float2bfloat16_rn(silu_f(sum.x * f) * (sum.z * f));
             }
             if (n0 + 1 < np) {
                 const float f = tsg * xinv[tab->pair_token[pb + n0 + 1]];
-                p.a[(size_t)(pb + n0 + 1) * I + j] = __float2bfloat16_rn(silu_f(sum.y * f) * (sum.w * f));
+                p.a[act_index(pb + n0 + 1, j)] = __float2bfloat16_rn(silu_f(sum.y * f) * (sum.w * f));
             }
         }
-        quad_sync(quad);   // the partial sums are read before the next unit writes them
     }
     if (!ok) {
         if (lane == 0) {
@@ -396,65 +381,82 @@ __global__ void __launch_bounds__(GN_WARPS * 32, 1) gateup_nvfp4_kernel(GateUpNv
 
 constexpr int DV_WARPS = 8;
 constexpr int DV_CTAS = H / 16;        // 128: CTA c owns rows 16c .. 16c + 15
-constexpr int DV_APAIRS = 64;          // activation rows staged in smem when the batch has at most this many
-constexpr int DV_AROW = I * 2 + 16;    // bytes per staged row (+16: conflict-free B loads)
+constexpr int DV_ACT = 8 * 256 * 2;    // an item's activation tile: 8 pairs x 256 columns, bf16
+constexpr int DV_SLOT = NV_PIECE + DV_ACT;
+static_assert(DV_SLOT % 16 == 0, "ring slots stay 16-byte aligned");
 
 struct DownNvParams {
     const uint8_t* nv;
     const float* ts;
     const float* logits;          // [T][E] router logits (final before this kernel starts)
-    const __nv_bfloat16* a;       // [pairs][I] bf16
+    const __nv_bfloat16* a;       // activations, act_index layout
     __nv_bfloat16* y;             // [T][H]
-    int ns;                       // ring chunks per warp
+    int ns;                       // ring slots per warp
     int T;
     uint32_t* status;
     uint64_t limit_ns;
 };
 
-// small batches keep the kernel small, so the next layer's gate/up CTAs fit beside it
-static inline int dv_ns(int T) { return T <= 2 ? 1 : (T <= 8 ? 2 : 4); }
-__host__ __device__ inline bool dv_staged(int T) { return (TOPK + 1) * T <= DV_APAIRS; }
-
-static inline size_t dv_smem_bytes(int T) {
-    return (size_t)DV_WARPS * dv_ns(T) * NV_CHUNK + (dv_staged(T) ? (size_t)(TOPK + 1) * T * DV_AROW : 0) +
-           (size_t)DV_WARPS * T * 16 * 4 + (DV_WARPS * dv_ns(T) + 1) * 8 + sizeof(DecodeTables) +
-           DEC_T * TOPK * 8 + 2 * E * 4;
+static inline size_t dv_fixed_bytes(int T) {
+    return (size_t)DV_WARPS * T * 16 * 4 + sizeof(DecodeTables) + DEC_T * TOPK * 8 + 2 * E * 4 +
+           (DEC_MAX_DOWN_ITEMS + 1) * 4;
 }
+// ring slots per warp: a warp has about 2 (T + 1) / 8 + 1 items at small T;
+// small batches keep the kernel small, so the next layer's gate/up CTAs fit
+// beside it
+static inline int dv_ns(int T) {
+    const int room = (int)(((size_t)NV_SMEM_BUDGET - dv_fixed_bytes(T)) / ((size_t)DV_WARPS * (DV_SLOT + 8)));
+    const int cap = T <= 2 ? 2 : 4;
+    return room < cap ? room : cap;
+}
+static inline size_t dv_smem_bytes(int T) { return (size_t)DV_WARPS * dv_ns(T) * (DV_SLOT + 8) + dv_fixed_bytes(T); }
 
+// Work items as in the bf16 down kernel: (slot, column half, tile of 8
+// tokens), item j to warp j % 8.  A ring slot holds half of the slot's
+// 16-row chunk (2 KiB of codes and 256 bytes of scales) and the tile's
+// activations (4 KiB, one bulk copy from the act_index layout).
 __global__ void __launch_bounds__(DV_WARPS * 32, 1) down_nvfp4_kernel(DownNvParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c = blockIdx.x, NS = p.ns, Tk = p.T;
-    const bool staged = dv_staged(Tk);
-    uint8_t* ring = smem + (size_t)warp * NS * NV_CHUNK;
-    uint8_t* astage = smem + (size_t)DV_WARPS * NS * NV_CHUNK;                           // [7T][DV_AROW]
-    float* yw_all = reinterpret_cast<float*>(astage + (staged ? (size_t)(TOPK + 1) * Tk * DV_AROW : 0));
+    uint8_t* ring = smem + (size_t)warp * NS * DV_SLOT;
+    float* yw_all = reinterpret_cast<float*>(smem + (size_t)DV_WARPS * NS * DV_SLOT);
     float* yw = yw_all + warp * Tk * 16;                                                  // [8][T][16]
     uint64_t* bars = reinterpret_cast<uint64_t*>(yw_all + DV_WARPS * Tk * 16);
     uint64_t* bar = bars + warp * NS;
-    uint64_t* abar = bars + DV_WARPS * NS;
-    DecodeTables* tab = reinterpret_cast<DecodeTables*>(abar + 1);
+    DecodeTables* tab = reinterpret_cast<DecodeTables*>(bars + DV_WARPS * NS);
     int* sel_e = reinterpret_cast<int*>(tab + 1);
     float* sel_w = reinterpret_cast<float*>(sel_e + DEC_T * TOPK);
     uint32_t* tmask = reinterpret_cast<uint32_t*>(sel_w + DEC_T * TOPK);
     int* pair0 = reinterpret_cast<int*>(tmask + E);
+    int* items = pair0 + E;
+    int* n_items_s = items + DEC_MAX_DOWN_ITEMS;
 
     if (lane == 0) {
         for (int s = 0; s < NS; ++s) mbar_init(&bar[s], 1);
-        if (warp == 0) mbar_init(abar, 1);
         fence_mbar_init();
     }
-    auto issue = [&](int i, int expert) {
-        const int s = i % NS;
-        const uint8_t* src = p.nv + (size_t)expert * NV_EXPERT_BYTES + NV_GU_BYTES + (size_t)c * NV_CHUNK;
-        mbar_arrive_expect_tx(&bar[s], NV_CHUNK);
-        bulk_g2s(ring + (size_t)s * NV_CHUNK, src, NV_CHUNK, &bar[s]);
+    auto item_of = [&](int k) { return items[warp + DV_WARPS * k]; };
+    auto copy_w = [&](int k) {
+        const int it = item_of(k), s = k % NS, hk = (it >> 2) & 1;
+        const uint8_t* chunk =
+            p.nv + (size_t)tab->slot_expert[it >> 3] * NV_EXPERT_BYTES + NV_GU_BYTES + (size_t)c * NV_CHUNK;
+        uint8_t* dst = ring + (size_t)s * DV_SLOT;
+        bulk_g2s(dst, chunk + hk * NV_PIECE_CODES, NV_PIECE_CODES, &bar[s]);
+        bulk_g2s(dst + NV_PIECE_CODES, chunk + NV_CODES + hk * (NV_PIECE - NV_PIECE_CODES),
+                 NV_PIECE - NV_PIECE_CODES, &bar[s]);
+    };
+    auto copy_a = [&](int k) {
+        const int it = item_of(k), s = k % NS;
+        const int p0 = tab->slot_pair0[it >> 3] + (it & 3) * 8;
+        bulk_g2s(ring + (size_t)s * DV_SLOT + NV_PIECE, p.a + ((size_t)((it >> 2) & 1) * DEC_ACT_ROWS + p0) * 256,
+                 DV_ACT, &bar[s]);
     };
     // Every gate/up CTA triggers this launch only after its own dependency
     // wait, which returns once the router grid has completed: the logits are
     // final here although the gate/up kernel may still be running.  Select
     // each token's experts and build the same tables the gate/up kernel
-    // builds, and start the weight chunks of this warp's first slots now, so
+    // builds, and start the weight pieces of this warp's first items now, so
     // they stream while the gate/up kernel runs.
     for (int t = warp; t < Tk; t += DV_WARPS) {
         float v[8];
@@ -470,128 +472,88 @@ __global__ void __launch_bounds__(DV_WARPS * 32, 1) down_nvfp4_kernel(DownNvPara
     }
     for (int k = threadIdx.x; k < DV_WARPS * Tk * 16; k += blockDim.x) yw_all[k] = 0.f;
     __syncthreads();
-    if (warp == 0) build_decode_tables_warp(Tk, sel_e, sel_w, tmask, pair0, tab, lane);
+    if (warp == 0) {
+        build_decode_tables_warp(Tk, sel_e, sel_w, tmask, pair0, tab, lane);
+        const int n = build_down_items_warp(tab, items, lane);
+        if (lane == 0) *n_items_s = n;
+    }
     __syncthreads();
-    const int n_slots = tab->n_slots, n_pairs = tab->n_pairs;
-    const int my_slots = n_slots > warp ? (n_slots - warp + DV_WARPS - 1) / DV_WARPS : 0;
+    const int n_items = *n_items_s;
+    const int my_items = n_items > warp ? (n_items - warp + DV_WARPS - 1) / DV_WARPS : 0;
+    // weights of the first items now (the phase waits for its arrival, which
+    // comes with the activations after the dependency wait)
     int issued = 0;
     if (lane == 0) {
-        for (int i = 0; i < NS && i < my_slots; ++i) {
-            issue(i, tab->slot_expert[warp + DV_WARPS * i]);
-            issued = i + 1;
+        for (int k = 0; k < NS && k < my_items; ++k) {
+            mbar_expect_tx(&bar[k], NV_PIECE);
+            copy_w(k);
+            issued = k + 1;
         }
     }
     pdl_wait();     // the gate/up kernel is complete: activations are visible
     pdl_trigger();
-    if (staged && threadIdx.x == 0) {
-        // every activation row, one bulk copy per row (padded rows in smem)
-        mbar_arrive_expect_tx(abar, n_pairs * I * 2);
-        for (int pr = 0; pr < n_pairs; ++pr) bulk_g2s(astage + (size_t)pr * DV_AROW, p.a + (size_t)pr * I, I * 2, abar);
+    if (lane == 0) {
+        for (int k = 0; k < issued; ++k) {
+            mbar_arrive_expect_tx(&bar[k], DV_ACT);
+            copy_a(k);
+        }
     }
-    bool ok = true;
-    if (staged && my_slots > 0) ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(abar, 0, p.limit_ns));
 
     const int g = lane >> 2, cq = lane & 3;
-    int i = 0;
-    for (; ok && i < my_slots; ++i) {
-        const int u = warp + DV_WARPS * i, s = i % NS;
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(&bar[s], (i / NS) & 1, p.limit_ns))) {
+    bool ok = true;
+    int k = 0;
+    for (; k < my_items; ++k) {
+        const int it = item_of(k), u = it >> 3, nt = it & 3;
+        const int pb = tab->slot_pair0[u], np = tab->slot_pair0[u + 1] - pb;
+        const int s = k % NS;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(&bar[s], (k / NS) & 1, p.limit_ns))) {
             ok = false;
             break;
         }
-        const uint8_t* buf = ring + (size_t)s * NV_CHUNK;
-        const int pb = tab->slot_pair0[u], np = tab->slot_pair0[u + 1] - pb;
-        const int ntile = (np + 7) >> 3;
-        int prow[4];
+        const uint8_t* buf = ring + (size_t)s * DV_SLOT;
+        // row g of the activation tile; chunk q of it sits at q ^ (pair % 8)
+        const uint8_t* ar = buf + NV_PIECE + g * 512 + 4 * cq;
+        const int sw = (pb + nt * 8 + g) & 7;
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-            const int n = nt * 8 + g;
-            prow[nt] = pb + (n < np ? n : np - 1);
-        }
-        float acc[4][4];
+        for (int kb = 0; kb < 16; ++kb) {
+            uint32_t a[4];
+            nv_a_frag(*reinterpret_cast<const uint32_t*>(buf + kb * 128 + 4 * lane),
+                      *reinterpret_cast<const uint16_t*>(buf + NV_PIECE_CODES + kb * 16 + 2 * g), a);
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-        if (staged) {
-#pragma unroll 4
-            for (int kb = 0; kb < NV_CHUNK_KB; ++kb) {
-                uint32_t a[4];
-                nv_a_frag(*reinterpret_cast<const uint32_t*>(buf + kb * 128 + 4 * lane),
-                          *reinterpret_cast<const uint16_t*>(buf + NV_CODES + kb * 16 + 2 * g), a);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) a[k] = f16x2_to_bf16x2(a[k]);
-#pragma unroll
-                for (int nt = 0; nt < 4; ++nt) {
-                    if (nt < ntile) {
-                        const uint8_t* ar = astage + (size_t)prow[nt] * DV_AROW + (kb * 16 + 2 * cq) * 2;
-                        mma_bf16_16816(acc[nt], a, *reinterpret_cast<const uint32_t*>(ar),
-                                       *reinterpret_cast<const uint32_t*>(ar + 16));
-                    }
-                }
-            }
-        } else {
-            // activations through L1 (read-only here; written by the previous
-            // grid): the first N tile's operands for 16 blocks are requested
-            // at once, the other tiles' as they are used
-#pragma unroll 1
-            for (int kh = 0; kh < NV_CHUNK_KB; kh += 16) {
-                uint32_t bq[16][2];
-                const unsigned int* a0 =
-                    reinterpret_cast<const unsigned int*>(p.a + (size_t)prow[0] * I + kh * 16 + 2 * cq);
-#pragma unroll
-                for (int kb = 0; kb < 16; ++kb) {
-                    bq[kb][0] = __ldg(a0 + kb * 8);
-                    bq[kb][1] = __ldg(a0 + kb * 8 + 4);
-                }
-#pragma unroll
-                for (int kb = 0; kb < 16; ++kb) {
-                    uint32_t a[4];
-                    nv_a_frag(*reinterpret_cast<const uint32_t*>(buf + (kh + kb) * 128 + 4 * lane),
-                              *reinterpret_cast<const uint16_t*>(buf + NV_CODES + (kh + kb) * 16 + 2 * g), a);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) a[k] = f16x2_to_bf16x2(a[k]);
-                    mma_bf16_16816(acc[0], a, bq[kb][0], bq[kb][1]);
-#pragma unroll
-                    for (int nt = 1; nt < 4; ++nt) {
-                        if (nt < ntile) {
-                            const unsigned int* ar = reinterpret_cast<const unsigned int*>(
-                                p.a + (size_t)prow[nt] * I + (kh + kb) * 16 + 2 * cq);
-                            mma_bf16_16816(acc[nt], a, __ldg(ar), __ldg(ar + 4));
-                        }
-                    }
-                }
-            }
+            for (int q = 0; q < 4; ++q) a[q] = f16x2_to_bf16x2(a[q]);
+            mma_bf16_16816(acc[kb & 1], a, *reinterpret_cast<const uint32_t*>(ar + (((2 * kb) ^ sw) << 4)),
+                           *reinterpret_cast<const uint32_t*>(ar + (((2 * kb + 1) ^ sw) << 4)));
         }
         __syncwarp();
-        if (lane == 0 && i + NS < my_slots) {
+        if (lane == 0 && k + NS < my_items) {
             fence_proxy_async_smem();
-            issue(i + NS, tab->slot_expert[warp + DV_WARPS * (i + NS)]);
-            issued = i + NS + 1;
+            mbar_arrive_expect_tx(&bar[s], NV_PIECE + DV_ACT);
+            copy_w(k + NS);
+            copy_a(k + NS);
+            issued = k + NS + 1;
         }
-        // lane (g, cq): rows g and g + 8 of this CTA's 16, tile columns 2cq, 2cq + 1
+        // lane (g, cq): rows g and g + 8 of this CTA's 16, tokens 2cq, 2cq + 1 of the tile
         const float tsd = __ldg(p.ts + 2 * tab->slot_expert[u] + 1);
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int n = nt * 8 + 2 * cq + hh;
-                if (nt < ntile && n < np) {
-                    const int pr = pb + n, t = tab->pair_token[pr];
-                    const float wgt = tab->pair_weight[pr] * tsd;
-                    yw[t * 16 + g] = fmaf(wgt, acc[nt][hh], yw[t * 16 + g]);
-                    yw[t * 16 + g + 8] = fmaf(wgt, acc[nt][2 + hh], yw[t * 16 + g + 8]);
-                }
+        for (int hh = 0; hh < 2; ++hh) {
+            const int n = nt * 8 + 2 * cq + hh;
+            if (n < np) {
+                const int pr = pb + n, t = tab->pair_token[pr];
+                const float wgt = tab->pair_weight[pr] * tsd;
+                yw[t * 16 + g] = fmaf(wgt, acc[0][hh] + acc[1][hh], yw[t * 16 + g]);
+                yw[t * 16 + g + 8] = fmaf(wgt, acc[0][2 + hh] + acc[1][2 + hh], yw[t * 16 + g + 8]);
             }
         }
     }
     if (!ok && lane == 0) {
         report_status(p.status, ST_TIMEOUT);
-        for (int k = i; k < issued; ++k) mbar_wait_bounded(&bar[k % NS], (k / NS) & 1, p.limit_ns);
-        if (staged && warp == 0) mbar_wait_bounded(abar, 0, p.limit_ns);
+        for (int q = k; q < issued; ++q) mbar_wait_bounded(&bar[q % NS], (q / NS) & 1, p.limit_ns);
     }
     __syncthreads();
     // y rows 16c .. 16c + 15: the eight warps' partial sums in warp order
-    for (int k = threadIdx.x; k < Tk * 16; k += blockDim.x) {
-        const int t = k >> 4, rr = k & 15;
+    for (int q = threadIdx.x; q < Tk * 16; q += blockDim.x) {
+        const int t = q >> 4, rr = q & 15;
         float sum = 0.f;
 #pragma unroll
         for (int w = 0; w < DV_WARPS; ++w) sum += yw_all[w * Tk * 16 + t * 16 + rr];
@@ -604,23 +566,27 @@ __global__ void __launch_bounds__(DV_WARPS * 32, 1) down_nvfp4_kernel(DownNvPara
 // ---------------------------------------------------------------------------
 
 cudaError_t decode_nvfp4_set_attributes() {
-    cudaError_t e = cudaFuncSetAttribute(gateup_nvfp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(gn_smem_bytes(DEC_T) > gn_smem_bytes(8) ? gn_smem_bytes(DEC_T)
-                                                                                       : gn_smem_bytes(8)));
+    size_t gmax = 0, dmax = 0;
+    for (int T = 1; T <= DEC_T; ++T) {
+        gmax = gn_smem_bytes(T) > gmax ? gn_smem_bytes(T) : gmax;
+        dmax = dv_smem_bytes(T) > dmax ? dv_smem_bytes(T) : dmax;
+    }
+    cudaError_t e = cudaFuncSetAttribute(gateup_nvfp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gmax);
     if (e != cudaSuccess) return e;
-    size_t dmax = 0;
-    for (int T = 1; T <= DEC_T; ++T) dmax = dv_smem_bytes(T) > dmax ? dv_smem_bytes(T) : dmax;
     return cudaFuncSetAttribute(down_nvfp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dmax);
 }
 
 cudaError_t launch_decode_experts_nvfp4(const LaunchCtx& L, const uint8_t* nv, const float* nv_ts,
                                         const float* logits, const __nv_bfloat16* x, int T, DecodeTables* tables,
-                                        int32_t* idx, float* w, float* a_buf, __nv_bfloat16* y) {
-    // the activations are kept as bf16 in the (fp32-sized) activation buffer
-    __nv_bfloat16* a16 = reinterpret_cast<__nv_bfloat16*>(a_buf);
+                                        int32_t* idx, float* w, __nv_bfloat16* a_buf, __nv_bfloat16* y) {
+    __nv_bfloat16* a16 = a_buf;
+    if (T < 1 || T > DEC_T) return cudaErrorInvalidValue;
     GateUpNvParams gp{nv, nv_ts, logits, x, T, gn_ns(T), tables, idx, w, a16, L.status, L.wait_limit_ns};
-    cudaError_t e = launch_hooked(L, FLINT_KERNEL_GATE_UP, gateup_nvfp4_kernel, dim3(L.num_sms),
-                                  dim3(GN_WARPS * 32), gn_smem_bytes(T), gp);
+    // at most 64 x (257 + 28) items over the grid: 72 CTAs or more keep every
+    // CTA's list within DEC_MAX_CTA_ITEMS
+    const int gi = L.num_sms >= 72 ? L.num_sms : 72;
+    cudaError_t e = launch_hooked(L, FLINT_KERNEL_GATE_UP, gateup_nvfp4_kernel, dim3(gi), dim3(GN_WARPS * 32),
+                                  gn_smem_bytes(T), gp);
     if (e != cudaSuccess) return e;
     DownNvParams dp{nv, nv_ts, logits, a16, y, dv_ns(T), T, L.status, L.wait_limit_ns};
     return launch_hooked(L, FLINT_KERNEL_DOWN, down_nvfp4_kernel, dim3(DV_CTAS), dim3(DV_WARPS * 32),

@@ -42,7 +42,7 @@ struct flint_moe {
     int32_t* idx;                  // [CHUNK][TOPK]
     float* w;                      // [CHUNK][TOPK]
     DecodeTables* dec_tables;
-    float* a_dec;                  // [DEC_PAIRS][I]
+    __nv_bfloat16* a_dec;          // decode activations (act_index layout)
     int32_t* local_rank;           // [CHUNK][TOPK]
     int32_t* blk_counts;           // [CHUNK/128][E]
     int32_t* blk_base;             // [CHUNK/128][E]
@@ -112,7 +112,7 @@ void carve_workspace(flint_moe* h, char* base, size_t* bytes_out) {
     h->idx = c.take<int32_t>((size_t)CHUNK * TOPK);
     h->w = c.take<float>((size_t)CHUNK * TOPK);
     h->dec_tables = c.take<DecodeTables>(1);
-    h->a_dec = c.take<float>((size_t)DEC_PAIRS * I);
+    h->a_dec = c.take<__nv_bfloat16>(DEC_ACT_BYTES / 2);
     h->local_rank = c.take<int32_t>((size_t)CHUNK * TOPK);
     h->blk_counts = c.take<int32_t>((size_t)(CHUNK / 128) * E);
     h->blk_base = c.take<int32_t>((size_t)(CHUNK / 128) * E);

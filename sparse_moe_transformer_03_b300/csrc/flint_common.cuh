@@ -37,6 +37,20 @@ struct DecodeTables {
     float pair_weight[DEC_PAIRS]; // routing weight of each pair (shared: 1)
 };
 
+// The decode activations a = silu(g) * u (bf16), written by the gate/up
+// kernels and read by the down kernels, in two column halves: half h holds
+// columns 256h .. 256h + 255 of every pair as [DEC_ACT_ROWS][256], so the
+// 8 pairs of one token tile are 4 KiB of contiguous bytes (one bulk copy).
+// Within a row the 16-byte chunk k sits at k ^ (pair % 8): the 8 rows of a
+// tile read the same column through different banks.  DEC_ACT_ROWS leaves 8
+// rows of slack after the last pair so a tile's copy stays inside its half.
+constexpr int DEC_ACT_ROWS = DEC_PAIRS + 8;
+constexpr size_t DEC_ACT_BYTES = (size_t)2 * DEC_ACT_ROWS * 256 * 2;
+__host__ __device__ __forceinline__ size_t act_index(int pair, int j) {
+    const int h = j >> 8, k = (j >> 3) & 31;
+    return ((size_t)h * DEC_ACT_ROWS + pair) * 256 + ((k ^ (pair & 7)) << 3) + (j & 7);
+}
+
 // ---------------------------------------------------------------------------
 // small helpers
 // ---------------------------------------------------------------------------
@@ -112,6 +126,12 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+// Raise the phase's expected transaction bytes without arriving.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
                  : "memory");
 }
 

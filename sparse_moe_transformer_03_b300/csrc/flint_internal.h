@@ -104,12 +104,12 @@ cudaError_t launch_repack_nvfp4(const uint8_t* packed, const uint8_t* scales, in
 cudaError_t decode_nvfp4_set_attributes();
 cudaError_t launch_decode_experts_nvfp4(const LaunchCtx& L, const uint8_t* nv, const float* nv_ts,
                                         const float* logits, const __nv_bfloat16* x, int T, DecodeTables* tables,
-                                        int32_t* idx, float* w, float* a_buf, __nv_bfloat16* y);
+                                        int32_t* idx, float* w, __nv_bfloat16* a_buf, __nv_bfloat16* y);
 
 // decode_mma.cu -- bf16 decode (T <= DEC_T) on mma.sync, from the tiled copy
 cudaError_t decode_mma_set_attributes();
 cudaError_t launch_decode_experts_mma(const LaunchCtx& L, const uint8_t* tiled, const float* logits,
                                       const __nv_bfloat16* x, int T, DecodeTables* tables, int32_t* idx, float* w,
-                                      float* a_buf, __nv_bfloat16* y);
+                                      __nv_bfloat16* a_buf, __nv_bfloat16* y);
 
 }  // namespace flint

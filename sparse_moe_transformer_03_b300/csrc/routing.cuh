@@ -1,6 +1,7 @@
 // routing.cuh -- device helpers shared by the router and the decode expert
-// kernels: warp-wide sigmoid top-6 with renormalisation, and the per-batch
-// (expert slot, token) tables of the decode path.
+// kernels: warp-wide sigmoid top-6 with renormalisation, the per-batch
+// (expert slot, token) tables of the decode path, and the decode kernels'
+// work-item lists.
 //
 // RecursiveSI/flint (vLLM recipe page), "Overview": top-6 sigmoid routing
 // over 256 experts plus an always-active shared expert.
@@ -136,6 +137,86 @@ __device__ __forceinline__ void build_decode_tables_warp(int T, const int* sel_e
         tab->pair_weight[q] = sel_w[p];
     }
     __syncwarp();
+}
+
+// ---------------------------------------------------------------------------
+// work items of the decode expert kernels
+// ---------------------------------------------------------------------------
+
+// Gate/up items: (slot u, unit r of the slot's DEC_UNITS, tile nt of 8 of
+// the slot's tokens), packed u << 8 | r << 2 | nt; in slot order, units in
+// order within a slot, tiles in order within a unit.  Item j of the grid
+// goes to CTA j % G.
+constexpr int DEC_UNITS = 64;              // 8 gate + 8 up rows per unit, I = 512
+constexpr int DEC_MAX_CTA_ITEMS = 256;     // per CTA; the grid has >= 72 CTAs
+static_assert(DEC_UNITS * 4 <= 256, "unit and tile fit in the low byte");
+
+// slot_item0[u] = first item of slot u, slot_item0[n_slots] = the total.
+// One warp.
+__device__ __forceinline__ void build_gateup_item_starts_warp(const DecodeTables* tab, int* slot_item0, int lane) {
+    int base = 0;
+    for (int u0 = 0; u0 < tab->n_slots; u0 += 32) {
+        const int u = u0 + lane;
+        const int n = u < tab->n_slots ? DEC_UNITS * ((tab->slot_pair0[u + 1] - tab->slot_pair0[u] + 7) >> 3) : 0;
+        int inc = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+            if (lane >= o) inc += v;
+        }
+        if (u < tab->n_slots) slot_item0[u] = base + inc - n;
+        base += __shfl_sync(0xFFFFFFFFu, inc, 31);
+    }
+    if (lane == 0) slot_item0[tab->n_slots] = base;
+}
+
+// CTA c's items c, c + G, ... into list[] (all threads of the CTA take part;
+// the caller synchronises before reading list).  Returns their count, or -1
+// when it exceeds DEC_MAX_CTA_ITEMS (the list is then left empty).
+__device__ __forceinline__ int list_gateup_items(const DecodeTables* tab, const int* slot_item0, int c, int G,
+                                                 int* list) {
+    const int n_slots = tab->n_slots, total = slot_item0[n_slots];
+    const int my_items = c < total ? (total - c + G - 1) / G : 0;
+    if (my_items > DEC_MAX_CTA_ITEMS) return -1;
+    for (int i = threadIdx.x; i < my_items; i += blockDim.x) {
+        const int j = c + G * i;
+        int lo = 0, hi = n_slots - 1;     // the last slot u with slot_item0[u] <= j
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (slot_item0[mid] <= j) lo = mid;
+            else hi = mid - 1;
+        }
+        const int l = j - slot_item0[lo];
+        const int ntu = (tab->slot_pair0[lo + 1] - tab->slot_pair0[lo] + 7) >> 3;
+        list[i] = (lo << 8) | ((l / ntu) << 2) | (l % ntu);
+    }
+    return my_items;
+}
+
+// Down items: (slot u, column half, tile nt of 8 tokens), packed u << 3 |
+// half << 2 | nt; in slot order, each slot's first half before its second
+// and the tiles in order within a half.  At most 2 x (slots + pairs / 8).
+constexpr int DEC_MAX_DOWN_ITEMS = 2 * (NEXP + DEC_PAIRS / 8);
+
+// Fills items[] and returns the count on every lane.  One warp.
+__device__ __forceinline__ int build_down_items_warp(const DecodeTables* tab, int* items, int lane) {
+    int base = 0;
+    for (int u0 = 0; u0 < tab->n_slots; u0 += 32) {
+        const int u = u0 + lane;
+        const int nt = u < tab->n_slots ? (tab->slot_pair0[u + 1] - tab->slot_pair0[u] + 7) >> 3 : 0;
+        int inc = nt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+            if (lane >= o) inc += v;
+        }
+        const int off = base + 2 * (inc - nt);
+        for (int hk = 0; hk < 2; ++hk)
+            for (int t = 0; t < nt; ++t) items[off + hk * nt + t] = (u << 3) | (hk << 2) | t;
+        base += 2 * __shfl_sync(0xFFFFFFFFu, inc, 31);
+    }
+    __syncwarp();
+    return base;
 }
 
 }  // namespace flint
