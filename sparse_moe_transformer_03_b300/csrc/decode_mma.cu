@@ -94,7 +94,7 @@ constexpr int MI_PART = 2 * MM_WARPS * 32 * 4;      // partial sums: [item parit
 
 static inline size_t mi_smem_bytes() {
     return (size_t)MM_WARPS * MI_NS * MM_CHUNK + (size_t)MI_PART * 4 + (size_t)MM_WARPS * MI_NS * 8 +
-           sizeof(DecodeTables) + DEC_T * TOPK * 8 + 2 * E * 4 + (NEXP + 1) * 4 + DEC_MAX_CTA_ITEMS * 4;
+           sizeof(DecodeTables) + DEC_T * TOPK * 8 + 2 * E * 4 + DEC_MAX_CTA_ITEMS * 4;
 }
 
 __global__ void __launch_bounds__(MM_WARPS * 32, 1) gateup_mma_kernel(GateUpMmaParams p) {
@@ -109,8 +109,7 @@ __global__ void __launch_bounds__(MM_WARPS * 32, 1) gateup_mma_kernel(GateUpMmaP
     float* sel_w = reinterpret_cast<float*>(sel_e + DEC_T * TOPK);
     uint32_t* tmask = reinterpret_cast<uint32_t*>(sel_w + DEC_T * TOPK);
     int* pair0 = reinterpret_cast<int*>(tmask + E);
-    int* slot_item0 = pair0 + E;                     // first item of each slot (+ the total)
-    int* list = slot_item0 + NEXP + 1;               // this CTA's items c, c + G, ...
+    int* list = pair0 + E;                           // this CTA's items c, c + G, ...
 
     if (lane == 0) {
         for (int s = 0; s < MI_NS; ++s) mbar_init(&bar[s], 1);
@@ -148,36 +147,17 @@ __global__ void __launch_bounds__(MM_WARPS * 32, 1) gateup_mma_kernel(GateUpMmaP
     pdl_trigger();
 
     // ---- top-6 of every token, then the (slot, token) tables ----
-    for (int t = warp; t < T; t += MM_WARPS) {
-        float v[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) v[k] = __ldcg(p.logits + (size_t)t * E + lane + 32 * k);
-        int sel[TOPK];
-        float wt[TOPK];
-        warp_top6(v, lane, sel, wt);
-        if (lane < TOPK) {
-            const int se = pick6(sel, lane);
-            const float sw = pick6(wt, lane);
-            sel_e[t * TOPK + lane] = se;
-            sel_w[t * TOPK + lane] = sw;
-            if (c == 0) {
-                p.idx_out[t * TOPK + lane] = se;
-                p.w_out[t * TOPK + lane] = sw;
-            }
-        }
-    }
+    select_tokens_warps(p.logits, T, warp, lane, sel_e, sel_w, c == 0 ? p.idx_out : nullptr,
+                        c == 0 ? p.w_out : nullptr);
     __syncthreads();
-    if (warp == 0) {
-        build_decode_tables_warp(T, sel_e, sel_w, tmask, pair0, tab, lane);
-        build_gateup_item_starts_warp(tab, slot_item0, lane);
-    }
+    if (warp == 0) build_decode_tables_warp(T, sel_e, sel_w, tmask, pair0, tab, lane);
     __syncthreads();
     if (c == 0) {
         const int* src = reinterpret_cast<const int*>(tab);
         int* dst = reinterpret_cast<int*>(p.tables_out);
         for (int k = threadIdx.x; k < (int)(sizeof(DecodeTables) / 4); k += blockDim.x) dst[k] = src[k];
     }
-    int my_items = list_gateup_items(tab, slot_item0, c, G, list);
+    int my_items = list_gateup_items(tab, c, G, list);
     if (my_items < 0) {   // the launcher sizes the grid so that this cannot happen
         if (threadIdx.x == 0) report_status(p.status, ST_BADINDEX);
         my_items = 0;
@@ -350,18 +330,7 @@ __global__ void __launch_bounds__(MM_WARPS * 32, 1) down_mma_kernel(DownMmaParam
     // wait, and this launch is triggered only after those waits: the logits
     // are final here.  Route for ourselves and start the weight chunks while
     // the gate/up kernel still runs.
-    for (int t = warp; t < Tk; t += MM_WARPS) {
-        float v[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) v[k] = __ldcg(p.logits + (size_t)t * E + lane + 32 * k);
-        int sel[TOPK];
-        float wt[TOPK];
-        warp_top6(v, lane, sel, wt);
-        if (lane < TOPK) {
-            sel_e[t * TOPK + lane] = pick6(sel, lane);
-            sel_w[t * TOPK + lane] = pick6(wt, lane);
-        }
-    }
+    select_tokens_warps(p.logits, Tk, warp, lane, sel_e, sel_w, nullptr, nullptr);
     for (int k = threadIdx.x; k < MM_WARPS * Tk * 16; k += blockDim.x) yw_all[k] = 0.f;
     __syncthreads();
     if (warp == 0) {

@@ -152,7 +152,7 @@ struct GateUpNvParams {
 
 static inline size_t gn_fixed_bytes(int T) {
     return (size_t)T * GN_XROW * 2 + DEC_T * 4 + (size_t)GN_PART * 4 + sizeof(DecodeTables) + DEC_T * TOPK * 8 +
-           2 * E * 4 + (NEXP + 1) * 4 + DEC_MAX_CTA_ITEMS * 4;
+           2 * E * 4 + DEC_MAX_CTA_ITEMS * 4 + 8;
 }
 // ring pieces per warp: what the shared memory left beside x holds, at most 8
 // (4 for one or two tokens, whose CTAs have about three items each)
@@ -178,16 +178,17 @@ __global__ void __launch_bounds__(GN_WARPS * 32, 1) gateup_nvfp4_kernel(GateUpNv
     float* xinv = reinterpret_cast<float*>(xh + (size_t)T * GN_XROW);
     float* part = xinv + DEC_T;
     uint64_t* bar = reinterpret_cast<uint64_t*>(part + GN_PART) + warp * NS;
-    DecodeTables* tab = reinterpret_cast<DecodeTables*>(reinterpret_cast<uint64_t*>(part + GN_PART) + GN_WARPS * NS);
+    uint64_t* xbar = reinterpret_cast<uint64_t*>(part + GN_PART) + GN_WARPS * NS;   // the raw x rows
+    DecodeTables* tab = reinterpret_cast<DecodeTables*>(xbar + 1);
     int* sel_e = reinterpret_cast<int*>(tab + 1);
     float* sel_w = reinterpret_cast<float*>(sel_e + DEC_T * TOPK);
     uint32_t* tmask = reinterpret_cast<uint32_t*>(sel_w + DEC_T * TOPK);
     int* pair0 = reinterpret_cast<int*>(tmask + E);
-    int* slot_item0 = pair0 + E;
-    int* list = slot_item0 + NEXP + 1;
+    int* list = pair0 + E;                           // this CTA's items c, c + G, ...
 
     if (lane == 0) {
         for (int s = 0; s < NS; ++s) mbar_init(&bar[s], 1);
+        if (warp == 0) mbar_init(xbar, 1);
         fence_mbar_init();
     }
     __syncthreads();
@@ -216,70 +217,64 @@ __global__ void __launch_bounds__(GN_WARPS * 32, 1) gateup_nvfp4_kernel(GateUpNv
     pdl_wait();     // router logits are complete (and x is ready)
     pdl_trigger();
 
-    // ---- x -> f16 times 2^e_t per token ----
-    for (int t = warp; t < T; t += GN_WARPS) {
-        uint4 v[8];
-        float mx = 0.f;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            v[k] = ldg16(p.x + (size_t)t * H + 8 * (lane + 32 * k));
-            mx = fmaxf(mx, fmaxf(fmaxf(fabsf(bf_lo(v[k].x)), fabsf(bf_hi(v[k].x))),
-                                 fmaxf(fabsf(bf_lo(v[k].y)), fabsf(bf_hi(v[k].y)))));
-            mx = fmaxf(mx, fmaxf(fmaxf(fabsf(bf_lo(v[k].z)), fabsf(bf_hi(v[k].z))),
-                                 fmaxf(fabsf(bf_lo(v[k].w)), fabsf(bf_hi(v[k].w)))));
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-        int e = mx > 0.f ? 14 - ilogbf(mx) : 0;
-        e = e > 126 ? 126 : e;
-        const float sc = ldexpf(1.f, e);
-        if (lane == 0) xinv[t] = ldexpf(1.f, -e);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const __half2 h0 = __floats2half2_rn(bf_lo(v[k].x) * sc, bf_hi(v[k].x) * sc);
-            const __half2 h1 = __floats2half2_rn(bf_lo(v[k].y) * sc, bf_hi(v[k].y) * sc);
-            const __half2 h2 = __floats2half2_rn(bf_lo(v[k].z) * sc, bf_hi(v[k].z) * sc);
-            const __half2 h3 = __floats2half2_rn(bf_lo(v[k].w) * sc, bf_hi(v[k].w) * sc);
-            uint4 o;
-            o.x = *reinterpret_cast<const uint32_t*>(&h0);
-            o.y = *reinterpret_cast<const uint32_t*>(&h1);
-            o.z = *reinterpret_cast<const uint32_t*>(&h2);
-            o.w = *reinterpret_cast<const uint32_t*>(&h3);
-            *reinterpret_cast<uint4*>(xh + (size_t)t * GN_XROW + 8 * (lane + 32 * k)) = o;
-        }
+    // ---- the raw bf16 x rows into their padded smem rows (lane t of warp 0
+    // copies token t; T <= 32), landing while the CTA ranks the experts ----
+    if (warp == 0) {
+        if (lane == 0) mbar_arrive_expect_tx(xbar, (uint32_t)T * H * 2);
+        __syncwarp();
+        if (lane < T) bulk_g2s(xh + (size_t)lane * GN_XROW, p.x + (size_t)lane * H, H * 2, xbar);
     }
 
     // ---- top-6 of every token, then the (slot, token) tables and the items ----
-    for (int t = warp; t < T; t += GN_WARPS) {
-        float v[8];
+    select_tokens_warps(p.logits, T, warp, lane, sel_e, sel_w, c == 0 ? p.idx_out : nullptr,
+                        c == 0 ? p.w_out : nullptr);
+    __syncthreads();
+    bool xok = true;
+    if (warp == 0) {
+        build_decode_tables_warp(T, sel_e, sel_w, tmask, pair0, tab, lane);
+    } else {
+        // meanwhile: x -> f16 times 2^e_t per token, in place
+        xok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(xbar, 0, p.limit_ns));
+        for (int t = warp - 1; xok && t < T; t += GN_WARPS - 1) {
+            uint4* row = reinterpret_cast<uint4*>(xh + (size_t)t * GN_XROW);
+            uint4 v[8];
+            float mx = 0.f;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) v[k] = __ldcg(p.logits + (size_t)t * E + lane + 32 * k);
-        int sel[TOPK];
-        float wt[TOPK];
-        warp_top6(v, lane, sel, wt);
-        if (lane < TOPK) {
-            const int se = pick6(sel, lane);
-            const float sw = pick6(wt, lane);
-            sel_e[t * TOPK + lane] = se;
-            sel_w[t * TOPK + lane] = sw;
-            if (c == 0) {
-                p.idx_out[t * TOPK + lane] = se;
-                p.w_out[t * TOPK + lane] = sw;
+            for (int k = 0; k < 8; ++k) {
+                v[k] = row[lane + 32 * k];
+                mx = fmaxf(mx, fmaxf(fmaxf(fabsf(bf_lo(v[k].x)), fabsf(bf_hi(v[k].x))),
+                                     fmaxf(fabsf(bf_lo(v[k].y)), fabsf(bf_hi(v[k].y)))));
+                mx = fmaxf(mx, fmaxf(fmaxf(fabsf(bf_lo(v[k].z)), fabsf(bf_hi(v[k].z))),
+                                     fmaxf(fabsf(bf_lo(v[k].w)), fabsf(bf_hi(v[k].w)))));
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+            int e = mx > 0.f ? 14 - ilogbf(mx) : 0;
+            e = e > 126 ? 126 : e;
+            const float sc = ldexpf(1.f, e);
+            if (lane == 0) xinv[t] = ldexpf(1.f, -e);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const __half2 h0 = __floats2half2_rn(bf_lo(v[k].x) * sc, bf_hi(v[k].x) * sc);
+                const __half2 h1 = __floats2half2_rn(bf_lo(v[k].y) * sc, bf_hi(v[k].y) * sc);
+                const __half2 h2 = __floats2half2_rn(bf_lo(v[k].z) * sc, bf_hi(v[k].z) * sc);
+                const __half2 h3 = __floats2half2_rn(bf_lo(v[k].w) * sc, bf_hi(v[k].w) * sc);
+                uint4 o;
+                o.x = *reinterpret_cast<const uint32_t*>(&h0);
+                o.y = *reinterpret_cast<const uint32_t*>(&h1);
+                o.z = *reinterpret_cast<const uint32_t*>(&h2);
+                o.w = *reinterpret_cast<const uint32_t*>(&h3);
+                row[lane + 32 * k] = o;
             }
         }
     }
-    __syncthreads();
-    if (warp == 0) {
-        build_decode_tables_warp(T, sel_e, sel_w, tmask, pair0, tab, lane);
-        build_gateup_item_starts_warp(tab, slot_item0, lane);
-    }
-    __syncthreads();
+    bool ok = __syncthreads_and(xok);
     if (c == 0) {
         const int* src = reinterpret_cast<const int*>(tab);
         int* dst = reinterpret_cast<int*>(p.tables_out);
         for (int k = threadIdx.x; k < (int)(sizeof(DecodeTables) / 4); k += blockDim.x) dst[k] = src[k];
     }
-    int my_items = list_gateup_items(tab, slot_item0, c, G, list);
+    int my_items = list_gateup_items(tab, c, G, list);
     if (my_items < 0) {   // the launcher sizes the grid so that this cannot happen
         if (threadIdx.x == 0) report_status(p.status, ST_BADINDEX);
         my_items = 0;
@@ -293,9 +288,8 @@ __global__ void __launch_bounds__(GN_WARPS * 32, 1) gateup_nvfp4_kernel(GateUpNv
     }
 
     const int g = lane >> 2, cq = lane & 3;
-    bool ok = true;
     int i = 0;
-    for (; i < my_items; ++i) {
+    for (; ok && i < my_items; ++i) {
         const int it = list[i], u = it >> 8;
         const int pb = tab->slot_pair0[u], np = tab->slot_pair0[u + 1] - pb;
         const int n = (it & 3) * 8 + g;
@@ -370,6 +364,7 @@ __global__ void __launch_bounds__(GN_WARPS * 32, 1) gateup_nvfp4_kernel(GateUpNv
             report_status(p.status, ST_TIMEOUT);
             // drain copies still in flight into this warp's ring (bounded)
             for (int k = i; k < issued; ++k) mbar_wait_bounded(&bar[k % NS], (k / NS) & 1, p.limit_ns);
+            if (warp == 0) mbar_wait_bounded(xbar, 0, p.limit_ns);
         }
         __syncwarp();
     }
@@ -458,18 +453,7 @@ __global__ void __launch_bounds__(DV_WARPS * 32, 1) down_nvfp4_kernel(DownNvPara
     // each token's experts and build the same tables the gate/up kernel
     // builds, and start the weight pieces of this warp's first items now, so
     // they stream while the gate/up kernel runs.
-    for (int t = warp; t < Tk; t += DV_WARPS) {
-        float v[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) v[k] = __ldcg(p.logits + (size_t)t * E + lane + 32 * k);
-        int sel[TOPK];
-        float wt[TOPK];
-        warp_top6(v, lane, sel, wt);
-        if (lane < TOPK) {
-            sel_e[t * TOPK + lane] = pick6(sel, lane);
-            sel_w[t * TOPK + lane] = pick6(wt, lane);
-        }
-    }
+    select_tokens_warps(p.logits, Tk, warp, lane, sel_e, sel_w, nullptr, nullptr);
     for (int k = threadIdx.x; k < DV_WARPS * Tk * 16; k += blockDim.x) yw_all[k] = 0.f;
     __syncthreads();
     if (warp == 0) {

@@ -33,6 +33,7 @@ struct DecodeTables {
     int pad_;
     int slot_expert[NEXP];        // expert id of each slot (256 = shared)
     int slot_pair0[NEXP + 1];     // first pair of each slot
+    int slot_tile0[NEXP + 1];     // first 8-token tile of each slot (tiles = ceil(pairs / 8))
     int pair_token[DEC_PAIRS];    // token of each pair
     float pair_weight[DEC_PAIRS]; // routing weight of each pair (shared: 1)
 };

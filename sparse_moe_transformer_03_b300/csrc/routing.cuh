@@ -73,10 +73,44 @@ __device__ __forceinline__ T pick6(const T (&a)[TOPK], int i) {
     return r;
 }
 
+// Top-6 of tokens warp, warp + 8, ..., warp + 24 (T <= 32, eight warps):
+// every one of the warp's tokens has its logits requested before the first
+// selection.  idx_out / w_out (global, or null) receive the choices too.
+__device__ __forceinline__ void select_tokens_warps(const float* logits, int T, int warp, int lane, int* sel_e,
+                                                    float* sel_w, int32_t* idx_out, float* w_out) {
+    float v[4][8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int t = warp + 8 * q;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[q][k] = t < T ? __ldcg(logits + (size_t)t * E + lane + 32 * k) : 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int t = warp + 8 * q;
+        if (t < T) {
+            int sel[TOPK];
+            float wt[TOPK];
+            warp_top6(v[q], lane, sel, wt);
+            if (lane < TOPK) {
+                const int se = pick6(sel, lane);
+                const float sw = pick6(wt, lane);
+                sel_e[t * TOPK + lane] = se;
+                sel_w[t * TOPK + lane] = sw;
+                if (idx_out) {
+                    idx_out[t * TOPK + lane] = se;
+                    w_out[t * TOPK + lane] = sw;
+                }
+            }
+        }
+    }
+}
+
 // Build the decode tables from sel_e/sel_w (token-major, T <= 32), by the
 // calling warp alone.  tmask[e] collects the tokens choosing expert e as a
 // bitmask, so a token's position in its expert's list (its popcount rank)
-// and the slot order (increasing expert id) are the same in every CTA.
+// and the slot order (increasing expert id) are the same in every CTA.  One
+// warp scan gives each slot its first pair and its first 8-token tile.
 // tmask and pair0 are E-entry scratch arrays.
 __device__ __forceinline__ void build_decode_tables_warp(int T, const int* sel_e, const float* sel_w,
                                                          uint32_t* tmask, int* pair0, DecodeTables* tab,
@@ -87,25 +121,29 @@ __device__ __forceinline__ void build_decode_tables_warp(int T, const int* sel_e
     for (int p = lane; p < T * TOPK; p += 32) atomicOr(&tmask[sel_e[p]], 1u << (p / TOPK));
     __syncwarp();
     uint32_t m[8];
-    int pres = 0, sum = 0;
+    int pres = 0, sum = 0, tiles = 0;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
         m[k] = tmask[lane * 8 + k];
         pres += m[k] != 0u;
         sum += __popc(m[k]);
+        tiles += (__popc(m[k]) + 7) >> 3;
     }
-    int ip = pres, is = sum;
+    int ip = pres, is = sum, it = tiles;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const int a = __shfl_up_sync(0xFFFFFFFFu, ip, o);
         const int b = __shfl_up_sync(0xFFFFFFFFu, is, o);
+        const int c = __shfl_up_sync(0xFFFFFFFFu, it, o);
         if (lane >= o) {
             ip += a;
             is += b;
+            it += c;
         }
     }
-    int slot = 1 + ip - pres;   // slot 0 is the shared expert
-    int pr = T + is - sum;      // pairs 0..T-1 are the shared expert's
+    int slot = 1 + ip - pres;               // slot 0 is the shared expert
+    int pr = T + is - sum;                  // pairs 0..T-1 are the shared expert's
+    int tile = ((T + 7) >> 3) + it - tiles; // and its ceil(T / 8) tiles come first
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
         const int e = lane * 8 + k;
@@ -113,17 +151,21 @@ __device__ __forceinline__ void build_decode_tables_warp(int T, const int* sel_e
         if (m[k]) {
             tab->slot_expert[slot] = e;
             tab->slot_pair0[slot] = pr;
+            tab->slot_tile0[slot] = tile;
             ++slot;
             pr += __popc(m[k]);
+            tile += (__popc(m[k]) + 7) >> 3;
         }
     }
     if (lane == 31) {
         tab->n_slots = slot;
         tab->n_pairs = pr;
         tab->slot_pair0[slot] = pr;
+        tab->slot_tile0[slot] = tile;
         tab->T = T;
         tab->slot_expert[0] = SHARED;
         tab->slot_pair0[0] = 0;
+        tab->slot_tile0[0] = 0;
     }
     for (int t = lane; t < T; t += 32) {
         tab->pair_token[t] = t;
@@ -145,49 +187,29 @@ __device__ __forceinline__ void build_decode_tables_warp(int T, const int* sel_e
 
 // Gate/up items: (slot u, unit r of the slot's DEC_UNITS, tile nt of 8 of
 // the slot's tokens), packed u << 8 | r << 2 | nt; in slot order, units in
-// order within a slot, tiles in order within a unit.  Item j of the grid
-// goes to CTA j % G.
+// order within a slot, tiles in order within a unit: slot u's items start at
+// DEC_UNITS x slot_tile0[u].  Item j of the grid goes to CTA j % G.
 constexpr int DEC_UNITS = 64;              // 8 gate + 8 up rows per unit, I = 512
 constexpr int DEC_MAX_CTA_ITEMS = 256;     // per CTA; the grid has >= 72 CTAs
 static_assert(DEC_UNITS * 4 <= 256, "unit and tile fit in the low byte");
 
-// slot_item0[u] = first item of slot u, slot_item0[n_slots] = the total.
-// One warp.
-__device__ __forceinline__ void build_gateup_item_starts_warp(const DecodeTables* tab, int* slot_item0, int lane) {
-    int base = 0;
-    for (int u0 = 0; u0 < tab->n_slots; u0 += 32) {
-        const int u = u0 + lane;
-        const int n = u < tab->n_slots ? DEC_UNITS * ((tab->slot_pair0[u + 1] - tab->slot_pair0[u] + 7) >> 3) : 0;
-        int inc = n;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(0xFFFFFFFFu, inc, o);
-            if (lane >= o) inc += v;
-        }
-        if (u < tab->n_slots) slot_item0[u] = base + inc - n;
-        base += __shfl_sync(0xFFFFFFFFu, inc, 31);
-    }
-    if (lane == 0) slot_item0[tab->n_slots] = base;
-}
-
 // CTA c's items c, c + G, ... into list[] (all threads of the CTA take part;
 // the caller synchronises before reading list).  Returns their count, or -1
 // when it exceeds DEC_MAX_CTA_ITEMS (the list is then left empty).
-__device__ __forceinline__ int list_gateup_items(const DecodeTables* tab, const int* slot_item0, int c, int G,
-                                                 int* list) {
-    const int n_slots = tab->n_slots, total = slot_item0[n_slots];
+__device__ __forceinline__ int list_gateup_items(const DecodeTables* tab, int c, int G, int* list) {
+    const int n_slots = tab->n_slots, total = DEC_UNITS * tab->slot_tile0[n_slots];
     const int my_items = c < total ? (total - c + G - 1) / G : 0;
     if (my_items > DEC_MAX_CTA_ITEMS) return -1;
     for (int i = threadIdx.x; i < my_items; i += blockDim.x) {
         const int j = c + G * i;
-        int lo = 0, hi = n_slots - 1;     // the last slot u with slot_item0[u] <= j
+        int lo = 0, hi = n_slots - 1;     // the last slot u with DEC_UNITS * slot_tile0[u] <= j
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if (slot_item0[mid] <= j) lo = mid;
+            if (DEC_UNITS * tab->slot_tile0[mid] <= j) lo = mid;
             else hi = mid - 1;
         }
-        const int l = j - slot_item0[lo];
-        const int ntu = (tab->slot_pair0[lo + 1] - tab->slot_pair0[lo] + 7) >> 3;
+        const int l = j - DEC_UNITS * tab->slot_tile0[lo];
+        const int ntu = tab->slot_tile0[lo + 1] - tab->slot_tile0[lo];
         list[i] = (lo << 8) | ((l / ntu) << 2) | (l % ntu);
     }
     return my_items;
@@ -195,28 +217,20 @@ __device__ __forceinline__ int list_gateup_items(const DecodeTables* tab, const 
 
 // Down items: (slot u, column half, tile nt of 8 tokens), packed u << 3 |
 // half << 2 | nt; in slot order, each slot's first half before its second
-// and the tiles in order within a half.  At most 2 x (slots + pairs / 8).
+// and the tiles in order within a half: slot u's items start at 2 x
+// slot_tile0[u].  At most 2 x (slots + pairs / 8).
 constexpr int DEC_MAX_DOWN_ITEMS = 2 * (NEXP + DEC_PAIRS / 8);
 
-// Fills items[] and returns the count on every lane.  One warp.
+// Fills items[] from the tables and returns the count.  One warp.
 __device__ __forceinline__ int build_down_items_warp(const DecodeTables* tab, int* items, int lane) {
-    int base = 0;
-    for (int u0 = 0; u0 < tab->n_slots; u0 += 32) {
-        const int u = u0 + lane;
-        const int nt = u < tab->n_slots ? (tab->slot_pair0[u + 1] - tab->slot_pair0[u] + 7) >> 3 : 0;
-        int inc = nt;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(0xFFFFFFFFu, inc, o);
-            if (lane >= o) inc += v;
-        }
-        const int off = base + 2 * (inc - nt);
+    const int n_slots = tab->n_slots;
+    for (int u = lane; u < n_slots; u += 32) {
+        const int t0 = tab->slot_tile0[u], nt = tab->slot_tile0[u + 1] - t0;
         for (int hk = 0; hk < 2; ++hk)
-            for (int t = 0; t < nt; ++t) items[off + hk * nt + t] = (u << 3) | (hk << 2) | t;
-        base += 2 * __shfl_sync(0xFFFFFFFFu, inc, 31);
+            for (int t = 0; t < nt; ++t) items[2 * t0 + hk * nt + t] = (u << 3) | (hk << 2) | t;
     }
     __syncwarp();
-    return base;
+    return 2 * tab->slot_tile0[n_slots];
 }
 
 }  // namespace flint
