@@ -53,10 +53,10 @@ NV_DOWN_BYTES = 2048 * 512 // 2 + 2048 * 512 // 16 + 4                  # 589,82
 K_ROUTER, K_GATE_UP, K_DOWN, K_COMBINE = 0, 1, 2, 3
 # the source files each timed kernel is built from (for the ncu traffic record)
 KERNEL_SOURCES = {
-    "gateup_nvfp4_kernel": ["decode_nvfp4.cu", "routing.cuh", "flint_common.cuh"],
+    "gateup_nvfp4_kernel": ["decode_nvfp4.cu", "mma_sync.cuh", "routing.cuh", "flint_common.cuh"],
     "gateup_mma_kernel": ["decode_mma.cu", "mma_sync.cuh", "routing.cuh", "flint_common.cuh"],
     "down_mma_kernel": ["decode_mma.cu", "mma_sync.cuh", "routing.cuh", "flint_common.cuh"],
-    "down_nvfp4_kernel": ["decode_nvfp4.cu", "flint_common.cuh"],
+    "down_nvfp4_kernel": ["decode_nvfp4.cu", "mma_sync.cuh", "routing.cuh", "flint_common.cuh"],
     "prefill_gateup_kernel": ["prefill.cu", "tc_ptx.cuh", "flint_common.cuh"],
     "prefill_down_kernel": ["prefill.cu", "tc_ptx.cuh", "flint_common.cuh"],
 }
