@@ -1,19 +1,26 @@
 """Benchmark of the Flint MoE FFN layer on B300.
 
-Default workload: the decode stack -- 47 distinct BF16 MoE layers of the
-H=2048 / I=512 / 256+1-expert shape (about 73 GB of weights resident, far
+Headline workload: the decode stack -- 47 distinct BF16 MoE layers of the
+H=2048 / I=512 / 256+1-expert shape (about 76 GB of weights resident, far
 larger than L2), per-expert router bias ~ N(0, 0.5), T=1 token per layer
 step, the layers applied one after another to the same x.  One step is one
-pass over the 47 layers (47 flint_moe_forward calls, replayed as one CUDA
-graph).  Metric: MoE-layer tokens per second = 47 * T / step time, and us per
-layer; roofline: unique bytes of touched expert weights per layer / us per
-layer, against the measured HBM copy bandwidth.
+pass over the 47 layers (replayed as one CUDA graph).  Metric: MoE-layer
+tokens per second = 47 * T / step time, and us per layer; roofline: unique
+bytes of touched expert weights per layer / us per layer, against the
+measured HBM copy bandwidth (and, beside it, the 8 TB/s nominal peak).
+
+The default run (--workload all) then times, in the same process, the
+other configurations of the metric and reports each under "configs": the
+BF16 stack at T=8 and T=32 (clustered tokens), the T=8192 prefill on the
+stack's first layer (tensor-core roofline) and the NVFP4 (W4A16) stack at
+T=1, 8 and 32.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl flint|reference]
-                    [--workload decode1|decode8|decode32]
+                    [--workload all|decode1|decode8|decode32|prefill8192|
+                                nvfp4_decode1|nvfp4_decode8|nvfp4_decode32]
 
 --impl reference times the fp64 CPU oracle on the host cores (a bounded
-sample of the same workload per step).  With N > 1 each rank runs its own
+sample of the headline workload per step).  With N > 1 each rank runs its own
 replica of the stack (the layer does not shard; no collective on the data
 path); value is the sum over ranks.
 """
@@ -68,9 +75,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="flint", choices=["flint", "reference"])
-    ap.add_argument("--workload", default="decode1", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="all", choices=["all"] + sorted(WORKLOADS))
     ap.add_argument("--layers", type=int, default=N_LAYERS, help=argparse.SUPPRESS)
-    ap.add_argument("--tokens", type=int, default=0, help=argparse.SUPPRESS)
     return ap.parse_args()
 
 
@@ -362,9 +368,10 @@ def layer_oracle(lw, q=None):
     return LayerOracle(lw.router_bits(), lw.bias_host(), mats, mats(lw.E), lw.E)
 
 
-def cpu_baseline(wl, stack_layers, cores_hint=None):
+def cpu_baseline(wl, stack_layers, seconds=10.0):
     """The oracle, as it stands, on one decode step of a 2-layer sample
-    (stack_layers: bf16 layers, or (bf16 layer, NVFP4 encoding) pairs)."""
+    (stack_layers: bf16 layers, or (bf16 layer, NVFP4 encoding) pairs), for
+    about `seconds` of host time."""
     T = wl["T"]
     xb = x_bits_for(wl)
     n = 2
@@ -378,7 +385,7 @@ def cpu_baseline(wl, stack_layers, cores_hint=None):
         for o in orcs:
             o.forward(xb)
         reps += 1
-        if time.perf_counter() - t0 > 10.0 or reps >= 50:
+        if time.perf_counter() - t0 > seconds or reps >= 50:
             break
     dt = (time.perf_counter() - t0) / reps
     return {"value": n * T / dt, "unit": "layer-tokens/s", "cores": os.cpu_count() or 1, "kind": "oracle",
@@ -388,7 +395,7 @@ def cpu_baseline(wl, stack_layers, cores_hint=None):
 PREFILL_SAMPLE = 256   # tokens of the prefill input the oracle runs per step
 
 
-def cpu_baseline_prefill(wl, lw, xb):
+def cpu_baseline_prefill(wl, lw, xb, seconds=10.0):
     """The oracle, as it stands, on the first PREFILL_SAMPLE tokens of the prefill input."""
     from oracle.reference import LayerOracle
     orc = LayerOracle.from_bf16_layer(lw)
@@ -399,7 +406,7 @@ def cpu_baseline_prefill(wl, lw, xb):
     while True:
         orc.forward(xs)
         reps += 1
-        if time.perf_counter() - t0 > 10.0 or reps >= 20:
+        if time.perf_counter() - t0 > seconds or reps >= 20:
             break
     dt = (time.perf_counter() - t0) / reps
     return {"value": PREFILL_SAMPLE / dt, "unit": "tokens/s", "cores": os.cpu_count() or 1, "kind": "oracle",
@@ -407,45 +414,78 @@ def cpu_baseline_prefill(wl, lw, xb):
                       f"(touched experts copied to host, copy untimed), {reps} reps"}
 
 
-def run_flint(args, wl, ws, rank, local):
+def timed_ms(torch, stream, fn, n):
+    """Mean device time (ms) of n calls of fn, CUDA events on `stream`."""
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    ev[0].record(stream)
+    for _ in range(n):
+        fn()
+    ev[1].record(stream)
+    ev[1].synchronize()
+    return ev[0].elapsed_time(ev[1]) / n
+
+
+def hbm_roof(achieved_gbs, peak_gbs, pk_kind):
+    """An HBM roofline entry: the fraction of the measured copy bandwidth and,
+    beside it, the fraction of the 8 TB/s nominal HBM3e peak."""
+    return {"achieved": achieved_gbs, "peak": peak_gbs, "unit": "GB/s", "frac": achieved_gbs / peak_gbs,
+            "peak_kind": f"{pk_kind} HBM copy bandwidth (burst)",
+            "frac_vs_8tbs": achieved_gbs / NOMINAL_HBM_GBS}
+
+
+NOMINAL_HBM_GBS = 8000.0
+
+
+def build_bf16_stack(flint, device, L, keep=2):
+    """L distinct BF16 layers of the decode stack (seed 1, skewed router bias).
+    The handle copies the experts into its own tiled layout, so the generated
+    bf16 experts are dropped after create except for the first `keep` layers
+    (the oracle samples them); the routers stay (the handle borrows them)."""
+    import torch
+    layers, handles = [], []
+    for l in range(L):
+        lw = device.LayerWeights(1, l, True)
+        handles.append(flint.flint_moe_create(lw.router_W, lw.router_b, list(lw.gate_up[:256]), list(lw.down[:256]),
+                                              (lw.gate_up[256], lw.down[256])))
+        if l >= keep:
+            lw.gate_up = lw.down = None
+        layers.append(lw)
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return layers, handles
+
+
+def build_nvfp4_stack(flint, device, L, keep=2):
+    """The same stack with NVFP4-encoded experts; the handle repacks them into
+    memory it owns, so only the first `keep` layers' encodings (for the oracle)
+    and every layer's router are kept."""
+    import torch
+    layers, handles = [], []
+    for l in range(L):
+        lw = device.LayerWeights(1, l, True)
+        q = device.LayerNVFP4(lw)
+        gu, dn, sh = q.create_args()
+        handles.append(flint.flint_moe_create(lw.router_W, lw.router_b, gu, dn, sh, dtype=flint.FLINT_NVFP4))
+        lw.gate_up = lw.down = None
+        layers.append((lw, q) if l < keep else (lw, None))
+        del gu, dn, sh
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return layers, handles
+
+
+def bench_decode(args, wl, name, layers, handles, ws, rank, nv, cpu_seconds):
+    """One decode configuration on a built stack: the L forwards of a step
+    replayed as one CUDA graph (weights far larger than L2, so each step
+    reads them from HBM again), plus the per-kernel rooflines, e2e through the
+    C ABI and the oracle's CPU baseline."""
     import numpy as np
     import torch
     from sparse_moe_transformer_03_b300 import flint
-    from synth import device
 
-    flint.load_library()
-    device.build()
     T = wl["T"]
-    L = args.layers
+    L = len(handles)
     pk, pk_kind = peaks()
-
-    nv = bool(wl.get("nvfp4"))
-    t_gen = time.perf_counter()
-    layers, handles, routers = [], [], []
-    resident = 0
-    for l in range(L):
-        lw = device.LayerWeights(1, l, True)
-        if nv:
-            # encode the experts to NVFP4; the handle repacks them into memory it owns, so the
-            # bf16 experts and the encoding are dropped (kept for the two layers the oracle samples)
-            q = device.LayerNVFP4(lw)
-            gu, dn, sh = q.create_args()
-            handles.append(flint.flint_moe_create(lw.router_W, lw.router_b, gu, dn, sh, dtype=flint.FLINT_NVFP4))
-            routers.append((lw.router_W, lw.router_b))
-            if l < 2:
-                layers.append((lw, q))
-            else:
-                del q, gu, dn, sh
-                lw.gate_up = lw.down = None
-            resident += 257 * (NV_GATE_UP_BYTES + NV_DOWN_BYTES)
-        else:
-            layers.append(lw)
-            handles.append(flint.flint_moe_create(lw.router_W, lw.router_b, list(lw.gate_up[:256]),
-                                                  list(lw.down[:256]), (lw.gate_up[256], lw.down[256])))
-            resident += lw.gate_up.numel() * 2 + lw.down.numel() * 2
-        del lw
-    torch.cuda.synchronize()
-    t_gen = time.perf_counter() - t_gen
     xb = x_bits_for(wl)
     x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
     ys = [torch.empty_like(x) for _ in range(L)]
@@ -467,7 +507,6 @@ def run_flint(args, wl, ws, rank, local):
         for l in range(L):
             flint.flint_moe_forward(handles[l], x, T, ys[l], stream)
 
-    # capture the 47-layer step as one graph
     with torch.cuda.stream(stream):
         step_direct()
         step_direct()
@@ -476,15 +515,6 @@ def run_flint(args, wl, ws, rank, local):
     with torch.cuda.graph(graph, stream=stream):
         step_direct()
     stream.synchronize()
-
-    def timed(fn, n):
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-        ev[0].record(stream)
-        for _ in range(n):
-            fn()
-        ev[1].record(stream)
-        ev[1].synchronize()
-        return ev[0].elapsed_time(ev[1]) / n
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -495,13 +525,13 @@ def run_flint(args, wl, ws, rank, local):
     torch.cuda.synchronize()
     with ClockSampler(torch.cuda.current_device()) as clk:
         with torch.cuda.stream(stream):
-            ms = timed(graph.replay, args.steps)
+            ms = timed_ms(torch, stream, graph.replay, args.steps)
     torch.cuda.synchronize()
     clocks = clk.summary()
     with torch.cuda.stream(stream):
-        ms_direct = timed(step_direct, max(3, args.steps // 2))
+        ms_direct = timed_ms(torch, stream, step_direct, max(3, args.steps // 2))
 
-    # end to end through the C ABI: pinned host x -> device, 47 forwards, all y -> host
+    # end to end through the C ABI: pinned host x -> device, L forwards, every y -> host
     x_host = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).pin_memory()
     y_host = torch.empty((L, T, 2048), dtype=torch.bfloat16).pin_memory()
     x_dev = torch.empty_like(x)
@@ -515,85 +545,70 @@ def run_flint(args, wl, ws, rank, local):
 
     with torch.cuda.stream(stream):
         step_e2e()
-        ms_e2e = timed(step_e2e, max(3, args.steps // 2))
+        ms_e2e = timed_ms(torch, stream, step_e2e, max(3, args.steps // 2))
     stream.synchronize()
-
     ms, ms_e2e = max_over_ranks([ms, ms_e2e])
 
-    # the dominant kernel, timed on its own (events around its launch, every layer)
+    # each expert kernel timed on its own (events around its launch, every layer)
     calls = [(handles[l], x, T, ys[l]) for l in range(L)]
     ksteps = max(3, min(args.steps, 10))
     kern = {}
     kernels = ((("gateup_nvfp4_kernel", K_GATE_UP, NV_GATE_UP_BYTES), ("down_nvfp4_kernel", K_DOWN, NV_DOWN_BYTES))
                if nv else (("gateup_mma_kernel", K_GATE_UP, GATE_UP_BYTES), ("down_mma_kernel", K_DOWN, DOWN_BYTES)))
-    for name, kid, per_expert in kernels:
+    for kname, kid, per_exp in kernels:
         d = kernel_durations(flint, torch, stream, calls, kid, ksteps)
         tot_ms = sum(sum(r) for r in d)
-        tot_bytes = ksteps * sum((u + 1) * per_expert for u in uniq)
-        kern[name] = {"us_per_launch": tot_ms * 1e3 / (ksteps * L), "bytes_per_launch": tot_bytes / (ksteps * L),
-                      "gbs": tot_bytes / (tot_ms * 1e-3) / 1e9, "launches_timed": ksteps * L}
+        tot_bytes = ksteps * sum((u + 1) * per_exp for u in uniq)
+        kern[kname] = {"us_per_launch": tot_ms * 1e3 / (ksteps * L), "bytes_per_launch": tot_bytes / (ksteps * L),
+                       "gbs": tot_bytes / (tot_ms * 1e-3) / 1e9, "launches_timed": ksteps * L}
     dom = max(kern, key=lambda k: kern[k]["us_per_launch"])
 
     us_layer = ms * 1e3 / L
-    value = whole_job_rate(L * T, ws, ms)
     achieved = bytes_per_step / (ms * 1e-3) / 1e9
     peak_hbm = float(pk["hbm_gbs"])
+    roof = {"bound": "hbm", **hbm_roof(kern[dom]["gbs"], peak_hbm, pk_kind),
+            "traffic": traffic_from_profiles(dom, name),
+            "kernel": dom, "bytes_per_launch": kern[dom]["bytes_per_launch"],
+            "us_per_launch": kern[dom]["us_per_launch"],
+            "what": "algorithmic bytes per launch (unique touched experts incl. the shared one x the matrices "
+                    "this kernel reads) / its device duration (CUDA events around its launch in every layer of "
+                    f"{ksteps} extra direct steps)"}
     line = {
         "metric": f"MoE-layer tokens/s, {'NVFP4 ' if nv else ''}decode stack T={T}",
-        "value": value, "unit": "layer-tokens/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "nvfp4 weights (e2m1 + e4m3 block scales), bf16 activations, f32 accumulation" if nv else "bf16",
-        "data": "synthetic (seeded counter-based generator; random-init weights)",
+        "value": whole_job_rate(L * T, ws, ms), "unit": "layer-tokens/s", "ms_per_step": ms,
         "us_per_layer": us_layer, "us_per_layer_no_graph": ms_direct * 1e3 / L,
+        "dtype": "nvfp4 weights (e2m1 + e4m3 block scales), bf16 activations, f32 accumulation" if nv else "bf16",
         "config": {"workload": f"decode stack: {L} distinct {'NVFP4 (W4A16)' if nv else 'BF16'} MoE layers (H=2048, "
                                f"I=512, 256 routed + 1 shared, top-6 sigmoid, router bias N(0,0.5)), T={T} tokens "
                                f"({wl['x']} x, seed {wl['x_seed']})",
-                   "weights_resident_gb": round(resident / 1e9, 2),
+                   "weights_resident_gb": round(L * 257 * per_expert / 1e9, 2),
                    "l2": "inputs larger than L2 (each layer's weights are read once per step)",
                    "parallelism": f"replicas x{ws}", "graph": True},
         "unique_experts_per_layer": {"mean": float(np.mean(uniq)), "min": int(min(uniq)), "max": int(max(uniq))},
-        "roofline": {"bound": "hbm", "achieved": kern[dom]["gbs"], "peak": peak_hbm, "unit": "GB/s",
-                     "frac": kern[dom]["gbs"] / peak_hbm,
-                     "traffic": traffic_from_profiles(dom, args.workload),
-                     "kernel": dom, "bytes_per_launch": kern[dom]["bytes_per_launch"],
-                     "us_per_launch": kern[dom]["us_per_launch"],
-                     "what": "algorithmic bytes per launch (unique touched experts incl. the shared one x the "
-                             "matrices this kernel reads) / its device duration (CUDA events around its launch in "
-                             f"every layer of {ksteps} extra direct steps); peak = {pk_kind} HBM copy bandwidth "
-                             "(burst)"},
+        "roofline": roof,
         "kernels": kern,
-        "layer_hbm": {"achieved": achieved, "peak": peak_hbm, "unit": "GB/s", "frac": achieved / peak_hbm,
+        "layer_hbm": {**hbm_roof(achieved, peak_hbm, pk_kind),
                       "what": "unique touched expert-weight bytes per layer / us per layer in the timed graph "
                               "(router, gate/up and down kernels chained by programmatic launch)"},
         "gpu_launches": 3 * L * args.steps,
         "clocks": clocks,
         "e2e": {"value": whole_job_rate(L * T, ws, ms_e2e), "unit": "layer-tokens/s",
                 "h2d_bytes_per_step": T * 2048 * 2, "d2h_bytes_per_step": L * T * 2048 * 2},
-        "gen_seconds": round(t_gen, 2),
     }
-    if rank == 0 and ws == 1:
-        line["cpu_baseline"] = cpu_baseline(wl, layers)
-    for h in handles:
-        flint.flint_moe_destroy(h)
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+    if rank == 0 and ws == 1 and cpu_seconds > 0:
+        line["cpu_baseline"] = cpu_baseline(wl, layers[:2], cpu_seconds)
+    return line
 
 
-def run_prefill(args, wl, ws, rank, local):
+def bench_prefill(args, wl, lw, h, ws, rank, cpu_seconds):
     """One MoE layer (layer 0 of the stack: skewed router bias) on T = 8192
     tokens; weights (1.6 GB) exceed L2, so each step streams them again."""
     import numpy as np
     import torch
     from sparse_moe_transformer_03_b300 import flint
-    from synth import device
 
-    flint.load_library()
-    device.build()
     T = wl["T"]
     pk, pk_kind = peaks()
-    lw = device.LayerWeights(1, 0, True)
-    h = flint.flint_moe_create(lw.router_W, lw.router_b, list(lw.gate_up[:256]), list(lw.down[:256]),
-                               (lw.gate_up[256], lw.down[256]))
     xb = x_bits_for(wl)
     x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
     y = torch.empty_like(x)
@@ -601,15 +616,6 @@ def run_prefill(args, wl, ws, rank, local):
 
     def step():
         flint.flint_moe_forward(h, x, T, y, stream)
-
-    def timed(fn, n):
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-        ev[0].record(stream)
-        for _ in range(n):
-            fn()
-        ev[1].record(stream)
-        ev[1].synchronize()
-        return ev[0].elapsed_time(ev[1]) / n
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -620,7 +626,7 @@ def run_prefill(args, wl, ws, rank, local):
     torch.cuda.synchronize()
     with ClockSampler(torch.cuda.current_device()) as clk:
         with torch.cuda.stream(stream):
-            ms = timed(step, args.steps)
+            ms = timed_ms(torch, stream, step, args.steps)
     torch.cuda.synchronize()
     clocks = clk.summary()
 
@@ -635,7 +641,7 @@ def run_prefill(args, wl, ws, rank, local):
 
     with torch.cuda.stream(stream):
         step_e2e()
-        ms_e2e = timed(step_e2e, max(3, args.steps // 2))
+        ms_e2e = timed_ms(torch, stream, step_e2e, max(3, args.steps // 2))
     ms, ms_e2e = max_over_ranks([ms, ms_e2e])
     # the dominant kernels timed on their own (events around each launch)
     ksteps = max(3, min(args.steps, 10))
@@ -647,12 +653,12 @@ def run_prefill(args, wl, ws, rank, local):
     gu_bytes = 257 * GATE_UP_BYTES + T * 2048 * 2 + slots * 512 * 2
     dn_bytes = 257 * DOWN_BYTES + slots * 512 * 2 + slots * 2048 * 2
     kern = {}
-    for name, kid, fl, by in (("prefill_gateup_kernel", K_GATE_UP, gu_flops, gu_bytes),
-                              ("prefill_down_kernel", K_DOWN, dn_flops, dn_bytes)):
+    for kname, kid, fl, by in (("prefill_gateup_kernel", K_GATE_UP, gu_flops, gu_bytes),
+                               ("prefill_down_kernel", K_DOWN, dn_flops, dn_bytes)):
         d = kernel_durations(flint, torch, stream, calls, kid, ksteps)
         us = sum(r[0] for r in d) * 1e3 / ksteps
-        kern[name] = {"us_per_launch": us, "flops_per_launch": fl, "bytes_per_launch": by,
-                      "tflops": fl / (us * 1e-6) / 1e12, "gbs": by / (us * 1e-6) / 1e9, "launches_timed": ksteps}
+        kern[kname] = {"us_per_launch": us, "flops_per_launch": fl, "bytes_per_launch": by,
+                       "tflops": fl / (us * 1e-6) / 1e12, "gbs": by / (us * 1e-6) / 1e9, "launches_timed": ksteps}
     dom = max(kern, key=lambda k: kern[k]["us_per_launch"])
     peak_hbm = float(pk["hbm_gbs"])
     peak_tc = float(pk["bf16_tflops"])
@@ -660,11 +666,11 @@ def run_prefill(args, wl, ws, rank, local):
     # the binding resource of the kernel's own roofline: the larger of bytes / bandwidth and flops / peak
     hbm_bound = kd["bytes_per_launch"] / peak_hbm / 1e9 >= kd["flops_per_launch"] / peak_tc / 1e12
     if hbm_bound:
-        roof = {"bound": "hbm", "achieved": kd["gbs"], "peak": peak_hbm, "unit": "GB/s", "frac": kd["gbs"] / peak_hbm}
+        roof = {"bound": "hbm", **hbm_roof(kd["gbs"], peak_hbm, pk_kind)}
     else:
         roof = {"bound": "tensor", "achieved": kd["tflops"], "peak": peak_tc, "unit": "TFLOP/s",
                 "frac": kd["tflops"] / peak_tc}
-    roof.update({"traffic": traffic_from_profiles(dom, args.workload), "kernel": dom,
+    roof.update({"traffic": traffic_from_profiles(dom, "prefill8192"), "kernel": dom,
                  "us_per_launch": kd["us_per_launch"], "bytes_per_launch": kd["bytes_per_launch"],
                  "flops_per_launch": kd["flops_per_launch"], "tensor_frac": kd["tflops"] / peak_tc,
                  "what": f"algorithmic bytes and flops per launch / its device duration (CUDA events around its "
@@ -672,44 +678,105 @@ def run_prefill(args, wl, ws, rank, local):
                          "burst; bound = the larger of bytes/bandwidth and flops/peak"})
     flops = FLOPS_PER_TOKEN * T
     achieved = flops / (ms * 1e-3) / 1e12
-    peak = float(pk["bf16_tflops"])
     line = {
         "metric": f"MoE-layer tokens/s, prefill T={T}", "value": whole_job_rate(T, ws, ms), "unit": "tokens/s",
-        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "us_per_layer": ms * 1e3,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded counter-based generator; random-init weights)",
+        "ms_per_step": ms, "us_per_layer": ms * 1e3, "dtype": "bf16",
         "config": {"workload": f"prefill: one BF16 MoE layer (H=2048, I=512, 256 routed + 1 shared, top-6 sigmoid, "
                                f"router bias N(0,0.5)), T={T} tokens (x ~ N(0,1) RMS-normalised, seed {wl['x_seed']})",
                    "l2": "inputs larger than L2 (1.6 GB of expert weights per step)", "parallelism": f"replicas x{ws}"},
         "roofline": roof,
         "kernels": kern,
-        "layer_tensor": {"achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+        "layer_tensor": {"achieved": achieved, "peak": peak_tc, "unit": "TFLOP/s", "frac": achieved / peak_tc,
+                         "peak_kind": f"{pk_kind} dense bf16 (burst)",
                          "what": f"dense layer FLOPs (experts {7 * 6 * 2048 * 512 * T / 1e9:.1f} GFLOP + router "
-                                 f"{2 * 256 * 2048 * T / 1e9:.1f}) / step time; peak = {pk_kind} bf16 burst"},
+                                 f"{2 * 256 * 2048 * T / 1e9:.1f}) / step time"},
         "gpu_launches": 6 * args.steps,
         "clocks": clocks,
         "e2e": {"value": whole_job_rate(T, ws, ms_e2e), "unit": "tokens/s", "h2d_bytes_per_step": T * 2048 * 2,
                 "d2h_bytes_per_step": T * 2048 * 2},
     }
-    if rank == 0 and ws == 1:
-        line["cpu_baseline"] = cpu_baseline_prefill(wl, lw, xb)
-    flint.flint_moe_destroy(h)
+    if rank == 0 and ws == 1 and cpu_seconds > 0:
+        line["cpu_baseline"] = cpu_baseline_prefill(wl, lw, xb, cpu_seconds)
+    return line
+
+
+COMMON_KEYS = ("n_gpus", "steps", "warmup", "higher_is_better", "scaling", "vs_baseline", "data")
+
+
+def run_flint(args, ws, rank, local):
+    """The flint arm.  --workload all (the default): the BF16 decode stack at
+    T = 1 (the headline line), then T = 8 and 32, the T = 8192 prefill on the
+    stack's first layer and the NVFP4 stack at T = 1, 8 and 32, each as an
+    entry of the line's "configs"; otherwise the named workload alone."""
+    import torch
+    from sparse_moe_transformer_03_b300 import flint
+    from synth import device
+
+    flint.load_library()
+    device.build()
+    names = ALL_ORDER if args.workload == "all" else [args.workload]
+    L = args.layers
+    results = {}
+    t_gen = time.perf_counter()
+    bf16_names = [n for n in names if not WORKLOADS[n].get("nvfp4")]
+    nv_names = [n for n in names if WORKLOADS[n].get("nvfp4")]
+    gen_s = {}
+    if bf16_names:
+        layers, handles = build_bf16_stack(flint, device, L if any(not WORKLOADS[n].get("prefill") for n in bf16_names)
+                                           else 1)
+        gen_s["bf16"] = round(time.perf_counter() - t_gen, 2)
+        for n in bf16_names:
+            wl = WORKLOADS[n]
+            cpu_s = HEADLINE_CPU_SECONDS if n == names[0] else CONFIG_CPU_SECONDS
+            if wl.get("prefill"):
+                results[n] = bench_prefill(args, wl, layers[0], handles[0], ws, rank, cpu_s)
+            else:
+                results[n] = bench_decode(args, wl, n, layers, handles, ws, rank, False, cpu_s)
+        for h in handles:
+            flint.flint_moe_destroy(h)
+        del layers, handles
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    if nv_names:
+        t0 = time.perf_counter()
+        layers, handles = build_nvfp4_stack(flint, device, L)
+        gen_s["nvfp4"] = round(time.perf_counter() - t0, 2)
+        for n in nv_names:
+            cpu_s = HEADLINE_CPU_SECONDS if n == names[0] else CONFIG_CPU_SECONDS
+            results[n] = bench_decode(args, WORKLOADS[n], n, layers, handles, ws, rank, True, cpu_s)
+        for h in handles:
+            flint.flint_moe_destroy(h)
+        del layers, handles
+        torch.cuda.empty_cache()
+
+    head = dict(results[names[0]])
+    line = {"metric": head.pop("metric"), "value": head.pop("value"), "unit": head.pop("unit"),
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "data": "synthetic (seeded counter-based generator; random-init weights)"}
+    line.update(head)
+    line["gen_seconds"] = gen_s
+    if len(names) > 1:
+        line["configs"] = {n: results[n] for n in names[1:]}
+        line["gpu_launches"] = sum(r["gpu_launches"] for r in results.values())
+        line["gpu_launches_headline"] = results[names[0]]["gpu_launches"]
     if rank == 0:
         print(json.dumps(line), flush=True)
 
 
+ALL_ORDER = ["decode1", "decode8", "decode32", "prefill8192", "nvfp4_decode1", "nvfp4_decode8", "nvfp4_decode32"]
+HEADLINE_CPU_SECONDS = 10.0
+CONFIG_CPU_SECONDS = 4.0
+
+
 def main():
     args = parse()
-    wl = dict(WORKLOADS[args.workload])
-    if args.tokens:
-        wl["T"] = args.tokens
     ws, rank, local = dist_setup(args)
     if args.impl == "reference":
+        wl = dict(WORKLOADS["decode1" if args.workload == "all" else args.workload])
         run_reference(args, wl, ws, rank)
-    elif wl.get("prefill"):
-        run_prefill(args, wl, ws, rank, local)
     else:
-        run_flint(args, wl, ws, rank, local)
+        run_flint(args, ws, rank, local)
     if ws > 1:
         import torch.distributed as dist
         dist.barrier()

@@ -67,7 +67,10 @@ typedef enum {
     FLINT_ERR_OOM = 3,             /* device allocation failed in create              */
     FLINT_ERR_DEVICE_TIMEOUT = 4,  /* a bounded device wait ran out (kernel returned) */
     FLINT_ERR_DEVICE_BADINDEX = 5, /* a kernel saw an expert/token index out of range */
-    FLINT_ERR_UNSUPPORTED = 6      /* no sm_103a device, or an unsupported request    */
+    FLINT_ERR_UNSUPPORTED = 6,     /* no sm_103a device, or an unsupported request    */
+    FLINT_ERR_INTERNAL = 7         /* a kernel's internal capacity check failed: a
+                                      library defect, not a caller error (the grid
+                                      sizes are chosen so that it cannot happen) */
 } flint_status_t;
 
 /* One NVFP4 matrix [R][K] (RecursiveSI/flint vLLM recipe page, "Overview":
@@ -96,7 +99,10 @@ typedef struct {
  * Ownership: bf16 expert weights are read during create only: the handle
  * owns a copy of every expert matrix cut into 16 KiB tensor-core operand
  * tiles (1.6 GB per layer), which both the decode and the many-token path
- * read, and the caller may free its buffers on return.  The router (bf16,
+ * read, and the caller may free its buffers on return.  While create runs,
+ * the caller's bf16 experts and the handle's copy both exist, so the peak
+ * device footprint of a layer is twice its expert bytes (3.2 GB) until the
+ * caller frees its own buffers.  The router (bf16,
  * both dtypes) is borrowed: it stays alive and unchanged until destroy.  The
  * handle owns a workspace for FLINT_CHUNK tokens (about 310 MB).  NVFP4
  * weights are repacked into a layout the handle owns (1.77 MB per
@@ -181,9 +187,10 @@ FLINT_API const char* flint_status_string(flint_status_t st);
  * The scratch is one array per device shared by every call: calls that
  * overlap in time (two streams, two host threads) race on it and must be
  * serialised by the caller.  The first call on a device looks up the array's
- * address; make that first call before capturing s into a graph.
- * Synchronises s.  Errors: INVALID_ARG, CUDA, DEVICE_BADINDEX (an id in idx
- * outside 0..255; outputs are then unspecified). */
+ * address on that device (cudaGetSymbolAddress).  Every call ends by
+ * reading the scratch's status word back to the host and synchronising s.
+ * Errors: INVALID_ARG, CUDA, DEVICE_BADINDEX (an id in idx outside 0..255;
+ * outputs are then unspecified). */
 FLINT_API flint_status_t flint_permute_static(const int32_t* idx, int T, int32_t* offsets,
                                               int32_t* gather_idx, cudaStream_t s);
 

@@ -7,8 +7,8 @@
  * shares no code, header, table or constant with the CUDA sources: only the
  * seeded input generators (the `synth` module) feed both sides.
  *
- * What it computes (Flint vLLM recipe page, "Overview": "256 experts, top-6
- * sigmoid routing plus a shared expert"; the expert activation, hidden and
+ * What it computes (Flint vLLM recipe page, "Overview": 256 routed experts,
+ * the top 6 chosen by sigmoid score, and one shared expert; the expert activation, hidden and
  * intermediate sizes, the renormalisation of the routing weights and the
  * unweighted shared expert are not printed on the pages and follow the
  * readings written next to each function):

@@ -158,8 +158,8 @@ __global__ void __launch_bounds__(MM_WARPS * 32, 1) gateup_mma_kernel(GateUpMmaP
         for (int k = threadIdx.x; k < (int)(sizeof(DecodeTables) / 4); k += blockDim.x) dst[k] = src[k];
     }
     int my_items = list_gateup_items(tab, c, G, list);
-    if (my_items < 0) {   // the launcher sizes the grid so that this cannot happen
-        if (threadIdx.x == 0) report_status(p.status, ST_BADINDEX);
+    if (my_items < 0) {   // ruled out by the grid size (DEC_MIN_GRID); drained below
+        if (threadIdx.x == 0) report_status(p.status, ST_INTERNAL);
         my_items = 0;
     }
     __syncthreads();
@@ -251,13 +251,14 @@ __global__ void __launch_bounds__(MM_WARPS * 32, 1) gateup_mma_kernel(GateUpMmaP
             bq[kb][1] = bn[kb][1];
         }
     }
-    if (!ok) {
-        if (lane == 0) {
-            report_status(p.status, ST_TIMEOUT);
-            for (int k = i; k < issued; ++k) mbar_wait_bounded(&bar[k % MI_NS], (k / MI_NS) & 1, p.limit_ns);
-        }
-        __syncwarp();
+    if (lane == 0) {
+        if (!ok) report_status(p.status, ST_TIMEOUT);
+        // copies still in flight into this warp's ring (after a timeout, or the
+        // shared slot's prefetched items when the item list came out empty):
+        // wait for them, bounded, before the CTA exits
+        for (int k = i; k < issued; ++k) mbar_wait_bounded(&bar[k % MI_NS], (k / MI_NS) & 1, p.limit_ns);
     }
+    __syncwarp();
 }
 
 // ---------------------------------------------------------------------------
@@ -443,7 +444,7 @@ cudaError_t launch_decode_experts_mma(const LaunchCtx& L, const uint8_t* tiled, 
     GateUpMmaParams gp{tiled, logits, x, T, tables, idx, w, a16, L.status, L.wait_limit_ns};
     // at most 64 x (257 + 28) items over the grid: 72 CTAs or more keep every
     // CTA's list within its 256 entries
-    const int gi = L.num_sms >= 72 ? L.num_sms : 72;
+    const int gi = L.num_sms >= DEC_MIN_GRID ? L.num_sms : DEC_MIN_GRID;
     cudaError_t e = launch_hooked(L, FLINT_KERNEL_GATE_UP, gateup_mma_kernel, dim3(gi), dim3(MM_WARPS * 32),
                                   mi_smem_bytes(), gp);
     if (e != cudaSuccess) return e;

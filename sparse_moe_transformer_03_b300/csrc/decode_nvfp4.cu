@@ -275,8 +275,8 @@ __global__ void __launch_bounds__(GN_WARPS * 32, 1) gateup_nvfp4_kernel(GateUpNv
         for (int k = threadIdx.x; k < (int)(sizeof(DecodeTables) / 4); k += blockDim.x) dst[k] = src[k];
     }
     int my_items = list_gateup_items(tab, c, G, list);
-    if (my_items < 0) {   // the launcher sizes the grid so that this cannot happen
-        if (threadIdx.x == 0) report_status(p.status, ST_BADINDEX);
+    if (my_items < 0) {   // ruled out by the grid size (DEC_MIN_GRID); drained below
+        if (threadIdx.x == 0) report_status(p.status, ST_INTERNAL);
         my_items = 0;
     }
     __syncthreads();
@@ -359,15 +359,17 @@ __global__ void __launch_bounds__(GN_WARPS * 32, 1) gateup_nvfp4_kernel(GateUpNv
             }
         }
     }
-    if (!ok) {
-        if (lane == 0) {
+    if (lane == 0) {
+        if (!ok) {
             report_status(p.status, ST_TIMEOUT);
-            // drain copies still in flight into this warp's ring (bounded)
-            for (int k = i; k < issued; ++k) mbar_wait_bounded(&bar[k % NS], (k / NS) & 1, p.limit_ns);
             if (warp == 0) mbar_wait_bounded(xbar, 0, p.limit_ns);
         }
-        __syncwarp();
+        // copies still in flight into this warp's ring (after a timeout, or the
+        // shared slot's prefetched pieces when the item list came out empty):
+        // wait for them, bounded, before the CTA exits
+        for (int k = i; k < issued; ++k) mbar_wait_bounded(&bar[k % NS], (k / NS) & 1, p.limit_ns);
     }
+    __syncwarp();
 }
 
 // ---------------------------------------------------------------------------
@@ -568,7 +570,7 @@ cudaError_t launch_decode_experts_nvfp4(const LaunchCtx& L, const uint8_t* nv, c
     GateUpNvParams gp{nv, nv_ts, logits, x, T, gn_ns(T), tables, idx, w, a16, L.status, L.wait_limit_ns};
     // at most 64 x (257 + 28) items over the grid: 72 CTAs or more keep every
     // CTA's list within DEC_MAX_CTA_ITEMS
-    const int gi = L.num_sms >= 72 ? L.num_sms : 72;
+    const int gi = L.num_sms >= DEC_MIN_GRID ? L.num_sms : DEC_MIN_GRID;
     cudaError_t e = launch_hooked(L, FLINT_KERNEL_GATE_UP, gateup_nvfp4_kernel, dim3(gi), dim3(GN_WARPS * 32),
                                   gn_smem_bytes(T), gp);
     if (e != cudaSuccess) return e;

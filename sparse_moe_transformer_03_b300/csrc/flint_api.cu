@@ -67,6 +67,7 @@ flint_status_t take_device_status(flint_moe* h) {
     *s = 0;
     if (v == ST_TIMEOUT) return FLINT_ERR_DEVICE_TIMEOUT;
     if (v == ST_BADINDEX) return FLINT_ERR_DEVICE_BADINDEX;
+    if (v == ST_INTERNAL) return FLINT_ERR_INTERNAL;
     return FLINT_ERR_CUDA;
 }
 
@@ -137,6 +138,7 @@ const char* flint_status_string(flint_status_t st) {
         case FLINT_ERR_DEVICE_TIMEOUT: return "FLINT_ERR_DEVICE_TIMEOUT";
         case FLINT_ERR_DEVICE_BADINDEX: return "FLINT_ERR_DEVICE_BADINDEX";
         case FLINT_ERR_UNSUPPORTED: return "FLINT_ERR_UNSUPPORTED";
+        case FLINT_ERR_INTERNAL: return "FLINT_ERR_INTERNAL";
     }
     return "FLINT_ERR_UNKNOWN";
 }

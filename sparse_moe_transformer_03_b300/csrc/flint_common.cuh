@@ -21,6 +21,7 @@ constexpr int DEC_PAIRS = DEC_T * (TOPK + 1);
 // device status codes (mirrors flint_status_t)
 constexpr uint32_t ST_TIMEOUT = 4;
 constexpr uint32_t ST_BADINDEX = 5;
+constexpr uint32_t ST_INTERNAL = 7;   // an internal capacity check failed (a library defect)
 
 // Per-call routing tables of the decode path, written by the router's last
 // CTA.  Slot 0 is the shared expert (all T tokens, weight 1); slots 1..U are

@@ -29,7 +29,8 @@ constexpr int RL_TOK = 8;
 
 __global__ void __launch_bounds__(RT_WARPS * 32) router_logits_decode_kernel(const __nv_bfloat16* x, int T,
                                                                            const __nv_bfloat16* Wr,
-                                                                           const float* bias, float* logits) {
+                                                                           const float* bias, float* logits,
+                                                                           uint32_t* status, uint64_t limit_ns) {
     __shared__ __align__(128) __nv_bfloat16 xs[RL_TOK * H];   // 32 KiB
     __shared__ __align__(8) uint64_t xbar;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -50,8 +51,11 @@ __global__ void __launch_bounds__(RT_WARPS * 32) router_logits_decode_kernel(con
         mbar_arrive_expect_tx(&xbar, nt * H * 2);
         bulk_g2s(xs, x + (size_t)t0 * H, nt * H * 2, &xbar);
     }
-    const bool ok = __syncthreads_and(mbar_wait_bounded(&xbar, 0, 1000000000ull));
-    if (!ok) return;   // the copy never completed (cannot happen for valid pointers); logits stay stale
+    const bool ok = __syncthreads_and(mbar_wait_bounded(&xbar, 0, limit_ns));
+    if (!ok) {         // the copy did not complete in time: the logits are not written
+        if (threadIdx.x == 0) report_status(status, ST_TIMEOUT);
+        return;
+    }
     for (int t = 0; t < nt; ++t) {
         const __nv_bfloat16* xr = xs + t * H;
         float acc = 0.f;
@@ -200,7 +204,8 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(const int32_t* idx, c
 cudaError_t launch_router_logits_decode(const LaunchCtx& L, const __nv_bfloat16* x, int T,
                                         const __nv_bfloat16* Wr, const float* bias, float* logits) {
     return launch_hooked(L, FLINT_KERNEL_ROUTER, router_logits_decode_kernel,
-                         dim3(RT_CTAS, (T + RL_TOK - 1) / RL_TOK), dim3(RT_WARPS * 32), 0, x, T, Wr, bias, logits);
+                         dim3(RT_CTAS, (T + RL_TOK - 1) / RL_TOK), dim3(RT_WARPS * 32), 0, x, T, Wr, bias, logits,
+                         L.status, L.wait_limit_ns);
 }
 
 cudaError_t launch_select(const LaunchCtx& L, const float* logits, int T, int32_t* idx, float* w) {

@@ -190,12 +190,21 @@ __device__ __forceinline__ void build_decode_tables_warp(int T, const int* sel_e
 // order within a slot, tiles in order within a unit: slot u's items start at
 // DEC_UNITS x slot_tile0[u].  Item j of the grid goes to CTA j % G.
 constexpr int DEC_UNITS = 64;              // 8 gate + 8 up rows per unit, I = 512
-constexpr int DEC_MAX_CTA_ITEMS = 256;     // per CTA; the grid has >= 72 CTAs
+constexpr int DEC_MAX_CTA_ITEMS = 256;     // per CTA
+constexpr int DEC_MIN_GRID = 72;           // the gate/up grids have at least this many CTAs
 static_assert(DEC_UNITS * 4 <= 256, "unit and tile fit in the low byte");
+// Most 8-token tiles a batch can have: ceil(T / 8) for the shared slot, and
+// for U routed slots holding 6T pairs in all, sum ceil(n_u / 8) <= (6T + 7U) / 8
+// with U <= min(E, 6T).  The item list of every CTA then fits its buffer.
+constexpr int DEC_MAX_ROUTED = DEC_T * TOPK < E ? DEC_T * TOPK : E;
+constexpr int DEC_MAX_TILES = (DEC_T + 7) / 8 + (DEC_T * TOPK + 7 * DEC_MAX_ROUTED) / 8;
+static_assert((DEC_UNITS * DEC_MAX_TILES + DEC_MIN_GRID - 1) / DEC_MIN_GRID <= DEC_MAX_CTA_ITEMS,
+              "a CTA's gate/up item list fits its buffer at the smallest grid");
 
 // CTA c's items c, c + G, ... into list[] (all threads of the CTA take part;
 // the caller synchronises before reading list).  Returns their count, or -1
-// when it exceeds DEC_MAX_CTA_ITEMS (the list is then left empty).
+// when it exceeds DEC_MAX_CTA_ITEMS (the list is then left empty; with G >=
+// DEC_MIN_GRID the static_assert above rules this out).
 __device__ __forceinline__ int list_gateup_items(const DecodeTables* tab, int c, int G, int* list) {
     const int n_slots = tab->n_slots, total = DEC_UNITS * tab->slot_tile0[n_slots];
     const int my_items = c < total ? (total - c + G - 1) / G : 0;

@@ -27,6 +27,7 @@ STATUS = {
     4: "FLINT_ERR_DEVICE_TIMEOUT",
     5: "FLINT_ERR_DEVICE_BADINDEX",
     6: "FLINT_ERR_UNSUPPORTED",
+    7: "FLINT_ERR_INTERNAL",
 }
 
 H, I, E, TOPK, CHUNK, DECODE_MAX_T = 2048, 512, 256, 6, 8192, 32

@@ -39,10 +39,10 @@ def test_prefill_small_full_compare(setup, T):
     assert res["ok"], res
 
 
-def sample_compare(orc, xb, y, rows):
-    sub = xb[rows]
-    ref, alt = orc.forward_with_alternatives(sub)
-    res = compare(y[rows].float().cpu().numpy(), ref, alt)
+def full_compare(orc, xb, y):
+    """Every row of the device output against the oracle, element by element."""
+    ref, alt = orc.forward_with_alternatives(xb)
+    res = compare(y.float().cpu().numpy(), ref, alt)
     assert res["ok"], res
     return res
 
@@ -52,31 +52,29 @@ def test_prefill_1000_tokens(setup):
     xb = gen.x_gaussian(14, 1000)
     y = run(h, xb)
     assert torch.isfinite(y.float()).all()
-    rows = np.concatenate([np.arange(0, 1000, 37), [999]])
-    sample_compare(orc, xb, y, rows)
+    full_compare(orc, xb, y)
 
 
 def test_prefill_8192_tokens_full_config(setup):
     """The prefill workload: 8192 tokens, x ~ N(0,1) RMS-normalised (seed 14),
-    skewed router bias; sampled rows across every 128-token block and the
-    last one, compared with the oracle token by token."""
+    skewed router bias.  All 8192 rows are compared with the oracle (so every
+    expert's every 256-token pass and its ragged last pass is covered), and
+    a second forward is bit-identical (every sum runs in a fixed order)."""
     lw, h, orc = setup
     xb = gen.x_gaussian(14, 8192)
     y = run(h, xb)
     assert torch.isfinite(y.float()).all()
-    rng = np.random.default_rng(0)
-    rows = np.unique(np.concatenate([np.arange(0, 8192, 128) + rng.integers(0, 128, 64), [0, 8191]]))
-    sample_compare(orc, xb, y, rows)
-    # deterministic: every sum runs in a fixed order
+    full_compare(orc, xb, y)
     y2 = run(h, xb)
     assert torch.equal(y2, y)
 
 
 def test_prefill_chunked_beyond_8192(setup):
+    """8269 tokens: one full 8192-token chunk and a ragged 77-token chunk,
+    every row compared."""
     lw, h, orc = setup
     T = 8192 + 77
     xb = gen.x_gaussian(15, T)
     y = run(h, xb)
     assert torch.isfinite(y.float()).all()
-    rows = np.array([0, 5000, 8191, 8192, 8200, T - 1])
-    sample_compare(orc, xb, y, rows)
+    full_compare(orc, xb, y)

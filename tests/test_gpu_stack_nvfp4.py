@@ -1,0 +1,55 @@
+"""The 47-layer NVFP4 (W4A16) decode stack at full size in the benchmark's
+launch configuration (the 47 forwards captured into one CUDA graph and
+replayed), every layer checked against the fp64 oracle run on the same NVFP4
+codes, at T = 1 and 32."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle.reference import LayerOracle, compare
+from sparse_moe_transformer_03_b300 import flint
+from synth import device, gen
+from tests.test_gpu_stack import replay_stack
+
+pytestmark = pytest.mark.gpu
+
+N_LAYERS = 47
+
+
+def nvfp4_oracle(lw, q):
+    def mats(e):
+        (pg, sg, tg), (pd, sd, td) = q.expert_parts(e)
+        return (oracle.Mat(packed=pg, scales=sg, tensor_scale=tg), oracle.Mat(packed=pd, scales=sd, tensor_scale=td))
+    return LayerOracle(lw.router_bits(), lw.bias_host(), mats, mats(lw.E), lw.E)
+
+
+@pytest.fixture(scope="module")
+def stack():
+    device.build()
+    layers, handles = [], []
+    for l in range(N_LAYERS):
+        lw = device.LayerWeights(1, l, True)
+        q = device.LayerNVFP4(lw)
+        gu, dn, sh = q.create_args()
+        handles.append(flint.flint_moe_create(lw.router_W, lw.router_b, gu, dn, sh, dtype=flint.FLINT_NVFP4))
+        lw.gate_up = lw.down = None          # the handle owns its repacked copy; the router stays borrowed
+        layers.append((lw, q))
+    torch.cuda.empty_cache()
+    yield layers, handles
+    for h in handles:
+        flint.flint_moe_destroy(h)
+    del layers
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("T,kind,seed", [(1, "gauss", 11), (32, "clustered", 13)])
+def test_nvfp4_stack_graph_replay_matches_oracle(stack, T, kind, seed):
+    layers, handles = stack
+    xb = gen.x_gaussian(seed, T) if kind == "gauss" else gen.x_clustered(seed, T)[0]
+    ys = replay_stack(handles, xb, T)
+    for l in range(N_LAYERS):
+        assert np.isfinite(ys[l]).all(), l
+        ref, alt = nvfp4_oracle(*layers[l]).forward_with_alternatives(xb)
+        res = compare(ys[l], ref, alt)
+        assert res["ok"], (l, res)

@@ -1,9 +1,12 @@
 """flint_permute_static (the permutation with a fixed device scratch array)
-against flint_moe_route_only's permutation, through the C ABI.  Kept in a
-file collected last so that it also runs after every other GPU test."""
+against the oracle's stable counting sort and against flint_moe_route_only's
+permutation, through the C ABI.  Kept in a file collected last so that it
+also runs after every other GPU test."""
 import numpy as np
 import pytest
 import torch
+
+import oracle
 
 from sparse_moe_transformer_03_b300 import flint
 from synth import device, gen
@@ -47,6 +50,9 @@ def test_static_scratch_matches_route_only_two_calls(h, Ts):
         off, gat = _static(idx, T)
         assert torch.equal(off, off_ref)
         assert torch.equal(gat, gat_ref)
+        off_o, gat_o = oracle.permutation(idx.cpu().numpy())
+        assert np.array_equal(off.numpy(), off_o)
+        assert np.array_equal(gat.numpy(), gat_o)
 
 
 def test_static_scratch_rejects_beyond_maximum():
