@@ -125,6 +125,31 @@ FLINT_API flint_status_t flint_moe_create(flint_moe_t* out, const void* router_W
  * device status left by an earlier call. */
 FLINT_API flint_status_t flint_moe_forward(flint_moe_t h, const void* x, int T, void* y, cudaStream_t s);
 
+/* n layers applied in order, y[l] = layer_l(x[l]) for l = 0 .. n-1, with the
+ * result of n flint_moe_forward calls on one stream (cross-layer decode; the
+ * recipe page's low-latency decode path and the mrchatgpt.org article's decode
+ * megakernel, section 4, name the idea).
+ *   layers  host array of n handles, all of one dtype, on one device.
+ *   x, y    host arrays of n device pointers, bf16 [T][2048] each; x[l] and
+ *           y[l] must not overlap.  Layer l reads x[l] only after every
+ *           earlier layer has written its y, so x[l + 1] may be y[l] (a
+ *           chained stack) or any other buffer.
+ *   T       tokens per layer, T >= 1.
+ * FLINT_BF16 with T <= FLINT_STACK_MAX_T: ONE persistent kernel launch per
+ * FLINT_STACK_MAX_LAYERS layers (one CTA per SM walks the layers; grid-wide
+ * device-scope barriers separate a layer's phases, each wait bounded).  The
+ * launch needs every SM of the device: do not run other kernels beside it.
+ * Otherwise (larger T, NVFP4 layers): n flint_moe_forward calls.
+ * Asynchronous on s, allocates nothing, capturable in a CUDA graph.  Scratch:
+ * layers[0]'s workspace, so layers[0] must not be used on another stream
+ * meanwhile; device errors are reported in layers[0]'s status word.
+ * Errors: INVALID_ARG (null, misaligned, overlapping x[l]/y[l], mixed
+ * dtypes or devices), CUDA, or a device status left by an earlier call. */
+#define FLINT_STACK_MAX_T 8
+#define FLINT_STACK_MAX_LAYERS 64
+FLINT_API flint_status_t flint_moe_forward_layers(const flint_moe_t* layers, int n, const void* const* x, int T,
+                                                  void* const* y, cudaStream_t s);
+
 /* Routing alone, for testing (synchronises s before returning).
  *   x       bf16 [T][2048] or NULL.
  *   logits  fp32 [T][256].  If x is NULL, logits is the INPUT: the router

@@ -15,6 +15,7 @@ struct flint_moe {
     flint_dtype_t dtype;
     int device;
     int num_sms;
+    int smem_optin;                // opt-in shared memory per block of the device
     uint64_t wait_limit_ns;
     int prof_kernel;               // profiling hook (flint_moe_set_kernel_events), -1 when unset
     cudaEvent_t prof_start, prof_stop;
@@ -51,6 +52,9 @@ struct flint_moe {
     int32_t* pair_slot;            // [CHUNK*TOPK] slot of each (token, choice) pair
     __nv_bfloat16* h_perm;         // [(TOPK+1)*CHUNK][I]
     __nv_bfloat16* o_perm;         // [(TOPK+1)*CHUNK][H]
+    // scratch of flint_moe_forward_layers when this handle is layers[0]
+    unsigned char* stack_clear;    // tagged logits, barrier counter, abort flag (STACK_CLEAR_BYTES)
+    __nv_bfloat16* stack_act;      // [STACK_MAX_T * 7][I]
 };
 
 namespace {
@@ -122,6 +126,8 @@ void carve_workspace(flint_moe* h, char* base, size_t* bytes_out) {
     h->pair_slot = c.take<int32_t>((size_t)CHUNK * TOPK);
     h->h_perm = c.take<__nv_bfloat16>((size_t)(TOPK + 1) * CHUNK * I);
     h->o_perm = c.take<__nv_bfloat16>((size_t)(TOPK + 1) * CHUNK * H);
+    h->stack_clear = c.take<unsigned char>(STACK_CLEAR_BYTES);
+    h->stack_act = c.take<__nv_bfloat16>(STACK_ACT_ELEMS);
     *bytes_out = c.off;
 }
 
@@ -175,6 +181,7 @@ flint_status_t flint_moe_create(flint_moe_t* out, const void* router_W, const fl
     h->dtype = dtype;
     h->device = dev;
     h->num_sms = prop.multiProcessorCount;
+    h->smem_optin = (int)prop.sharedMemPerBlockOptin;
     h->wait_limit_ns = 1000000000ull;   // one second
     h->prof_kernel = -1;
     h->router_W = static_cast<const __nv_bfloat16*>(router_W);
@@ -244,6 +251,7 @@ flint_status_t flint_moe_create(flint_moe_t* out, const void* router_W, const fl
     if (st == FLINT_OK) st = from_cuda(prefill_set_attributes());
     if (st == FLINT_OK) st = from_cuda(decode_nvfp4_set_attributes());
     if (st == FLINT_OK) st = from_cuda(decode_mma_set_attributes());
+    if (st == FLINT_OK) st = from_cuda(stack_decode_set_attributes(h->smem_optin));
     if (st == FLINT_OK) st = from_cuda(cudaDeviceSynchronize());
     if (st != FLINT_OK) {
         cudaGetLastError();
@@ -302,6 +310,61 @@ flint_status_t flint_moe_forward(flint_moe_t h, const void* x, int T, void* y, c
             e = launch_prefill_experts(L, xc, h->h_map, Tc, h->offsets, h->gather, h->pair_slot, h->w, h->tiled,
                                        h->h_perm, h->o_perm, ys + (size_t)t0 * H);
         if (e != cudaSuccess) return FLINT_ERR_CUDA;
+    }
+    return FLINT_OK;
+}
+
+flint_status_t flint_moe_forward_layers(const flint_moe_t* layers, int n, const void* const* x, int T,
+                                        void* const* y, cudaStream_t s) {
+    if (!layers || !x || !y || n < 1 || T < 1) return FLINT_ERR_INVALID_ARG;
+    flint_moe* h0 = layers[0];
+    if (!h0) return FLINT_ERR_INVALID_ARG;
+    const size_t bytes = (size_t)T * H * 2;
+    for (int l = 0; l < n; ++l) {
+        const flint_moe* h = layers[l];
+        if (!h || h->dtype != h0->dtype || h->device != h0->device) return FLINT_ERR_INVALID_ARG;
+        if (!x[l] || !y[l] || !aligned16(x[l]) || !aligned16(y[l])) return FLINT_ERR_INVALID_ARG;
+        const char* xb = static_cast<const char*>(x[l]);
+        const char* yb = static_cast<const char*>(y[l]);
+        if (xb < yb + bytes && yb < xb + bytes) return FLINT_ERR_INVALID_ARG;
+    }
+    flint_status_t st = take_device_status(h0);
+    if (st != FLINT_OK) {
+        // a stack launch that gave up may have left its barrier counter and
+        // tagged logits mid-way: start the next one from a clean scratch
+        if (cudaMemsetAsync(h0->stack_clear, 0, STACK_CLEAR_BYTES, s) != cudaSuccess) return FLINT_ERR_CUDA;
+        return st;
+    }
+    const bool persistent = h0->dtype == FLINT_BF16 && T <= STACK_MAX_T && h0->num_sms >= 128 && h0->num_sms <= E;
+    if (!persistent) {
+        // larger batches and NVFP4 layers: one forward per layer, in order
+        for (int l = 0; l < n; ++l) {
+            st = flint_moe_forward(layers[l], x[l], T, y[l], s);
+            if (st != FLINT_OK) return st;
+        }
+        return FLINT_OK;
+    }
+    const LaunchCtx L = ctx_of(h0, s);
+    for (int l0 = 0; l0 < n; l0 += STACK_MAX_LAYERS) {
+        StackParams p;
+        std::memset(&p, 0, sizeof p);
+        p.n_layers = n - l0 < STACK_MAX_LAYERS ? n - l0 : STACK_MAX_LAYERS;
+        p.T = T;
+        for (int i = 0; i < p.n_layers; ++i) {
+            const flint_moe* h = layers[l0 + i];
+            p.layer[i].tiled = reinterpret_cast<const uint8_t*>(h->tiled);
+            p.layer[i].router = h->router_W;
+            p.layer[i].bias = h->router_b;
+            p.layer[i].x = static_cast<const __nv_bfloat16*>(x[l0 + i]);
+            p.layer[i].y = static_cast<__nv_bfloat16*>(y[l0 + i]);
+        }
+        p.logits = reinterpret_cast<unsigned long long*>(h0->stack_clear);
+        p.bar = reinterpret_cast<unsigned long long*>(h0->stack_clear + STACK_LOGITS_BYTES);
+        p.abort_flag = reinterpret_cast<uint32_t*>(h0->stack_clear + STACK_LOGITS_BYTES + 8);
+        p.act = h0->stack_act;
+        p.status = h0->status_dev;
+        p.limit_ns = h0->wait_limit_ns;
+        if (launch_stack_decode(L, p, h0->smem_optin) != cudaSuccess) return FLINT_ERR_CUDA;
     }
     return FLINT_OK;
 }

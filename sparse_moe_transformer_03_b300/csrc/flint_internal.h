@@ -106,6 +106,37 @@ cudaError_t launch_decode_experts_nvfp4(const LaunchCtx& L, const uint8_t* nv, c
                                         const float* logits, const __nv_bfloat16* x, int T, DecodeTables* tables,
                                         int32_t* idx, float* w, __nv_bfloat16* a_buf, __nv_bfloat16* y);
 
+// stack_decode.cu -- every layer of a stack in one persistent launch (bf16,
+// T <= STACK_MAX_T).  Layer l reads x of its own and writes its y; layer l
+// starts only after every CTA finished layer l - 1, so x[l] may be y[l - 1].
+constexpr int STACK_MAX_T = 8;
+constexpr int STACK_MAX_LAYERS = 64;
+struct StackLayerArgs {
+    const uint8_t* tiled;            // the layer handle's tiled experts
+    const __nv_bfloat16* router;     // [E][H]
+    const float* bias;               // [E] or null
+    const __nv_bfloat16* x;          // [T][H]
+    __nv_bfloat16* y;                // [T][H]
+};
+struct StackParams {
+    StackLayerArgs layer[STACK_MAX_LAYERS];
+    int n_layers, T;
+    uint32_t smem_bytes;             // the device's opt-in shared memory per block
+    unsigned long long* logits;      // [STACK_MAX_T][E] tagged logits (scratch)
+    __nv_bfloat16* act;              // [STACK_MAX_T * 7][I] activations (scratch)
+    unsigned long long* bar;         // grid barrier counter (scratch, follows logits)
+    uint32_t* abort_flag;            // set by a CTA whose bounded wait ran out
+    uint32_t* status;
+    uint64_t limit_ns;
+};
+// scratch of a stack launch inside a handle's workspace: logits, barrier
+// counter and abort flag contiguous (cleared together after a device error)
+constexpr size_t STACK_LOGITS_BYTES = (size_t)STACK_MAX_T * E * 8;
+constexpr size_t STACK_CLEAR_BYTES = STACK_LOGITS_BYTES + 16;
+constexpr size_t STACK_ACT_ELEMS = (size_t)STACK_MAX_T * (TOPK + 1) * I;
+cudaError_t stack_decode_set_attributes(int max_optin);
+cudaError_t launch_stack_decode(const LaunchCtx& L, StackParams& p, int max_optin);
+
 // decode_mma.cu -- bf16 decode (T <= DEC_T) on mma.sync, from the tiled copy
 cudaError_t decode_mma_set_attributes();
 cudaError_t launch_decode_experts_mma(const LaunchCtx& L, const uint8_t* tiled, const float* logits,

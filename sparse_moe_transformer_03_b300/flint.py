@@ -31,6 +31,7 @@ STATUS = {
 }
 
 H, I, E, TOPK, CHUNK, DECODE_MAX_T = 2048, 512, 256, 6, 8192, 32
+STACK_MAX_T, STACK_MAX_LAYERS = 8, 64
 
 
 class FlintError(RuntimeError):
@@ -59,6 +60,8 @@ def load_library():
     lib.flint_moe_create.argtypes = [ctypes.POINTER(P), P, P, P, P, P, I32]
     lib.flint_moe_forward.restype = I32
     lib.flint_moe_forward.argtypes = [P, P, I32, P, P]
+    lib.flint_moe_forward_layers.restype = I32
+    lib.flint_moe_forward_layers.argtypes = [P, I32, P, I32, P, P]
     lib.flint_moe_route_only.restype = I32
     lib.flint_moe_route_only.argtypes = [P, P, P, I32, P, P, P, P, P]
     lib.flint_moe_destroy.restype = I32
@@ -141,6 +144,19 @@ def flint_moe_create(router_W, router_b, gate_up, down, shared, dtype=FLINT_BF16
 def flint_moe_forward(h, x, T, y, stream=None):
     _check("flint_moe_forward", load_library().flint_moe_forward(ctypes.c_void_p(h), _ptr(x), int(T), _ptr(y),
                                                                  _stream(stream)))
+
+
+def flint_moe_forward_layers(handles, xs, T, ys, stream=None):
+    """n layers in order: ys[l] = layer handles[l] applied to xs[l] (device
+    buffers bf16 [T][2048]; xs[l + 1] may be ys[l])."""
+    n = len(handles)
+    if len(xs) != n or len(ys) != n:
+        raise ValueError("one x and one y per layer")
+    hs = (ctypes.c_void_p * n)(*[int(h) for h in handles])
+    xa = (ctypes.c_void_p * n)(*[_ptr(x).value for x in xs])
+    ya = (ctypes.c_void_p * n)(*[_ptr(y).value for y in ys])
+    _check("flint_moe_forward_layers",
+           load_library().flint_moe_forward_layers(hs, n, xa, int(T), ya, _stream(stream)))
 
 
 def flint_moe_route_only(h, x, logits, T, idx, w, offsets=None, gather_idx=None, stream=None):

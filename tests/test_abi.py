@@ -32,6 +32,8 @@ def test_header_constants_match_binding():
     assert int(consts["FLINT_TOPK"]) == flint.TOPK
     assert int(consts["FLINT_CHUNK"]) == flint.CHUNK
     assert int(consts["FLINT_DECODE_MAX_T"]) == flint.DECODE_MAX_T
+    assert int(consts["FLINT_STACK_MAX_T"]) == flint.STACK_MAX_T
+    assert int(consts["FLINT_STACK_MAX_LAYERS"]) == flint.STACK_MAX_LAYERS
     enums = dict(re.findall(r"(FLINT_(?:OK|ERR_\w+)) = (\d+)", src))
     assert {int(v): k for k, v in enums.items()} == flint.STATUS
 
@@ -60,6 +62,15 @@ def test_host_argument_checks(lib):
     arr[3] = 4096 * 4 + 8
     assert lib.flint_moe_create(ctypes.byref(h), P(256), None, arr, arr, sh, 0) == 1  # misaligned expert
     assert lib.flint_debug_bounded_wait(0, None) == 1
+    # the stack call: null arrays, no layers, bad T, a null handle
+    hs = (P * 2)()
+    xs = (P * 2)(4096, 8192 * 4)
+    ys = (P * 2)(4096 * 64, 4096 * 128)
+    assert lib.flint_moe_forward_layers(None, 2, xs, 1, ys, None) == 1
+    assert lib.flint_moe_forward_layers(hs, 0, xs, 1, ys, None) == 1
+    assert lib.flint_moe_forward_layers(hs, 2, xs, 0, ys, None) == 1
+    assert lib.flint_moe_forward_layers(hs, 2, None, 1, ys, None) == 1
+    assert lib.flint_moe_forward_layers(hs, 2, xs, 1, ys, None) == 1      # null handles
 
 
 def test_kernel_event_hook_rejects_bad_arguments():

@@ -63,3 +63,102 @@ def test_stack_graph_replay_matches_oracle(stack, T, kind, seed):
         ref, alt = LayerOracle.from_bf16_layer(layers[l]).forward_with_alternatives(xb)
         res = compare(ys[l], ref, alt)
         assert res["ok"], (l, res)
+
+
+# ---------------------------------------------------------------------------
+# flint_moe_forward_layers: the whole stack in one persistent launch
+# ---------------------------------------------------------------------------
+
+def stack_call(handles, xs, T, stream=None):
+    ys = [torch.full_like(xs[0], float("nan")) for _ in handles]
+    flint.flint_moe_forward_layers(handles, xs, T, ys, stream)
+    torch.cuda.synchronize()
+    return ys
+
+
+@pytest.mark.parametrize("T,kind,seed", [(1, "gauss", 11), (3, "gauss", 21), (8, "clustered", 12)])
+def test_stack_call_matches_oracle_every_layer(stack, T, kind, seed):
+    """47 layers in one launch, the same x for every layer (the benchmark's
+    stack): every layer's output against the oracle."""
+    layers, handles = stack
+    xb = gen.x_gaussian(seed, T) if kind == "gauss" else gen.x_clustered(seed, T)[0]
+    x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
+    ys = stack_call(handles, [x] * N_LAYERS, T)
+    for l in range(N_LAYERS):
+        y = ys[l].float().cpu().numpy()
+        assert np.isfinite(y).all(), l
+        ref, alt = LayerOracle.from_bf16_layer(layers[l]).forward_with_alternatives(xb)
+        res = compare(y, ref, alt)
+        assert res["ok"], (l, res)
+
+
+def test_stack_call_chained_layers_read_the_previous_output(stack):
+    """x[l + 1] = y[l]: every layer must see the complete output of the layer
+    before it (the launch separates layers by a grid-wide barrier).  Each
+    layer is checked against the oracle on the input the device consumed."""
+    layers, handles = stack
+    T, n = 4, 6
+    xb = gen.x_gaussian(31, T)
+    x0 = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
+    ys = [torch.full_like(x0, float("nan")) for _ in range(n)]
+    xs = [x0] + ys[:-1]
+    flint.flint_moe_forward_layers(handles[:n], xs, T, ys)
+    torch.cuda.synchronize()
+    inp = xb
+    for l in range(n):
+        y = ys[l].float().cpu().numpy()
+        assert np.isfinite(y).all(), l
+        ref, alt = LayerOracle.from_bf16_layer(layers[l]).forward_with_alternatives(inp)
+        res = compare(y, ref, alt)
+        assert res["ok"], (l, res)
+        inp = ys[l].view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def test_stack_call_graph_replay_is_bit_identical(stack):
+    """Captured once and replayed: the same bits as a direct call, every time."""
+    layers, handles = stack
+    T = 8
+    xb = gen.x_clustered(12, T)[0]
+    x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
+    direct = stack_call(handles, [x] * N_LAYERS, T)
+    ys = [torch.full_like(x, float("nan")) for _ in handles]
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        flint.flint_moe_forward_layers(handles, [x] * N_LAYERS, T, ys, s)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        flint.flint_moe_forward_layers(handles, [x] * N_LAYERS, T, ys, s)
+    for rep in range(3):
+        for y in ys:
+            y.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        for l in range(N_LAYERS):
+            assert torch.equal(ys[l], direct[l]), (rep, l)
+
+
+def test_stack_call_above_eight_tokens_is_the_per_layer_path(stack):
+    """T > 8 runs one forward per layer: bit-identical to those calls."""
+    layers, handles = stack
+    T = 32
+    xb = gen.x_clustered(13, T)[0]
+    x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
+    ys = stack_call(handles[:5], [x] * 5, T)
+    for l in range(5):
+        y = torch.empty_like(x)
+        flint.flint_moe_forward(handles[l], x, T, y)
+        torch.cuda.synchronize()
+        assert torch.equal(ys[l], y), l
+
+
+def test_stack_call_argument_checks(stack):
+    layers, handles = stack
+    x = torch.zeros((4, 2048), dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros_like(x)
+    with pytest.raises(flint.FlintError) as ei:       # x and y overlap
+        flint.flint_moe_forward_layers(handles[:2], [x, x], 4, [y, x])
+    assert ei.value.code == 1
+    with pytest.raises(flint.FlintError) as ei:       # misaligned
+        flint.flint_moe_forward_layers(handles[:1], [x.data_ptr() + 2], 4, [y])
+    assert ei.value.code == 1
