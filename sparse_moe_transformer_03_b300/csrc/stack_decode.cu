@@ -46,6 +46,8 @@
 #include "mma_sync.cuh"
 #include "routing.cuh"
 
+#include <cstddef>
+
 namespace flint {
 
 namespace {
@@ -76,11 +78,20 @@ struct SkShared {
     int pair0[E];
     int tok_pair[SK_MAX_SLOTS][STACK_MAX_T];      // pair of (slot, token), -1: token not routed there
     float tok_w[SK_MAX_SLOTS][STACK_MAX_T];       // its routing weight (0 when not routed)
-    float part[SK_CW][128];                       // per-warp partial sums (shared unit: [lane][4];
-                                                  // down: [row group][token][row])
+    alignas(16) float part[SK_CW][128];           // per-warp partial sums (shared unit: [lane][4], read
+                                                  // as float4; down: [row group][token][row])
     uint64_t route_bar;                           // consumers -> producer: tables of the layer are built
+    // Ring slot i was last handed out for sequence number slot_seq[i] - 1.  A
+    // consumer waits for its sequence number here before the slot's full
+    // barrier: several warps consume the ring, so one may reach use u of a
+    // slot before use u - 1 has landed, and a parity wait for phase u would
+    // then succeed on phase u - 1.
+    uint32_t slot_seq[32];
     int abort;
 };
+
+static_assert(offsetof(SkShared, part) % 16 == 0, "float4 access to the partial sums");
+static_assert(offsetof(SkShared, route_bar) % 8 == 0, "mbarrier alignment");
 
 // 128 x 64 tile-copy offsets (repack.cu layout): in-tile row r, 16-byte chunk c
 __device__ __forceinline__ uint32_t sw_chunk(int r, int c) { return (uint32_t)(((c ^ (r & 7)) << 4)); }
@@ -160,6 +171,38 @@ __device__ __forceinline__ bool sk_wait(const SkState& s, uint64_t* bar, uint32_
     }
 }
 
+__device__ __forceinline__ void st_release_shared(uint32_t* p, uint32_t v) {
+    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_shared(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
+    return v;
+}
+
+// Wait until ring sequence number q has landed in its slot: first until the
+// producer has handed the slot out for q (so the slot's full barrier is at
+// q's phase or past it), then on the full barrier.
+__device__ __forceinline__ bool sk_wait_full(const SkState& s, uint32_t q) {
+    const int slot = (int)(q % (uint32_t)s.nslot);
+    const uint32_t* ss = &s.sh->slot_seq[slot];
+    if (ld_acquire_shared(ss) != q + 1u) {
+        const uint64_t t0 = globaltimer_ns();
+        for (;;) {
+#pragma unroll 1
+            for (int i = 0; i < 64; ++i)
+                if (ld_acquire_shared(ss) == q + 1u) goto issued;
+            if (sk_aborted(s)) return false;
+            if (globaltimer_ns() - t0 > s.p->limit_ns) {
+                sk_fail(s);
+                return false;
+            }
+        }
+    }
+issued:
+    return sk_wait(s, &s.full[slot], (q / (uint32_t)s.nslot) & 1);
+}
+
 // Grid barrier (one thread, after the consumer warps synchronised): arrive,
 // then wait until every CTA of the grid has arrived `target` - base times.
 __device__ bool sk_grid_barrier(const SkState& s, unsigned long long target) {
@@ -212,6 +255,7 @@ struct SkProducer {
         if (use > 0 && !sk_wait(s, &s.empty[slot], (use - 1) & 1)) return false;
         fence_proxy_async_smem();
         mbar_arrive_expect_tx(&s.full[slot], bytes);
+        st_release_shared(&s.sh->slot_seq[slot], seq + 1u);
         *dst = s.ring + (size_t)slot * SK_SLOT;
         *bar = &s.full[slot];
         ++seq;
@@ -344,8 +388,7 @@ __device__ __forceinline__ bool sk_gateup_mma(const SkState& s, uint32_t sq, int
     for (int kt = kt0; kt < kt1; ++kt) {
         const int sk = kt >> 3;
         if (sk != waited) {
-            const uint32_t qq = sq + (uint32_t)sk;
-            if (!__all_sync(0xFFFFFFFFu, sk_wait(s, &s.full[qq % s.nslot], (qq / s.nslot) & 1))) return false;
+            if (!__all_sync(0xFFFFFFFFu, sk_wait_full(s, sq + (uint32_t)sk))) return false;
             waited = sk;
         }
         const uint8_t* piece = s.ring + (size_t)((sq + sk) % s.nslot) * SK_SLOT + (kt & 7) * 1024 + boff;
@@ -420,7 +463,7 @@ __device__ void sk_consumers(const SkState& s, int warp, int lane) {
         const uint32_t seqR = seq;
         seq += nr ? 1 : 0;
         if (nr) {
-            fail = !__all_sync(0xFFFFFFFFu, sk_wait(s, &s.full[seqR % s.nslot], (seqR / s.nslot) & 1));
+            fail = !__all_sync(0xFFFFFFFFu, sk_wait_full(s, seqR));
             const uint8_t* rows = s.ring + (size_t)(seqR % s.nslot) * SK_SLOT;
             for (int pi = warp; !fail && pi < nr * T; pi += SK_CW) {
                 const int i = pi / T, t = pi % T, e = c + i * G;
@@ -490,8 +533,10 @@ __device__ void sk_consumers(const SkState& s, int warp, int lane) {
                     got = true;
                     break;
                 }
-                if (sk_aborted(s) || *reinterpret_cast<volatile uint32_t*>(p.abort_flag)) break;
-                if (globaltimer_ns() - t0 > p.limit_ns) {
+                // warp-uniform decisions: every lane leaves the loop together
+                if (__any_sync(0xFFFFFFFFu, sk_aborted(s) || *reinterpret_cast<volatile uint32_t*>(p.abort_flag)))
+                    break;
+                if (__any_sync(0xFFFFFFFFu, globaltimer_ns() - t0 > p.limit_ns)) {
                     if (lane == 0) sk_fail(s);
                     break;
                 }
@@ -564,7 +609,7 @@ __device__ void sk_consumers(const SkState& s, int warp, int lane) {
         for (int it = warp; it < nd && !fail; it += SK_CW) {
             const int u = it / nrg, ri = it % nrg;
             const uint32_t qq = seqD + (uint32_t)it;
-            if (!__all_sync(0xFFFFFFFFu, sk_wait(s, &s.full[qq % s.nslot], (qq / s.nslot) & 1))) {
+            if (!__all_sync(0xFFFFFFFFu, sk_wait_full(s, qq))) {
                 fail = true;
                 break;
             }
@@ -639,6 +684,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1) stack_decode_kernel(const __gri
             mbar_init(&s.empty[i], 1);
         }
         mbar_init(&s.sh->route_bar, 1);
+        for (int i = 0; i < 32; ++i) s.sh->slot_seq[i] = 0u;
         s.sh->abort = 0;
         fence_mbar_init();
     }
