@@ -54,6 +54,7 @@ struct flint_moe {
     __nv_bfloat16* o_perm;         // [(TOPK+1)*CHUNK][H]
     // scratch of flint_moe_forward_layers when this handle is layers[0]
     unsigned char* stack_clear;    // tagged logits, barrier counter, abort flag (STACK_CLEAR_BYTES)
+    CUtensorMap* stack_maps;       // [2] this layer's tiled experts as 4-D tensor maps (bf16 handles)
     __nv_bfloat16* stack_act;      // [STACK_MAX_T * 7][I]
 };
 
@@ -128,6 +129,7 @@ void carve_workspace(flint_moe* h, char* base, size_t* bytes_out) {
     h->o_perm = c.take<__nv_bfloat16>((size_t)(TOPK + 1) * CHUNK * H);
     h->stack_clear = c.take<unsigned char>(STACK_CLEAR_BYTES);
     h->stack_act = c.take<__nv_bfloat16>(STACK_ACT_ELEMS);
+    h->stack_maps = c.take<CUtensorMap>(2);
     *bytes_out = c.off;
 }
 
@@ -248,6 +250,13 @@ flint_status_t flint_moe_create(flint_moe_t* out, const void* router_W, const fl
                          encode_bf16_2d(&h->h_map, h->h_perm, (uint64_t)(TOPK + 1) * CHUNK, I, I, 256, 64);
         if (!enc) st = FLINT_ERR_CUDA;
     }
+    if (st == FLINT_OK && dtype == FLINT_BF16) {
+        // the tiled experts as 4-D tensors for the persistent stack kernel
+        CUtensorMap maps[2];
+        if (!encode_tiled_experts_4d(&maps[0], h->tiled, 4, 16) || !encode_tiled_experts_4d(&maps[1], h->tiled, 8, 8) ||
+            cudaMemcpy(h->stack_maps, maps, sizeof maps, cudaMemcpyHostToDevice) != cudaSuccess)
+            st = FLINT_ERR_CUDA;
+    }
     if (st == FLINT_OK) st = from_cuda(prefill_set_attributes());
     if (st == FLINT_OK) st = from_cuda(decode_nvfp4_set_attributes());
     if (st == FLINT_OK) st = from_cuda(decode_mma_set_attributes());
@@ -352,7 +361,7 @@ flint_status_t flint_moe_forward_layers(const flint_moe_t* layers, int n, const 
         p.T = T;
         for (int i = 0; i < p.n_layers; ++i) {
             const flint_moe* h = layers[l0 + i];
-            p.layer[i].tiled = reinterpret_cast<const uint8_t*>(h->tiled);
+            p.layer[i].maps = h->stack_maps;
             p.layer[i].router = h->router_W;
             p.layer[i].bias = h->router_b;
             p.layer[i].x = static_cast<const __nv_bfloat16*>(x[l0 + i]);

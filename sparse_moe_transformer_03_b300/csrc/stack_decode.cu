@@ -45,6 +45,7 @@
 #include "flint_internal.h"
 #include "mma_sync.cuh"
 #include "routing.cuh"
+#include "tc_ptx.cuh"
 
 #include <cstddef>
 
@@ -57,11 +58,9 @@ constexpr int SK_THREADS = (SK_CW + 1) * 32;      // + one producer warp
 constexpr int SK_SLOT = 8192;                     // ring slot bytes
 constexpr int SK_GU_UNITS = I / 4;                // 128 gate/up units per expert
 constexpr int SK_RG = H / 8;                      // 256 down row groups per expert
+constexpr int SK_GU_TILES = (2 * I / 128) * (H / 64);  // 256 gate/up tiles of an expert precede its down tiles
 constexpr int SK_XSTRIDE = H * 2 + 16;            // padded x row in shared memory
 constexpr int SK_MAX_SLOTS = 1 + STACK_MAX_T * TOPK;   // 49
-constexpr size_t SK_TILE = 16384;
-constexpr size_t SK_EXPERT = (size_t)3 * H * I * 2;
-constexpr size_t SK_DOWN_OFF = (size_t)2 * I * H * 2;
 constexpr int SK_NAMED = 1;                       // named barrier of the consumer warps
 
 // Activation rows: pair p's 512 bf16, its 16-byte chunk c stored at c ^ (p % 8)
@@ -263,115 +262,83 @@ struct SkProducer {
     }
 };
 
-// Router rows of CTA c for layer l (one slot).
-__device__ __forceinline__ bool sk_issue_router(const SkState& s, SkProducer& pr, int l, int lane) {
+// Router rows of CTA c for layer l (one slot, plain bulk copies).  Lane 0 only.
+__device__ __forceinline__ bool sk_issue_router(const SkState& s, SkProducer& pr, int l) {
     const int nr = sk_router_rows(s.c, s.G);
     if (nr == 0) return true;
     uint8_t* dst = nullptr;
     uint64_t* bar = nullptr;
-    int ok = 1;
-    if (lane == 0) ok = pr.take(s, (uint32_t)nr * H * 2, &dst, &bar);
-    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-    if (!ok) return false;
-    const uint64_t d = __shfl_sync(0xFFFFFFFFu, (unsigned long long)dst, 0);
-    const uint64_t b = __shfl_sync(0xFFFFFFFFu, (unsigned long long)bar, 0);
-    if (lane < nr)
-        bulk_g2s(reinterpret_cast<uint8_t*>(d) + lane * H * 2, s.p->layer[l].router + (size_t)(s.c + lane * s.G) * H,
-                 H * 2, reinterpret_cast<uint64_t*>(b));
+    if (!pr.take(s, (uint32_t)nr * H * 2, &dst, &bar)) return false;
+    for (int i = 0; i < nr; ++i)
+        bulk_g2s(dst + i * H * 2, s.p->layer[l].router + (size_t)(s.c + i * s.G) * H, H * 2, bar);
     return true;
 }
 
-// One gate/up unit (4 slots): lane i copies column tile i (gate and up pieces).
-__device__ __forceinline__ bool sk_issue_gateup(const SkState& s, SkProducer& pr, const uint8_t* tiled, int expert,
-                                                int q, int lane) {
-    uint8_t* dst[4];
-    uint64_t* bar[4];
-    int ok = 1;
-    if (lane == 0)
-        for (int k = 0; k < 4 && ok; ++k) ok = pr.take(s, SK_SLOT, &dst[k], &bar[k]);
-    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-    if (!ok) return false;
-    const int k = lane >> 3;
-    uint64_t d = 0, b = 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const uint64_t dj = __shfl_sync(0xFFFFFFFFu, (unsigned long long)dst[j], 0);
-        const uint64_t bj = __shfl_sync(0xFFFFFFFFu, (unsigned long long)bar[j], 0);
-        if (j == k) {
-            d = dj;
-            b = bj;
-        }
+// One gate/up unit (4 slots, one 8 KiB tensor box each): gate rows 4q ..
+// 4q + 3 over column tiles 0..15 and 16..31, then the matching up rows.
+// Lane 0 only.
+__device__ __forceinline__ bool sk_issue_gateup(const SkState& s, SkProducer& pr, const CUtensorMap* maps,
+                                                int expert, int q) {
+    const int r0 = 4 * q, rb = r0 >> 7;
+    for (int k = 0; k < 4; ++k) {
+        uint8_t* dst = nullptr;
+        uint64_t* bar = nullptr;
+        if (!pr.take(s, SK_SLOT, &dst, &bar)) return false;
+        const int tile = ((k >> 1) * 4 + rb) * (H / 64) + (k & 1) * 16;   // up rows: row blocks 4..7
+        tc::tma_load_4d(dst, &maps[0], 0, r0 & 127, tile, expert, bar);
     }
-    const int r0 = 4 * q;    // first gate row of the unit
-    const uint8_t* ex = tiled + (size_t)expert * SK_EXPERT;
-    const size_t in_tile = (size_t)(r0 & 127) * 128;
-    const int kt = lane;
-    uint8_t* dp = reinterpret_cast<uint8_t*>(d) + (kt & 7) * 1024;
-    bulk_g2s(dp, ex + ((size_t)(r0 >> 7) * (H / 64) + kt) * SK_TILE + in_tile, 512, reinterpret_cast<uint64_t*>(b));
-    bulk_g2s(dp + 512, ex + ((size_t)((r0 >> 7) + 4) * (H / 64) + kt) * SK_TILE + in_tile, 512,
-             reinterpret_cast<uint64_t*>(b));
     return true;
 }
 
-// One down row group of one expert (one slot): lane i < 8 copies column tile i.
-__device__ __forceinline__ bool sk_issue_down(const SkState& s, SkProducer& pr, const uint8_t* tiled, int expert,
-                                              int rg, int lane) {
+// One down row group of one expert (one slot, one 8 KiB box: 8 rows x the 8
+// column tiles of K = 512).  Lane 0 only.
+__device__ __forceinline__ bool sk_issue_down(const SkState& s, SkProducer& pr, const CUtensorMap* maps, int expert,
+                                              int rg) {
     uint8_t* dst = nullptr;
     uint64_t* bar = nullptr;
-    int ok = 1;
-    if (lane == 0) ok = pr.take(s, SK_SLOT, &dst, &bar);
-    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-    if (!ok) return false;
-    const uint64_t d = __shfl_sync(0xFFFFFFFFu, (unsigned long long)dst, 0);
-    const uint64_t b = __shfl_sync(0xFFFFFFFFu, (unsigned long long)bar, 0);
-    if (lane < 8) {
-        const uint8_t* src = tiled + (size_t)expert * SK_EXPERT + SK_DOWN_OFF +
-                             ((size_t)(rg >> 4) * (I / 64) + lane) * SK_TILE + (size_t)((rg & 15) * 8) * 128;
-        bulk_g2s(reinterpret_cast<uint8_t*>(d) + lane * 1024, src, 1024, reinterpret_cast<uint64_t*>(b));
-    }
+    if (!pr.take(s, SK_SLOT, &dst, &bar)) return false;
+    tc::tma_load_4d(dst, &maps[1], 0, (rg & 15) * 8, SK_GU_TILES + (rg >> 4) * (I / 64), expert, bar);
     return true;
 }
 
 __device__ void sk_producer(const SkState& s, int lane) {
+    if (lane != 0) return;
     SkProducer pr;
     const StackParams& p = *s.p;
-    bool ok = sk_issue_router(s, pr, 0, lane);
-    if (ok && sk_has_sg(s.c)) ok = sk_issue_gateup(s, pr, p.layer[0].tiled, SHARED, s.c, lane);
+    bool ok = sk_issue_router(s, pr, 0);
+    if (ok && sk_has_sg(s.c)) ok = sk_issue_gateup(s, pr, p.layer[0].maps, SHARED, s.c);
     for (int l = 0; ok && l < p.n_layers; ++l) {
         // the consumers publish the layer's tables
-        int got = 1;
-        if (lane == 0) got = sk_wait(s, &s.sh->route_bar, l & 1);
-        if (!__shfl_sync(0xFFFFFFFFu, got, 0)) break;
+        if (!sk_wait(s, &s.sh->route_bar, l & 1)) break;
         const DecodeTables& tab = s.sh->tab;
         const int U = tab.n_slots - 1;
-        const uint8_t* tiled = p.layer[l].tiled;
+        const CUtensorMap* maps = p.layer[l].maps;
         const int k0 = sk_rcum(s.c - 1, s.G, U), k1 = sk_rcum(s.c, s.G, U);
         for (int k = k0; ok && k < k1; ++k)
-            ok = sk_issue_gateup(s, pr, tiled, tab.slot_expert[1 + k / SK_GU_UNITS], k % SK_GU_UNITS, lane);
+            ok = sk_issue_gateup(s, pr, maps, tab.slot_expert[1 + k / SK_GU_UNITS], k % SK_GU_UNITS);
         const int nrg = sk_n_rg(s.c, s.G);
         for (int u = 0; ok && u <= U; ++u)
-            for (int i = 0; ok && i < nrg; ++i)
-                ok = sk_issue_down(s, pr, tiled, tab.slot_expert[u], sk_rg(s.c, s.G, i), lane);
+            for (int i = 0; ok && i < nrg; ++i) ok = sk_issue_down(s, pr, maps, tab.slot_expert[u], sk_rg(s.c, s.G, i));
         if (ok && l + 1 < p.n_layers) {
-            ok = sk_issue_router(s, pr, l + 1, lane);
-            if (ok && sk_has_sg(s.c)) ok = sk_issue_gateup(s, pr, p.layer[l + 1].tiled, SHARED, s.c, lane);
+            ok = sk_issue_router(s, pr, l + 1);
+            if (ok && sk_has_sg(s.c)) ok = sk_issue_gateup(s, pr, p.layer[l + 1].maps, SHARED, s.c);
         }
     }
     // copies still in flight (only after an abort): wait for them before exiting
     // (a slot whose copies were never issued does not complete: short limit)
-    if (lane == 0 && sk_aborted(s)) {
+    if (sk_aborted(s)) {
         const uint32_t first = pr.seq > (uint32_t)s.nslot ? pr.seq - (uint32_t)s.nslot : 0u;
         for (uint32_t q = first; q < pr.seq; ++q)
             mbar_wait_bounded(&s.full[q % s.nslot], (q / s.nslot) & 1, 10000000ull);
     }
-    __syncwarp();
 }
 
 // ---------------------------------------------------------------------------
 // consumers
 // ---------------------------------------------------------------------------
 
-// Gate/up unit q of slot u on the ring slots starting at sequence number sq,
+// Gate/up unit q of slot u on the ring slots starting at sequence number sq
+// (gate rows over column tiles 0..15, 16..31, then the up rows likewise),
 // column tiles [kt0, kt1) only (the shared unit is split over the warps).
 // acc receives D[token][n] for weight rows n = (gate r, up r) interleaved.
 __device__ __forceinline__ bool sk_gateup_mma(const SkState& s, uint32_t sq, int q, int kt0, int kt1, int lane,
@@ -380,18 +347,21 @@ __device__ __forceinline__ bool sk_gateup_mma(const SkState& s, uint32_t sq, int
     // A (x rows by token): row r + 8 (m & 1), 16-byte chunk (m >> 1) of the k-step
     const int ta = r + 8 * (m & 1);
     const uint8_t* xa = s.ubuf + (size_t)(ta < s.T ? ta : 0) * SK_XSTRIDE + (m >> 1) * 16;
-    // B (weight rows): n = r: gate row 4q + r / 2 (r even) or up row (r odd)
+    // B (weight rows): n = r: gate row 4q + r / 2 (r even) or the up row (r odd)
     const int rr = (4 * q + (r >> 1)) & 127;
-    const uint32_t boff = (uint32_t)((r & 1) * 512 + (r >> 1) * 128);
+    const uint32_t boff = (uint32_t)((r >> 1) * 128);
     float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
     int waited = -1;
+    const uint8_t* bslot = nullptr;
     for (int kt = kt0; kt < kt1; ++kt) {
-        const int sk = kt >> 3;
-        if (sk != waited) {
-            if (!__all_sync(0xFFFFFFFFu, sk_wait_full(s, sq + (uint32_t)sk))) return false;
-            waited = sk;
+        const int half = kt >> 4;
+        if (half != waited) {
+            const bool got = sk_wait_full(s, sq + (uint32_t)half) && sk_wait_full(s, sq + 2u + (uint32_t)half);
+            if (!__all_sync(0xFFFFFFFFu, got)) return false;
+            waited = half;
+            bslot = s.ring + (size_t)((sq + (uint32_t)(2 * (r & 1) + half)) % s.nslot) * SK_SLOT + boff;
         }
-        const uint8_t* piece = s.ring + (size_t)((sq + sk) % s.nslot) * SK_SLOT + (kt & 7) * 1024 + boff;
+        const uint8_t* piece = bslot + (kt & 15) * 512;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {     // two 32-column halves of the 64-column tile
             uint32_t b[4], a[4], a2[4];

@@ -93,25 +93,28 @@ def test_stack_call_matches_oracle_every_layer(stack, T, kind, seed):
 
 
 def test_stack_call_chained_layers_read_the_previous_output(stack):
-    """x[l + 1] = y[l]: every layer must see the complete output of the layer
-    before it (the launch separates layers by a grid-wide barrier).  Each
+    """Every odd layer reads the output of the layer before it (x[l] = y[l - 1]),
+    every even layer the fresh x: each layer must see the complete output of
+    the one before (the launch separates layers by a grid-wide barrier).  A
+    layer of this stack maps an RMS-1 input to an output of RMS ~0.3 and
+    shrinks faster below that, so chains deeper than a few layers leave the
+    normal bf16 range; one step of chaining keeps every value normal.  Each
     layer is checked against the oracle on the input the device consumed."""
     layers, handles = stack
-    T, n = 4, 6
+    T = 4
     xb = gen.x_gaussian(31, T)
     x0 = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
-    ys = [torch.full_like(x0, float("nan")) for _ in range(n)]
-    xs = [x0] + ys[:-1]
-    flint.flint_moe_forward_layers(handles[:n], xs, T, ys)
+    ys = [torch.full_like(x0, float("nan")) for _ in range(N_LAYERS)]
+    xs = [x0 if l % 2 == 0 else ys[l - 1] for l in range(N_LAYERS)]
+    flint.flint_moe_forward_layers(handles, xs, T, ys)
     torch.cuda.synchronize()
-    inp = xb
-    for l in range(n):
+    for l in range(N_LAYERS):
         y = ys[l].float().cpu().numpy()
         assert np.isfinite(y).all(), l
+        inp = xb if l % 2 == 0 else ys[l - 1].view(torch.int16).cpu().numpy().view(np.uint16)
         ref, alt = LayerOracle.from_bf16_layer(layers[l]).forward_with_alternatives(inp)
         res = compare(y, ref, alt)
         assert res["ok"], (l, res)
-        inp = ys[l].view(torch.int16).cpu().numpy().view(np.uint16)
 
 
 def test_stack_call_graph_replay_is_bit_identical(stack):
