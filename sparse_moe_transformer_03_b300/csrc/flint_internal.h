@@ -70,7 +70,7 @@ cudaError_t launch_perm_scan_scatter(const LaunchCtx& L, const int32_t* idx, int
 bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t pitch,
                     uint32_t box_rows, uint32_t box_cols);
 
-bool encode_tiled_experts_4d(CUtensorMap* map, const void* tiled, uint32_t box_rows, uint32_t box_tiles);
+bool encode_tiled_experts_4d(CUtensorMap* map, const void* tiled, uint32_t box_quads, uint32_t box_tiles);
 
 // repack.cu
 cudaError_t launch_repack_tiled(const __nv_bfloat16* in, __nv_bfloat16* out, int R, int K, cudaStream_t s);
@@ -115,7 +115,7 @@ constexpr int STACK_MAX_T = 8;
 constexpr int STACK_MAX_LAYERS = 64;
 struct StackLayerArgs {
     const CUtensorMap* maps;         // the layer's tiled experts as 4-D tensor maps (device memory):
-                                     // [0] gate/up boxes (4 rows x 16 tiles), [1] down boxes (8 rows x 8 tiles)
+                                     // [0] gate/up boxes (1 row quad x 16 tiles), [1] down boxes (2 quads x 8 tiles)
     const __nv_bfloat16* router;     // [E][H]
     const float* bias;               // [E] or null
     const __nv_bfloat16* x;          // [T][H]

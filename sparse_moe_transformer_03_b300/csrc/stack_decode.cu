@@ -70,7 +70,9 @@ __host__ __device__ __forceinline__ int sk_act_index(int p, int j) {
 }
 
 struct SkShared {
-    DecodeTables tab;
+    DecodeTables tab;                             // n_slots, n_pairs, slot_expert, slot_pair0 are used
+    int slot_of[E];                               // slot of each routed expert of the batch
+    float bias[STACK_MAX_LAYERS][2];              // router bias of this CTA's experts, every layer
     int sel_e[STACK_MAX_T * TOPK];
     float sel_w[STACK_MAX_T * TOPK];
     uint32_t tmask[E];
@@ -240,6 +242,75 @@ __device__ __forceinline__ int sk_rcum(int c, int G, int U) {
     return r < 0 ? 0 : r;
 }
 
+// Slots and pairs of a batch of T <= 8 tokens from their top-6 (one warp):
+// slot 0 is the shared expert (pair t = token t), then the routed experts by
+// increasing id, each with its tokens in increasing order.  tok_pair[u][t] /
+// tok_w[u][t]: the pair and routing weight of token t in slot u (-1 / 0 when
+// t is not routed there).  Every lane works on its own experts and pairs.
+__device__ void sk_build_tables(int T, SkShared* sh, int lane) {
+    DecodeTables* tab = &sh->tab;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) sh->tmask[lane * 8 + k] = 0u;
+    __syncwarp();
+    for (int p = lane; p < T * TOPK; p += 32) atomicOr(&sh->tmask[sh->sel_e[p]], 1u << (p / TOPK));
+    __syncwarp();
+    uint32_t m[8];
+    int pres = 0, sum = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        m[k] = sh->tmask[lane * 8 + k];
+        pres += m[k] != 0u;
+        sum += __popc(m[k]);
+    }
+    int ip = pres, is = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int a = __shfl_up_sync(0xFFFFFFFFu, ip, o);
+        const int b = __shfl_up_sync(0xFFFFFFFFu, is, o);
+        if (lane >= o) {
+            ip += a;
+            is += b;
+        }
+    }
+    int slot = 1 + ip - pres, pr = T + is - sum;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int e = lane * 8 + k;
+        sh->pair0[e] = pr;
+        if (m[k]) {
+            tab->slot_expert[slot] = e;
+            tab->slot_pair0[slot] = pr;
+            sh->slot_of[e] = slot;
+            ++slot;
+            pr += __popc(m[k]);
+        }
+    }
+    const int ns = __shfl_sync(0xFFFFFFFFu, slot, 31);
+    if (lane == 31) {
+        tab->n_slots = slot;
+        tab->n_pairs = pr;
+        tab->slot_pair0[slot] = pr;
+        tab->T = T;
+        tab->slot_expert[0] = SHARED;
+        tab->slot_pair0[0] = 0;
+    }
+    for (int i = lane; i < ns * STACK_MAX_T; i += 32) {
+        sh->tok_pair[i / STACK_MAX_T][i % STACK_MAX_T] = -1;
+        sh->tok_w[i / STACK_MAX_T][i % STACK_MAX_T] = 0.f;
+    }
+    __syncwarp();
+    if (lane < T) {
+        sh->tok_pair[0][lane] = lane;
+        sh->tok_w[0][lane] = 1.f;
+    }
+    for (int p = lane; p < T * TOPK; p += 32) {
+        const int t = p / TOPK, e = sh->sel_e[p], u = sh->slot_of[e];
+        sh->tok_pair[u][t] = sh->pair0[e] + __popc(sh->tmask[e] & ((1u << t) - 1u));
+        sh->tok_w[u][t] = sh->sel_w[p];
+    }
+    __syncwarp();
+}
+
 // ---------------------------------------------------------------------------
 // producer
 // ---------------------------------------------------------------------------
@@ -252,7 +323,6 @@ struct SkProducer {
         const int slot = (int)(seq % (uint32_t)s.nslot);
         const uint32_t use = seq / (uint32_t)s.nslot;
         if (use > 0 && !sk_wait(s, &s.empty[slot], (use - 1) & 1)) return false;
-        fence_proxy_async_smem();
         mbar_arrive_expect_tx(&s.full[slot], bytes);
         st_release_shared(&s.sh->slot_seq[slot], seq + 1u);
         *dst = s.ring + (size_t)slot * SK_SLOT;
@@ -285,7 +355,7 @@ __device__ __forceinline__ bool sk_issue_gateup(const SkState& s, SkProducer& pr
         uint64_t* bar = nullptr;
         if (!pr.take(s, SK_SLOT, &dst, &bar)) return false;
         const int tile = ((k >> 1) * 4 + rb) * (H / 64) + (k & 1) * 16;   // up rows: row blocks 4..7
-        tc::tma_load_4d(dst, &maps[0], 0, r0 & 127, tile, expert, bar);
+        tc::tma_load_4d(dst, &maps[0], 0, (r0 & 127) >> 2, tile, expert, bar);
     }
     return true;
 }
@@ -297,7 +367,7 @@ __device__ __forceinline__ bool sk_issue_down(const SkState& s, SkProducer& pr, 
     uint8_t* dst = nullptr;
     uint64_t* bar = nullptr;
     if (!pr.take(s, SK_SLOT, &dst, &bar)) return false;
-    tc::tma_load_4d(dst, &maps[1], 0, (rg & 15) * 8, SK_GU_TILES + (rg >> 4) * (I / 64), expert, bar);
+    tc::tma_load_4d(dst, &maps[1], 0, (rg & 15) * 2, SK_GU_TILES + (rg >> 4) * (I / 64), expert, bar);
     return true;
 }
 
@@ -406,6 +476,12 @@ __device__ void sk_consumers(const SkState& s, int warp, int lane) {
     const StackParams& p = *s.p;
     const int T = s.T, c = s.c, G = s.G, tid = warp * 32 + lane;
     SkShared* sh = s.sh;
+    // router bias of this CTA's experts for every layer (weights: read before
+    // the dependency wait)
+    for (int i = tid; i < p.n_layers * 2; i += SK_CW * 32) {
+        const int l = i >> 1, e = c + (i & 1) * G;
+        sh->bias[l][i & 1] = (e < E && p.layer[l].bias) ? __ldg(p.layer[l].bias + e) : 0.f;
+    }
     pdl_wait();
     // the barrier counter's value at the launch, rounded down to the grid: every
     // CTA reads it before its own first arrival, when fewer than G have arrived
@@ -454,7 +530,7 @@ __device__ void sk_consumers(const SkState& s, int warp, int lane) {
                 }
                 acc = warp_sum(acc);
                 if (lane == 0) {
-                    const float v = acc + (Ly.bias ? __ldg(Ly.bias + e) : 0.f);
+                    const float v = acc + sh->bias[l][i];
                     st_relaxed_u64(p.logits + (size_t)t * E + e,
                                    ((unsigned long long)tag << 32) | (unsigned long long)__float_as_uint(v));
                 }
@@ -525,20 +601,7 @@ __device__ void sk_consumers(const SkState& s, int warp, int lane) {
         if (sk_phase_end(s, fail)) break;
         // ---- 5. tables: slots (shared first, then the routed experts by id), pairs ----
         if (warp == 0) {
-            build_decode_tables_warp(T, sh->sel_e, sh->sel_w, sh->tmask, sh->pair0, &sh->tab, lane);
-            const int ns = sh->tab.n_slots;
-            for (int i = lane; i < ns * STACK_MAX_T; i += 32) {
-                sh->tok_pair[i / STACK_MAX_T][i % STACK_MAX_T] = -1;
-                sh->tok_w[i / STACK_MAX_T][i % STACK_MAX_T] = 0.f;
-            }
-            __syncwarp();
-            for (int u = 0; u < ns; ++u)
-                for (int pp = sh->tab.slot_pair0[u] + lane; pp < sh->tab.slot_pair0[u + 1]; pp += 32) {
-                    const int t = sh->tab.pair_token[pp];
-                    sh->tok_pair[u][t] = pp;
-                    sh->tok_w[u][t] = sh->tab.pair_weight[pp];
-                }
-            __syncwarp();
+            sk_build_tables(T, sh, lane);
             if (lane == 0) mbar_arrive(&sh->route_bar);
         }
         if (sk_phase_end(s, false)) break;

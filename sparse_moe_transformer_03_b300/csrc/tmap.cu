@@ -35,17 +35,19 @@ bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The handle's tiled experts (repack.cu) as a 4-D bf16 tensor: 64 columns x
-// 128 rows x 384 tiles (256 gate/up tiles, then 128 down tiles) x 257
-// experts, no swizzle (the bytes are already in the tensor core's order), so
-// one box of box_rows rows x box_tiles consecutive tiles lands in shared
-// memory as [tile][row][128 bytes].
-bool encode_tiled_experts_4d(CUtensorMap* map, const void* tiled, uint32_t box_rows, uint32_t box_tiles) {
+// The handle's tiled experts (repack.cu) as a 4-D bf16 tensor whose
+// innermost line is four tile rows (512 bytes, contiguous in a tile): 256
+// elements x 32 row quads x 384 tiles (256 gate/up tiles, then 128 down
+// tiles) x 257 experts, no swizzle (the bytes are already in the tensor
+// core's order).  A box of box_quads quads x box_tiles consecutive tiles
+// lands in shared memory as [tile][quad][512 bytes]; each 512-byte line is
+// one request of the copy engine.
+bool encode_tiled_experts_4d(CUtensorMap* map, const void* tiled, uint32_t box_quads, uint32_t box_tiles) {
     auto fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t gdim[4] = {64, 128, 384, 257};
-    cuuint64_t gstride[3] = {128, 16384, (cuuint64_t)384 * 16384};
-    cuuint32_t box[4] = {64, box_rows, box_tiles, 1};
+    cuuint64_t gdim[4] = {256, 32, 384, 257};
+    cuuint64_t gstride[3] = {512, 16384, (cuuint64_t)384 * 16384};
+    cuuint32_t box[4] = {256, box_quads, box_tiles, 1};
     cuuint32_t estride[4] = {1, 1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(tiled), gdim, gstride, box, estride,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
