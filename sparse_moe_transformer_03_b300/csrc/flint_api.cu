@@ -253,7 +253,7 @@ flint_status_t flint_moe_create(flint_moe_t* out, const void* router_W, const fl
     if (st == FLINT_OK && dtype == FLINT_BF16) {
         // the tiled experts as 4-D tensors for the persistent stack kernel
         CUtensorMap maps[2];
-        if (!encode_tiled_experts_4d(&maps[0], h->tiled, 1, 16) || !encode_tiled_experts_4d(&maps[1], h->tiled, 2, 8) ||
+        if (!encode_tiled_experts_4d(&maps[0], h->tiled, 2, 16) || !encode_tiled_experts_4d(&maps[1], h->tiled, 4, 8) ||
             cudaMemcpy(h->stack_maps, maps, sizeof maps, cudaMemcpyHostToDevice) != cudaSuccess)
             st = FLINT_ERR_CUDA;
     }

@@ -115,7 +115,7 @@ constexpr int STACK_MAX_T = 8;
 constexpr int STACK_MAX_LAYERS = 64;
 struct StackLayerArgs {
     const CUtensorMap* maps;         // the layer's tiled experts as 4-D tensor maps (device memory):
-                                     // [0] gate/up boxes (1 row quad x 16 tiles), [1] down boxes (2 quads x 8 tiles)
+                                     // [0] gate/up boxes (8 rows x 16 tiles), [1] down boxes (16 rows x 8 tiles)
     const __nv_bfloat16* router;     // [E][H]
     const float* bias;               // [E] or null
     const __nv_bfloat16* x;          // [T][H]

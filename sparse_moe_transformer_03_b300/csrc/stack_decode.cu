@@ -17,29 +17,30 @@
 //      (prefetched during the previous layer) with every token and publishes
 //      the fp32 logits as 64-bit words tagged with the layer's epoch, so the
 //      other CTAs read them as soon as they land (no barrier);
-//   2. meanwhile the shared expert's gate/up unit of the CTA (prefetched too)
-//      is multiplied; every CTA then waits for the 256 tagged logits of each
-//      token, takes the top-6 (warp_top6) and builds the (slot, token) tables;
+//   2. meanwhile CTAs 0..63 multiply their unit of the shared expert
+//      (prefetched too); every CTA then waits for the 256 tagged logits of
+//      each token, takes the top-6 (warp_top6) and builds the (slot, token)
+//      tables;
 //   3. a producer warp streams the CTA's routed gate/up units and then its
-//      down row groups into a ring of 8 KiB slots by cp.async.bulk; eight
-//      consumer warps multiply them on the warp-level tensor core
-//      (mma.sync m16n8k16, tokens as the M rows, weight rows as the 8 N
-//      columns) and write a = silu(g) * u (bf16) to a global buffer;
+//      down row group of every slot into a ring of 16 KiB slots, one TMA
+//      tensor box per slot; eight consumer warps multiply them on the
+//      warp-level tensor core (mma.sync m16n8k16: 16 weight rows x 16
+//      columns against up to 8 tokens), the K dimension split over the
+//      warps, and write a = silu(g) * u (bf16) to a global buffer;
 //   4. grid barrier; the CTA copies every pair's activations into shared
-//      memory and applies its down row groups (8 output rows x all slots,
-//      the routing weight folded in per token, slots summed in order):
-//      y is written once, deterministically;
+//      memory and applies its 16 down rows to every slot (the routing weight
+//      folded in per token, each warp summing its K slice over the slots in
+//      order, then the warps in order): y is written once, deterministically;
 //   5. grid barrier (layer l + 1 may read y_l), while the producer already
 //      streams layer l + 1's router rows and shared-expert unit.
 //
-// Work split: a gate/up unit is 4 gate rows + the 4 matching up rows x 2048
-// columns (32 KiB); an expert has 128.  CTA c owns shared unit c (c < 128)
-// and a contiguous range of the routed units chosen so every CTA gets the
-// same number of units.  A down row group is 8 rows of Wd x 512 columns
-// (8 KiB per slot); CTA c owns row groups c and c + G.  Every output element
-// is produced by one CTA, so nothing is reduced across CTAs.  The ring is
-// deep (about 200 KiB at T = 1): a CTA requests most of its bytes at once
-// and the GPU-wide HBM bandwidth, not the per-CTA split, sets the pace.
+// Work split, in 16 KiB blocks: a gate/up unit is 8 gate rows + the 8
+// matching up rows x 2048 columns (4 blocks, 64 units per expert); a down
+// item is 16 rows of Wd x 512 columns (1 block, 128 per expert).  CTA c < 64
+// owns shared unit c, CTA c < 128 owns down rows 16c .. 16c + 15 of every
+// slot, and the routed units are dealt in contiguous ranges so that every CTA
+// has the same number of blocks.  Every output element is produced by one
+// CTA: nothing is reduced across CTAs.
 #include "flint_common.cuh"
 #include "../../include/flint_moe.h"
 #include "flint_internal.h"
@@ -55,16 +56,17 @@ namespace {
 
 constexpr int SK_CW = 8;                          // consumer warps
 constexpr int SK_THREADS = (SK_CW + 1) * 32;      // + one producer warp
-constexpr int SK_SLOT = 8192;                     // ring slot bytes
-constexpr int SK_GU_UNITS = I / 4;                // 128 gate/up units per expert
-constexpr int SK_RG = H / 8;                      // 256 down row groups per expert
+constexpr int SK_SLOT = 16384;                    // ring slot bytes: one tensor box
+constexpr int SK_GU_UNITS = I / 8;                // 64 gate/up units per expert
+constexpr int SK_DN_ITEMS = H / 16;               // 128 down row groups per expert
 constexpr int SK_GU_TILES = (2 * I / 128) * (H / 64);  // 256 gate/up tiles of an expert precede its down tiles
 constexpr int SK_XSTRIDE = H * 2 + 16;            // padded x row in shared memory
 constexpr int SK_MAX_SLOTS = 1 + STACK_MAX_T * TOPK;   // 49
+constexpr int SK_MAX_RING = 16;
 constexpr int SK_NAMED = 1;                       // named barrier of the consumer warps
 
 // Activation rows: pair p's 512 bf16, its 16-byte chunk c stored at c ^ (p % 8)
-// (the tokens of one MMA read eight rows through different banks).
+// (the eight token rows of one MMA operand read through different banks).
 __host__ __device__ __forceinline__ int sk_act_index(int p, int j) {
     return p * I + ((((j >> 3) ^ (p & 7))) << 3) + (j & 7);
 }
@@ -79,22 +81,19 @@ struct SkShared {
     int pair0[E];
     int tok_pair[SK_MAX_SLOTS][STACK_MAX_T];      // pair of (slot, token), -1: token not routed there
     float tok_w[SK_MAX_SLOTS][STACK_MAX_T];       // its routing weight (0 when not routed)
-    alignas(16) float part[SK_CW][128];           // per-warp partial sums (shared unit: [lane][4], read
-                                                  // as float4; down: [row group][token][row])
+    alignas(16) float part[2][SK_CW][32 * 4];     // per-warp partial sums (gate/up: by unit parity;
+                                                  // down: [0][warp][lane x 4])
     uint64_t route_bar;                           // consumers -> producer: tables of the layer are built
     // Ring slot i was last handed out for sequence number slot_seq[i] - 1.  A
     // consumer waits for its sequence number here before the slot's full
-    // barrier: several warps consume the ring, so one may reach use u of a
-    // slot before use u - 1 has landed, and a parity wait for phase u would
-    // then succeed on phase u - 1.
-    uint32_t slot_seq[32];
+    // barrier, so a parity wait never mistakes an older phase for its own.
+    uint32_t slot_seq[SK_MAX_RING];
     int abort;
 };
-
 static_assert(offsetof(SkShared, part) % 16 == 0, "float4 access to the partial sums");
 static_assert(offsetof(SkShared, route_bar) % 8 == 0, "mbarrier alignment");
 
-// 128 x 64 tile-copy offsets (repack.cu layout): in-tile row r, 16-byte chunk c
+// 128-byte rows of the tiled layout: in-tile row r keeps its 16-byte chunk c at c ^ (r % 8)
 __device__ __forceinline__ uint32_t sw_chunk(int r, int c) { return (uint32_t)(((c ^ (r & 7)) << 4)); }
 
 __device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
@@ -108,6 +107,14 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
     unsigned long long v;
     asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_shared(uint32_t* p, uint32_t v) {
+    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_shared(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
     return v;
 }
 
@@ -125,13 +132,13 @@ __host__ __device__ __forceinline__ uint32_t sk_ubuf_bytes(int T) {
 
 __host__ __device__ __forceinline__ SkLayout sk_layout(int T, uint32_t max_smem) {
     SkLayout L;
-    const uint32_t fixed = sk_ubuf_bytes(T) + (uint32_t)((sizeof(SkShared) + 127) & ~size_t(127));
-    int ns = (int)((max_smem - fixed - 64 * 16) / (SK_SLOT + 16));
-    if (ns > 32) ns = 32;
+    const uint32_t fixed = sk_ubuf_bytes(T) + (uint32_t)((sizeof(SkShared) + 127) & ~size_t(127)) + 256;
+    int ns = (int)((max_smem - fixed) / SK_SLOT);
+    if (ns > SK_MAX_RING) ns = SK_MAX_RING;
     L.nslot = ns;
     L.ubuf_off = (uint32_t)ns * SK_SLOT;
     L.bars_off = L.ubuf_off + sk_ubuf_bytes(T);
-    L.sh_off = L.bars_off + (uint32_t)(((2 * ns * 8) + 127) & ~127);
+    L.sh_off = L.bars_off + 256;                  // 2 x SK_MAX_RING mbarriers
     L.total = L.sh_off + (uint32_t)((sizeof(SkShared) + 127) & ~size_t(127));
     return L;
 }
@@ -172,15 +179,6 @@ __device__ __forceinline__ bool sk_wait(const SkState& s, uint64_t* bar, uint32_
     }
 }
 
-__device__ __forceinline__ void st_release_shared(uint32_t* p, uint32_t v) {
-    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
-}
-__device__ __forceinline__ uint32_t ld_acquire_shared(const uint32_t* p) {
-    uint32_t v;
-    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
-    return v;
-}
-
 // Wait until ring sequence number q has landed in its slot: first until the
 // producer has handed the slot out for q (so the slot's full barrier is at
 // q's phase or past it), then on the full barrier.
@@ -202,6 +200,16 @@ __device__ __forceinline__ bool sk_wait_full(const SkState& s, uint32_t q) {
     }
 issued:
     return sk_wait(s, &s.full[slot], (q / (uint32_t)s.nslot) & 1);
+}
+
+__device__ __forceinline__ uint8_t* sk_slot_ptr(const SkState& s, uint32_t q) {
+    return s.ring + (size_t)(q % (uint32_t)s.nslot) * SK_SLOT;
+}
+
+// Release ring sequence number q (every consumer warp arrives once).
+__device__ __forceinline__ void sk_release(const SkState& s, uint32_t q, int lane) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&s.empty[q % (uint32_t)s.nslot]);
 }
 
 // Grid barrier (one thread, after the consumer warps synchronised): arrive,
@@ -227,19 +235,21 @@ __device__ bool sk_grid_barrier(const SkState& s, unsigned long long target) {
 
 __device__ __forceinline__ int sk_router_rows(int c, int G) { return (c < E ? 1 : 0) + (c + G < E ? 1 : 0); }
 __device__ __forceinline__ int sk_has_sg(int c) { return c < SK_GU_UNITS ? 1 : 0; }
-__device__ __forceinline__ int sk_n_rg(int c, int G) { return (c < SK_RG ? 1 : 0) + (c + G < SK_RG ? 1 : 0); }
-__device__ __forceinline__ int sk_rg(int c, int G, int i) { return c + i * G; }
+__device__ __forceinline__ int sk_has_dn(int c) { return c < SK_DN_ITEMS ? 1 : 0; }
 
-// End of CTA c's range of routed gate/up units (units of slot 1.. in order):
-// the cumulative share of all (U + 1) x 128 units minus the shared units the
-// CTAs up to c own.
-__device__ __forceinline__ int sk_rcum(int c, int G, int U) {
+// End of CTA c's range of routed gate/up units (the units of slots 1..U in
+// order): every CTA's share of all 16 KiB blocks of the layer (4 per gate/up
+// unit, 1 per down item) minus the shared units and down items that the CTAs
+// up to c own.  Non-decreasing in c for U >= 1 and equal to 64 U at the last
+// CTA (checked on the host for every U).
+__host__ __device__ __forceinline__ int sk_rcum(int c, int G, int U) {
     if (c < 0) return 0;
-    const int ntot = SK_GU_UNITS * (U + 1);
-    const int tcum = (int)(((long long)(c + 1) * ntot) / G);
-    const int scum = c + 1 < SK_GU_UNITS ? c + 1 : SK_GU_UNITS;
-    const int r = tcum - scum;
-    return r < 0 ? 0 : r;
+    const int total = (4 * SK_GU_UNITS + SK_DN_ITEMS) * (U + 1);
+    const int bcum = (int)(((long long)(c + 1) * total) / G);
+    const int scum = 4 * (c + 1 < SK_GU_UNITS ? c + 1 : SK_GU_UNITS);
+    const int dcum = (c + 1 < SK_DN_ITEMS ? c + 1 : SK_DN_ITEMS) * (U + 1);
+    const int r = (bcum - scum - dcum) >> 2;
+    return r < 0 ? 0 : (r > SK_GU_UNITS * U ? SK_GU_UNITS * U : r);
 }
 
 // Slots and pairs of a batch of T <= 8 tokens from their top-6 (one warp):
@@ -312,13 +322,13 @@ __device__ void sk_build_tables(int T, SkShared* sh, int lane) {
 }
 
 // ---------------------------------------------------------------------------
-// producer
+// producer (lane 0 of the producer warp)
 // ---------------------------------------------------------------------------
 
 struct SkProducer {
     uint32_t seq = 0;   // ring slots handed out so far
 
-    // Take the next slot for a copy of `bytes`; lane 0 only.
+    // Take the next slot for a copy of `bytes`.
     __device__ __forceinline__ bool take(const SkState& s, uint32_t bytes, uint8_t** dst, uint64_t** bar) {
         const int slot = (int)(seq % (uint32_t)s.nslot);
         const uint32_t use = seq / (uint32_t)s.nslot;
@@ -332,7 +342,7 @@ struct SkProducer {
     }
 };
 
-// Router rows of CTA c for layer l (one slot, plain bulk copies).  Lane 0 only.
+// Router rows of CTA c for layer l (one slot, plain bulk copies).
 __device__ __forceinline__ bool sk_issue_router(const SkState& s, SkProducer& pr, int l) {
     const int nr = sk_router_rows(s.c, s.G);
     if (nr == 0) return true;
@@ -344,12 +354,11 @@ __device__ __forceinline__ bool sk_issue_router(const SkState& s, SkProducer& pr
     return true;
 }
 
-// One gate/up unit (4 slots, one 8 KiB tensor box each): gate rows 4q ..
-// 4q + 3 over column tiles 0..15 and 16..31, then the matching up rows.
-// Lane 0 only.
+// Gate/up unit q of an expert: 4 slots, one box each: gate rows 8q .. 8q + 7
+// over column tiles 0..15 and 16..31, then the matching up rows likewise.
 __device__ __forceinline__ bool sk_issue_gateup(const SkState& s, SkProducer& pr, const CUtensorMap* maps,
                                                 int expert, int q) {
-    const int r0 = 4 * q, rb = r0 >> 7;
+    const int r0 = 8 * q, rb = r0 >> 7;
     for (int k = 0; k < 4; ++k) {
         uint8_t* dst = nullptr;
         uint64_t* bar = nullptr;
@@ -360,14 +369,13 @@ __device__ __forceinline__ bool sk_issue_gateup(const SkState& s, SkProducer& pr
     return true;
 }
 
-// One down row group of one expert (one slot, one 8 KiB box: 8 rows x the 8
-// column tiles of K = 512).  Lane 0 only.
+// Down rows 16 g .. 16 g + 15 of an expert (one slot: the 8 column tiles of K = 512).
 __device__ __forceinline__ bool sk_issue_down(const SkState& s, SkProducer& pr, const CUtensorMap* maps, int expert,
-                                              int rg) {
+                                              int g) {
     uint8_t* dst = nullptr;
     uint64_t* bar = nullptr;
     if (!pr.take(s, SK_SLOT, &dst, &bar)) return false;
-    tc::tma_load_4d(dst, &maps[1], 0, (rg & 15) * 2, SK_GU_TILES + (rg >> 4) * (I / 64), expert, bar);
+    tc::tma_load_4d(dst, &maps[1], 0, (g & 7) * 4, SK_GU_TILES + (g >> 3) * (I / 64), expert, bar);
     return true;
 }
 
@@ -386,9 +394,8 @@ __device__ void sk_producer(const SkState& s, int lane) {
         const int k0 = sk_rcum(s.c - 1, s.G, U), k1 = sk_rcum(s.c, s.G, U);
         for (int k = k0; ok && k < k1; ++k)
             ok = sk_issue_gateup(s, pr, maps, tab.slot_expert[1 + k / SK_GU_UNITS], k % SK_GU_UNITS);
-        const int nrg = sk_n_rg(s.c, s.G);
-        for (int u = 0; ok && u <= U; ++u)
-            for (int i = 0; ok && i < nrg; ++i) ok = sk_issue_down(s, pr, maps, tab.slot_expert[u], sk_rg(s.c, s.G, i));
+        if (sk_has_dn(s.c))
+            for (int u = 0; ok && u <= U; ++u) ok = sk_issue_down(s, pr, maps, tab.slot_expert[u], s.c);
         if (ok && l + 1 < p.n_layers) {
             ok = sk_issue_router(s, pr, l + 1);
             if (ok && sk_has_sg(s.c)) ok = sk_issue_gateup(s, pr, p.layer[l + 1].maps, SHARED, s.c);
@@ -407,56 +414,6 @@ __device__ void sk_producer(const SkState& s, int lane) {
 // consumers
 // ---------------------------------------------------------------------------
 
-// Gate/up unit q of slot u on the ring slots starting at sequence number sq
-// (gate rows over column tiles 0..15, 16..31, then the up rows likewise),
-// column tiles [kt0, kt1) only (the shared unit is split over the warps).
-// acc receives D[token][n] for weight rows n = (gate r, up r) interleaved.
-__device__ __forceinline__ bool sk_gateup_mma(const SkState& s, uint32_t sq, int q, int kt0, int kt1, int lane,
-                                              float (&acc)[4]) {
-    const int m = lane >> 3, r = lane & 7;
-    // A (x rows by token): row r + 8 (m & 1), 16-byte chunk (m >> 1) of the k-step
-    const int ta = r + 8 * (m & 1);
-    const uint8_t* xa = s.ubuf + (size_t)(ta < s.T ? ta : 0) * SK_XSTRIDE + (m >> 1) * 16;
-    // B (weight rows): n = r: gate row 4q + r / 2 (r even) or the up row (r odd)
-    const int rr = (4 * q + (r >> 1)) & 127;
-    const uint32_t boff = (uint32_t)((r >> 1) * 128);
-    float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
-    int waited = -1;
-    const uint8_t* bslot = nullptr;
-    for (int kt = kt0; kt < kt1; ++kt) {
-        const int half = kt >> 4;
-        if (half != waited) {
-            const bool got = sk_wait_full(s, sq + (uint32_t)half) && sk_wait_full(s, sq + 2u + (uint32_t)half);
-            if (!__all_sync(0xFFFFFFFFu, got)) return false;
-            waited = half;
-            bslot = s.ring + (size_t)((sq + (uint32_t)(2 * (r & 1) + half)) % s.nslot) * SK_SLOT + boff;
-        }
-        const uint8_t* piece = bslot + (kt & 15) * 512;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {     // two 32-column halves of the 64-column tile
-            uint32_t b[4], a[4], a2[4];
-            ldmatrix_x4(b, piece + sw_chunk(rr, 4 * h + m));
-            const int k0 = kt * 64 + 32 * h;
-            ldmatrix_x4(a, xa + (size_t)k0 * 2);
-            ldmatrix_x4(a2, xa + (size_t)(k0 + 16) * 2);
-            mma_bf16_16816(a0, a, b[0], b[1]);
-            mma_bf16_16816(a1, a2, b[2], b[3]);
-        }
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) acc[i] = a0[i] + a1[i];
-    return true;
-}
-
-// a = silu(g) * u of unit q of slot u for the tokens routed to it.
-__device__ __forceinline__ void sk_store_act(const SkState& s, int u, int q, int lane, const float (&d)[4]) {
-    const int g = lane >> 2, cq = lane & 3;
-    if (g < s.T) {
-        const int pp = s.sh->tok_pair[u][g];
-        if (pp >= 0) s.p->act[sk_act_index(pp, 4 * q + cq)] = __float2bfloat16_rn(silu_f(d[0]) * d[1]);
-    }
-}
-
 // End of a phase of the consumer warps: a named barrier that also ORs every
 // consumer thread's failure flag (and the CTA's abort flag as each thread
 // sees it), so all 256 threads take the same branch afterwards.
@@ -470,6 +427,65 @@ __device__ __forceinline__ bool sk_phase_end(const SkState& s, bool fail) {
         : "memory");
     if (r) s.sh->abort = 1;
     return r != 0;
+}
+
+// One gate/up unit (slots sq .. sq + 3: gate tiles 0..15, 16..31, up tiles
+// 0..15, 16..31) against the tokens: warp w multiplies column tiles 4w ..
+// 4w + 3, 16 weight rows (8 gate over 8 up) x 256 columns, into d[] (lane
+// (g, cq): gate row g and up row g for tokens 2 cq and 2 cq + 1).  All 32
+// lanes take part; returns false if a wait gave up.
+__device__ __forceinline__ bool sk_gateup_part(const SkState& s, uint32_t sq, int warp, int lane, float (&d)[4]) {
+    const int half = warp >> 2;
+    const bool got = sk_wait_full(s, sq + (uint32_t)half) && sk_wait_full(s, sq + 2u + (uint32_t)half);
+    if (!__all_sync(0xFFFFFFFFu, got)) return false;
+    const int m = lane >> 3, r = lane & 7;
+    // A: matrix m: row r of the gate (m even) or up (m odd) box, chunk (m >> 1) of the k-step
+    const uint8_t* arow = sk_slot_ptr(s, sq + (uint32_t)(2 * (m & 1) + half)) + r * 128;
+    // B: token rows of x (padding tokens read token 0; their columns are not used)
+    const uint8_t* xrow = s.ubuf + (size_t)(r < s.T ? r : 0) * SK_XSTRIDE + m * 16;
+    float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int kt = 4 * warp + i;                      // column tile 0..31
+        const uint8_t* tile = arow + (kt & 15) * 1024;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {                     // two 32-column halves = two k-step pairs
+            uint32_t a[4], a2[4], b[4];
+            ldmatrix_x4(a, tile + sw_chunk(r, 4 * h + (m >> 1)));
+            ldmatrix_x4(a2, tile + sw_chunk(r, 4 * h + 2 + (m >> 1)));
+            ldmatrix_x4(b, xrow + (size_t)(kt * 64 + 32 * h) * 2);
+            mma_bf16_16816(a0, a, b[0], b[1]);
+            mma_bf16_16816(a1, a2, b[2], b[3]);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d[i] = a0[i] + a1[i];
+    return true;
+}
+
+// The unit's eight partial sums (part[par][w]) added in warp order by one
+// warp; a = silu(gate) * up for the tokens routed to slot u.
+__device__ __forceinline__ void sk_gateup_finish(const SkState& s, int par, int u, int q, int lane) {
+    SkShared* sh = s.sh;
+    float4 sum = *reinterpret_cast<const float4*>(&sh->part[par][0][lane * 4]);
+#pragma unroll
+    for (int w = 1; w < SK_CW; ++w) {
+        const float4 v = *reinterpret_cast<const float4*>(&sh->part[par][w][lane * 4]);
+        sum.x += v.x;
+        sum.y += v.y;
+        sum.z += v.z;
+        sum.w += v.w;
+    }
+    const int g = lane >> 2, cq = lane & 3, j = 8 * q + g;
+    const int t0 = 2 * cq, t1 = 2 * cq + 1;
+    if (t0 < s.T) {
+        const int pp = sh->tok_pair[u][t0];
+        if (pp >= 0) s.p->act[sk_act_index(pp, j)] = __float2bfloat16_rn(silu_f(sum.x) * sum.z);
+    }
+    if (t1 < s.T) {
+        const int pp = sh->tok_pair[u][t1];
+        if (pp >= 0) s.p->act[sk_act_index(pp, j)] = __float2bfloat16_rn(silu_f(sum.y) * sum.w);
+    }
 }
 
 __device__ void sk_consumers(const SkState& s, int warp, int lane) {
@@ -492,7 +508,7 @@ __device__ void sk_consumers(const SkState& s, int warp, int lane) {
     int nbar = 0;
     uint32_t seq = 0;
     const int m = lane >> 3, r = lane & 7;
-    const int g = lane >> 2, cq = lane & 3;
+    const int cq = lane & 3;
     for (int l = 0; l < p.n_layers; ++l) {
         const StackLayerArgs& Ly = p.layer[l];
         const unsigned int tag = (unsigned int)(base / (unsigned long long)G) + (unsigned int)l + 1u;
@@ -510,7 +526,7 @@ __device__ void sk_consumers(const SkState& s, int warp, int lane) {
         seq += nr ? 1 : 0;
         if (nr) {
             fail = !__all_sync(0xFFFFFFFFu, sk_wait_full(s, seqR));
-            const uint8_t* rows = s.ring + (size_t)(seqR % s.nslot) * SK_SLOT;
+            const uint8_t* rows = sk_slot_ptr(s, seqR);
             for (int pi = warp; !fail && pi < nr * T; pi += SK_CW) {
                 const int i = pi / T, t = pi % T, e = c + i * G;
                 const uint4* wr = reinterpret_cast<const uint4*>(rows + i * H * 2);
@@ -535,32 +551,22 @@ __device__ void sk_consumers(const SkState& s, int warp, int lane) {
                                    ((unsigned long long)tag << 32) | (unsigned long long)__float_as_uint(v));
                 }
             }
-            if (sk_phase_end(s, fail)) break;
-            if (tid == 0) mbar_arrive(&s.empty[seqR % s.nslot]);
+            if (!fail) sk_release(s, seqR, lane);
         }
-        // ---- 3. the shared expert's unit of this CTA, its columns split over the warps ----
+        // ---- 3. the shared expert's unit of this CTA (CTAs 0..63) ----
         const int has_sg = sk_has_sg(c);
         const uint32_t seqSG = seq;
         seq += has_sg ? 4 : 0;
-        if (has_sg) {
-            float d[4] = {0.f, 0.f, 0.f, 0.f};
-            fail = !__all_sync(0xFFFFFFFFu, sk_gateup_mma(s, seqSG, c, 4 * warp, 4 * warp + 4, lane, d));
-            *reinterpret_cast<float4*>(&sh->part[warp][lane * 4]) = make_float4(d[0], d[1], d[2], d[3]);
-            if (sk_phase_end(s, fail)) break;
-            if (warp == 0) {
-                float4 sum = *reinterpret_cast<const float4*>(&sh->part[0][lane * 4]);
-                for (int w = 1; w < SK_CW; ++w) {
-                    const float4 v = *reinterpret_cast<const float4*>(&sh->part[w][lane * 4]);
-                    sum.x += v.x;
-                    sum.y += v.y;
-                    sum.z += v.z;
-                    sum.w += v.w;
-                }
-                if (g < T)   // the shared slot holds every token: pair = token
-                    p.act[sk_act_index(g, 4 * c + cq)] = __float2bfloat16_rn(silu_f(sum.x) * sum.y);
-                if (lane < 4) mbar_arrive(&s.empty[(seqSG + lane) % s.nslot]);
+        if (has_sg && !fail) {
+            float d[4];
+            fail = !sk_gateup_part(s, seqSG, warp, lane, d);
+            if (!fail) {
+                for (int k = 0; k < 4; ++k) sk_release(s, seqSG + k, lane);
+                *reinterpret_cast<float4*>(&sh->part[0][warp][lane * 4]) = make_float4(d[0], d[1], d[2], d[3]);
             }
         }
+        if (sk_phase_end(s, fail)) break;
+        if (has_sg && warp == 0) sk_gateup_finish(s, 0, 0, c, lane);
         // ---- 4. every token's 256 logits (tagged with this layer's epoch), top-6 ----
         if (warp < T) {
             float v[8];
@@ -606,23 +612,34 @@ __device__ void sk_consumers(const SkState& s, int warp, int lane) {
         }
         if (sk_phase_end(s, false)) break;
         const int U = sh->tab.n_slots - 1;
-        // ---- 6. routed gate/up units: unit j of the CTA's range goes to warp j % 8 ----
+        // ---- 6. routed gate/up units of the CTA's range, one at a time, K split
+        // over the warps; warp j % 8 finishes unit j ----
         const int k0 = sk_rcum(c - 1, G, U), k1 = sk_rcum(c, G, U);
         const uint32_t seqRG = seq;
         seq += 4u * (uint32_t)(k1 - k0);
-        for (int j = warp; j < k1 - k0 && !fail; j += SK_CW) {
-            const int k = k0 + j, u = 1 + k / SK_GU_UNITS, q = k % SK_GU_UNITS;
+        bool stop = false;
+        for (int j = 0; j < k1 - k0; ++j) {
             float d[4];
-            if (!__all_sync(0xFFFFFFFFu, sk_gateup_mma(s, seqRG + 4u * j, q, 0, H / 64, lane, d))) {
-                fail = true;
+            const uint32_t sq = seqRG + 4u * j;
+            fail = !sk_gateup_part(s, sq, warp, lane, d);
+            if (!fail) {
+                for (int k = 0; k < 4; ++k) sk_release(s, sq + k, lane);
+                *reinterpret_cast<float4*>(&sh->part[j & 1][warp][lane * 4]) = make_float4(d[0], d[1], d[2], d[3]);
+            }
+            if (sk_phase_end(s, fail)) {
+                stop = true;
                 break;
             }
-            __syncwarp();
-            if (lane < 4) mbar_arrive(&s.empty[(seqRG + 4u * j + lane) % s.nslot]);
-            sk_store_act(s, u, q, lane, d);
+            // the parity buffer j & 1 is written again only after the phase end
+            // of unit j + 1, which this warp reaches after the sum
+            if (warp == (j & (SK_CW - 1))) {
+                const int k = k0 + j;
+                sk_gateup_finish(s, j & 1, 1 + k / SK_GU_UNITS, k % SK_GU_UNITS, lane);
+            }
         }
+        if (stop) break;
         // ---- 7. every CTA's activations are written (grid barrier) ----
-        if (sk_phase_end(s, fail)) break;
+        if (sk_phase_end(s, false)) break;
         if (tid == 0) {
             ++nbar;
             if (!sk_grid_barrier(s, base + (unsigned long long)nbar * G)) sh->abort = 1;
@@ -633,56 +650,57 @@ __device__ void sk_consumers(const SkState& s, int warp, int lane) {
         for (int i = tid; i < npairs * (I / 8); i += SK_CW * 32)
             *reinterpret_cast<uint4*>(s.ubuf + (size_t)i * 16) = __ldcg(reinterpret_cast<const uint4*>(p.act) + i);
         if (sk_phase_end(s, false)) break;
-        // ---- 9. down row groups: item (slot u, row group i) -> warp (u * nrg + i) % 8 ----
-        const int nrg = sk_n_rg(c, G);
+        // ---- 9. down rows 16c .. 16c + 15 of every slot: warp w takes column
+        // tile w of each, the routing weights folded in per token ----
+        const int has_dn = sk_has_dn(c);
         const uint32_t seqD = seq;
-        const int nd = nrg * (U + 1);
-        seq += (uint32_t)nd;
-        float yacc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-        for (int it = warp; it < nd && !fail; it += SK_CW) {
-            const int u = it / nrg, ri = it % nrg;
-            const uint32_t qq = seqD + (uint32_t)it;
+        seq += has_dn ? (uint32_t)(U + 1) : 0u;
+        float yacc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int u = 0; has_dn && u <= U && !fail; ++u) {
+            const uint32_t qq = seqD + (uint32_t)u;
             if (!__all_sync(0xFFFFFFFFu, sk_wait_full(s, qq))) {
                 fail = true;
                 break;
             }
-            const uint8_t* wd = s.ring + (size_t)(qq % s.nslot) * SK_SLOT + r * 128;
-            // A row: token r (rows 8..15 repeat it; they are never used) -> its pair in slot u
-            int pa = r < T ? sh->tok_pair[u][r] : -1;
-            pa = pa < 0 ? 0 : pa;
-            const uint8_t* ar = s.ubuf + (size_t)pa * (I * 2);
+            // A: rows r (m even) or 8 + r (m odd) of column tile `warp`;
+            // B: token rows -> their pairs in slot u (token r: lane's row)
+            const uint8_t* wt = sk_slot_ptr(s, qq) + warp * 2048 + (r + 8 * (m & 1)) * 128;
+            int pb = r < T ? sh->tok_pair[u][r] : -1;
+            pb = pb < 0 ? 0 : pb;
+            const uint8_t* br = s.ubuf + (size_t)pb * (I * 2);
             float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-            for (int kk = 0; kk < I / 32; ++kk) {     // two k-steps of 16 per iteration
-                uint32_t b[4], a[4], a2[4];
-                const int kt = kk >> 1, h = kk & 1;
-                ldmatrix_x4(b, wd + kt * 1024 + sw_chunk(r, 4 * h + m));
-                const int ch = 4 * kk + (m >> 1);     // A: 16-byte chunk of the activation row
-                ldmatrix_x4(a, ar + ((ch ^ (pa & 7)) << 4));
-                ldmatrix_x4(a2, ar + (((ch + 2) ^ (pa & 7)) << 4));
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t a[4], a2[4], b[4];
+                ldmatrix_x4(a, wt + sw_chunk(r, 4 * h + (m >> 1)));
+                ldmatrix_x4(a2, wt + sw_chunk(r, 4 * h + 2 + (m >> 1)));
+                const int ch = 8 * warp + 4 * h + m;           // 16-byte chunk of the activation row
+                ldmatrix_x4(b, br + ((ch ^ (pb & 7)) << 4));
                 mma_bf16_16816(d0, a, b[0], b[1]);
                 mma_bf16_16816(d1, a2, b[2], b[3]);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s.empty[qq % s.nslot]);
-            // token g's weight for slot u (0 when g is not routed there)
-            const float wgt = g < T ? sh->tok_w[u][g] : 0.f;
-            yacc[ri][0] = fmaf(wgt, d0[0] + d1[0], yacc[ri][0]);
-            yacc[ri][1] = fmaf(wgt, d0[1] + d1[1], yacc[ri][1]);
+            sk_release(s, qq, lane);
+            // lane (g, cq): rows g and g + 8, tokens 2 cq and 2 cq + 1
+            const float w0 = 2 * cq < T ? sh->tok_w[u][2 * cq] : 0.f;
+            const float w1 = 2 * cq + 1 < T ? sh->tok_w[u][2 * cq + 1] : 0.f;
+            yacc[0] = fmaf(w0, d0[0] + d1[0], yacc[0]);
+            yacc[1] = fmaf(w1, d0[1] + d1[1], yacc[1]);
+            yacc[2] = fmaf(w0, d0[2] + d1[2], yacc[2]);
+            yacc[3] = fmaf(w1, d0[3] + d1[3], yacc[3]);
         }
-#pragma unroll
-        for (int ri = 0; ri < 2; ++ri) {
-            sh->part[warp][ri * 64 + g * 8 + 2 * cq] = yacc[ri][0];
-            sh->part[warp][ri * 64 + g * 8 + 2 * cq + 1] = yacc[ri][1];
-        }
+        *reinterpret_cast<float4*>(&sh->part[0][warp][lane * 4]) = make_float4(yacc[0], yacc[1], yacc[2], yacc[3]);
         if (sk_phase_end(s, fail)) break;
         // ---- 10. y: the warps' partial sums added in warp order ----
-        for (int i = tid; i < nrg * T * 8; i += SK_CW * 32) {
-            const int ri = i / (T * 8), t = (i / 8) % T, row = i % 8;
-            float sum = 0.f;
+        if (has_dn) {
+            for (int i = tid; i < 16 * T; i += SK_CW * 32) {
+                const int row = i & 15, t = i >> 4;
+                // the lane holding (row, token t): g = row % 8, cq = t / 2; element 2 (row >= 8) + t % 2
+                const int ln = (row & 7) * 4 + (t >> 1), el = (row >> 3) * 2 + (t & 1);
+                float sum = 0.f;
 #pragma unroll
-            for (int w = 0; w < SK_CW; ++w) sum += sh->part[w][ri * 64 + t * 8 + row];
-            Ly.y[(size_t)t * H + sk_rg(c, G, ri) * 8 + row] = __float2bfloat16_rn(sum);
+                for (int w = 0; w < SK_CW; ++w) sum += sh->part[0][w][ln * 4 + el];
+                Ly.y[(size_t)t * H + 16 * c + row] = __float2bfloat16_rn(sum);
+            }
         }
         // ---- 11. y of this layer is complete everywhere before the next layer reads x ----
         if (l + 1 < p.n_layers) {
@@ -705,7 +723,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1) stack_decode_kernel(const __gri
     s.ring = smem;
     s.ubuf = smem + Lo.ubuf_off;
     s.full = reinterpret_cast<uint64_t*>(smem + Lo.bars_off);
-    s.empty = s.full + Lo.nslot;
+    s.empty = s.full + SK_MAX_RING;
     s.sh = reinterpret_cast<SkShared*>(smem + Lo.sh_off);
     s.nslot = Lo.nslot;
     s.T = p.T;
@@ -714,10 +732,10 @@ __global__ void __launch_bounds__(SK_THREADS, 1) stack_decode_kernel(const __gri
     if (threadIdx.x == 0) {
         for (int i = 0; i < Lo.nslot; ++i) {
             mbar_init(&s.full[i], 1);
-            mbar_init(&s.empty[i], 1);
+            mbar_init(&s.empty[i], SK_CW);         // every consumer warp releases every slot
+            s.sh->slot_seq[i] = 0u;
         }
         mbar_init(&s.sh->route_bar, 1);
-        for (int i = 0; i < 32; ++i) s.sh->slot_seq[i] = 0u;
         s.sh->abort = 0;
         fence_mbar_init();
     }
@@ -736,10 +754,10 @@ cudaError_t stack_decode_set_attributes(int max_optin) {
 
 cudaError_t launch_stack_decode(const LaunchCtx& L, StackParams& p, int max_optin) {
     if (p.T < 1 || p.T > STACK_MAX_T || p.n_layers < 1 || p.n_layers > STACK_MAX_LAYERS) return cudaErrorInvalidValue;
-    if (L.num_sms < SK_GU_UNITS || L.num_sms > E) return cudaErrorInvalidValue;
+    if (L.num_sms < SK_DN_ITEMS || L.num_sms > E) return cudaErrorInvalidValue;
     p.smem_bytes = (uint32_t)max_optin;
     const SkLayout Lo = sk_layout(p.T, (uint32_t)max_optin);
-    if (Lo.nslot < 8) return cudaErrorInvalidValue;
+    if (Lo.nslot < 6) return cudaErrorInvalidValue;
     return launch_hooked(L, FLINT_KERNEL_GATE_UP, stack_decode_kernel, dim3(L.num_sms), dim3(SK_THREADS), Lo.total, p);
 }
 

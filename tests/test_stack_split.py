@@ -1,0 +1,80 @@
+"""Host checks of the persistent stack kernel's static plan (csrc/stack_decode.cu,
+compiled as host code): the routed gate/up units are dealt to the CTAs in
+contiguous, non-decreasing ranges that cover every unit exactly once, every
+CTA gets about the same number of 16 KiB blocks, and the shared-memory layout
+fits the device limit with a ring deep enough for every T <= 8."""
+import os
+import shutil
+import subprocess
+
+import numpy as np
+import pytest
+
+from sparse_moe_transformer_03_b300 import build as flint_build
+
+CSRC = os.path.join(os.path.dirname(flint_build.__file__), "csrc")
+PROG = r"""
+#include "stack_decode.cu"
+#include <cstdio>
+int main() {
+    using namespace flint;
+    for (int G : {128, 132, 148, 160, 256})
+        for (int U = 1; U <= 48; ++U) {
+            std::printf("R %d %d", G, U);
+            for (int c = -1; c < G; ++c) std::printf(" %d", sk_rcum(c, G, U));
+            std::printf("\n");
+        }
+    for (int T = 1; T <= 8; ++T) {
+        SkLayout L = sk_layout(T, 232448);
+        std::printf("L %d %d %u %u %u\n", T, L.nslot, L.ubuf_off, L.sh_off, L.total);
+    }
+    return 0;
+}
+"""
+
+
+@pytest.fixture(scope="module")
+def plan(tmp_path_factory):
+    nvcc = flint_build.nvcc()
+    if not shutil.which(nvcc) and not os.path.exists(nvcc):
+        pytest.skip("nvcc not found")
+    d = tmp_path_factory.mktemp("stack_split")
+    src, exe = d / "plan.cu", d / "plan"
+    src.write_text(PROG)
+    subprocess.check_call([nvcc, *flint_build.ARCH, "-std=c++17", "--expt-relaxed-constexpr", "-I", CSRC,
+                           "-I", os.path.join(CSRC, "..", "..", "include"), "-o", str(exe), str(src)])
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.splitlines()
+    ranges, layouts = {}, {}
+    for ln in out:
+        f = ln.split()
+        if f[0] == "R":
+            ranges[(int(f[1]), int(f[2]))] = np.array(f[3:], dtype=np.int64)
+        else:
+            layouts[int(f[1])] = tuple(int(v) for v in f[2:])
+    return ranges, layouts
+
+
+def test_routed_units_are_dealt_once_in_order(plan):
+    ranges, _ = plan
+    for (G, U), r in ranges.items():
+        assert r[0] == 0 and r[-1] == 64 * U, (G, U)
+        assert (np.diff(r) >= 0).all(), (G, U)
+
+
+def test_every_cta_gets_about_the_same_bytes(plan):
+    """Blocks of 16 KiB per CTA: 4 per gate/up unit (routed and shared) and
+    one per down item (CTA c < 128 owns one down item per slot)."""
+    ranges, _ = plan
+    for (G, U), r in ranges.items():
+        c = np.arange(G)
+        blocks = 4 * np.diff(r) + 4 * (c < 64) + (c < 128) * (U + 1)
+        mean = (4 * 64 + 128) * (U + 1) / G
+        assert blocks.max() - mean <= 4.5, (G, U, blocks.max(), mean)
+
+
+def test_shared_memory_fits_with_a_deep_ring(plan):
+    _, layouts = plan
+    for T, (nslot, ubuf_off, sh_off, total) in layouts.items():
+        assert total <= 232448, T
+        assert nslot >= 8, (T, nslot)
+        assert ubuf_off == nslot * 16384
