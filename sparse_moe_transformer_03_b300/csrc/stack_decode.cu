@@ -464,7 +464,9 @@ __device__ __forceinline__ bool sk_gateup_part(const SkState& s, uint32_t sq, in
 }
 
 // The unit's eight partial sums (part[par][w]) added in warp order by one
-// warp; a = silu(gate) * up for the tokens routed to slot u.
+// warp; a = silu(gate) * up for the tokens routed to slot u (u = 0: the
+// shared expert, whose pair of token t is t; it runs before the layer's
+// tables exist).
 __device__ __forceinline__ void sk_gateup_finish(const SkState& s, int par, int u, int q, int lane) {
     SkShared* sh = s.sh;
     float4 sum = *reinterpret_cast<const float4*>(&sh->part[par][0][lane * 4]);
@@ -479,11 +481,11 @@ __device__ __forceinline__ void sk_gateup_finish(const SkState& s, int par, int 
     const int g = lane >> 2, cq = lane & 3, j = 8 * q + g;
     const int t0 = 2 * cq, t1 = 2 * cq + 1;
     if (t0 < s.T) {
-        const int pp = sh->tok_pair[u][t0];
+        const int pp = u == 0 ? t0 : sh->tok_pair[u][t0];
         if (pp >= 0) s.p->act[sk_act_index(pp, j)] = __float2bfloat16_rn(silu_f(sum.x) * sum.z);
     }
     if (t1 < s.T) {
-        const int pp = sh->tok_pair[u][t1];
+        const int pp = u == 0 ? t1 : sh->tok_pair[u][t1];
         if (pp >= 0) s.p->act[sk_act_index(pp, j)] = __float2bfloat16_rn(silu_f(sum.y) * sum.w);
     }
 }
