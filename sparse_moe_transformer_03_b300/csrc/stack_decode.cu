@@ -81,8 +81,8 @@ struct SkShared {
     int pair0[E];
     int tok_pair[SK_MAX_SLOTS][STACK_MAX_T];      // pair of (slot, token), -1: token not routed there
     float tok_w[SK_MAX_SLOTS][STACK_MAX_T];       // its routing weight (0 when not routed)
-    alignas(16) float part[2][SK_CW][32 * 4];     // per-warp partial sums (gate/up: by unit parity;
-                                                  // down: [0][warp][lane x 4])
+    alignas(16) float part[2][2][4][32 * 4];      // gate/up partial sums [quad][unit parity][warp of
+                                                  // the quad][lane x 4]; down: [0][0..1] as [warp][lane x 4]
     uint64_t route_bar;                           // consumers -> producer: tables of the layer are built
     // Ring slot i was last handed out for sequence number slot_seq[i] - 1.  A
     // consumer waits for its sequence number here before the slot's full
@@ -206,10 +206,14 @@ __device__ __forceinline__ uint8_t* sk_slot_ptr(const SkState& s, uint32_t q) {
     return s.ring + (size_t)(q % (uint32_t)s.nslot) * SK_SLOT;
 }
 
-// Release ring sequence number q (every consumer warp arrives once).
-__device__ __forceinline__ void sk_release(const SkState& s, uint32_t q, int lane) {
+// Release ring sequence number q: the warp's share of the slot's SK_CW
+// expected arrivals (cnt = SK_CW when it is the slot's only reader).
+__device__ __forceinline__ void sk_release(const SkState& s, uint32_t q, int lane, uint32_t cnt) {
     __syncwarp();
-    if (lane == 0) mbar_arrive(&s.empty[q % (uint32_t)s.nslot]);
+    if (lane == 0)
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(&s.empty[q % (uint32_t)s.nslot])),
+                     "r"(cnt)
+                     : "memory");
 }
 
 // Grid barrier (one thread, after the consumer warps synchronised): arrive,
@@ -430,12 +434,13 @@ __device__ __forceinline__ bool sk_phase_end(const SkState& s, bool fail) {
 }
 
 // One gate/up unit (slots sq .. sq + 3: gate tiles 0..15, 16..31, up tiles
-// 0..15, 16..31) against the tokens: warp w multiplies column tiles 4w ..
-// 4w + 3, 16 weight rows (8 gate over 8 up) x 256 columns, into d[] (lane
-// (g, cq): gate row g and up row g for tokens 2 cq and 2 cq + 1).  All 32
-// lanes take part; returns false if a wait gave up.
-__device__ __forceinline__ bool sk_gateup_part(const SkState& s, uint32_t sq, int warp, int lane, float (&d)[4]) {
-    const int half = warp >> 2;
+// 0..15, 16..31) against the tokens, by a quad of warps: warp wq of the quad
+// multiplies column tiles 8 wq .. 8 wq + 7, 16 weight rows (8 gate over 8 up)
+// x 512 columns, into d[] (lane (g, cq): gate row g and up row g for tokens
+// 2 cq and 2 cq + 1), then releases the two slots it read.  All 32 lanes
+// take part; returns false if a wait gave up.
+__device__ __forceinline__ bool sk_gateup_part(const SkState& s, uint32_t sq, int wq, int lane, float (&d)[4]) {
+    const int half = wq >> 1;
     const bool got = sk_wait_full(s, sq + (uint32_t)half) && sk_wait_full(s, sq + 2u + (uint32_t)half);
     if (!__all_sync(0xFFFFFFFFu, got)) return false;
     const int m = lane >> 3, r = lane & 7;
@@ -443,10 +448,10 @@ __device__ __forceinline__ bool sk_gateup_part(const SkState& s, uint32_t sq, in
     const uint8_t* arow = sk_slot_ptr(s, sq + (uint32_t)(2 * (m & 1) + half)) + r * 128;
     // B: token rows of x (padding tokens read token 0; their columns are not used)
     const uint8_t* xrow = s.ubuf + (size_t)(r < s.T ? r : 0) * SK_XSTRIDE + m * 16;
-    float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
+    float acc[4][4] = {};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int kt = 4 * warp + i;                      // column tile 0..31
+    for (int i = 0; i < 8; ++i) {
+        const int kt = 8 * wq + i;                        // column tile 0..31
         const uint8_t* tile = arow + (kt & 15) * 1024;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {                     // two 32-column halves = two k-step pairs
@@ -454,25 +459,27 @@ __device__ __forceinline__ bool sk_gateup_part(const SkState& s, uint32_t sq, in
             ldmatrix_x4(a, tile + sw_chunk(r, 4 * h + (m >> 1)));
             ldmatrix_x4(a2, tile + sw_chunk(r, 4 * h + 2 + (m >> 1)));
             ldmatrix_x4(b, xrow + (size_t)(kt * 64 + 32 * h) * 2);
-            mma_bf16_16816(a0, a, b[0], b[1]);
-            mma_bf16_16816(a1, a2, b[2], b[3]);
+            mma_bf16_16816(acc[2 * h], a, b[0], b[1]);
+            mma_bf16_16816(acc[2 * h + 1], a2, b[2], b[3]);
         }
     }
+    sk_release(s, sq + (uint32_t)half, lane, 4);
+    sk_release(s, sq + 2u + (uint32_t)half, lane, 4);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) d[i] = a0[i] + a1[i];
+    for (int i = 0; i < 4; ++i) d[i] = (acc[0][i] + acc[1][i]) + (acc[2][i] + acc[3][i]);
     return true;
 }
 
-// The unit's eight partial sums (part[par][w]) added in warp order by one
-// warp; a = silu(gate) * up for the tokens routed to slot u (u = 0: the
+// The unit's four partial sums (part[quad][par][w]) added in warp order by
+// one warp; a = silu(gate) * up for the tokens routed to slot u (u = 0: the
 // shared expert, whose pair of token t is t; it runs before the layer's
 // tables exist).
-__device__ __forceinline__ void sk_gateup_finish(const SkState& s, int par, int u, int q, int lane) {
+__device__ __forceinline__ void sk_gateup_finish(const SkState& s, int quad, int par, int u, int q, int lane) {
     SkShared* sh = s.sh;
-    float4 sum = *reinterpret_cast<const float4*>(&sh->part[par][0][lane * 4]);
+    float4 sum = *reinterpret_cast<const float4*>(&sh->part[quad][par][0][lane * 4]);
 #pragma unroll
-    for (int w = 1; w < SK_CW; ++w) {
-        const float4 v = *reinterpret_cast<const float4*>(&sh->part[par][w][lane * 4]);
+    for (int w = 1; w < 4; ++w) {
+        const float4 v = *reinterpret_cast<const float4*>(&sh->part[quad][par][w][lane * 4]);
         sum.x += v.x;
         sum.y += v.y;
         sum.z += v.z;
@@ -488,6 +495,20 @@ __device__ __forceinline__ void sk_gateup_finish(const SkState& s, int par, int 
         const int pp = u == 0 ? t1 : sh->tok_pair[u][t1];
         if (pp >= 0) s.p->act[sk_act_index(pp, j)] = __float2bfloat16_rn(silu_f(sum.y) * sum.w);
     }
+}
+
+// Named barrier of one quad of consumer warps (ids 2 and 3) that ORs the
+// threads' failure flags, like sk_phase_end.
+__device__ __forceinline__ bool sk_quad_sync(const SkState& s, int quad, bool fail) {
+    const uint32_t v = (fail || sk_aborted(s)) ? 1u : 0u;
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, 128, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"(v), "r"(2 + quad)
+        : "memory");
+    if (r) s.sh->abort = 1;
+    return r != 0;
 }
 
 __device__ void sk_consumers(const SkState& s, int warp, int lane) {
@@ -553,22 +574,20 @@ __device__ void sk_consumers(const SkState& s, int warp, int lane) {
                                    ((unsigned long long)tag << 32) | (unsigned long long)__float_as_uint(v));
                 }
             }
-            if (!fail) sk_release(s, seqR, lane);
+            if (!fail) sk_release(s, seqR, lane, 1);
         }
         // ---- 3. the shared expert's unit of this CTA (CTAs 0..63) ----
         const int has_sg = sk_has_sg(c);
         const uint32_t seqSG = seq;
         seq += has_sg ? 4 : 0;
-        if (has_sg && !fail) {
+        if (has_sg && !fail && warp < 4) {   // quad 0
             float d[4];
             fail = !sk_gateup_part(s, seqSG, warp, lane, d);
-            if (!fail) {
-                for (int k = 0; k < 4; ++k) sk_release(s, seqSG + k, lane);
-                *reinterpret_cast<float4*>(&sh->part[0][warp][lane * 4]) = make_float4(d[0], d[1], d[2], d[3]);
-            }
+            if (!fail)
+                *reinterpret_cast<float4*>(&sh->part[0][0][warp][lane * 4]) = make_float4(d[0], d[1], d[2], d[3]);
         }
         if (sk_phase_end(s, fail)) break;
-        if (has_sg && warp == 0) sk_gateup_finish(s, 0, 0, c, lane);
+        if (has_sg && warp == 0) sk_gateup_finish(s, 0, 0, 0, c, lane);
         // ---- 4. every token's 256 logits (tagged with this layer's epoch), top-6 ----
         if (warp < T) {
             float v[8];
@@ -614,32 +633,29 @@ __device__ void sk_consumers(const SkState& s, int warp, int lane) {
         }
         if (sk_phase_end(s, false)) break;
         const int U = sh->tab.n_slots - 1;
-        // ---- 6. routed gate/up units of the CTA's range, one at a time, K split
-        // over the warps; warp j % 8 finishes unit j ----
+        // ---- 6. routed gate/up units of the CTA's range: quad q (warps 4q ..
+        // 4q + 3) takes units q, q + 2, ..., K split over its warps; warp
+        // (j / 2) % 4 of the quad finishes unit j ----
         const int k0 = sk_rcum(c - 1, G, U), k1 = sk_rcum(c, G, U);
         const uint32_t seqRG = seq;
         seq += 4u * (uint32_t)(k1 - k0);
-        bool stop = false;
-        for (int j = 0; j < k1 - k0; ++j) {
-            float d[4];
-            const uint32_t sq = seqRG + 4u * j;
-            fail = !sk_gateup_part(s, sq, warp, lane, d);
-            if (!fail) {
-                for (int k = 0; k < 4; ++k) sk_release(s, sq + k, lane);
-                *reinterpret_cast<float4*>(&sh->part[j & 1][warp][lane * 4]) = make_float4(d[0], d[1], d[2], d[3]);
-            }
-            if (sk_phase_end(s, fail)) {
-                stop = true;
-                break;
-            }
-            // the parity buffer j & 1 is written again only after the phase end
-            // of unit j + 1, which this warp reaches after the sum
-            if (warp == (j & (SK_CW - 1))) {
-                const int k = k0 + j;
-                sk_gateup_finish(s, j & 1, 1 + k / SK_GU_UNITS, k % SK_GU_UNITS, lane);
+        {
+            const int quad = warp >> 2, wq = warp & 3;
+            for (int j = quad; j < k1 - k0; j += 2) {
+                float d[4];
+                const bool f = !sk_gateup_part(s, seqRG + 4u * j, wq, lane, d);
+                const int par = (j >> 1) & 1;
+                if (!f)
+                    *reinterpret_cast<float4*>(&sh->part[quad][par][wq][lane * 4]) = make_float4(d[0], d[1], d[2], d[3]);
+                // the parity buffer is written again two units later, after this
+                // quad's next barrier, which the finishing warp reaches after the sum
+                if (sk_quad_sync(s, quad, f)) break;
+                if (wq == ((j >> 1) & 3)) {
+                    const int k = k0 + j;
+                    sk_gateup_finish(s, quad, par, 1 + k / SK_GU_UNITS, k % SK_GU_UNITS, lane);
+                }
             }
         }
-        if (stop) break;
         // ---- 7. every CTA's activations are written (grid barrier) ----
         if (sk_phase_end(s, false)) break;
         if (tid == 0) {
@@ -652,45 +668,52 @@ __device__ void sk_consumers(const SkState& s, int warp, int lane) {
         for (int i = tid; i < npairs * (I / 8); i += SK_CW * 32)
             *reinterpret_cast<uint4*>(s.ubuf + (size_t)i * 16) = __ldcg(reinterpret_cast<const uint4*>(p.act) + i);
         if (sk_phase_end(s, false)) break;
-        // ---- 9. down rows 16c .. 16c + 15 of every slot: warp w takes column
-        // tile w of each, the routing weights folded in per token ----
+        // ---- 9. down rows 16c .. 16c + 15 of every slot: warp u % 8 takes slot
+        // u's item whole, the routing weights folded in per token ----
         const int has_dn = sk_has_dn(c);
         const uint32_t seqD = seq;
         seq += has_dn ? (uint32_t)(U + 1) : 0u;
         float yacc[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int u = 0; has_dn && u <= U && !fail; ++u) {
+        for (int u = warp; has_dn && u <= U && !fail; u += SK_CW) {
             const uint32_t qq = seqD + (uint32_t)u;
             if (!__all_sync(0xFFFFFFFFu, sk_wait_full(s, qq))) {
                 fail = true;
                 break;
             }
-            // A: rows r (m even) or 8 + r (m odd) of column tile `warp`;
+            // A: rows r (m even) or 8 + r (m odd) of the 8 column tiles;
             // B: token rows -> their pairs in slot u (token r: lane's row)
-            const uint8_t* wt = sk_slot_ptr(s, qq) + warp * 2048 + (r + 8 * (m & 1)) * 128;
+            const uint8_t* wrow = sk_slot_ptr(s, qq) + (r + 8 * (m & 1)) * 128;
             int pb = r < T ? sh->tok_pair[u][r] : -1;
             pb = pb < 0 ? 0 : pb;
             const uint8_t* br = s.ubuf + (size_t)pb * (I * 2);
-            float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+            float acc[4][4] = {};
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t a[4], a2[4], b[4];
-                ldmatrix_x4(a, wt + sw_chunk(r, 4 * h + (m >> 1)));
-                ldmatrix_x4(a2, wt + sw_chunk(r, 4 * h + 2 + (m >> 1)));
-                const int ch = 8 * warp + 4 * h + m;           // 16-byte chunk of the activation row
-                ldmatrix_x4(b, br + ((ch ^ (pb & 7)) << 4));
-                mma_bf16_16816(d0, a, b[0], b[1]);
-                mma_bf16_16816(d1, a2, b[2], b[3]);
+            for (int kt = 0; kt < I / 64; ++kt) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t a[4], a2[4], b[4];
+                    ldmatrix_x4(a, wrow + kt * 2048 + sw_chunk(r, 4 * h + (m >> 1)));
+                    ldmatrix_x4(a2, wrow + kt * 2048 + sw_chunk(r, 4 * h + 2 + (m >> 1)));
+                    const int ch = 8 * kt + 4 * h + m;         // 16-byte chunk of the activation row
+                    ldmatrix_x4(b, br + ((ch ^ (pb & 7)) << 4));
+                    mma_bf16_16816(acc[2 * h], a, b[0], b[1]);
+                    mma_bf16_16816(acc[2 * h + 1], a2, b[2], b[3]);
+                }
             }
-            sk_release(s, qq, lane);
+            sk_release(s, qq, lane, SK_CW);
             // lane (g, cq): rows g and g + 8, tokens 2 cq and 2 cq + 1
             const float w0 = 2 * cq < T ? sh->tok_w[u][2 * cq] : 0.f;
             const float w1 = 2 * cq + 1 < T ? sh->tok_w[u][2 * cq + 1] : 0.f;
-            yacc[0] = fmaf(w0, d0[0] + d1[0], yacc[0]);
-            yacc[1] = fmaf(w1, d0[1] + d1[1], yacc[1]);
-            yacc[2] = fmaf(w0, d0[2] + d1[2], yacc[2]);
-            yacc[3] = fmaf(w1, d0[3] + d1[3], yacc[3]);
+            float dd[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dd[i] = (acc[0][i] + acc[1][i]) + (acc[2][i] + acc[3][i]);
+            yacc[0] = fmaf(w0, dd[0], yacc[0]);
+            yacc[1] = fmaf(w1, dd[1], yacc[1]);
+            yacc[2] = fmaf(w0, dd[2], yacc[2]);
+            yacc[3] = fmaf(w1, dd[3], yacc[3]);
         }
-        *reinterpret_cast<float4*>(&sh->part[0][warp][lane * 4]) = make_float4(yacc[0], yacc[1], yacc[2], yacc[3]);
+        float* ypart = &sh->part[0][0][0][0];
+        *reinterpret_cast<float4*>(&ypart[(warp * 32 + lane) * 4]) = make_float4(yacc[0], yacc[1], yacc[2], yacc[3]);
         if (sk_phase_end(s, fail)) break;
         // ---- 10. y: the warps' partial sums added in warp order ----
         if (has_dn) {
@@ -700,7 +723,7 @@ __device__ void sk_consumers(const SkState& s, int warp, int lane) {
                 const int ln = (row & 7) * 4 + (t >> 1), el = (row >> 3) * 2 + (t & 1);
                 float sum = 0.f;
 #pragma unroll
-                for (int w = 0; w < SK_CW; ++w) sum += sh->part[0][w][ln * 4 + el];
+                for (int w = 0; w < SK_CW; ++w) sum += ypart[(w * 32 + ln) * 4 + el];
                 Ly.y[(size_t)t * H + 16 * c + row] = __float2bfloat16_rn(sum);
             }
         }
