@@ -53,9 +53,8 @@ struct flint_moe {
     __nv_bfloat16* h_perm;         // [(TOPK+1)*CHUNK][I]
     __nv_bfloat16* o_perm;         // [(TOPK+1)*CHUNK][H]
     // scratch of flint_moe_forward_layers when this handle is layers[0]
-    unsigned char* stack_clear;    // tagged logits, barrier counter, abort flag (STACK_CLEAR_BYTES)
+    unsigned char* stack_clear;    // tagged logits and activations, barrier counter, abort flag
     CUtensorMap* stack_maps;       // [2] this layer's tiled experts as 4-D tensor maps (bf16 handles)
-    __nv_bfloat16* stack_act;      // [STACK_MAX_T * 7][I]
 };
 
 namespace {
@@ -128,7 +127,6 @@ void carve_workspace(flint_moe* h, char* base, size_t* bytes_out) {
     h->h_perm = c.take<__nv_bfloat16>((size_t)(TOPK + 1) * CHUNK * I);
     h->o_perm = c.take<__nv_bfloat16>((size_t)(TOPK + 1) * CHUNK * H);
     h->stack_clear = c.take<unsigned char>(STACK_CLEAR_BYTES);
-    h->stack_act = c.take<__nv_bfloat16>(STACK_ACT_ELEMS);
     h->stack_maps = c.take<CUtensorMap>(2);
     *bytes_out = c.off;
 }
@@ -368,9 +366,9 @@ flint_status_t flint_moe_forward_layers(const flint_moe_t* layers, int n, const 
             p.layer[i].y = static_cast<__nv_bfloat16*>(y[l0 + i]);
         }
         p.logits = reinterpret_cast<unsigned long long*>(h0->stack_clear);
-        p.bar = reinterpret_cast<unsigned long long*>(h0->stack_clear + STACK_LOGITS_BYTES);
-        p.abort_flag = reinterpret_cast<uint32_t*>(h0->stack_clear + STACK_LOGITS_BYTES + 8);
-        p.act = h0->stack_act;
+        p.act = reinterpret_cast<unsigned long long*>(h0->stack_clear + STACK_LOGITS_BYTES);
+        p.bar = reinterpret_cast<unsigned long long*>(h0->stack_clear + STACK_LOGITS_BYTES + STACK_ACT_BYTES);
+        p.abort_flag = reinterpret_cast<uint32_t*>(h0->stack_clear + STACK_LOGITS_BYTES + STACK_ACT_BYTES + 8);
         p.status = h0->status_dev;
         p.limit_ns = h0->wait_limit_ns;
         if (launch_stack_decode(L, p, h0->smem_optin) != cudaSuccess) return FLINT_ERR_CUDA;

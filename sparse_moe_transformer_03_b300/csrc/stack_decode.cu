@@ -26,11 +26,13 @@
 //      tensor box per slot; eight consumer warps multiply them on the
 //      warp-level tensor core (mma.sync m16n8k16: 16 weight rows x 16
 //      columns against up to 8 tokens), the K dimension split over the
-//      warps, and write a = silu(g) * u (bf16) to a global buffer;
-//   4. grid barrier; the CTA copies every pair's activations into shared
-//      memory and applies its 16 down rows to every slot (the routing weight
-//      folded in per token, each warp summing its K slice over the slots in
-//      order, then the warps in order): y is written once, deterministically;
+//      warps, and compute a = silu(g) * u (bf16);
+//   4. the activations are published as 64-bit words tagged with the layer's
+//      epoch too; each CTA copies every pair's activations into shared memory
+//      as soon as all their tags are this layer's and applies its 16 down rows
+//      to every slot (the routing weight folded in per token, each warp
+//      summing its slots in order, then the warps in order): y is written
+//      once, deterministically;
 //   5. grid barrier (layer l + 1 may read y_l), while the producer already
 //      streams layer l + 1's router rows and shared-expert unit.
 //
@@ -39,8 +41,9 @@
 // item is 16 rows of Wd x 512 columns (1 block, 128 per expert).  CTA c < 64
 // owns shared unit c, CTA c < 128 owns down rows 16c .. 16c + 15 of every
 // slot, and the routed units are dealt in contiguous ranges so that every CTA
-// has the same number of blocks.  Every output element is produced by one
-// CTA: nothing is reduced across CTAs.
+// has the same number of gate/up units (those precede the activation barrier;
+// the down items stream while they run and after it).  Every output element
+// is produced by one CTA: nothing is reduced across CTAs.
 #include "flint_common.cuh"
 #include "../../include/flint_moe.h"
 #include "flint_internal.h"
@@ -64,12 +67,6 @@ constexpr int SK_XSTRIDE = H * 2 + 16;            // padded x row in shared memo
 constexpr int SK_MAX_SLOTS = 1 + STACK_MAX_T * TOPK;   // 49
 constexpr int SK_MAX_RING = 16;
 constexpr int SK_NAMED = 1;                       // named barrier of the consumer warps
-
-// Activation rows: pair p's 512 bf16, its 16-byte chunk c stored at c ^ (p % 8)
-// (the eight token rows of one MMA operand read through different banks).
-__host__ __device__ __forceinline__ int sk_act_index(int p, int j) {
-    return p * I + ((((j >> 3) ^ (p & 7))) << 3) + (j & 7);
-}
 
 struct SkShared {
     DecodeTables tab;                             // n_slots, n_pairs, slot_expert, slot_pair0 are used
@@ -102,6 +99,11 @@ __device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned l
 __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
     unsigned long long v;
     asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ ulonglong2 ld_relaxed_v2u64(const unsigned long long* p) {
+    ulonglong2 v;
+    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(v.x), "=l"(v.y) : "l"(p) : "memory");
     return v;
 }
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
@@ -242,17 +244,17 @@ __device__ __forceinline__ int sk_has_sg(int c) { return c < SK_GU_UNITS ? 1 : 0
 __device__ __forceinline__ int sk_has_dn(int c) { return c < SK_DN_ITEMS ? 1 : 0; }
 
 // End of CTA c's range of routed gate/up units (the units of slots 1..U in
-// order): every CTA's share of all 16 KiB blocks of the layer (4 per gate/up
-// unit, 1 per down item) minus the shared units and down items that the CTAs
-// up to c own.  Non-decreasing in c for U >= 1 and equal to 64 U at the last
-// CTA (checked on the host for every U).
+// order): every CTA's share of all 64 (U + 1) gate/up units minus the shared
+// units the CTAs up to c own.  Only the gate/up units have to be done before
+// the activations are complete (the down items are applied after that grid
+// barrier), so they alone are balanced.  Non-decreasing in c and equal to
+// 64 U at the last CTA (checked on the host for every U).
 __host__ __device__ __forceinline__ int sk_rcum(int c, int G, int U) {
     if (c < 0) return 0;
-    const int total = (4 * SK_GU_UNITS + SK_DN_ITEMS) * (U + 1);
-    const int bcum = (int)(((long long)(c + 1) * total) / G);
-    const int scum = 4 * (c + 1 < SK_GU_UNITS ? c + 1 : SK_GU_UNITS);
-    const int dcum = (c + 1 < SK_DN_ITEMS ? c + 1 : SK_DN_ITEMS) * (U + 1);
-    const int r = (bcum - scum - dcum) >> 2;
+    const int total = SK_GU_UNITS * (U + 1);
+    const int ucum = (int)(((long long)(c + 1) * total) / G);
+    const int scum = c + 1 < SK_GU_UNITS ? c + 1 : SK_GU_UNITS;
+    const int r = ucum - scum;
     return r < 0 ? 0 : (r > SK_GU_UNITS * U ? SK_GU_UNITS * U : r);
 }
 
@@ -473,8 +475,11 @@ __device__ __forceinline__ bool sk_gateup_part(const SkState& s, uint32_t sq, in
 // The unit's four partial sums (part[quad][par][w]) added in warp order by
 // one warp; a = silu(gate) * up for the tokens routed to slot u (u = 0: the
 // shared expert, whose pair of token t is t; it runs before the layer's
-// tables exist).
-__device__ __forceinline__ void sk_gateup_finish(const SkState& s, int quad, int par, int u, int q, int lane) {
+// tables exist), published as tagged words of two columns: lane (g, cq)
+// computes column 8q + g of tokens 2 cq and 2 cq + 1, and the even-g lane
+// of each column pair stores the word.
+__device__ __forceinline__ void sk_gateup_finish(const SkState& s, int quad, int par, int u, int q, int lane,
+                                                 unsigned int tag) {
     SkShared* sh = s.sh;
     float4 sum = *reinterpret_cast<const float4*>(&sh->part[quad][par][0][lane * 4]);
 #pragma unroll
@@ -485,15 +490,22 @@ __device__ __forceinline__ void sk_gateup_finish(const SkState& s, int quad, int
         sum.z += v.z;
         sum.w += v.w;
     }
-    const int g = lane >> 2, cq = lane & 3, j = 8 * q + g;
+    const int g = lane >> 2, cq = lane & 3;
+    const uint32_t a0 = __bfloat16_as_ushort(__float2bfloat16_rn(silu_f(sum.x) * sum.z));   // token 2 cq
+    const uint32_t a1 = __bfloat16_as_ushort(__float2bfloat16_rn(silu_f(sum.y) * sum.w));   // token 2 cq + 1
+    const uint32_t b0 = __shfl_down_sync(0xFFFFFFFFu, a0, 4);    // column 8q + g + 1 (lane of g + 1)
+    const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, a1, 4);
+    if (g & 1) return;
+    const int word = 4 * q + (g >> 1);
+    const unsigned long long hi = (unsigned long long)tag << 32;
     const int t0 = 2 * cq, t1 = 2 * cq + 1;
     if (t0 < s.T) {
         const int pp = u == 0 ? t0 : sh->tok_pair[u][t0];
-        if (pp >= 0) s.p->act[sk_act_index(pp, j)] = __float2bfloat16_rn(silu_f(sum.x) * sum.z);
+        if (pp >= 0) st_relaxed_u64(s.p->act + (size_t)pp * (I / 2) + word, hi | a0 | (b0 << 16));
     }
     if (t1 < s.T) {
         const int pp = u == 0 ? t1 : sh->tok_pair[u][t1];
-        if (pp >= 0) s.p->act[sk_act_index(pp, j)] = __float2bfloat16_rn(silu_f(sum.y) * sum.w);
+        if (pp >= 0) st_relaxed_u64(s.p->act + (size_t)pp * (I / 2) + word, hi | a1 | (b1 << 16));
     }
 }
 
@@ -554,20 +566,20 @@ __device__ void sk_consumers(const SkState& s, int warp, int lane) {
                 const int i = pi / T, t = pi % T, e = c + i * G;
                 const uint4* wr = reinterpret_cast<const uint4*>(rows + i * H * 2);
                 const uint4* xr = reinterpret_cast<const uint4*>(s.ubuf + (size_t)t * SK_XSTRIDE);
-                float acc = 0.f;
+                float ac[4] = {0.f, 0.f, 0.f, 0.f};      // four independent chains
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const uint4 w = wr[lane + 32 * k], xv = xr[lane + 32 * k];
-                    acc = fmaf(bf_lo(w.x), bf_lo(xv.x), acc);
-                    acc = fmaf(bf_hi(w.x), bf_hi(xv.x), acc);
-                    acc = fmaf(bf_lo(w.y), bf_lo(xv.y), acc);
-                    acc = fmaf(bf_hi(w.y), bf_hi(xv.y), acc);
-                    acc = fmaf(bf_lo(w.z), bf_lo(xv.z), acc);
-                    acc = fmaf(bf_hi(w.z), bf_hi(xv.z), acc);
-                    acc = fmaf(bf_lo(w.w), bf_lo(xv.w), acc);
-                    acc = fmaf(bf_hi(w.w), bf_hi(xv.w), acc);
+                    ac[0] = fmaf(bf_lo(w.x), bf_lo(xv.x), ac[0]);
+                    ac[1] = fmaf(bf_hi(w.x), bf_hi(xv.x), ac[1]);
+                    ac[2] = fmaf(bf_lo(w.y), bf_lo(xv.y), ac[2]);
+                    ac[3] = fmaf(bf_hi(w.y), bf_hi(xv.y), ac[3]);
+                    ac[0] = fmaf(bf_lo(w.z), bf_lo(xv.z), ac[0]);
+                    ac[1] = fmaf(bf_hi(w.z), bf_hi(xv.z), ac[1]);
+                    ac[2] = fmaf(bf_lo(w.w), bf_lo(xv.w), ac[2]);
+                    ac[3] = fmaf(bf_hi(w.w), bf_hi(xv.w), ac[3]);
                 }
-                acc = warp_sum(acc);
+                const float acc = warp_sum((ac[0] + ac[1]) + (ac[2] + ac[3]));
                 if (lane == 0) {
                     const float v = acc + sh->bias[l][i];
                     st_relaxed_u64(p.logits + (size_t)t * E + e,
@@ -587,7 +599,7 @@ __device__ void sk_consumers(const SkState& s, int warp, int lane) {
                 *reinterpret_cast<float4*>(&sh->part[0][0][warp][lane * 4]) = make_float4(d[0], d[1], d[2], d[3]);
         }
         if (sk_phase_end(s, fail)) break;
-        if (has_sg && warp == 0) sk_gateup_finish(s, 0, 0, 0, c, lane);
+        if (has_sg && warp == 0) sk_gateup_finish(s, 0, 0, 0, c, lane, tag);
         // ---- 4. every token's 256 logits (tagged with this layer's epoch), top-6 ----
         if (warp < T) {
             float v[8];
@@ -652,22 +664,49 @@ __device__ void sk_consumers(const SkState& s, int warp, int lane) {
                 if (sk_quad_sync(s, quad, f)) break;
                 if (wq == ((j >> 1) & 3)) {
                     const int k = k0 + j;
-                    sk_gateup_finish(s, quad, par, 1 + k / SK_GU_UNITS, k % SK_GU_UNITS, lane);
+                    sk_gateup_finish(s, quad, par, 1 + k / SK_GU_UNITS, k % SK_GU_UNITS, lane, tag);
                 }
             }
         }
-        // ---- 7. every CTA's activations are written (grid barrier) ----
+        // ---- 7. every pair's activations (tagged with this layer's epoch: they
+        // are complete once every CTA finished its units) into shared memory,
+        // 16-byte chunk c of pair p's row at c ^ (p % 8); x is no longer read ----
         if (sk_phase_end(s, false)) break;
-        if (tid == 0) {
-            ++nbar;
-            if (!sk_grid_barrier(s, base + (unsigned long long)nbar * G)) sh->abort = 1;
+        {
+            // 16-byte units (two tagged words, four columns): eight per thread
+            // requested before any tag is checked
+            const int nu = sh->tab.n_pairs * (I / 4);
+            const uint64_t t0 = globaltimer_ns();
+            for (int u0 = tid; u0 < nu && !fail; u0 += 8 * SK_CW * 32) {
+                ulonglong2 v[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int i = u0 + k * SK_CW * 32;
+                    if (i < nu) v[k] = ld_relaxed_v2u64(p.act + 2 * (size_t)i);
+                }
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int i = u0 + k * SK_CW * 32;
+                    if (i >= nu || fail) continue;
+                    while ((unsigned int)(v[k].x >> 32) != tag || (unsigned int)(v[k].y >> 32) != tag) {
+                        if (sk_aborted(s) || *reinterpret_cast<volatile uint32_t*>(p.abort_flag)) {
+                            fail = true;
+                            break;
+                        }
+                        if (globaltimer_ns() - t0 > p.limit_ns) {
+                            sk_fail(s);
+                            fail = true;
+                            break;
+                        }
+                        v[k] = ld_relaxed_v2u64(p.act + 2 * (size_t)i);
+                    }
+                    const int pp = i / (I / 4), w = 2 * (i % (I / 4));   // pair, first word (columns 2w .. 2w + 3)
+                    *reinterpret_cast<uint2*>(s.ubuf + (size_t)pp * (I * 2) + ((((w >> 2) ^ (pp & 7))) << 4) +
+                                              (w & 3) * 4) = make_uint2((uint32_t)v[k].x, (uint32_t)v[k].y);
+                }
+            }
         }
-        if (sk_phase_end(s, false)) break;
-        // ---- 8. all pairs' activations into shared memory (x is no longer read) ----
-        const int npairs = sh->tab.n_pairs;
-        for (int i = tid; i < npairs * (I / 8); i += SK_CW * 32)
-            *reinterpret_cast<uint4*>(s.ubuf + (size_t)i * 16) = __ldcg(reinterpret_cast<const uint4*>(p.act) + i);
-        if (sk_phase_end(s, false)) break;
+        if (sk_phase_end(s, fail)) break;
         // ---- 9. down rows 16c .. 16c + 15 of every slot: warp u % 8 takes slot
         // u's item whole, the routing weights folded in per token ----
         const int has_dn = sk_has_dn(c);
@@ -737,6 +776,10 @@ __device__ void sk_consumers(const SkState& s, int warp, int lane) {
             if (sk_phase_end(s, false)) break;
         }
     }
+    // One more arrival per CTA at the end (nothing waits on it): a launch
+    // advances the counter by G x n_layers, so the epoch tags base / G + l + 1
+    // of two launches never meet, and the next launch still reads a multiple of G.
+    if (tid == 0 && !sk_aborted(s)) atomicAdd(p.bar, 1ull);
 }
 
 __global__ void __launch_bounds__(SK_THREADS, 1) stack_decode_kernel(const __grid_constant__ StackParams p) {
