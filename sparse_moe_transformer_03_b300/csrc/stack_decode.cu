@@ -684,22 +684,37 @@ __device__ void sk_consumers(const SkState& s, int warp, int lane) {
                     const int i = u0 + k * SK_CW * 32;
                     if (i < nu) v[k] = ld_relaxed_v2u64(p.act + 2 * (size_t)i);
                 }
+                // re-request every unit of the batch that is not this layer's yet,
+                // all at once, until none is left
+                for (;;) {
+                    bool pending = false;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const int i = u0 + k * SK_CW * 32;
+                        pending |= i < nu && ((unsigned int)(v[k].x >> 32) != tag || (unsigned int)(v[k].y >> 32) != tag);
+                    }
+                    if (!pending) break;
+                    if (sk_aborted(s) || *reinterpret_cast<volatile uint32_t*>(p.abort_flag)) {
+                        fail = true;
+                        break;
+                    }
+                    if (globaltimer_ns() - t0 > p.limit_ns) {
+                        sk_fail(s);
+                        fail = true;
+                        break;
+                    }
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const int i = u0 + k * SK_CW * 32;
+                        if (i < nu && ((unsigned int)(v[k].x >> 32) != tag || (unsigned int)(v[k].y >> 32) != tag))
+                            v[k] = ld_relaxed_v2u64(p.act + 2 * (size_t)i);
+                    }
+                }
+                if (fail) break;
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const int i = u0 + k * SK_CW * 32;
-                    if (i >= nu || fail) continue;
-                    while ((unsigned int)(v[k].x >> 32) != tag || (unsigned int)(v[k].y >> 32) != tag) {
-                        if (sk_aborted(s) || *reinterpret_cast<volatile uint32_t*>(p.abort_flag)) {
-                            fail = true;
-                            break;
-                        }
-                        if (globaltimer_ns() - t0 > p.limit_ns) {
-                            sk_fail(s);
-                            fail = true;
-                            break;
-                        }
-                        v[k] = ld_relaxed_v2u64(p.act + 2 * (size_t)i);
-                    }
+                    if (i >= nu) continue;
                     const int pp = i / (I / 4), w = 2 * (i % (I / 4));   // pair, first word (columns 2w .. 2w + 3)
                     *reinterpret_cast<uint2*>(s.ubuf + (size_t)pp * (I * 2) + ((((w >> 2) ^ (pp & 7))) << 4) +
                                               (w & 3) * 4) = make_uint2((uint32_t)v[k].x, (uint32_t)v[k].y);
