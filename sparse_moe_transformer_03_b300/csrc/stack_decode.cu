@@ -263,6 +263,7 @@ __host__ __device__ __forceinline__ int sk_rcum(int c, int G, int U) {
 // increasing id, each with its tokens in increasing order.  tok_pair[u][t] /
 // tok_w[u][t]: the pair and routing weight of token t in slot u (-1 / 0 when
 // t is not routed there).  Every lane works on its own experts and pairs.
+// The producer is released (route_bar) as soon as the slots' experts exist.
 __device__ void sk_build_tables(int T, SkShared* sh, int lane) {
     DecodeTables* tab = &sh->tab;
 #pragma unroll
@@ -310,6 +311,9 @@ __device__ void sk_build_tables(int T, SkShared* sh, int lane) {
         tab->slot_expert[0] = SHARED;
         tab->slot_pair0[0] = 0;
     }
+    __syncwarp();
+    // the producer needs only the slots' experts: let it start the routed copies
+    if (lane == 0) mbar_arrive(&sh->route_bar);
     for (int i = lane; i < ns * STACK_MAX_T; i += 32) {
         sh->tok_pair[i / STACK_MAX_T][i % STACK_MAX_T] = -1;
         sh->tok_w[i / STACK_MAX_T][i % STACK_MAX_T] = 0.f;
@@ -592,18 +596,23 @@ __device__ void sk_consumers(const SkState& s, int warp, int lane) {
         const int has_sg = sk_has_sg(c);
         const uint32_t seqSG = seq;
         seq += has_sg ? 4 : 0;
-        if (has_sg && !fail && warp < 4) {   // quad 0
-            float d[4];
-            fail = !sk_gateup_part(s, seqSG, warp, lane, d);
-            if (!fail)
-                *reinterpret_cast<float4*>(&sh->part[0][0][warp][lane * 4]) = make_float4(d[0], d[1], d[2], d[3]);
+        if (has_sg && warp < 4) {   // quad 0 (every warp of it reaches the quad barrier); quad 1
+                                    // meanwhile waits for the logits
+            if (!fail) {
+                float d[4];
+                fail = !sk_gateup_part(s, seqSG, warp, lane, d);
+                if (!fail)
+                    *reinterpret_cast<float4*>(&sh->part[0][0][warp][lane * 4]) = make_float4(d[0], d[1], d[2], d[3]);
+            }
+            if (sk_quad_sync(s, 0, fail)) fail = true;
+            else if (warp == 0) sk_gateup_finish(s, 0, 0, 0, c, lane, tag);
         }
-        if (sk_phase_end(s, fail)) break;
-        if (has_sg && warp == 0) sk_gateup_finish(s, 0, 0, 0, c, lane, tag);
-        // ---- 4. every token's 256 logits (tagged with this layer's epoch), top-6 ----
-        if (warp < T) {
+        // ---- 4. every token's 256 logits (tagged with this layer's epoch), top-6:
+        // token t on warp (t + 4) % 8 (quad 1 first) ----
+        const int tw = (warp + 4) & (SK_CW - 1);   // this warp's token
+        if (tw < T && !fail) {
             float v[8];
-            const unsigned long long* lg = p.logits + (size_t)warp * E + lane;
+            const unsigned long long* lg = p.logits + (size_t)tw * E + lane;
             const uint64_t t0 = globaltimer_ns();
             bool got = false;
             for (;;) {
@@ -632,17 +641,14 @@ __device__ void sk_consumers(const SkState& s, int warp, int lane) {
                 float wt[TOPK];
                 warp_top6(v, lane, sel, wt);
                 if (lane < TOPK) {
-                    sh->sel_e[warp * TOPK + lane] = pick6(sel, lane);
-                    sh->sel_w[warp * TOPK + lane] = pick6(wt, lane);
+                    sh->sel_e[tw * TOPK + lane] = pick6(sel, lane);
+                    sh->sel_w[tw * TOPK + lane] = pick6(wt, lane);
                 }
             }
         }
         if (sk_phase_end(s, fail)) break;
         // ---- 5. tables: slots (shared first, then the routed experts by id), pairs ----
-        if (warp == 0) {
-            sk_build_tables(T, sh, lane);
-            if (lane == 0) mbar_arrive(&sh->route_bar);
-        }
+        if (warp == 0) sk_build_tables(T, sh, lane);
         if (sk_phase_end(s, false)) break;
         const int U = sh->tab.n_slots - 1;
         // ---- 6. routed gate/up units of the CTA's range: quad q (warps 4q ..
