@@ -365,8 +365,8 @@ flint_status_t flint_moe_forward_layers(const flint_moe_t* layers, int n, const 
             p.layer[i].x = static_cast<const __nv_bfloat16*>(x[l0 + i]);
             p.layer[i].y = static_cast<__nv_bfloat16*>(y[l0 + i]);
         }
-        p.logits = reinterpret_cast<unsigned long long*>(h0->stack_clear);
-        p.act = reinterpret_cast<unsigned long long*>(h0->stack_clear + STACK_LOGITS_BYTES);
+        p.logits = reinterpret_cast<float*>(h0->stack_clear);
+        p.act = reinterpret_cast<__nv_bfloat16*>(h0->stack_clear + STACK_LOGITS_BYTES);
         p.bar = reinterpret_cast<unsigned long long*>(h0->stack_clear + STACK_LOGITS_BYTES + STACK_ACT_BYTES);
         p.abort_flag = reinterpret_cast<uint32_t*>(h0->stack_clear + STACK_LOGITS_BYTES + STACK_ACT_BYTES + 8);
         p.status = h0->status_dev;

@@ -125,18 +125,18 @@ struct StackParams {
     StackLayerArgs layer[STACK_MAX_LAYERS];
     int n_layers, T;
     uint32_t smem_bytes;             // the device's opt-in shared memory per block
-    unsigned long long* logits;      // [STACK_MAX_T][E] tagged logits (scratch)
-    unsigned long long* act;         // [STACK_MAX_T * 7][I / 2] tagged activation pairs (scratch)
-    unsigned long long* bar;         // grid barrier counter (scratch, follows the activations)
+    float* logits;                   // [STACK_MAX_T][E] router logits (scratch)
+    __nv_bfloat16* act;              // [STACK_MAX_T * 7][I] activations, chunk-swizzled rows (scratch)
+    unsigned long long* bar;         // grid barrier counter (scratch)
     uint32_t* abort_flag;            // set by a CTA whose bounded wait ran out
     uint32_t* status;
     uint64_t limit_ns;
 };
-// scratch of a stack launch inside a handle's workspace: tagged logits,
-// tagged activations, barrier counter and abort flag, contiguous (cleared
-// together after a device error)
-constexpr size_t STACK_LOGITS_BYTES = (size_t)STACK_MAX_T * E * 8;
-constexpr size_t STACK_ACT_BYTES = (size_t)STACK_MAX_T * (TOPK + 1) * (I / 2) * 8;
+// scratch of a stack launch inside a handle's workspace: logits,
+// activations, barrier counter and abort flag, contiguous (cleared together
+// after a device error)
+constexpr size_t STACK_LOGITS_BYTES = (size_t)STACK_MAX_T * E * 4;
+constexpr size_t STACK_ACT_BYTES = (size_t)STACK_MAX_T * (TOPK + 1) * I * 2;
 constexpr size_t STACK_CLEAR_BYTES = STACK_LOGITS_BYTES + STACK_ACT_BYTES + 16;
 cudaError_t stack_decode_set_attributes(int max_optin);
 cudaError_t launch_stack_decode(const LaunchCtx& L, StackParams& p, int max_optin);

@@ -7,6 +7,12 @@
 // mrchatgpt.org article (section 4) a decode megakernel; this kernel is this
 // library's design of that idea for B300.
 //
+// Cross-CTA exchanges cost about half a microsecond one way on B300 and a
+// 148-CTA barrier about 1.1 us (a polled counter); an exchange in which every
+// CTA polls every other CTA's data measured far slower (about 4 us), so the
+// three exchanges of a layer (logits, activations, y) are barriers followed
+// by one read.
+//
 // Why: at decode sizes a layer moves (U + 1) x 6 MiB of expert weights (U =
 // distinct routed experts) and little else, so it should run at HBM speed.
 // Three kernels per layer leave HBM idle while one kernel drains and the next
@@ -14,11 +20,10 @@
 // (one CTA per SM) walks the layers.  Per layer:
 //
 //   1. x (T rows) -> shared memory; each CTA dots its one or two router rows
-//      (prefetched during the previous layer) with every token and publishes
-//      the fp32 logits as 64-bit words tagged with the layer's epoch, so the
-//      other CTAs read them as soon as they land (no barrier);
+//      (prefetched during the previous layer) with every token, writes the
+//      fp32 logits and arrives at a grid barrier;
 //   2. meanwhile CTAs 0..63 multiply their unit of the shared expert
-//      (prefetched too); every CTA then waits for the 256 tagged logits of
+//      (prefetched too); after the barrier every CTA reads the 256 logits of
 //      each token, takes the top-6 (warp_top6) and builds the (slot, token)
 //      tables;
 //   3. a producer warp streams the CTA's routed gate/up units and then its
@@ -26,13 +31,11 @@
 //      tensor box per slot; eight consumer warps multiply them on the
 //      warp-level tensor core (mma.sync m16n8k16: 16 weight rows x 16
 //      columns against up to 8 tokens), the K dimension split over the
-//      warps, and compute a = silu(g) * u (bf16);
-//   4. the activations are published as 64-bit words tagged with the layer's
-//      epoch too; each CTA copies every pair's activations into shared memory
-//      as soon as all their tags are this layer's and applies its 16 down rows
-//      to every slot (the routing weight folded in per token, each warp
-//      summing its slots in order, then the warps in order): y is written
-//      once, deterministically;
+//      warps, and write a = silu(g) * u (bf16) to a scratch buffer;
+//   4. grid barrier; each CTA copies every pair's activations into shared
+//      memory and applies its 16 down rows to every slot (the routing weight
+//      folded in per token, each warp summing its slots in order, then the
+//      warps in order): y is written once, deterministically;
 //   5. grid barrier (layer l + 1 may read y_l), while the producer already
 //      streams layer l + 1's router rows and shared-expert unit.
 //
@@ -93,19 +96,6 @@ static_assert(offsetof(SkShared, route_bar) % 8 == 0, "mbarrier alignment");
 // 128-byte rows of the tiled layout: in-tile row r keeps its 16-byte chunk c at c ^ (r % 8)
 __device__ __forceinline__ uint32_t sw_chunk(int r, int c) { return (uint32_t)(((c ^ (r & 7)) << 4)); }
 
-__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
-    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
-    unsigned long long v;
-    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ ulonglong2 ld_relaxed_v2u64(const unsigned long long* p) {
-    ulonglong2 v;
-    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(v.x), "=l"(v.y) : "l"(p) : "memory");
-    return v;
-}
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
     unsigned long long v;
     asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
@@ -218,11 +208,16 @@ __device__ __forceinline__ void sk_release(const SkState& s, uint32_t q, int lan
                      : "memory");
 }
 
-// Grid barrier (one thread, after the consumer warps synchronised): arrive,
-// then wait until every CTA of the grid has arrived `target` - base times.
-__device__ bool sk_grid_barrier(const SkState& s, unsigned long long target) {
+// Grid barrier, split so that work can run between arriving and waiting.
+// Arrive (one thread, after the consumer warps synchronised, so that the
+// CTA's writes are ordered before it by the fence): count this CTA in.
+__device__ __forceinline__ void sk_grid_arrive(const SkState& s) {
     __threadfence();
     atomicAdd(s.p->bar, 1ull);
+}
+
+// Wait until every CTA of the grid has arrived `target` - base times.
+__device__ bool sk_grid_wait(const SkState& s, unsigned long long target) {
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
         if (ld_acquire_u64(s.p->bar) >= target) return true;
@@ -235,6 +230,11 @@ __device__ bool sk_grid_barrier(const SkState& s, unsigned long long target) {
             return false;
         }
     }
+}
+
+__device__ __forceinline__ bool sk_grid_barrier(const SkState& s, unsigned long long target) {
+    sk_grid_arrive(s);
+    return sk_grid_wait(s, target);
 }
 
 // ---- per-CTA work of a layer (identical formulas in producer and consumers) ----
@@ -476,14 +476,19 @@ __device__ __forceinline__ bool sk_gateup_part(const SkState& s, uint32_t sq, in
     return true;
 }
 
+// Activation rows in the scratch buffer: pair p's 512 bf16, its 16-byte
+// chunk c stored at c ^ (p % 8), so that the eight token rows of one MMA
+// operand read through different banks once copied into shared memory.
+__device__ __forceinline__ int sk_act_index(int p, int j) {
+    return p * I + ((((j >> 3) ^ (p & 7))) << 3) + (j & 7);
+}
+
 // The unit's four partial sums (part[quad][par][w]) added in warp order by
 // one warp; a = silu(gate) * up for the tokens routed to slot u (u = 0: the
 // shared expert, whose pair of token t is t; it runs before the layer's
-// tables exist), published as tagged words of two columns: lane (g, cq)
-// computes column 8q + g of tokens 2 cq and 2 cq + 1, and the even-g lane
-// of each column pair stores the word.
-__device__ __forceinline__ void sk_gateup_finish(const SkState& s, int quad, int par, int u, int q, int lane,
-                                                 unsigned int tag) {
+// tables exist).  Lane (g, cq) computes column 8q + g of tokens 2 cq and
+// 2 cq + 1.
+__device__ __forceinline__ void sk_gateup_finish(const SkState& s, int quad, int par, int u, int q, int lane) {
     SkShared* sh = s.sh;
     float4 sum = *reinterpret_cast<const float4*>(&sh->part[quad][par][0][lane * 4]);
 #pragma unroll
@@ -494,22 +499,15 @@ __device__ __forceinline__ void sk_gateup_finish(const SkState& s, int quad, int
         sum.z += v.z;
         sum.w += v.w;
     }
-    const int g = lane >> 2, cq = lane & 3;
-    const uint32_t a0 = __bfloat16_as_ushort(__float2bfloat16_rn(silu_f(sum.x) * sum.z));   // token 2 cq
-    const uint32_t a1 = __bfloat16_as_ushort(__float2bfloat16_rn(silu_f(sum.y) * sum.w));   // token 2 cq + 1
-    const uint32_t b0 = __shfl_down_sync(0xFFFFFFFFu, a0, 4);    // column 8q + g + 1 (lane of g + 1)
-    const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, a1, 4);
-    if (g & 1) return;
-    const int word = 4 * q + (g >> 1);
-    const unsigned long long hi = (unsigned long long)tag << 32;
+    const int g = lane >> 2, cq = lane & 3, j = 8 * q + g;
     const int t0 = 2 * cq, t1 = 2 * cq + 1;
     if (t0 < s.T) {
         const int pp = u == 0 ? t0 : sh->tok_pair[u][t0];
-        if (pp >= 0) st_relaxed_u64(s.p->act + (size_t)pp * (I / 2) + word, hi | a0 | (b0 << 16));
+        if (pp >= 0) s.p->act[sk_act_index(pp, j)] = __float2bfloat16_rn(silu_f(sum.x) * sum.z);
     }
     if (t1 < s.T) {
         const int pp = u == 0 ? t1 : sh->tok_pair[u][t1];
-        if (pp >= 0) st_relaxed_u64(s.p->act + (size_t)pp * (I / 2) + word, hi | a1 | (b1 << 16));
+        if (pp >= 0) s.p->act[sk_act_index(pp, j)] = __float2bfloat16_rn(silu_f(sum.y) * sum.w);
     }
 }
 
@@ -550,7 +548,6 @@ __device__ void sk_consumers(const SkState& s, int warp, int lane) {
     const int cq = lane & 3;
     for (int l = 0; l < p.n_layers; ++l) {
         const StackLayerArgs& Ly = p.layer[l];
-        const unsigned int tag = (unsigned int)(base / (unsigned long long)G) + (unsigned int)l + 1u;
         bool fail = false;
         // ---- 1. x rows into shared memory (16-byte loads through L2) ----
         for (int i = tid; i < T * (H / 8); i += SK_CW * 32) {
@@ -559,7 +556,7 @@ __device__ void sk_consumers(const SkState& s, int warp, int lane) {
             *reinterpret_cast<uint4*>(s.ubuf + (size_t)t * SK_XSTRIDE + k * 16) = v;
         }
         if (sk_phase_end(s, false)) break;
-        // ---- 2. this CTA's router rows: tagged fp32 logits (bias included) ----
+        // ---- 2. this CTA's router rows: fp32 logits (bias included) ----
         const int nr = sk_router_rows(c, G);
         const uint32_t seqR = seq;
         seq += nr ? 1 : 0;
@@ -584,20 +581,19 @@ __device__ void sk_consumers(const SkState& s, int warp, int lane) {
                     ac[3] = fmaf(bf_hi(w.w), bf_hi(xv.w), ac[3]);
                 }
                 const float acc = warp_sum((ac[0] + ac[1]) + (ac[2] + ac[3]));
-                if (lane == 0) {
-                    const float v = acc + sh->bias[l][i];
-                    st_relaxed_u64(p.logits + (size_t)t * E + e,
-                                   ((unsigned long long)tag << 32) | (unsigned long long)__float_as_uint(v));
-                }
+                if (lane == 0) p.logits[(size_t)t * E + e] = acc + sh->bias[l][i];
             }
             if (!fail) sk_release(s, seqR, lane, 1);
         }
+        // the CTA's logits are written: count it in at the logits barrier now,
+        // wait for the others after the shared unit
+        if (sk_phase_end(s, fail)) break;
+        if (tid == 0) sk_grid_arrive(s);
         // ---- 3. the shared expert's unit of this CTA (CTAs 0..63) ----
         const int has_sg = sk_has_sg(c);
         const uint32_t seqSG = seq;
         seq += has_sg ? 4 : 0;
-        if (has_sg && warp < 4) {   // quad 0 (every warp of it reaches the quad barrier); quad 1
-                                    // meanwhile waits for the logits
+        if (has_sg && warp < 4) {   // quad 0 (every warp of it reaches the quad barrier)
             if (!fail) {
                 float d[4];
                 fail = !sk_gateup_part(s, seqSG, warp, lane, d);
@@ -605,48 +601,29 @@ __device__ void sk_consumers(const SkState& s, int warp, int lane) {
                     *reinterpret_cast<float4*>(&sh->part[0][0][warp][lane * 4]) = make_float4(d[0], d[1], d[2], d[3]);
             }
             if (sk_quad_sync(s, 0, fail)) fail = true;
-            else if (warp == 0) sk_gateup_finish(s, 0, 0, 0, c, lane, tag);
+            else if (warp == 0) sk_gateup_finish(s, 0, 0, 0, c, lane);
         }
-        // ---- 4. every token's 256 logits (tagged with this layer's epoch), top-6:
-        // token t on warp (t + 4) % 8 (quad 1 first) ----
-        const int tw = (warp + 4) & (SK_CW - 1);   // this warp's token
-        if (tw < T && !fail) {
-            float v[8];
-            const unsigned long long* lg = p.logits + (size_t)tw * E + lane;
-            const uint64_t t0 = globaltimer_ns();
-            bool got = false;
-            for (;;) {
-                bool mine = true;
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const unsigned long long w = ld_relaxed_u64(lg + 32 * k);
-                    mine = mine && (unsigned int)(w >> 32) == tag;
-                    v[k] = __uint_as_float((unsigned int)w);
-                }
-                if (__all_sync(0xFFFFFFFFu, mine)) {
-                    got = true;
-                    break;
-                }
-                // warp-uniform decisions: every lane leaves the loop together
-                if (__any_sync(0xFFFFFFFFu, sk_aborted(s) || *reinterpret_cast<volatile uint32_t*>(p.abort_flag)))
-                    break;
-                if (__any_sync(0xFFFFFFFFu, globaltimer_ns() - t0 > p.limit_ns)) {
-                    if (lane == 0) sk_fail(s);
-                    break;
-                }
-            }
-            fail = !got;
-            if (got) {
-                int sel[TOPK];
-                float wt[TOPK];
-                warp_top6(v, lane, sel, wt);
-                if (lane < TOPK) {
-                    sh->sel_e[tw * TOPK + lane] = pick6(sel, lane);
-                    sh->sel_w[tw * TOPK + lane] = pick6(wt, lane);
-                }
-            }
-        }
+        // ---- 4. every CTA's logits are written (the barrier's wait; the shared
+        // unit's multiply above overlapped it); top-6 of token t on warp t ----
         if (sk_phase_end(s, fail)) break;
+        if (tid == 0) {
+            ++nbar;
+            if (!sk_grid_wait(s, base + (unsigned long long)nbar * G)) sh->abort = 1;
+        }
+        if (sk_phase_end(s, false)) break;
+        if (warp < T) {
+            float v[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] = __ldcg(p.logits + (size_t)warp * E + lane + 32 * k);
+            int sel[TOPK];
+            float wt[TOPK];
+            warp_top6(v, lane, sel, wt);
+            if (lane < TOPK) {
+                sh->sel_e[warp * TOPK + lane] = pick6(sel, lane);
+                sh->sel_w[warp * TOPK + lane] = pick6(wt, lane);
+            }
+        }
+        if (sk_phase_end(s, false)) break;
         // ---- 5. tables: slots (shared first, then the routed experts by id), pairs ----
         if (warp == 0) sk_build_tables(T, sh, lane);
         if (sk_phase_end(s, false)) break;
@@ -670,64 +647,24 @@ __device__ void sk_consumers(const SkState& s, int warp, int lane) {
                 if (sk_quad_sync(s, quad, f)) break;
                 if (wq == ((j >> 1) & 3)) {
                     const int k = k0 + j;
-                    sk_gateup_finish(s, quad, par, 1 + k / SK_GU_UNITS, k % SK_GU_UNITS, lane, tag);
+                    sk_gateup_finish(s, quad, par, 1 + k / SK_GU_UNITS, k % SK_GU_UNITS, lane);
                 }
             }
         }
-        // ---- 7. every pair's activations (tagged with this layer's epoch: they
-        // are complete once every CTA finished its units) into shared memory,
-        // 16-byte chunk c of pair p's row at c ^ (p % 8); x is no longer read ----
+        // ---- 7. every CTA's activations are written (grid barrier) ----
         if (sk_phase_end(s, false)) break;
-        {
-            // 16-byte units (two tagged words, four columns): eight per thread
-            // requested before any tag is checked
-            const int nu = sh->tab.n_pairs * (I / 4);
-            const uint64_t t0 = globaltimer_ns();
-            for (int u0 = tid; u0 < nu && !fail; u0 += 8 * SK_CW * 32) {
-                ulonglong2 v[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const int i = u0 + k * SK_CW * 32;
-                    if (i < nu) v[k] = ld_relaxed_v2u64(p.act + 2 * (size_t)i);
-                }
-                // re-request every unit of the batch that is not this layer's yet,
-                // all at once, until none is left
-                for (;;) {
-                    bool pending = false;
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const int i = u0 + k * SK_CW * 32;
-                        pending |= i < nu && ((unsigned int)(v[k].x >> 32) != tag || (unsigned int)(v[k].y >> 32) != tag);
-                    }
-                    if (!pending) break;
-                    if (sk_aborted(s) || *reinterpret_cast<volatile uint32_t*>(p.abort_flag)) {
-                        fail = true;
-                        break;
-                    }
-                    if (globaltimer_ns() - t0 > p.limit_ns) {
-                        sk_fail(s);
-                        fail = true;
-                        break;
-                    }
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const int i = u0 + k * SK_CW * 32;
-                        if (i < nu && ((unsigned int)(v[k].x >> 32) != tag || (unsigned int)(v[k].y >> 32) != tag))
-                            v[k] = ld_relaxed_v2u64(p.act + 2 * (size_t)i);
-                    }
-                }
-                if (fail) break;
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const int i = u0 + k * SK_CW * 32;
-                    if (i >= nu) continue;
-                    const int pp = i / (I / 4), w = 2 * (i % (I / 4));   // pair, first word (columns 2w .. 2w + 3)
-                    *reinterpret_cast<uint2*>(s.ubuf + (size_t)pp * (I * 2) + ((((w >> 2) ^ (pp & 7))) << 4) +
-                                              (w & 3) * 4) = make_uint2((uint32_t)v[k].x, (uint32_t)v[k].y);
-                }
-            }
+        if (tid == 0) {
+            ++nbar;
+            if (!sk_grid_barrier(s, base + (unsigned long long)nbar * G)) sh->abort = 1;
         }
-        if (sk_phase_end(s, fail)) break;
+        if (sk_phase_end(s, false)) break;
+        // ---- 8. all pairs' activations into shared memory (x is no longer read) ----
+        {
+            const int n16 = sh->tab.n_pairs * (I / 8);
+            for (int i = tid; i < n16; i += SK_CW * 32)
+                *reinterpret_cast<uint4*>(s.ubuf + (size_t)i * 16) = __ldcg(reinterpret_cast<const uint4*>(p.act) + i);
+        }
+        if (sk_phase_end(s, false)) break;
         // ---- 9. down rows 16c .. 16c + 15 of every slot: warp u % 8 takes slot
         // u's item whole, the routing weights folded in per token ----
         const int has_dn = sk_has_dn(c);
@@ -797,10 +734,6 @@ __device__ void sk_consumers(const SkState& s, int warp, int lane) {
             if (sk_phase_end(s, false)) break;
         }
     }
-    // One more arrival per CTA at the end (nothing waits on it): a launch
-    // advances the counter by G x n_layers, so the epoch tags base / G + l + 1
-    // of two launches never meet, and the next launch still reads a multiple of G.
-    if (tid == 0 && !sk_aborted(s)) atomicAdd(p.bar, 1ull);
 }
 
 __global__ void __launch_bounds__(SK_THREADS, 1) stack_decode_kernel(const __grid_constant__ StackParams p) {
