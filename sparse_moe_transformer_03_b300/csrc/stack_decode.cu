@@ -395,7 +395,14 @@ __device__ void sk_producer(const SkState& s, int lane) {
     const StackParams& p = *s.p;
     bool ok = sk_issue_router(s, pr, 0);
     if (ok && sk_has_sg(s.c)) ok = sk_issue_gateup(s, pr, p.layer[0].maps, SHARED, s.c);
+    tc::prefetch_tensormap(&p.layer[0].maps[0]);
+    tc::prefetch_tensormap(&p.layer[0].maps[1]);
     for (int l = 0; ok && l < p.n_layers; ++l) {
+        // the next layer's descriptors, ahead of their first use
+        if (l + 1 < p.n_layers) {
+            tc::prefetch_tensormap(&p.layer[l + 1].maps[0]);
+            tc::prefetch_tensormap(&p.layer[l + 1].maps[1]);
+        }
         // the consumers publish the layer's tables
         if (!sk_wait(s, &s.sh->route_bar, l & 1)) break;
         const DecodeTables& tab = s.sh->tab;
@@ -588,7 +595,7 @@ __device__ void sk_consumers(const SkState& s, int warp, int lane) {
         // the CTA's logits are written: count it in at the logits barrier now,
         // wait for the others after the shared unit
         if (sk_phase_end(s, fail)) break;
-        if (tid == 0) sk_grid_arrive(s);
+        if (tid == 4 * 32) sk_grid_arrive(s);   // warp 4: quad 0 goes on with the shared unit
         // ---- 3. the shared expert's unit of this CTA (CTAs 0..63) ----
         const int has_sg = sk_has_sg(c);
         const uint32_t seqSG = seq;
