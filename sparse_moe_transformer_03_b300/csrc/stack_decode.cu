@@ -210,10 +210,9 @@ __device__ __forceinline__ void sk_release(const SkState& s, uint32_t q, int lan
 
 // Grid barrier, split so that work can run between arriving and waiting.
 // Arrive (one thread, after the consumer warps synchronised, so that the
-// CTA's writes are ordered before it by the fence): count this CTA in.
+// CTA's writes are ordered before it by the release): count this CTA in.
 __device__ __forceinline__ void sk_grid_arrive(const SkState& s) {
-    __threadfence();
-    atomicAdd(s.p->bar, 1ull);
+    asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(s.p->bar) : "memory");
 }
 
 // Wait until every CTA of the grid has arrived `target` - base times.
@@ -557,10 +556,19 @@ __device__ void sk_consumers(const SkState& s, int warp, int lane) {
         const StackLayerArgs& Ly = p.layer[l];
         bool fail = false;
         // ---- 1. x rows into shared memory (16-byte loads through L2) ----
-        for (int i = tid; i < T * (H / 8); i += SK_CW * 32) {
-            const int t = i / (H / 8), k = i % (H / 8);
-            const uint4 v = __ldcg(reinterpret_cast<const uint4*>(Ly.x + (size_t)t * H) + k);
-            *reinterpret_cast<uint4*>(s.ubuf + (size_t)t * SK_XSTRIDE + k * 16) = v;
+        for (int i0 = tid; i0 < T * (H / 8); i0 += 8 * SK_CW * 32) {   // 8 loads in flight per thread
+            uint4 v[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int i = i0 + k * SK_CW * 32;
+                if (i < T * (H / 8)) v[k] = __ldcg(reinterpret_cast<const uint4*>(Ly.x + (size_t)(i / (H / 8)) * H) + i % (H / 8));
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int i = i0 + k * SK_CW * 32;
+                if (i < T * (H / 8))
+                    *reinterpret_cast<uint4*>(s.ubuf + (size_t)(i / (H / 8)) * SK_XSTRIDE + (i % (H / 8)) * 16) = v[k];
+            }
         }
         if (sk_phase_end(s, false)) break;
         // ---- 2. this CTA's router rows: fp32 logits (bias included) ----
@@ -668,8 +676,19 @@ __device__ void sk_consumers(const SkState& s, int warp, int lane) {
         // ---- 8. all pairs' activations into shared memory (x is no longer read) ----
         {
             const int n16 = sh->tab.n_pairs * (I / 8);
-            for (int i = tid; i < n16; i += SK_CW * 32)
-                *reinterpret_cast<uint4*>(s.ubuf + (size_t)i * 16) = __ldcg(reinterpret_cast<const uint4*>(p.act) + i);
+            for (int i0 = tid; i0 < n16; i0 += 8 * SK_CW * 32) {   // 8 loads in flight per thread
+                uint4 v[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int i = i0 + k * SK_CW * 32;
+                    if (i < n16) v[k] = __ldcg(reinterpret_cast<const uint4*>(p.act) + i);
+                }
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int i = i0 + k * SK_CW * 32;
+                    if (i < n16) *reinterpret_cast<uint4*>(s.ubuf + (size_t)i * 16) = v[k];
+                }
+            }
         }
         if (sk_phase_end(s, false)) break;
         // ---- 9. down rows 16c .. 16c + 15 of every slot: warp u % 8 takes slot
