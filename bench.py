@@ -492,8 +492,8 @@ def bench_decode(args, wl, name, layers, handles, ws, rank, nv, cpu_seconds):
     x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
     y_all = torch.empty((L, T, 2048), dtype=torch.bfloat16, device="cuda")
     ys = [y_all[l] for l in range(L)]
-    # T <= 8 bf16: the whole stack in one persistent launch (flint_moe_forward_layers)
-    use_stack = (not nv) and T <= STACK_MAX_T
+    # T <= 8: the whole stack in one persistent launch (flint_moe_forward_layers)
+    use_stack = T <= STACK_MAX_T
 
     # unique touched experts per layer (for the algorithmic byte count)
     uniq = []
@@ -619,7 +619,7 @@ def bench_decode(args, wl, name, layers, handles, ws, rank, nv, cpu_seconds):
                 "kernel": "stack_decode_kernel", "bytes_per_launch": stack["bytes_per_launch"],
                 "us_per_launch": stack["us_per_launch"],
                 "what": f"algorithmic bytes per launch (all {L} layers: unique touched experts incl. the shared one, "
-                        "6,291,456 B each) / its device duration (CUDA events around the launch, "
+                        f"{per_expert:,} B each) / its device duration (CUDA events around the launch, "
                         f"{stack['launches_timed']} extra launches)"}
     else:
         roof = {"bound": "hbm", **hbm_roof(kern[dom]["gbs"], peak_hbm, pk_kind),

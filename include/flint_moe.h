@@ -135,11 +135,11 @@ FLINT_API flint_status_t flint_moe_forward(flint_moe_t h, const void* x, int T, 
  *           earlier layer has written its y, so x[l + 1] may be y[l] (a
  *           chained stack) or any other buffer.
  *   T       tokens per layer, T >= 1.
- * FLINT_BF16 with T <= FLINT_STACK_MAX_T: ONE persistent kernel launch per
- * FLINT_STACK_MAX_LAYERS layers (one CTA per SM walks the layers; grid-wide
- * device-scope barriers separate a layer's phases, each wait bounded).  The
- * launch needs every SM of the device: do not run other kernels beside it.
- * Otherwise (larger T, NVFP4 layers): n flint_moe_forward calls.
+ * T <= FLINT_STACK_MAX_T (bf16 or NVFP4 layers): ONE persistent kernel
+ * launch per FLINT_STACK_MAX_LAYERS layers (one CTA per SM walks the layers;
+ * grid-wide device-scope barriers separate a layer's phases, each wait
+ * bounded).  The launch needs every SM of the device: do not run other
+ * kernels beside it.  Larger T: n flint_moe_forward calls.
  * Asynchronous on s, allocates nothing, capturable in a CUDA graph.  Scratch:
  * layers[0]'s workspace, so layers[0] must not be used on another stream
  * meanwhile; device errors are reported in layers[0]'s status word.

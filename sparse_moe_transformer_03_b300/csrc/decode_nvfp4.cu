@@ -46,6 +46,7 @@
 #include "../../include/flint_moe.h"
 #include "flint_internal.h"
 #include "mma_sync.cuh"
+#include "nvfp4_frag.cuh"
 #include "routing.cuh"
 
 namespace flint {
@@ -94,33 +95,6 @@ cudaError_t launch_repack_nvfp4(const uint8_t* packed, const uint8_t* scales, in
     const int total = nchunks * NV_CHUNK_KB * 32;
     repack_nvfp4_kernel<<<(total + 255) / 256, 256, 0, s>>>(packed, scales, kind, out);
     return cudaGetLastError();
-}
-
-// ---------------------------------------------------------------------------
-// fragments and MMAs
-// ---------------------------------------------------------------------------
-
-// A fragment (f16) of one 16 x 16 block: codes = this lane's 4 code bytes,
-// sc2 = E4M3 scales of its rows (g, g + 8).
-__device__ __forceinline__ void nv_a_frag(uint32_t codes, uint16_t sc2, uint32_t (&a)[4]) {
-    uint32_t s;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s) : "h"(sc2));
-    const __half2 s2 = *reinterpret_cast<const __half2*>(&s);
-    const __half2 sg = __low2half2(s2), s8 = __high2half2(s2);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        uint32_t h;
-        asm("{\n .reg .b8 t;\n cvt.u8.u32 t, %1;\n cvt.rn.f16x2.e2m1x2 %0, t;\n}\n" : "=r"(h) : "r"(codes >> (8 * k)));
-        const __half2 q = *reinterpret_cast<const __half2*>(&h);
-        const __half2 r = __hmul2(q, (k & 1) ? s8 : sg);
-        a[k] = *reinterpret_cast<const uint32_t*>(&r);
-    }
-}
-
-__device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t v) {
-    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&v));
-    const __nv_bfloat162 b = __float22bfloat162_rn(f);   // exact: at most 6 significant bits
-    return *reinterpret_cast<const uint32_t*>(&b);
 }
 
 // ---------------------------------------------------------------------------

@@ -342,9 +342,9 @@ flint_status_t flint_moe_forward_layers(const flint_moe_t* layers, int n, const 
         if (cudaMemsetAsync(h0->stack_clear, 0, STACK_CLEAR_BYTES, s) != cudaSuccess) return FLINT_ERR_CUDA;
         return st;
     }
-    const bool persistent = h0->dtype == FLINT_BF16 && T <= STACK_MAX_T && h0->num_sms >= 128 && h0->num_sms <= E;
+    const bool persistent = T <= STACK_MAX_T && h0->num_sms >= 128 && h0->num_sms <= E;
     if (!persistent) {
-        // larger batches and NVFP4 layers: one forward per layer, in order
+        // larger batches: one forward per layer, in order
         for (int l = 0; l < n; ++l) {
             st = flint_moe_forward(layers[l], x[l], T, y[l], s);
             if (st != FLINT_OK) return st;
@@ -357,9 +357,12 @@ flint_status_t flint_moe_forward_layers(const flint_moe_t* layers, int n, const 
         std::memset(&p, 0, sizeof p);
         p.n_layers = n - l0 < STACK_MAX_LAYERS ? n - l0 : STACK_MAX_LAYERS;
         p.T = T;
+        p.nvfp4 = h0->dtype == FLINT_NVFP4 ? 1 : 0;
         for (int i = 0; i < p.n_layers; ++i) {
             const flint_moe* h = layers[l0 + i];
             p.layer[i].maps = h->stack_maps;
+            p.layer[i].nv = h->nv;
+            p.layer[i].nv_ts = h->nv_ts;
             p.layer[i].router = h->router_W;
             p.layer[i].bias = h->router_b;
             p.layer[i].x = static_cast<const __nv_bfloat16*>(x[l0 + i]);

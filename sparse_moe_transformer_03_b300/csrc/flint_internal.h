@@ -108,14 +108,16 @@ cudaError_t launch_decode_experts_nvfp4(const LaunchCtx& L, const uint8_t* nv, c
                                         const float* logits, const __nv_bfloat16* x, int T, DecodeTables* tables,
                                         int32_t* idx, float* w, __nv_bfloat16* a_buf, __nv_bfloat16* y);
 
-// stack_decode.cu -- every layer of a stack in one persistent launch (bf16,
-// T <= STACK_MAX_T).  Layer l reads x of its own and writes its y; layer l
+// stack_decode.cu -- every layer of a stack in one persistent launch (bf16 or
+// NVFP4 experts, T <= STACK_MAX_T).  Layer l reads x of its own and writes its y; layer l
 // starts only after every CTA finished layer l - 1, so x[l] may be y[l - 1].
 constexpr int STACK_MAX_T = 8;
 constexpr int STACK_MAX_LAYERS = 64;
 struct StackLayerArgs {
-    const CUtensorMap* maps;         // the layer's tiled experts as 4-D tensor maps (device memory):
+    const CUtensorMap* maps;         // bf16: the layer's tiled experts as 4-D tensor maps (device memory):
                                      // [0] gate/up boxes (8 rows x 16 tiles), [1] down boxes (16 rows x 8 tiles)
+    const uint8_t* nv;               // NVFP4: the layer's owned experts (NV_EXPERT_BYTES each)
+    const float* nv_ts;              // NVFP4: tensor scales [NEXP][2] (gate_up, down)
     const __nv_bfloat16* router;     // [E][H]
     const float* bias;               // [E] or null
     const __nv_bfloat16* x;          // [T][H]
@@ -124,6 +126,7 @@ struct StackLayerArgs {
 struct StackParams {
     StackLayerArgs layer[STACK_MAX_LAYERS];
     int n_layers, T;
+    int nvfp4;                       // the layers' expert format: 0 bf16, 1 NVFP4
     uint32_t smem_bytes;             // the device's opt-in shared memory per block
     float* logits;                   // [STACK_MAX_T][E] router logits (scratch)
     __nv_bfloat16* act;              // [STACK_MAX_T * 7][I] activations, chunk-swizzled rows (scratch)

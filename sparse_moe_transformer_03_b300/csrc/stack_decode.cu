@@ -51,6 +51,7 @@
 #include "../../include/flint_moe.h"
 #include "flint_internal.h"
 #include "mma_sync.cuh"
+#include "nvfp4_frag.cuh"
 #include "routing.cuh"
 #include "tc_ptx.cuh"
 
@@ -62,13 +63,15 @@ namespace {
 
 constexpr int SK_CW = 8;                          // consumer warps
 constexpr int SK_THREADS = (SK_CW + 1) * 32;      // + one producer warp
-constexpr int SK_SLOT = 16384;                    // ring slot bytes: one tensor box
+constexpr int SK_SLOT_BF16 = 16384;               // bf16 ring slot: one tensor box
+constexpr int SK_SLOT_NV = NV_CHUNK;              // NVFP4 ring slot: one 4608-byte chunk
 constexpr int SK_GU_UNITS = I / 8;                // 64 gate/up units per expert
 constexpr int SK_DN_ITEMS = H / 16;               // 128 down row groups per expert
 constexpr int SK_GU_TILES = (2 * I / 128) * (H / 64);  // 256 gate/up tiles of an expert precede its down tiles
 constexpr int SK_XSTRIDE = H * 2 + 16;            // padded x row in shared memory
 constexpr int SK_MAX_SLOTS = 1 + STACK_MAX_T * TOPK;   // 49
-constexpr int SK_MAX_RING = 16;
+constexpr int SK_MAX_RING_BF16 = 16;
+constexpr int SK_MAX_RING = 48;                   // NVFP4 (the larger of the two)
 constexpr int SK_NAMED = 1;                       // named barrier of the consumer warps
 
 struct SkShared {
@@ -83,6 +86,7 @@ struct SkShared {
     float tok_w[SK_MAX_SLOTS][STACK_MAX_T];       // its routing weight (0 when not routed)
     alignas(16) float part[2][2][4][32 * 4];      // gate/up partial sums [quad][unit parity][warp of
                                                   // the quad][lane x 4]; down: [0][0..1] as [warp][lane x 4]
+    float xinv[STACK_MAX_T];                      // NVFP4: 2^-e of token t's f16 staging of x
     uint64_t route_bar;                           // consumers -> producer: tables of the layer are built
     // Ring slot i was last handed out for sequence number slot_seq[i] - 1.  A
     // consumer waits for its sequence number here before the slot's full
@@ -122,15 +126,20 @@ __host__ __device__ __forceinline__ uint32_t sk_ubuf_bytes(int T) {
     return ((xb > ab ? xb : ab) + 127u) & ~127u;
 }
 
-__host__ __device__ __forceinline__ SkLayout sk_layout(int T, uint32_t max_smem) {
+__host__ __device__ __forceinline__ uint32_t sk_slot_bytes(bool nv) { return nv ? SK_SLOT_NV : SK_SLOT_BF16; }
+
+__host__ __device__ __forceinline__ SkLayout sk_layout(int T, uint32_t max_smem, bool nv) {
     SkLayout L;
-    const uint32_t fixed = sk_ubuf_bytes(T) + (uint32_t)((sizeof(SkShared) + 127) & ~size_t(127)) + 256;
-    int ns = (int)((max_smem - fixed) / SK_SLOT);
-    if (ns > SK_MAX_RING) ns = SK_MAX_RING;
+    const uint32_t bars = 2 * SK_MAX_RING * 8;
+    const uint32_t fixed = sk_ubuf_bytes(T) + (uint32_t)((sizeof(SkShared) + 127) & ~size_t(127)) + bars;
+    int ns = (int)((max_smem - fixed) / sk_slot_bytes(nv));
+    const int cap = nv ? SK_MAX_RING : SK_MAX_RING_BF16;
+    if (ns > cap) ns = cap;
     L.nslot = ns;
-    L.ubuf_off = (uint32_t)ns * SK_SLOT;
+    L.ubuf_off = (uint32_t)ns * sk_slot_bytes(nv);
+    L.ubuf_off = (L.ubuf_off + 127u) & ~127u;
     L.bars_off = L.ubuf_off + sk_ubuf_bytes(T);
-    L.sh_off = L.bars_off + 256;                  // 2 x SK_MAX_RING mbarriers
+    L.sh_off = L.bars_off + bars;
     L.total = L.sh_off + (uint32_t)((sizeof(SkShared) + 127) & ~size_t(127));
     return L;
 }
@@ -143,6 +152,7 @@ struct SkState {
     uint64_t* empty;
     SkShared* sh;
     int nslot, T, c, G;
+    uint32_t slot;                                // ring slot bytes
 };
 
 __device__ __forceinline__ void sk_fail(const SkState& s) {
@@ -195,7 +205,7 @@ issued:
 }
 
 __device__ __forceinline__ uint8_t* sk_slot_ptr(const SkState& s, uint32_t q) {
-    return s.ring + (size_t)(q % (uint32_t)s.nslot) * SK_SLOT;
+    return s.ring + (size_t)(q % (uint32_t)s.nslot) * s.slot;
 }
 
 // Release ring sequence number q: the warp's share of the slot's SK_CW
@@ -344,7 +354,7 @@ struct SkProducer {
         if (use > 0 && !sk_wait(s, &s.empty[slot], (use - 1) & 1)) return false;
         mbar_arrive_expect_tx(&s.full[slot], bytes);
         st_release_shared(&s.sh->slot_seq[slot], seq + 1u);
-        *dst = s.ring + (size_t)slot * SK_SLOT;
+        *dst = s.ring + (size_t)slot * s.slot;
         *bar = &s.full[slot];
         ++seq;
         return true;
@@ -371,7 +381,7 @@ __device__ __forceinline__ bool sk_issue_gateup(const SkState& s, SkProducer& pr
     for (int k = 0; k < 4; ++k) {
         uint8_t* dst = nullptr;
         uint64_t* bar = nullptr;
-        if (!pr.take(s, SK_SLOT, &dst, &bar)) return false;
+        if (!pr.take(s, SK_SLOT_BF16, &dst, &bar)) return false;
         const int tile = ((k >> 1) * 4 + rb) * (H / 64) + (k & 1) * 16;   // up rows: row blocks 4..7
         tc::tma_load_4d(dst, &maps[0], 0, (r0 & 127) >> 2, tile, expert, bar);
     }
@@ -383,38 +393,81 @@ __device__ __forceinline__ bool sk_issue_down(const SkState& s, SkProducer& pr, 
                                               int g) {
     uint8_t* dst = nullptr;
     uint64_t* bar = nullptr;
-    if (!pr.take(s, SK_SLOT, &dst, &bar)) return false;
+    if (!pr.take(s, SK_SLOT_BF16, &dst, &bar)) return false;
     tc::tma_load_4d(dst, &maps[1], 0, (g & 7) * 4, SK_GU_TILES + (g >> 3) * (I / 64), expert, bar);
     return true;
 }
 
+// NVFP4 gate/up unit q of an expert: 4 slots, one 4608-byte chunk each (K
+// blocks 32 k .. 32 k + 31 of its 8 gate and 8 up rows, in the owned layout).
+__device__ __forceinline__ bool sk_issue_gateup_nv(const SkState& s, SkProducer& pr, const uint8_t* nv, int expert,
+                                                   int q) {
+    const uint8_t* unit = nv + (size_t)expert * NV_EXPERT_BYTES + (size_t)q * NV_GU_CHUNKS * NV_CHUNK;
+    for (int k = 0; k < NV_GU_CHUNKS; ++k) {
+        uint8_t* dst = nullptr;
+        uint64_t* bar = nullptr;
+        if (!pr.take(s, NV_CHUNK, &dst, &bar)) return false;
+        bulk_g2s(dst, unit + (size_t)k * NV_CHUNK, NV_CHUNK, bar);
+    }
+    return true;
+}
+
+// NVFP4 down rows 16 g .. 16 g + 15 of an expert (one slot: one chunk, K = 512).
+__device__ __forceinline__ bool sk_issue_down_nv(const SkState& s, SkProducer& pr, const uint8_t* nv, int expert,
+                                                 int g) {
+    uint8_t* dst = nullptr;
+    uint64_t* bar = nullptr;
+    if (!pr.take(s, NV_CHUNK, &dst, &bar)) return false;
+    bulk_g2s(dst, nv + (size_t)expert * NV_EXPERT_BYTES + NV_GU_BYTES + (size_t)g * NV_CHUNK, NV_CHUNK, bar);
+    return true;
+}
+
+template <bool NV>
+__device__ __forceinline__ bool sk_issue_unit(const SkState& s, SkProducer& pr, const StackLayerArgs& Ly, int expert,
+                                              int q) {
+    if constexpr (NV)
+        return sk_issue_gateup_nv(s, pr, Ly.nv, expert, q);
+    else
+        return sk_issue_gateup(s, pr, Ly.maps, expert, q);
+}
+
+template <bool NV>
 __device__ void sk_producer(const SkState& s, int lane) {
     if (lane != 0) return;
     SkProducer pr;
     const StackParams& p = *s.p;
     bool ok = sk_issue_router(s, pr, 0);
-    if (ok && sk_has_sg(s.c)) ok = sk_issue_gateup(s, pr, p.layer[0].maps, SHARED, s.c);
-    tc::prefetch_tensormap(&p.layer[0].maps[0]);
-    tc::prefetch_tensormap(&p.layer[0].maps[1]);
+    if (ok && sk_has_sg(s.c)) ok = sk_issue_unit<NV>(s, pr, p.layer[0], SHARED, s.c);
+    if constexpr (!NV) {
+        tc::prefetch_tensormap(&p.layer[0].maps[0]);
+        tc::prefetch_tensormap(&p.layer[0].maps[1]);
+    }
     for (int l = 0; ok && l < p.n_layers; ++l) {
         // the next layer's descriptors, ahead of their first use
-        if (l + 1 < p.n_layers) {
-            tc::prefetch_tensormap(&p.layer[l + 1].maps[0]);
-            tc::prefetch_tensormap(&p.layer[l + 1].maps[1]);
+        if constexpr (!NV) {
+            if (l + 1 < p.n_layers) {
+                tc::prefetch_tensormap(&p.layer[l + 1].maps[0]);
+                tc::prefetch_tensormap(&p.layer[l + 1].maps[1]);
+            }
         }
         // the consumers publish the layer's tables
         if (!sk_wait(s, &s.sh->route_bar, l & 1)) break;
         const DecodeTables& tab = s.sh->tab;
         const int U = tab.n_slots - 1;
-        const CUtensorMap* maps = p.layer[l].maps;
+        const StackLayerArgs& Ly = p.layer[l];
         const int k0 = sk_rcum(s.c - 1, s.G, U), k1 = sk_rcum(s.c, s.G, U);
         for (int k = k0; ok && k < k1; ++k)
-            ok = sk_issue_gateup(s, pr, maps, tab.slot_expert[1 + k / SK_GU_UNITS], k % SK_GU_UNITS);
+            ok = sk_issue_unit<NV>(s, pr, Ly, tab.slot_expert[1 + k / SK_GU_UNITS], k % SK_GU_UNITS);
         if (sk_has_dn(s.c))
-            for (int u = 0; ok && u <= U; ++u) ok = sk_issue_down(s, pr, maps, tab.slot_expert[u], s.c);
+            for (int u = 0; ok && u <= U; ++u) {
+                if constexpr (NV)
+                    ok = sk_issue_down_nv(s, pr, Ly.nv, tab.slot_expert[u], s.c);
+                else
+                    ok = sk_issue_down(s, pr, Ly.maps, tab.slot_expert[u], s.c);
+            }
         if (ok && l + 1 < p.n_layers) {
             ok = sk_issue_router(s, pr, l + 1);
-            if (ok && sk_has_sg(s.c)) ok = sk_issue_gateup(s, pr, p.layer[l + 1].maps, SHARED, s.c);
+            if (ok && sk_has_sg(s.c)) ok = sk_issue_unit<NV>(s, pr, p.layer[l + 1], SHARED, s.c);
         }
     }
     // copies still in flight (only after an abort): wait for them before exiting
@@ -482,6 +535,44 @@ __device__ __forceinline__ bool sk_gateup_part(const SkState& s, uint32_t sq, in
     return true;
 }
 
+// NVFP4 gate/up unit (slots sq .. sq + 3: its four chunks of K blocks) by a
+// quad of warps: warp wq dequantises chunk wq straight into A fragments (16
+// rows: 8 gate over 8 up, 512 columns) and multiplies them with x staged as
+// f16 (token t scaled by 2^e_t).  Releases the chunk's slot.
+__device__ __forceinline__ bool sk_gateup_part_nv(const SkState& s, uint32_t sq, int wq, int lane, float (&d)[4]) {
+    if (!__all_sync(0xFFFFFFFFu, sk_wait_full(s, sq + (uint32_t)wq))) return false;
+    const uint8_t* buf = sk_slot_ptr(s, sq + (uint32_t)wq);
+    const int g = lane >> 2, cq = lane & 3;
+    // B: token g's f16 row (padding tokens read token 0), columns 512 wq + 16 kb + 2 cq
+    const __half* xb =
+        reinterpret_cast<const __half*>(s.ubuf + (size_t)(g < s.T ? g : 0) * SK_XSTRIDE) + 512 * wq + 2 * cq;
+    float acc[4][4] = {};
+#pragma unroll
+    for (int kb = 0; kb < NV_CHUNK_KB; kb += 4) {
+        uint32_t a[4][4];
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch)
+            nv_a_frag(*reinterpret_cast<const uint32_t*>(buf + (kb + ch) * 128 + 4 * lane),
+                      *reinterpret_cast<const uint16_t*>(buf + NV_CODES + (kb + ch) * 16 + 2 * g), a[ch]);
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch)
+            mma_f16_16816(acc[ch], a[ch], *reinterpret_cast<const uint32_t*>(xb + (kb + ch) * 16),
+                          *reinterpret_cast<const uint32_t*>(xb + (kb + ch) * 16 + 8));
+    }
+    sk_release(s, sq + (uint32_t)wq, lane, SK_CW);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d[i] = (acc[0][i] + acc[1][i]) + (acc[2][i] + acc[3][i]);
+    return true;
+}
+
+template <bool NV>
+__device__ __forceinline__ bool sk_unit_part(const SkState& s, uint32_t sq, int wq, int lane, float (&d)[4]) {
+    if constexpr (NV)
+        return sk_gateup_part_nv(s, sq, wq, lane, d);
+    else
+        return sk_gateup_part(s, sq, wq, lane, d);
+}
+
 // Activation rows in the scratch buffer: pair p's 512 bf16, its 16-byte
 // chunk c stored at c ^ (p % 8), so that the eight token rows of one MMA
 // operand read through different banks once copied into shared memory.
@@ -494,7 +585,11 @@ __device__ __forceinline__ int sk_act_index(int p, int j) {
 // shared expert, whose pair of token t is t; it runs before the layer's
 // tables exist).  Lane (g, cq) computes column 8q + g of tokens 2 cq and
 // 2 cq + 1.
-__device__ __forceinline__ void sk_gateup_finish(const SkState& s, int quad, int par, int u, int q, int lane) {
+// NVFP4: the sums are scaled by the tensor scale tsg and the token's 2^-e_t
+// first.
+template <bool NV>
+__device__ __forceinline__ void sk_gateup_finish(const SkState& s, int quad, int par, int u, int q, int lane,
+                                                 const float* ts) {
     SkShared* sh = s.sh;
     float4 sum = *reinterpret_cast<const float4*>(&sh->part[quad][par][0][lane * 4]);
 #pragma unroll
@@ -507,6 +602,15 @@ __device__ __forceinline__ void sk_gateup_finish(const SkState& s, int quad, int
     }
     const int g = lane >> 2, cq = lane & 3, j = 8 * q + g;
     const int t0 = 2 * cq, t1 = 2 * cq + 1;
+    if constexpr (NV) {
+        const int expert = u == 0 ? SHARED : sh->tab.slot_expert[u];
+        const float tsg = __ldg(ts + 2 * expert);
+        const float f0 = t0 < s.T ? tsg * sh->xinv[t0] : 0.f, f1 = t1 < s.T ? tsg * sh->xinv[t1] : 0.f;
+        sum.x *= f0;
+        sum.z *= f0;
+        sum.y *= f1;
+        sum.w *= f1;
+    }
     if (t0 < s.T) {
         const int pp = u == 0 ? t0 : sh->tok_pair[u][t0];
         if (pp >= 0) s.p->act[sk_act_index(pp, j)] = __float2bfloat16_rn(silu_f(sum.x) * sum.z);
@@ -531,6 +635,7 @@ __device__ __forceinline__ bool sk_quad_sync(const SkState& s, int quad, bool fa
     return r != 0;
 }
 
+template <bool NV>
 __device__ void sk_consumers(const SkState& s, int warp, int lane) {
     const StackParams& p = *s.p;
     const int T = s.T, c = s.c, G = s.G, tid = warp * 32 + lane;
@@ -604,6 +709,44 @@ __device__ void sk_consumers(const SkState& s, int warp, int lane) {
         // wait for the others after the shared unit
         if (sk_phase_end(s, fail)) break;
         if (tid == 4 * 32) sk_grid_arrive(s);   // warp 4: quad 0 goes on with the shared unit
+        if constexpr (NV) {
+            // x -> f16 times 2^e_t in place, token t on warp t (the router is done
+            // with the bf16 rows): the token's largest |x| lands in [2^14, 2^15),
+            // exact for every bf16 value within 28 binades of it
+            if (warp < T) {
+                uint4* row = reinterpret_cast<uint4*>(s.ubuf + (size_t)warp * SK_XSTRIDE);
+                uint4 v[8];
+                float mx = 0.f;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    v[k] = row[lane + 32 * k];
+                    mx = fmaxf(mx, fmaxf(fmaxf(fabsf(bf_lo(v[k].x)), fabsf(bf_hi(v[k].x))),
+                                         fmaxf(fabsf(bf_lo(v[k].y)), fabsf(bf_hi(v[k].y)))));
+                    mx = fmaxf(mx, fmaxf(fmaxf(fabsf(bf_lo(v[k].z)), fabsf(bf_hi(v[k].z))),
+                                         fmaxf(fabsf(bf_lo(v[k].w)), fabsf(bf_hi(v[k].w)))));
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+                int e = mx > 0.f ? 14 - ilogbf(mx) : 0;
+                e = e > 126 ? 126 : e;
+                const float sc = ldexpf(1.f, e);
+                if (lane == 0) sh->xinv[warp] = ldexpf(1.f, -e);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const __half2 h0 = __floats2half2_rn(bf_lo(v[k].x) * sc, bf_hi(v[k].x) * sc);
+                    const __half2 h1 = __floats2half2_rn(bf_lo(v[k].y) * sc, bf_hi(v[k].y) * sc);
+                    const __half2 h2 = __floats2half2_rn(bf_lo(v[k].z) * sc, bf_hi(v[k].z) * sc);
+                    const __half2 h3 = __floats2half2_rn(bf_lo(v[k].w) * sc, bf_hi(v[k].w) * sc);
+                    uint4 o;
+                    o.x = *reinterpret_cast<const uint32_t*>(&h0);
+                    o.y = *reinterpret_cast<const uint32_t*>(&h1);
+                    o.z = *reinterpret_cast<const uint32_t*>(&h2);
+                    o.w = *reinterpret_cast<const uint32_t*>(&h3);
+                    row[lane + 32 * k] = o;
+                }
+            }
+            if (sk_phase_end(s, false)) break;
+        }
         // ---- 3. the shared expert's unit of this CTA (CTAs 0..63) ----
         const int has_sg = sk_has_sg(c);
         const uint32_t seqSG = seq;
@@ -611,12 +754,12 @@ __device__ void sk_consumers(const SkState& s, int warp, int lane) {
         if (has_sg && warp < 4) {   // quad 0 (every warp of it reaches the quad barrier)
             if (!fail) {
                 float d[4];
-                fail = !sk_gateup_part(s, seqSG, warp, lane, d);
+                fail = !sk_unit_part<NV>(s, seqSG, warp, lane, d);
                 if (!fail)
                     *reinterpret_cast<float4*>(&sh->part[0][0][warp][lane * 4]) = make_float4(d[0], d[1], d[2], d[3]);
             }
             if (sk_quad_sync(s, 0, fail)) fail = true;
-            else if (warp == 0) sk_gateup_finish(s, 0, 0, 0, c, lane);
+            else if (warp == 0) sk_gateup_finish<NV>(s, 0, 0, 0, c, lane, Ly.nv_ts);
         }
         // ---- 4. every CTA's logits are written (the barrier's wait; the shared
         // unit's multiply above overlapped it); top-6 of token t on warp t ----
@@ -653,7 +796,7 @@ __device__ void sk_consumers(const SkState& s, int warp, int lane) {
             const int quad = warp >> 2, wq = warp & 3;
             for (int j = quad; j < k1 - k0; j += 2) {
                 float d[4];
-                const bool f = !sk_gateup_part(s, seqRG + 4u * j, wq, lane, d);
+                const bool f = !sk_unit_part<NV>(s, seqRG + 4u * j, wq, lane, d);
                 const int par = (j >> 1) & 1;
                 if (!f)
                     *reinterpret_cast<float4*>(&sh->part[quad][par][wq][lane * 4]) = make_float4(d[0], d[1], d[2], d[3]);
@@ -662,7 +805,7 @@ __device__ void sk_consumers(const SkState& s, int warp, int lane) {
                 if (sk_quad_sync(s, quad, f)) break;
                 if (wq == ((j >> 1) & 3)) {
                     const int k = k0 + j;
-                    sk_gateup_finish(s, quad, par, 1 + k / SK_GU_UNITS, k % SK_GU_UNITS, lane);
+                    sk_gateup_finish<NV>(s, quad, par, 1 + k / SK_GU_UNITS, k % SK_GU_UNITS, lane, Ly.nv_ts);
                 }
             }
         }
@@ -703,30 +846,52 @@ __device__ void sk_consumers(const SkState& s, int warp, int lane) {
                 fail = true;
                 break;
             }
-            // A: rows r (m even) or 8 + r (m odd) of the 8 column tiles;
-            // B: token rows -> their pairs in slot u (token r: lane's row)
-            const uint8_t* wrow = sk_slot_ptr(s, qq) + (r + 8 * (m & 1)) * 128;
-            int pb = r < T ? sh->tok_pair[u][r] : -1;
-            pb = pb < 0 ? 0 : pb;
-            const uint8_t* br = s.ubuf + (size_t)pb * (I * 2);
             float acc[4][4] = {};
+            if constexpr (NV) {
+                // A: the chunk's 32 K blocks dequantised to bf16 fragments; B: token g's
+                // pair row in slot u (4-byte reads of the chunk-swizzled activations)
+                const uint8_t* buf = sk_slot_ptr(s, qq);
+                const int g = lane >> 2;
+                int pb = g < T ? sh->tok_pair[u][g] : -1;
+                pb = pb < 0 ? 0 : pb;
+                const uint8_t* ar = s.ubuf + (size_t)pb * (I * 2) + 4 * cq;
+#pragma unroll 8
+                for (int kb = 0; kb < NV_CHUNK_KB; ++kb) {
+                    uint32_t a[4];
+                    nv_a_frag(*reinterpret_cast<const uint32_t*>(buf + kb * 128 + 4 * lane),
+                              *reinterpret_cast<const uint16_t*>(buf + NV_CODES + kb * 16 + 2 * g), a);
 #pragma unroll
-            for (int kt = 0; kt < I / 64; ++kt) {
+                    for (int q = 0; q < 4; ++q) a[q] = f16x2_to_bf16x2(a[q]);
+                    mma_bf16_16816(acc[kb & 3], a, *reinterpret_cast<const uint32_t*>(ar + (((2 * kb) ^ (pb & 7)) << 4)),
+                                   *reinterpret_cast<const uint32_t*>(ar + (((2 * kb + 1) ^ (pb & 7)) << 4)));
+                }
+            } else {
+                // A: rows r (m even) or 8 + r (m odd) of the 8 column tiles;
+                // B: token rows -> their pairs in slot u (token r: lane's row)
+                const uint8_t* wrow = sk_slot_ptr(s, qq) + (r + 8 * (m & 1)) * 128;
+                int pb = r < T ? sh->tok_pair[u][r] : -1;
+                pb = pb < 0 ? 0 : pb;
+                const uint8_t* br = s.ubuf + (size_t)pb * (I * 2);
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t a[4], a2[4], b[4];
-                    ldmatrix_x4(a, wrow + kt * 2048 + sw_chunk(r, 4 * h + (m >> 1)));
-                    ldmatrix_x4(a2, wrow + kt * 2048 + sw_chunk(r, 4 * h + 2 + (m >> 1)));
-                    const int ch = 8 * kt + 4 * h + m;         // 16-byte chunk of the activation row
-                    ldmatrix_x4(b, br + ((ch ^ (pb & 7)) << 4));
-                    mma_bf16_16816(acc[2 * h], a, b[0], b[1]);
-                    mma_bf16_16816(acc[2 * h + 1], a2, b[2], b[3]);
+                for (int kt = 0; kt < I / 64; ++kt) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t a[4], a2[4], b[4];
+                        ldmatrix_x4(a, wrow + kt * 2048 + sw_chunk(r, 4 * h + (m >> 1)));
+                        ldmatrix_x4(a2, wrow + kt * 2048 + sw_chunk(r, 4 * h + 2 + (m >> 1)));
+                        const int ch = 8 * kt + 4 * h + m;         // 16-byte chunk of the activation row
+                        ldmatrix_x4(b, br + ((ch ^ (pb & 7)) << 4));
+                        mma_bf16_16816(acc[2 * h], a, b[0], b[1]);
+                        mma_bf16_16816(acc[2 * h + 1], a2, b[2], b[3]);
+                    }
                 }
             }
             sk_release(s, qq, lane, SK_CW);
-            // lane (g, cq): rows g and g + 8, tokens 2 cq and 2 cq + 1
-            const float w0 = 2 * cq < T ? sh->tok_w[u][2 * cq] : 0.f;
-            const float w1 = 2 * cq + 1 < T ? sh->tok_w[u][2 * cq + 1] : 0.f;
+            // lane (g, cq): rows g and g + 8, tokens 2 cq and 2 cq + 1 (NVFP4: times
+            // the down matrix's tensor scale)
+            const float tsd = NV ? __ldg(Ly.nv_ts + 2 * sh->tab.slot_expert[u] + 1) : 1.f;
+            const float w0 = 2 * cq < T ? sh->tok_w[u][2 * cq] * tsd : 0.f;
+            const float w1 = 2 * cq + 1 < T ? sh->tok_w[u][2 * cq + 1] * tsd : 0.f;
             float dd[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) dd[i] = (acc[0][i] + acc[1][i]) + (acc[2][i] + acc[3][i]);
@@ -762,10 +927,11 @@ __device__ void sk_consumers(const SkState& s, int warp, int lane) {
     }
 }
 
+template <bool NV>
 __global__ void __launch_bounds__(SK_THREADS, 1) stack_decode_kernel(const __grid_constant__ StackParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const SkLayout Lo = sk_layout(p.T, p.smem_bytes);
+    const SkLayout Lo = sk_layout(p.T, p.smem_bytes, NV);
     SkState s;
     s.p = &p;
     s.ring = smem;
@@ -777,10 +943,11 @@ __global__ void __launch_bounds__(SK_THREADS, 1) stack_decode_kernel(const __gri
     s.T = p.T;
     s.c = blockIdx.x;
     s.G = gridDim.x;
+    s.slot = sk_slot_bytes(NV);
     if (threadIdx.x == 0) {
         for (int i = 0; i < Lo.nslot; ++i) {
             mbar_init(&s.full[i], 1);
-            mbar_init(&s.empty[i], SK_CW);         // every consumer warp releases every slot
+            mbar_init(&s.empty[i], SK_CW);         // every consumer warp's share of a release
             s.sh->slot_seq[i] = 0u;
         }
         mbar_init(&s.sh->route_bar, 1);
@@ -789,24 +956,32 @@ __global__ void __launch_bounds__(SK_THREADS, 1) stack_decode_kernel(const __gri
     }
     __syncthreads();
     if (warp == SK_CW)
-        sk_producer(s, lane);
+        sk_producer<NV>(s, lane);
     else
-        sk_consumers(s, warp, lane);
+        sk_consumers<NV>(s, warp, lane);
 }
 
 }  // namespace
 
 cudaError_t stack_decode_set_attributes(int max_optin) {
-    return cudaFuncSetAttribute(stack_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_optin);
+    const cudaError_t e =
+        cudaFuncSetAttribute(stack_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_optin);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(stack_decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_optin);
 }
 
 cudaError_t launch_stack_decode(const LaunchCtx& L, StackParams& p, int max_optin) {
     if (p.T < 1 || p.T > STACK_MAX_T || p.n_layers < 1 || p.n_layers > STACK_MAX_LAYERS) return cudaErrorInvalidValue;
     if (L.num_sms < SK_DN_ITEMS || L.num_sms > E) return cudaErrorInvalidValue;
     p.smem_bytes = (uint32_t)max_optin;
-    const SkLayout Lo = sk_layout(p.T, (uint32_t)max_optin);
-    if (Lo.nslot < 6) return cudaErrorInvalidValue;
-    return launch_hooked(L, FLINT_KERNEL_GATE_UP, stack_decode_kernel, dim3(L.num_sms), dim3(SK_THREADS), Lo.total, p);
+    const bool nv = p.nvfp4 != 0;
+    const SkLayout Lo = sk_layout(p.T, (uint32_t)max_optin, nv);
+    if (Lo.nslot < (nv ? 16 : 6)) return cudaErrorInvalidValue;
+    if (nv)
+        return launch_hooked(L, FLINT_KERNEL_GATE_UP, stack_decode_kernel<true>, dim3(L.num_sms), dim3(SK_THREADS),
+                             Lo.total, p);
+    return launch_hooked(L, FLINT_KERNEL_GATE_UP, stack_decode_kernel<false>, dim3(L.num_sms), dim3(SK_THREADS),
+                         Lo.total, p);
 }
 
 }  // namespace flint

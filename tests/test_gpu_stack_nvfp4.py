@@ -53,3 +53,54 @@ def test_nvfp4_stack_graph_replay_matches_oracle(stack, T, kind, seed):
         ref, alt = nvfp4_oracle(*layers[l]).forward_with_alternatives(xb)
         res = compare(ys[l], ref, alt)
         assert res["ok"], (l, res)
+
+
+@pytest.mark.parametrize("T,kind,seed", [(1, "gauss", 11), (5, "gauss", 22), (8, "clustered", 12)])
+def test_nvfp4_stack_call_matches_oracle_every_layer(stack, T, kind, seed):
+    """All 47 NVFP4 layers in one persistent launch (flint_moe_forward_layers),
+    the same x for every layer: every layer against the oracle on the same
+    NVFP4 codes."""
+    layers, handles = stack
+    xb = gen.x_gaussian(seed, T) if kind == "gauss" else gen.x_clustered(seed, T)[0]
+    x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
+    ys = [torch.full_like(x, float("nan")) for _ in handles]
+    flint.flint_moe_forward_layers(handles, [x] * N_LAYERS, T, ys)
+    torch.cuda.synchronize()
+    for l in range(N_LAYERS):
+        y = ys[l].float().cpu().numpy()
+        assert np.isfinite(y).all(), l
+        ref, alt = nvfp4_oracle(*layers[l]).forward_with_alternatives(xb)
+        res = compare(y, ref, alt)
+        assert res["ok"], (l, res)
+
+
+def test_nvfp4_stack_call_chained_and_graph_replay(stack):
+    """Odd layers read the previous layer's output; the captured launch
+    replays to the same bits as the direct call."""
+    layers, handles = stack
+    T = 4
+    xb = gen.x_gaussian(33, T)
+    x0 = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
+    ys = [torch.full_like(x0, float("nan")) for _ in range(N_LAYERS)]
+    xs = [x0 if l % 2 == 0 else ys[l - 1] for l in range(N_LAYERS)]
+    flint.flint_moe_forward_layers(handles, xs, T, ys)
+    torch.cuda.synchronize()
+    direct = [y.clone() for y in ys]
+    for l in range(N_LAYERS):
+        y = ys[l].float().cpu().numpy()
+        assert np.isfinite(y).all(), l
+        inp = xb if l % 2 == 0 else ys[l - 1].view(torch.int16).cpu().numpy().view(np.uint16)
+        ref, alt = nvfp4_oracle(*layers[l]).forward_with_alternatives(inp)
+        res = compare(y, ref, alt)
+        assert res["ok"], (l, res)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        flint.flint_moe_forward_layers(handles, xs, T, ys, s)
+    for _ in range(2):
+        for y in ys:
+            y.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        for l in range(N_LAYERS):
+            assert torch.equal(ys[l], direct[l]), l

@@ -24,10 +24,11 @@ int main() {
             for (int c = -1; c < G; ++c) std::printf(" %d", sk_rcum(c, G, U));
             std::printf("\n");
         }
-    for (int T = 1; T <= 8; ++T) {
-        SkLayout L = sk_layout(T, 232448);
-        std::printf("L %d %d %u %u %u\n", T, L.nslot, L.ubuf_off, L.sh_off, L.total);
-    }
+    for (int nv = 0; nv < 2; ++nv)
+        for (int T = 1; T <= 8; ++T) {
+            SkLayout L = sk_layout(T, 232448, nv != 0);
+            std::printf("L %d %d %d %u %u %u\n", nv, T, L.nslot, L.ubuf_off, L.sh_off, L.total);
+        }
     return 0;
 }
 """
@@ -50,7 +51,7 @@ def plan(tmp_path_factory):
         if f[0] == "R":
             ranges[(int(f[1]), int(f[2]))] = np.array(f[3:], dtype=np.int64)
         else:
-            layouts[int(f[1])] = tuple(int(v) for v in f[2:])
+            layouts[(int(f[1]), int(f[2]))] = tuple(int(v) for v in f[3:])
     return ranges, layouts
 
 
@@ -73,8 +74,10 @@ def test_every_cta_gets_about_the_same_gate_up_units(plan):
 
 
 def test_shared_memory_fits_with_a_deep_ring(plan):
+    """bf16 slots are 16 KiB tensor boxes, NVFP4 slots 4608-byte chunks; the
+    ring holds at least two gate/up units (8 / 16 slots)."""
     _, layouts = plan
-    for T, (nslot, ubuf_off, sh_off, total) in layouts.items():
-        assert total <= 232448, T
-        assert nslot >= 8, (T, nslot)
-        assert ubuf_off == nslot * 16384
+    for (nv, T), (nslot, ubuf_off, sh_off, total) in layouts.items():
+        assert total <= 232448, (nv, T)
+        assert nslot >= (16 if nv else 8), (nv, T, nslot)
+        assert ubuf_off >= nslot * (4608 if nv else 16384) and ubuf_off % 128 == 0
