@@ -349,6 +349,7 @@ struct SkProducer {
 
     // Take the next slot for a copy of `bytes`.
     __device__ __forceinline__ bool take(const SkState& s, uint32_t bytes, uint8_t** dst, uint64_t** bar) {
+        if (bytes > s.slot) return false;    // never reached: every item fits its slot
         const int slot = (int)(seq % (uint32_t)s.nslot);
         const uint32_t use = seq / (uint32_t)s.nslot;
         if (use > 0 && !sk_wait(s, &s.empty[slot], (use - 1) & 1)) return false;
@@ -361,15 +362,27 @@ struct SkProducer {
     }
 };
 
-// Router rows of CTA c for layer l (one slot, plain bulk copies).
+// Ring slots of CTA c's router rows: both rows in one 16 KiB bf16 slot, one
+// row (4 KiB) per 4608-byte NVFP4 slot.
+__device__ __forceinline__ int sk_router_slots(const SkState& s) {
+    const int nr = sk_router_rows(s.c, s.G);
+    return s.slot >= (uint32_t)(2 * H * 2) ? (nr ? 1 : 0) : nr;
+}
+__device__ __forceinline__ const uint8_t* sk_router_row(const SkState& s, uint32_t seqR, int i) {
+    return s.slot >= (uint32_t)(2 * H * 2) ? sk_slot_ptr(s, seqR) + i * H * 2 : sk_slot_ptr(s, seqR + (uint32_t)i);
+}
+
+// Router rows of CTA c for layer l (plain bulk copies).
 __device__ __forceinline__ bool sk_issue_router(const SkState& s, SkProducer& pr, int l) {
     const int nr = sk_router_rows(s.c, s.G);
-    if (nr == 0) return true;
-    uint8_t* dst = nullptr;
-    uint64_t* bar = nullptr;
-    if (!pr.take(s, (uint32_t)nr * H * 2, &dst, &bar)) return false;
-    for (int i = 0; i < nr; ++i)
-        bulk_g2s(dst + i * H * 2, s.p->layer[l].router + (size_t)(s.c + i * s.G) * H, H * 2, bar);
+    const int per = sk_router_slots(s) == nr ? 1 : nr;    // rows per slot
+    for (int i = 0; i < nr; i += per) {
+        uint8_t* dst = nullptr;
+        uint64_t* bar = nullptr;
+        if (!pr.take(s, (uint32_t)per * H * 2, &dst, &bar)) return false;
+        for (int k = 0; k < per; ++k)
+            bulk_g2s(dst + k * H * 2, s.p->layer[l].router + (size_t)(s.c + (i + k) * s.G) * H, H * 2, bar);
+    }
     return true;
 }
 
@@ -677,15 +690,16 @@ __device__ void sk_consumers(const SkState& s, int warp, int lane) {
         }
         if (sk_phase_end(s, false)) break;
         // ---- 2. this CTA's router rows: fp32 logits (bias included) ----
-        const int nr = sk_router_rows(c, G);
+        const int nr = sk_router_rows(c, G), nrs = sk_router_slots(s);
         const uint32_t seqR = seq;
-        seq += nr ? 1 : 0;
+        seq += (uint32_t)nrs;
         if (nr) {
-            fail = !__all_sync(0xFFFFFFFFu, sk_wait_full(s, seqR));
-            const uint8_t* rows = sk_slot_ptr(s, seqR);
+            bool got = true;
+            for (int k = 0; k < nrs; ++k) got = got && sk_wait_full(s, seqR + (uint32_t)k);
+            fail = !__all_sync(0xFFFFFFFFu, got);
             for (int pi = warp; !fail && pi < nr * T; pi += SK_CW) {
                 const int i = pi / T, t = pi % T, e = c + i * G;
-                const uint4* wr = reinterpret_cast<const uint4*>(rows + i * H * 2);
+                const uint4* wr = reinterpret_cast<const uint4*>(sk_router_row(s, seqR, i));
                 const uint4* xr = reinterpret_cast<const uint4*>(s.ubuf + (size_t)t * SK_XSTRIDE);
                 float ac[4] = {0.f, 0.f, 0.f, 0.f};      // four independent chains
 #pragma unroll
@@ -703,7 +717,8 @@ __device__ void sk_consumers(const SkState& s, int warp, int lane) {
                 const float acc = warp_sum((ac[0] + ac[1]) + (ac[2] + ac[3]));
                 if (lane == 0) p.logits[(size_t)t * E + e] = acc + sh->bias[l][i];
             }
-            if (!fail) sk_release(s, seqR, lane, 1);
+            if (!fail)
+                for (int k = 0; k < nrs; ++k) sk_release(s, seqR + (uint32_t)k, lane, 1);
         }
         // the CTA's logits are written: count it in at the logits barrier now,
         // wait for the others after the shared unit
