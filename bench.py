@@ -48,6 +48,7 @@ WORKLOADS = {
     "nvfp4_decode1": {"T": 1, "x": "gauss", "x_seed": 11, "nvfp4": True},
     "nvfp4_decode8": {"T": 8, "x": "clustered", "x_seed": 12, "nvfp4": True},
     "nvfp4_decode32": {"T": 32, "x": "clustered", "x_seed": 13, "nvfp4": True},
+    "nvfp4_prefill8192": {"T": 8192, "x": "gauss", "x_seed": 14, "prefill": True, "nvfp4": True},
 }
 # dense flops of one layer per token: 7 experts x (gate, up, down) + router
 FLOPS_PER_TOKEN = 7 * 2 * 3 * 2048 * 512 + 2 * 256 * 2048
@@ -67,6 +68,10 @@ KERNEL_SOURCES = {
     "down_nvfp4_kernel": ["decode_nvfp4.cu", "mma_sync.cuh", "routing.cuh", "flint_common.cuh"],
     "prefill_gateup_kernel": ["prefill.cu", "tc_ptx.cuh", "flint_common.cuh"],
     "prefill_down_kernel": ["prefill.cu", "tc_ptx.cuh", "flint_common.cuh"],
+    "prefill_gateup_nvfp4_kernel": ["prefill_nvfp4.cu", "prefill_common.cuh", "nvfp4_frag.cuh", "tc_ptx.cuh",
+                                    "flint_common.cuh"],
+    "prefill_down_nvfp4_kernel": ["prefill_nvfp4.cu", "prefill_common.cuh", "nvfp4_frag.cuh", "tc_ptx.cuh",
+                                  "flint_common.cuh"],
     "stack_decode_kernel": ["stack_decode.cu", "mma_sync.cuh", "routing.cuh", "flint_common.cuh"],
 }
 
@@ -397,10 +402,10 @@ def cpu_baseline(wl, stack_layers, seconds=10.0):
 PREFILL_SAMPLE = 256   # tokens of the prefill input the oracle runs per step
 
 
-def cpu_baseline_prefill(wl, lw, xb, seconds=10.0):
-    """The oracle, as it stands, on the first PREFILL_SAMPLE tokens of the prefill input."""
-    from oracle.reference import LayerOracle
-    orc = LayerOracle.from_bf16_layer(lw)
+def cpu_baseline_prefill(wl, lw, xb, seconds=10.0, q=None):
+    """The oracle, as it stands, on the first PREFILL_SAMPLE tokens of the prefill input
+    (bf16 experts, or their NVFP4 encoding q)."""
+    orc = layer_oracle(lw, q)
     xs = xb[:PREFILL_SAMPLE]
     orc.forward(xs)                    # host copies of touched experts (untimed)
     t0 = time.perf_counter()
@@ -667,9 +672,11 @@ def bench_decode(args, wl, name, layers, handles, ws, rank, nv, cpu_seconds):
     return line
 
 
-def bench_prefill(args, wl, lw, h, ws, rank, cpu_seconds):
+def bench_prefill(args, wl, lw, h, ws, rank, cpu_seconds, q=None):
     """One MoE layer (layer 0 of the stack: skewed router bias) on T = 8192
-    tokens; weights (1.6 GB) exceed L2, so each step streams them again."""
+    tokens; weights (1.6 GB bf16, 0.45 GB NVFP4) exceed L2, so each step
+    streams them again.  q: the NVFP4 encoding of the layer (NVFP4 handle)."""
+    nv = q is not None
     import numpy as np
     import torch
     from sparse_moe_transformer_03_b300 import flint
@@ -717,11 +724,13 @@ def bench_prefill(args, wl, lw, h, ws, rank, cpu_seconds):
     gu_flops, dn_flops = 2.0 * slots * 2048 * 1024, 2.0 * slots * 512 * 2048
     # algorithmic bytes: every expert's matrices once (all 257 are touched at this T), the activations
     # the kernel reads once and the outputs it writes once
-    gu_bytes = 257 * GATE_UP_BYTES + T * 2048 * 2 + slots * 512 * 2
-    dn_bytes = 257 * DOWN_BYTES + slots * 512 * 2 + slots * 2048 * 2
+    gu_w, dn_w = (NV_GATE_UP_BYTES, NV_DOWN_BYTES) if nv else (GATE_UP_BYTES, DOWN_BYTES)
+    gu_bytes = 257 * gu_w + T * 2048 * 2 + slots * 512 * 2
+    dn_bytes = 257 * dn_w + slots * 512 * 2 + slots * 2048 * 2
+    sfx = "_nvfp4" if nv else ""
     kern = {}
-    for kname, kid, fl, by in (("prefill_gateup_kernel", K_GATE_UP, gu_flops, gu_bytes),
-                               ("prefill_down_kernel", K_DOWN, dn_flops, dn_bytes)):
+    for kname, kid, fl, by in ((f"prefill_gateup{sfx}_kernel", K_GATE_UP, gu_flops, gu_bytes),
+                               (f"prefill_down{sfx}_kernel", K_DOWN, dn_flops, dn_bytes)):
         d = kernel_durations(flint, torch, stream, calls, kid, ksteps)
         us = sum(r[0] for r in d) * 1e3 / ksteps
         kern[kname] = {"us_per_launch": us, "flops_per_launch": fl, "bytes_per_launch": by,
@@ -737,7 +746,7 @@ def bench_prefill(args, wl, lw, h, ws, rank, cpu_seconds):
     else:
         roof = {"bound": "tensor", "achieved": kd["tflops"], "peak": peak_tc, "unit": "TFLOP/s",
                 "frac": kd["tflops"] / peak_tc}
-    roof.update({"traffic": traffic_from_profiles(dom, "prefill8192"), "kernel": dom,
+    roof.update({"traffic": traffic_from_profiles(dom, "nvfp4_prefill8192" if nv else "prefill8192"), "kernel": dom,
                  "us_per_launch": kd["us_per_launch"], "bytes_per_launch": kd["bytes_per_launch"],
                  "flops_per_launch": kd["flops_per_launch"], "tensor_frac": kd["tflops"] / peak_tc,
                  "what": f"algorithmic bytes and flops per launch / its device duration (CUDA events around its "
@@ -747,10 +756,14 @@ def bench_prefill(args, wl, lw, h, ws, rank, cpu_seconds):
     achieved = flops / (ms * 1e-3) / 1e12
     line = {
         "metric": f"MoE-layer tokens/s, prefill T={T}", "value": whole_job_rate(T, ws, ms), "unit": "tokens/s",
-        "ms_per_step": ms, "us_per_layer": ms * 1e3, "dtype": "bf16",
-        "config": {"workload": f"prefill: one BF16 MoE layer (H=2048, I=512, 256 routed + 1 shared, top-6 sigmoid, "
-                               f"router bias N(0,0.5)), T={T} tokens (x ~ N(0,1) RMS-normalised, seed {wl['x_seed']})",
-                   "l2": "inputs larger than L2 (1.6 GB of expert weights per step)", "parallelism": f"replicas x{ws}"},
+        "ms_per_step": ms, "us_per_layer": ms * 1e3,
+        "dtype": ("nvfp4 weights (e2m1 + e4m3 block scales) dequantised to bf16 in shared memory, bf16 activations, "
+                  "f32 accumulation") if nv else "bf16",
+        "config": {"workload": f"prefill: one {'NVFP4 (W4A16)' if nv else 'BF16'} MoE layer (H=2048, I=512, 256 routed "
+                               f"+ 1 shared, top-6 sigmoid, router bias N(0,0.5)), T={T} tokens (x ~ N(0,1) "
+                               f"RMS-normalised, seed {wl['x_seed']})",
+                   "l2": f"inputs larger than L2 ({'0.45' if nv else '1.6'} GB of expert weights per step)",
+                   "parallelism": f"replicas x{ws}"},
         "roofline": roof,
         "kernels": kern,
         "layer_tensor": {"achieved": achieved, "peak": peak_tc, "unit": "TFLOP/s", "frac": achieved / peak_tc,
@@ -763,7 +776,7 @@ def bench_prefill(args, wl, lw, h, ws, rank, cpu_seconds):
                 "d2h_bytes_per_step": T * 2048 * 2},
     }
     if rank == 0 and ws == 1 and cpu_seconds > 0:
-        line["cpu_baseline"] = cpu_baseline_prefill(wl, lw, xb, cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline_prefill(wl, lw, xb, cpu_seconds, q)
     return line
 
 
@@ -773,8 +786,9 @@ COMMON_KEYS = ("n_gpus", "steps", "warmup", "higher_is_better", "scaling", "vs_b
 def run_flint(args, ws, rank, local):
     """The flint arm.  --workload all (the default): the BF16 decode stack at
     T = 1 (the headline line), then T = 8 and 32, the T = 8192 prefill on the
-    stack's first layer and the NVFP4 stack at T = 1, 8 and 32, each as an
-    entry of the line's "configs"; otherwise the named workload alone."""
+    stack's first layer, the NVFP4 stack at T = 1, 8 and 32 and the NVFP4
+    T = 8192 prefill, each as an entry of the line's "configs"; otherwise the
+    named workload alone."""
     import torch
     from sparse_moe_transformer_03_b300 import flint
     from synth import device
@@ -806,11 +820,16 @@ def run_flint(args, ws, rank, local):
         torch.cuda.empty_cache()
     if nv_names:
         t0 = time.perf_counter()
-        layers, handles = build_nvfp4_stack(flint, device, L)
+        layers, handles = build_nvfp4_stack(flint, device, L if any(not WORKLOADS[n].get("prefill") for n in nv_names)
+                                            else 1)
         gen_s["nvfp4"] = round(time.perf_counter() - t0, 2)
         for n in nv_names:
+            wl = WORKLOADS[n]
             cpu_s = HEADLINE_CPU_SECONDS if n == names[0] else CONFIG_CPU_SECONDS
-            results[n] = bench_decode(args, WORKLOADS[n], n, layers, handles, ws, rank, True, cpu_s)
+            if wl.get("prefill"):
+                results[n] = bench_prefill(args, wl, layers[0][0], handles[0], ws, rank, cpu_s, layers[0][1])
+            else:
+                results[n] = bench_decode(args, wl, n, layers, handles, ws, rank, True, cpu_s)
         for h in handles:
             flint.flint_moe_destroy(h)
         del layers, handles
@@ -831,7 +850,8 @@ def run_flint(args, ws, rank, local):
         print(json.dumps(line), flush=True)
 
 
-ALL_ORDER = ["decode1", "decode8", "decode32", "prefill8192", "nvfp4_decode1", "nvfp4_decode8", "nvfp4_decode32"]
+ALL_ORDER = ["decode1", "decode8", "decode32", "prefill8192", "nvfp4_decode1", "nvfp4_decode8", "nvfp4_decode32",
+             "nvfp4_prefill8192"]
 HEADLINE_CPU_SECONDS = 10.0
 CONFIG_CPU_SECONDS = 4.0
 

@@ -29,6 +29,7 @@ struct flint_moe {
     // NVFP4: owned repacked experts (NV_EXPERT_BYTES each) and tensor scales [NEXP][2]
     uint8_t* nv;
     float* nv_ts;
+    CUtensorMap nv_maps[4];        // NVFP4: gate/up codes and scales, down codes and scales (prefill boxes)
     CUtensorMap wr_map;            // router, boxes 64 x 256
     CUtensorMap h_map;             // h_perm, boxes 64 x 256
 
@@ -228,6 +229,7 @@ flint_status_t flint_moe_create(flint_moe_t* out, const void* router_W, const fl
         }
         if (st == FLINT_OK && cudaMemcpy(h->nv_ts, ts, sizeof ts, cudaMemcpyHostToDevice) != cudaSuccess)
             st = FLINT_ERR_CUDA;
+        if (st == FLINT_OK && !encode_nvfp4_prefill_maps(h->nv_maps, h->nv)) st = FLINT_ERR_CUDA;
     }
     if (st == FLINT_OK && dtype == FLINT_BF16) {
         if (cudaMalloc(&h->tiled, (size_t)NEXP * expert_elems * sizeof(__nv_bfloat16)) != cudaSuccess)
@@ -257,6 +259,7 @@ flint_status_t flint_moe_create(flint_moe_t* out, const void* router_W, const fl
     }
     if (st == FLINT_OK) st = from_cuda(prefill_set_attributes());
     if (st == FLINT_OK) st = from_cuda(decode_nvfp4_set_attributes());
+    if (st == FLINT_OK) st = from_cuda(prefill_nvfp4_set_attributes());
     if (st == FLINT_OK) st = from_cuda(decode_mma_set_attributes());
     if (st == FLINT_OK) st = from_cuda(stack_decode_set_attributes(h->smem_optin));
     if (st == FLINT_OK) st = from_cuda(cudaDeviceSynchronize());
@@ -282,18 +285,12 @@ flint_status_t flint_moe_forward(flint_moe_t h, const void* x, int T, void* y, c
     const LaunchCtx L = ctx_of(h, s);
     const __nv_bfloat16* xs = static_cast<const __nv_bfloat16*>(x);
     __nv_bfloat16* ys = static_cast<__nv_bfloat16*>(y);
-    if (h->dtype == FLINT_NVFP4) {
-        // weight-streaming kernels, in pieces of up to FLINT_DECODE_MAX_T tokens
-        for (int t0 = 0; t0 < T; t0 += DEC_T) {
-            const int Tc = T - t0 < DEC_T ? T - t0 : DEC_T;
-            cudaError_t e = launch_router_logits_decode(L, xs + (size_t)t0 * H, Tc, h->router_W, h->router_b,
-                                                        h->logits);
-            if (e == cudaSuccess)
-                e = launch_decode_experts_nvfp4(L, h->nv, h->nv_ts, h->logits, xs + (size_t)t0 * H, Tc,
-                                                h->dec_tables, h->idx, h->w, h->a_dec, ys + (size_t)t0 * H);
-            if (e != cudaSuccess) return FLINT_ERR_CUDA;
-        }
-        return FLINT_OK;
+    if (h->dtype == FLINT_NVFP4 && T <= DEC_T) {
+        cudaError_t e = launch_router_logits_decode(L, xs, T, h->router_W, h->router_b, h->logits);
+        if (e == cudaSuccess)
+            e = launch_decode_experts_nvfp4(L, h->nv, h->nv_ts, h->logits, xs, T, h->dec_tables, h->idx, h->w,
+                                            h->a_dec, ys);
+        return from_cuda(e);
     }
     if (T <= DEC_T) {
         cudaError_t e = launch_router_logits_decode(L, xs, T, h->router_W, h->router_b, h->logits);
@@ -313,9 +310,15 @@ flint_status_t flint_moe_forward(flint_moe_t h, const void* x, int T, void* y, c
         if (e == cudaSuccess)
             e = launch_perm_scan_scatter(L, h->idx, Tc, h->local_rank, h->blk_counts, h->blk_base, h->offsets,
                                          h->gather, h->pair_slot);
-        if (e == cudaSuccess)
-            e = launch_prefill_experts(L, xc, h->h_map, Tc, h->offsets, h->gather, h->pair_slot, h->w, h->tiled,
-                                       h->h_perm, h->o_perm, ys + (size_t)t0 * H);
+        if (e == cudaSuccess) {
+            if (h->dtype == FLINT_NVFP4)
+                e = launch_prefill_experts_nvfp4(L, xc, h->h_map, h->nv_maps, Tc, h->offsets, h->gather,
+                                                 h->pair_slot, h->w, h->nv_ts, h->h_perm, h->o_perm,
+                                                 ys + (size_t)t0 * H);
+            else
+                e = launch_prefill_experts(L, xc, h->h_map, Tc, h->offsets, h->gather, h->pair_slot, h->w,
+                                           h->tiled, h->h_perm, h->o_perm, ys + (size_t)t0 * H);
+        }
         if (e != cudaSuccess) return FLINT_ERR_CUDA;
     }
     return FLINT_OK;

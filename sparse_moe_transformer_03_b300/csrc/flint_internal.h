@@ -84,6 +84,9 @@ cudaError_t launch_prefill_experts(const LaunchCtx& L, const __nv_bfloat16* x, c
                                    const int32_t* offsets, const int32_t* gather, const int32_t* pair_slot,
                                    const float* w_route, const __nv_bfloat16* tiled, __nv_bfloat16* h_perm,
                                    __nv_bfloat16* o_perm, __nv_bfloat16* y);
+// y[t] = routed slots' outputs x routing weights + the shared slot, fixed order
+cudaError_t launch_prefill_combine(const LaunchCtx& L, const __nv_bfloat16* o_perm, const int32_t* pair_slot,
+                                   const float* w_route, int T, __nv_bfloat16* y);
 
 // decode_nvfp4.cu -- owned NVFP4 expert layout.  A chunk holds 16 matrix
 // rows x 512 columns (32 blocks of 16 columns): 32 x 128 bytes of E2M1 codes
@@ -107,6 +110,21 @@ cudaError_t decode_nvfp4_set_attributes();
 cudaError_t launch_decode_experts_nvfp4(const LaunchCtx& L, const uint8_t* nv, const float* nv_ts,
                                         const float* logits, const __nv_bfloat16* x, int T, DecodeTables* tables,
                                         int32_t* idx, float* w, __nv_bfloat16* a_buf, __nv_bfloat16* y);
+
+// tmap.cu: the owned NVFP4 experts as TMA tensors of 32-bit words
+bool encode_nvfp4_gateup(CUtensorMap* map, const uint8_t* nv, uint32_t box_words, uint32_t box_units);
+bool encode_nvfp4_down(CUtensorMap* map, const uint8_t* nv, uint32_t box_words, uint32_t box_units);
+
+// prefill_nvfp4.cu -- grouped tcgen05 GEMMs with the NVFP4 weight operand
+// dequantised in shared memory.  maps: gate/up codes, gate/up scales, down
+// codes, down scales (encode_nvfp4_prefill_maps).
+cudaError_t prefill_nvfp4_set_attributes();
+bool encode_nvfp4_prefill_maps(CUtensorMap (&maps)[4], const uint8_t* nv);
+cudaError_t launch_prefill_experts_nvfp4(const LaunchCtx& L, const __nv_bfloat16* x, const CUtensorMap& h_map,
+                                         const CUtensorMap (&maps)[4], int T, const int32_t* offsets,
+                                         const int32_t* gather, const int32_t* pair_slot, const float* w_route,
+                                         const float* nv_ts, __nv_bfloat16* h_perm, __nv_bfloat16* o_perm,
+                                         __nv_bfloat16* y);
 
 // stack_decode.cu -- every layer of a stack in one persistent launch (bf16 or
 // NVFP4 experts, T <= STACK_MAX_T).  Layer l reads x of its own and writes its y; layer l

@@ -54,4 +54,34 @@ bool encode_tiled_experts_4d(CUtensorMap* map, const void* tiled, uint32_t box_q
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The owned NVFP4 experts (decode_nvfp4.cu) viewed as 32-bit words, so a
+// 512-byte line of codes is one 128-element box row.  Gate/up view: 1152
+// words of a 4608-byte chunk x 4 chunks of a unit x 64 units x 257 experts;
+// a box of box_words x 1 chunk x box_units units.  Down view: 1152 words x
+// 128 units x 257 experts from the down part of expert 0; a box of box_words
+// x box_units units.  No swizzle: the bytes land as stored.
+static bool encode_u32(CUtensorMap* map, const void* base, int rank, const cuuint64_t* gdim,
+                       const cuuint64_t* gstride, const cuuint32_t* box) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint32_t estride[4] = {1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, rank, const_cast<void*>(base), gdim, gstride, box, estride,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_nvfp4_gateup(CUtensorMap* map, const uint8_t* nv, uint32_t box_words, uint32_t box_units) {
+    const cuuint64_t gdim[4] = {NV_CHUNK / 4, NV_GU_CHUNKS, NV_GU_UNITS, NEXP};
+    const cuuint64_t gstride[3] = {NV_CHUNK, (cuuint64_t)NV_GU_CHUNKS * NV_CHUNK, NV_EXPERT_BYTES};
+    const cuuint32_t box[4] = {box_words, 1, box_units, 1};
+    return encode_u32(map, nv, 4, gdim, gstride, box);
+}
+
+bool encode_nvfp4_down(CUtensorMap* map, const uint8_t* nv, uint32_t box_words, uint32_t box_units) {
+    const cuuint64_t gdim[3] = {NV_CHUNK / 4, NV_DN_UNITS, NEXP};
+    const cuuint64_t gstride[2] = {NV_CHUNK, NV_EXPERT_BYTES};
+    const cuuint32_t box[3] = {box_words, box_units, 1};
+    return encode_u32(map, nv + NV_GU_BYTES, 3, gdim, gstride, box);
+}
+
 }  // namespace flint

@@ -29,6 +29,18 @@ def handle_for(lw):
                                   (lw.gate_up[256], lw.down[256]))
 
 
+def nvfp4_oracle(lw, q):
+    """fp64 oracle layer on the exactly decoded NVFP4 weights of `q`
+    (device.LayerNVFP4 of `lw`); the router stays bf16."""
+    import oracle
+    from oracle.reference import LayerOracle
+
+    def mats(e):
+        (pg, sg, tg), (pd, sd, td) = q.expert_parts(e)
+        return (oracle.Mat(packed=pg, scales=sg, tensor_scale=tg), oracle.Mat(packed=pd, scales=sd, tensor_scale=td))
+    return LayerOracle(lw.router_bits(), lw.bias_host(), mats, mats(lw.E), lw.E)
+
+
 def x_for(kind, seed, T):
     if kind == "gauss":
         return gen.x_gaussian(seed, T)

@@ -6,19 +6,13 @@ import pytest
 import torch
 
 import oracle
-from oracle.reference import LayerOracle, compare
+from oracle.reference import compare
 from sparse_moe_transformer_03_b300 import flint
 from synth import device, gen
-from tests.gpu_common import layer, to_dev_bf16, x_for
+from tests.gpu_common import nvfp4_oracle, layer, to_dev_bf16, x_for
 
 pytestmark = pytest.mark.gpu
 
-
-def nvfp4_oracle(lw, q):
-    def mats(e):
-        (pg, sg, tg), (pd, sd, td) = q.expert_parts(e)
-        return (oracle.Mat(packed=pg, scales=sg, tensor_scale=tg), oracle.Mat(packed=pd, scales=sd, tensor_scale=td))
-    return LayerOracle(lw.router_bits(), lw.bias_host(), mats, mats(lw.E), lw.E)
 
 
 @pytest.fixture(scope="module", params=[(0, 0, False), (1, 0, True)], ids=["seed0", "seed1-bias"])

@@ -6,22 +6,15 @@ import numpy as np
 import pytest
 import torch
 
-import oracle
-from oracle.reference import LayerOracle, compare
+from oracle.reference import compare
 from sparse_moe_transformer_03_b300 import flint
 from synth import device, gen
+from tests.gpu_common import nvfp4_oracle
 from tests.test_gpu_stack import replay_stack
 
 pytestmark = pytest.mark.gpu
 
 N_LAYERS = 47
-
-
-def nvfp4_oracle(lw, q):
-    def mats(e):
-        (pg, sg, tg), (pd, sd, td) = q.expert_parts(e)
-        return (oracle.Mat(packed=pg, scales=sg, tensor_scale=tg), oracle.Mat(packed=pd, scales=sd, tensor_scale=td))
-    return LayerOracle(lw.router_bits(), lw.bias_host(), mats, mats(lw.E), lw.E)
 
 
 @pytest.fixture(scope="module")
