@@ -66,13 +66,13 @@ KERNEL_SOURCES = {
     "gateup_mma_kernel": ["decode_mma.cu", "mma_sync.cuh", "routing.cuh", "flint_common.cuh"],
     "down_mma_kernel": ["decode_mma.cu", "mma_sync.cuh", "routing.cuh", "flint_common.cuh"],
     "down_nvfp4_kernel": ["decode_nvfp4.cu", "mma_sync.cuh", "routing.cuh", "flint_common.cuh"],
-    "prefill_gateup_kernel": ["prefill.cu", "tc_ptx.cuh", "flint_common.cuh"],
-    "prefill_down_kernel": ["prefill.cu", "tc_ptx.cuh", "flint_common.cuh"],
-    "prefill_gateup_nvfp4_kernel": ["prefill_nvfp4.cu", "prefill_common.cuh", "nvfp4_frag.cuh", "tc_ptx.cuh",
+    "prefill_gateup_kernel": ["prefill.cu", "prefill_common.cuh", "tc_ptx.cuh", "flint_common.cuh"],
+    "prefill_down_kernel": ["prefill.cu", "prefill_common.cuh", "tc_ptx.cuh", "flint_common.cuh"],
+    "prefill_gateup_nvfp4_kernel": ["prefill_nvfp4.cu", "prefill_common.cuh", "tc_ptx.cuh",
                                     "flint_common.cuh"],
-    "prefill_down_nvfp4_kernel": ["prefill_nvfp4.cu", "prefill_common.cuh", "nvfp4_frag.cuh", "tc_ptx.cuh",
+    "prefill_down_nvfp4_kernel": ["prefill_nvfp4.cu", "prefill_common.cuh", "tc_ptx.cuh",
                                   "flint_common.cuh"],
-    "stack_decode_kernel": ["stack_decode.cu", "mma_sync.cuh", "routing.cuh", "flint_common.cuh"],
+    "stack_decode_kernel": ["stack_decode.cu", "mma_sync.cuh", "nvfp4_frag.cuh", "routing.cuh", "flint_common.cuh"],
 }
 
 

@@ -7,7 +7,7 @@
 //     block scales straight out of the owned NVFP4 layout (decode_nvfp4.cu:
 //     4608-byte chunks of 16 rows x 512 columns, codes in mma.sync A-fragment
 //     order) into a raw ring: 576 bytes per 16 rows;
-//   * four dequantising warps turn them into a bf16 tile in the canonical
+//   * eight dequantising warps turn them into a bf16 tile in the canonical
 //     128-byte-swizzle K-major layout the MMA reads.  code x block scale is
 //     exact in bf16 (at most 6 significant bits); the fp32 tensor scale
 //     multiplies the accumulator in the epilogue;
@@ -30,7 +30,7 @@
 
 namespace flint {
 
-constexpr int NQ_WARPS = 4;      // dequantising warps
+constexpr int NQ_WARPS = 8;      // dequantising warps
 constexpr int NQ_WBUF = 2;       // bf16 weight stages
 
 // Raw ring entry of one K step (4 K blocks) of a 128-row block made of
@@ -68,7 +68,7 @@ __device__ __forceinline__ void nq_drain(uint64_t* bars, int stages, int issued)
 // GEMM 1: gate/up + SwiGLU
 // ---------------------------------------------------------------------------
 // Warps: 0 = TMA of the raw weights (lane 0) and token gather, 1 = TMEM and
-// MMA issue, 2..9 = epilogue, 10 = token gather, 11..14 = dequantisation.
+// MMA issue, 2..9 = epilogue, 10 = token gather, 11..18 = dequantisation.
 // Rings: NQ_WBUF bf16 weight stages (gate tile, up tile), N1_STAGES stages of
 // (token tile, raw weights).
 
@@ -78,7 +78,8 @@ constexpr int N1_STAGES = 3;
 constexpr int N1_STAGE = GP_B_BYTES + N1_RAW;                 // 41 KiB
 constexpr int N1_WSTAGE = 2 * PF_TILE_BYTES;                  // 32 KiB
 constexpr int N1_BLOCKS = I / PF_TILE;                        // 4 row blocks
-constexpr int N1_THREADS = G1_THREADS + 32 * NQ_WARPS;        // 480
+constexpr int N1_THREADS = G1_THREADS + 32 * NQ_WARPS;        // 608
+constexpr int N1_UPW = N1_UNITS / NQ_WARPS;                   // owned units per dequantising warp
 constexpr int N1_DQ0 = G1_THREADS / 32;                       // first dequantising warp
 constexpr int N1_SMEM =
     1024 + NQ_WBUF * N1_WSTAGE + N1_STAGES * N1_STAGE + 512 + (int)sizeof(Sched) + 16 + GP_EPI_WARPS * STG_WARP;
@@ -150,6 +151,12 @@ __global__ void __launch_bounds__(N1_THREADS, 1)
         int kc_all = 0;
         for (int u = blockIdx.x; u < total && !__shfl_sync(0xFFFFFFFFu, *abort, 0); u += gridDim.x) {
             const Unit U = decode_unit(S, u);
+            if (warp == 0 && lane == 0 && u + (int)gridDim.x < total) {
+                // the CTA's next unit: its 128-row block (16 owned units x 4 chunks, contiguous) into L2
+                const Unit N = decode_unit(S, u + gridDim.x);
+                bulk_prefetch_l2(p.nv + (size_t)N.e * NV_EXPERT_BYTES + (size_t)N1_UNITS * N.blk * NV_GU_CHUNKS * NV_CHUNK,
+                                 N1_UNITS * NV_GU_CHUNKS * NV_CHUNK);
+            }
             const int nrows = U.npad >> 3;
             int tk[GP_N / 8];
 #pragma unroll
@@ -216,8 +223,8 @@ __global__ void __launch_bounds__(N1_THREADS, 1)
         }
         __syncwarp();
     } else if (warp >= N1_DQ0) {
-        // dequantisation: warp d takes owned units 4d .. 4d + 3 of the block
-        // (gate and up rows 32d .. 32d + 31)
+        // dequantisation: warp d takes owned units N1_UPW d .. N1_UPW (d + 1) - 1
+        // of the block (gate and up rows 8 N1_UPW d ..)
         const int d = warp - N1_DQ0, g = lane >> 2;
         int kc_all = 0;
         bool ok = true;
@@ -230,8 +237,8 @@ __global__ void __launch_bounds__(N1_THREADS, 1)
                 const uint8_t* raw = sring + s * N1_STAGE + GP_B_BYTES;
                 uint8_t* gt = wring + w * N1_WSTAGE;
 #pragma unroll
-                for (int qi = 0; qi < 4; ++qi) {
-                    const int ql = 4 * d + qi;
+                for (int qi = 0; qi < N1_UPW; ++qi) {
+                    const int ql = N1_UPW * d + qi;
                     const uint8_t* codes = raw + ql * 512;
                     const uint8_t* scales = raw + nq_raw_codes(N1_UNITS) + ql * 64;
                     uint8_t* row_g = gt + (8 * ql + g) * 128;            // gate row 8 ql + g of the block
@@ -286,7 +293,7 @@ __global__ void __launch_bounds__(N1_THREADS, 1)
 // GEMM 2: down projection
 // ---------------------------------------------------------------------------
 // Warps: 0 = TMA of activation tiles and raw weights (lane 0), 1 = TMEM and
-// MMA issue, 2..9 = epilogue (two TMEM accumulators), 10..13 = dequantisation.
+// MMA issue, 2..9 = epilogue (two TMEM accumulators), 10..17 = dequantisation.
 
 constexpr int N2_UNITS = PF_TILE / 16;                        // owned down units per 128-row block
 constexpr int N2_RAW = nq_raw_bytes(N2_UNITS);                // 4.5 KiB
@@ -294,7 +301,8 @@ constexpr int N2_STAGES = 4;
 constexpr int N2_STAGE = GP_B_BYTES + 5 * 1024;               // activations, raw (padded): 37 KiB
 constexpr int N2_WSTAGE = PF_TILE_BYTES;                      // 16 KiB
 constexpr int N2_BLOCKS = H / PF_TILE;                        // 16 row blocks
-constexpr int N2_THREADS = GP_THREADS + 32 * NQ_WARPS;        // 448
+constexpr int N2_THREADS = GP_THREADS + 32 * NQ_WARPS;        // 576
+constexpr int N2_UPW = N2_UNITS / NQ_WARPS;
 constexpr int N2_DQ0 = GP_THREADS / 32;
 constexpr int N2_SMEM =
     1024 + NQ_WBUF * N2_WSTAGE + N2_STAGES * N2_STAGE + 512 + (int)sizeof(Sched) + 16 + GP_EPI_WARPS * STG_WARP;
@@ -363,6 +371,12 @@ __global__ void __launch_bounds__(N2_THREADS, 1)
             int kc_all = 0;
             for (int u = blockIdx.x; u < total && !*abort; u += gridDim.x) {
                 const Unit U = decode_unit(S, u);
+                if (u + (int)gridDim.x < total) {
+                    // the CTA's next unit: its 8 owned down units (contiguous) into L2
+                    const Unit N = decode_unit(S, u + gridDim.x);
+                    bulk_prefetch_l2(p.nv + (size_t)N.e * NV_EXPERT_BYTES + NV_GU_BYTES + (size_t)N2_UNITS * N.blk * NV_CHUNK,
+                                     N2_UNITS * NV_CHUNK);
+                }
                 for (int kc = 0; kc < KC; ++kc) {
                     const int s = kc_all % N2_STAGES;
                     if (!pf_wait(&sempty[s], ((kc_all / N2_STAGES) & 1) ^ 1, p.limit_ns, abort)) break;
@@ -414,7 +428,7 @@ __global__ void __launch_bounds__(N2_THREADS, 1)
         }
         __syncwarp();
     } else if (warp >= N2_DQ0) {
-        // dequantisation: warp d takes owned units 2d, 2d + 1 (rows 32d .. 32d + 31)
+        // dequantisation: warp d takes owned units N2_UPW d .. (rows 16 N2_UPW d ..)
         const int d = warp - N2_DQ0, g = lane >> 2;
         int kc_all = 0;
         bool ok = true;
@@ -427,8 +441,8 @@ __global__ void __launch_bounds__(N2_THREADS, 1)
                 const uint8_t* raw = sring + s * N2_STAGE + GP_B_BYTES;
                 uint8_t* tile = wring + w * N2_WSTAGE;
 #pragma unroll
-                for (int vi = 0; vi < 2; ++vi) {
-                    const int v = 2 * d + vi;
+                for (int vi = 0; vi < N2_UPW; ++vi) {
+                    const int v = N2_UPW * d + vi;
                     const uint8_t* codes = raw + v * 512;
                     const uint8_t* scales = raw + nq_raw_codes(N2_UNITS) + v * 64;
                     uint8_t* row_lo = tile + (16 * v + g) * 128;
@@ -497,9 +511,9 @@ bool encode_nvfp4_prefill_maps(CUtensorMap (&maps)[4], const uint8_t* nv) {
 cudaError_t launch_prefill_experts_nvfp4(const LaunchCtx& L, const __nv_bfloat16* x, const CUtensorMap& h_map,
                                          const CUtensorMap (&maps)[4], int T, const int32_t* offsets,
                                          const int32_t* gather, const int32_t* pair_slot, const float* w_route,
-                                         const float* nv_ts, __nv_bfloat16* h_perm, __nv_bfloat16* o_perm,
-                                         __nv_bfloat16* y) {
-    GroupedParams gp{T, offsets, gather, w_route, nullptr, h_perm, o_perm, L.status, L.wait_limit_ns, nv_ts};
+                                         const uint8_t* nv, const float* nv_ts, __nv_bfloat16* h_perm,
+                                         __nv_bfloat16* o_perm, __nv_bfloat16* y) {
+    GroupedParams gp{T, offsets, gather, w_route, nullptr, h_perm, o_perm, L.status, L.wait_limit_ns, nv_ts, nv};
     cudaError_t e = launch_hooked(L, FLINT_KERNEL_GATE_UP, prefill_gateup_nvfp4_kernel, dim3(L.num_sms),
                                   dim3(N1_THREADS), N1_SMEM, x, maps[0], maps[1], gp);
     if (e != cudaSuccess) return e;
