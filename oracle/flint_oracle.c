@@ -245,6 +245,37 @@ void oracle_expert(int H, int I, const oracle_mat* gate_up, const oracle_mat* do
 }
 
 /* ------------------------------------------------------------------------ */
+/* output layer                                                             */
+/* ------------------------------------------------------------------------ */
+
+/* The 4-bit output layer (lm_head) as a plain matrix-vector product: the
+ * pages report that the output head was quantised to 4 bits too (the
+ * mrchatgpt.org article, section 4, the quantisation item; the
+ * qantcore.space review, section 04, the quantised variants).  The
+ * vocabulary size is not on the pages.  logits[t][j] = sum_h x[t][h] * W[rows[j]][h]
+ * for the nrows requested rows of W ([V][H], bf16 or NVFP4, decoded
+ * exactly), all of them in order when rows is NULL (nrows = V). */
+void oracle_lm_head(int T, int H, const uint16_t* x, const oracle_mat* W,
+                    int nrows, const int32_t* rows, double* out)
+{
+    double* w = (double*)malloc(sizeof(double) * (size_t)H);
+    double* xd = (double*)malloc(sizeof(double) * (size_t)T * H);
+    for (size_t i = 0; i < (size_t)T * H; ++i)
+        xd[i] = oracle_bf16_to_double(x[i]);
+    for (int j = 0; j < nrows; ++j) {
+        mat_row(W, rows ? rows[j] : j, w);
+        for (int t = 0; t < T; ++t) {
+            double acc = 0.0;
+            for (int h = 0; h < H; ++h)
+                acc += xd[(size_t)t * H + h] * w[h];
+            out[(size_t)t * nrows + j] = acc;
+        }
+    }
+    free(xd);
+    free(w);
+}
+
+/* ------------------------------------------------------------------------ */
 /* the layer                                                                */
 /* ------------------------------------------------------------------------ */
 

@@ -71,6 +71,8 @@ def _load():
         lib.oracle_moe_forward.argtypes = [i, i, i, i, i, P, P, P, P, P, P, P, P, P, P, P, P, i]
         lib.oracle_permutation.restype = None
         lib.oracle_permutation.argtypes = [i, i, i, P, P, P]
+        lib.oracle_lm_head.argtypes = [i, i, P, ctypes.POINTER(OracleMat), i, P, P]
+        lib.oracle_lm_head.restype = None
         _lib = lib
     return _lib
 
@@ -236,6 +238,21 @@ def moe_forward(x_bits, Wr_bits, bias, gate_up, down, shared, k: int = 6,
     return {"y": y, "logits": logits, "idx": idx, "w": w}
 
 
+def lm_head(x_bits, W: Mat, rows=None) -> np.ndarray:
+    """Output-layer logits [T][len(rows)] (every row of W when rows is None)
+    of x (bf16 bits [T][H]) against W ([V][H], bf16 or NVFP4)."""
+    x = _u16(x_bits)
+    T, H = x.shape
+    assert W.s.cols == H
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int32)
+    n = W.s.rows if r is None else len(r)
+    if r is not None:
+        assert ((r >= 0) & (r < W.s.rows)).all()
+    out = np.empty((T, n), dtype=np.float64)
+    _load().oracle_lm_head(T, H, _p(x), ctypes.byref(W.s), n, _p(r), _p(out))
+    return out
+
+
 def permutation(idx, E: int = 256):
     i = np.ascontiguousarray(idx, dtype=np.int32)
     T, k = i.shape
@@ -247,4 +264,4 @@ def permutation(idx, E: int = 256):
 
 __all__ = ["build", "Mat", "OracleMat", "bf16_to_double", "e2m1_decode", "e4m3_decode",
            "sigmoid", "silu", "nvfp4_dequant", "router_logits", "select", "expert",
-           "moe_forward", "permutation"]
+           "moe_forward", "permutation", "lm_head"]

@@ -33,6 +33,7 @@ T_CENTROID0 = 2          # 2..5: the four cluster centroids
 T_CLUSTER = 6            # cluster id per token
 T_ROUTER_W = 10
 T_ROUTER_B = 11
+T_LM_HEAD = 20           # output layer (lm_head) [V][H]
 T_GATE_UP0 = 100         # gate_up of expert e: 100 + 2e  (e = 256 is the shared expert)
 T_DOWN0 = 101            # down    of expert e: 101 + 2e
 
