@@ -49,7 +49,12 @@ WORKLOADS = {
     "nvfp4_decode8": {"T": 8, "x": "clustered", "x_seed": 12, "nvfp4": True},
     "nvfp4_decode32": {"T": 32, "x": "clustered", "x_seed": 13, "nvfp4": True},
     "nvfp4_prefill8192": {"T": 8192, "x": "gauss", "x_seed": 14, "prefill": True, "nvfp4": True},
+    "nvfp4_lm_head1": {"T": 1, "x": "gauss", "x_seed": 11, "lm_head": True},
+    "nvfp4_lm_head32": {"T": 32, "x": "clustered", "x_seed": 13, "lm_head": True},
 }
+LM_HEAD_V = 131072        # assumed vocabulary (not on the pages): the head is about 10.7% of 2.5B active
+LM_HEAD_SEED = 5
+LM_HEAD_SAMPLE_ROWS = 2048   # rows of the head the oracle evaluates per CPU-baseline step
 # dense flops of one layer per token: 7 experts x (gate, up, down) + router
 FLOPS_PER_TOKEN = 7 * 2 * 3 * 2048 * 512 + 2 * 256 * 2048
 GATE_UP_BYTES = 2 * 512 * 2048 * 2            # one expert's gate and up matrices, bf16
@@ -72,6 +77,7 @@ KERNEL_SOURCES = {
                                     "flint_common.cuh"],
     "prefill_down_nvfp4_kernel": ["prefill_nvfp4.cu", "prefill_common.cuh", "tc_ptx.cuh",
                                   "flint_common.cuh"],
+    "lm_head_nvfp4_kernel": ["lm_head.cu", "mma_sync.cuh", "nvfp4_frag.cuh", "flint_common.cuh"],
     "stack_decode_kernel": ["stack_decode.cu", "mma_sync.cuh", "nvfp4_frag.cuh", "routing.cuh", "flint_common.cuh"],
 }
 
@@ -311,6 +317,9 @@ def run_reference(args, wl, ws, rank):
     device.build()
     T = wl["T"]
     xb = x_bits_for(wl)
+    if wl.get("lm_head"):
+        run_reference_lm_head(args, wl, xb)
+        return
     prefill = bool(wl.get("prefill"))
     n_layers = 1 if prefill else 2
     xs = xb[:PREFILL_SAMPLE] if prefill else xb
@@ -353,6 +362,42 @@ def run_reference(args, wl, ws, rank):
             "config": {"workload": workload, "H": 2048, "I": 512, "experts": 257, "top_k": 6},
             "vs_baseline": None,
             "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_reference_lm_head(args, wl, xb):
+    """The oracle on the first LM_HEAD_SAMPLE_ROWS rows of the output layer
+    per step (the head generated and quantised by the input generator, not
+    by the library), scaled to the whole vocabulary."""
+    import torch
+    import oracle
+    from synth import device, gen
+    # the tensor scale depends on the whole head: quantise all of it, keep the sample rows
+    full = torch.empty((LM_HEAD_V, gen.H), dtype=torch.bfloat16, device="cuda")
+    device.fill_normal_bf16(full, LM_HEAD_SEED, 0, gen.T_LM_HEAD, gen.WEIGHT_STD)
+    pk, sc, ts = device.nvfp4_quantize(full)
+    m = oracle.Mat(packed=pk[0][:LM_HEAD_SAMPLE_ROWS].cpu().numpy(), scales=sc[0][:LM_HEAD_SAMPLE_ROWS].cpu().numpy(),
+                   tensor_scale=float(ts[0].item()))
+    del full, pk, sc
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.lm_head(xb, m)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    step = sum(times) / len(times) * LM_HEAD_V / LM_HEAD_SAMPLE_ROWS
+    T = wl["T"]
+    value, unit = T / step, "tokens/s"
+    sample = (f"first {LM_HEAD_SAMPLE_ROWS} of the {LM_HEAD_V} head rows at T={T} per step, scaled by "
+              f"{LM_HEAD_V // LM_HEAD_SAMPLE_ROWS} to the whole head")
+    line = {"metric": f"output-layer tokens/s, NVFP4 lm_head T={T}", "value": value, "unit": unit,
+            "impl": "reference", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": step * 1e3, "higher_is_better": True, "scaling": "weak", "us_per_call": step * 1e6,
+            "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"output layer: NVFP4 head [{LM_HEAD_V}][2048], T={T}; {sample}"},
+            "vs_baseline": None,
+            "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -780,6 +825,114 @@ def bench_prefill(args, wl, lw, h, ws, rank, cpu_seconds, q=None):
     return line
 
 
+def build_lm_head(flint, device, V, seed):
+    """A seeded bf16 head [V][2048] quantised to NVFP4 on the device and its
+    handle; returns (handle, host packed, host scales, tensor scale)."""
+    import torch
+    from synth import gen
+    w = torch.empty((V, gen.H), dtype=torch.bfloat16, device="cuda")
+    device.fill_normal_bf16(w, seed, 0, gen.T_LM_HEAD, gen.WEIGHT_STD)
+    pk, sc, ts = device.nvfp4_quantize(w)
+    del w
+    t = float(ts[0].item())
+    h = flint.flint_lm_head_create((pk[0], sc[0], t), V)
+    parts = (pk[0][:LM_HEAD_SAMPLE_ROWS].cpu().numpy(), sc[0][:LM_HEAD_SAMPLE_ROWS].cpu().numpy(), t)
+    del pk, sc
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return h, parts
+
+
+def bench_lm_head(args, wl, ws, rank, cpu_seconds):
+    """The 4-bit output layer: one flint_lm_head_forward per step on a
+    V x 2048 NVFP4 head (151 MB, larger than L2, so each step streams it)."""
+    import numpy as np
+    import torch
+    from sparse_moe_transformer_03_b300 import flint
+    from synth import device
+
+    T, V = wl["T"], LM_HEAD_V
+    pk_, pk_kind = peaks()
+    h, parts = build_lm_head(flint, device, V, LM_HEAD_SEED)
+    xb = x_bits_for(wl)
+    x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
+    logits = torch.empty((T, V), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.Stream()
+
+    def step():
+        flint.flint_lm_head_forward(h, x, T, logits, stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    stream.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        with torch.cuda.stream(stream):
+            ms = timed_ms(torch, stream, step, args.steps)
+    torch.cuda.synchronize()
+    clocks = clk.summary()
+    x_host = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).pin_memory()
+    l_host = torch.empty((T, V), dtype=torch.float32).pin_memory()
+    x_dev = torch.empty_like(x)
+
+    def step_e2e():
+        x_dev.copy_(x_host, non_blocking=True)
+        flint.flint_lm_head_forward(h, x_dev, T, logits, stream)
+        l_host.copy_(logits, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        step_e2e()
+        ms_e2e = timed_ms(torch, stream, step_e2e, max(3, args.steps // 2))
+    ms, ms_e2e = max_over_ranks([ms, ms_e2e])
+    flint.flint_lm_head_destroy(h)
+    # algorithmic bytes: every code and block scale once, x once, the logits written once
+    w_bytes = V * (2048 // 2 + 2048 // 16)
+    by = w_bytes + T * 2048 * 2 + T * V * 4
+    gbs = by / (ms * 1e-3) / 1e9
+    line = {
+        "metric": f"output-layer tokens/s, NVFP4 lm_head T={T}", "value": whole_job_rate(T, ws, ms),
+        "unit": "tokens/s", "ms_per_step": ms, "us_per_call": ms * 1e3,
+        "dtype": "nvfp4 weights (e2m1 + e4m3 block scales), bf16 activations, f32 accumulation and logits",
+        "config": {"workload": f"output layer: NVFP4 (W4A16) head [{V}][2048] (vocabulary assumed; the pages give "
+                               f"none), T={T} tokens ({wl['x']} x, seed {wl['x_seed']})",
+                   "l2": "inputs larger than L2 (151 MB of head weights per step)", "parallelism": f"replicas x{ws}"},
+        "roofline": {"bound": "hbm", **hbm_roof(gbs, float(pk_["hbm_gbs"]), pk_kind),
+                     "traffic": traffic_from_profiles("lm_head_nvfp4_kernel", wl["name"]),
+                     "kernel": "lm_head_nvfp4_kernel", "bytes_per_launch": by, "us_per_launch": ms * 1e3,
+                     "what": "algorithmic bytes per launch (V x 1152 bytes of codes and scales + x + the fp32 logits "
+                             "written) / its device duration (CUDA events around each step's single launch)"},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "e2e": {"value": whole_job_rate(T, ws, ms_e2e), "unit": "tokens/s", "h2d_bytes_per_step": T * 2048 * 2,
+                "d2h_bytes_per_step": T * V * 4},
+    }
+    if rank == 0 and ws == 1 and cpu_seconds > 0:
+        line["cpu_baseline"] = cpu_baseline_lm_head(wl, xb, parts, cpu_seconds)
+    return line
+
+
+def cpu_baseline_lm_head(wl, xb, parts, seconds):
+    """The oracle, as it stands, on the head's first LM_HEAD_SAMPLE_ROWS rows,
+    scaled to the full vocabulary."""
+    import oracle
+    pk, sc, ts = parts
+    m = oracle.Mat(packed=pk, scales=sc, tensor_scale=ts)
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.lm_head(xb, m)
+        reps += 1
+        if time.perf_counter() - t0 > seconds or reps >= 20:
+            break
+    dt = (time.perf_counter() - t0) / reps * LM_HEAD_V / LM_HEAD_SAMPLE_ROWS
+    return {"value": wl["T"] / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {LM_HEAD_SAMPLE_ROWS} of the {LM_HEAD_V} rows at T={wl['T']}, {reps} reps, "
+                      f"scaled by {LM_HEAD_V // LM_HEAD_SAMPLE_ROWS} to the whole head"}
+
+
 COMMON_KEYS = ("n_gpus", "steps", "warmup", "higher_is_better", "scaling", "vs_baseline", "data")
 
 
@@ -799,8 +952,9 @@ def run_flint(args, ws, rank, local):
     L = args.layers
     results = {}
     t_gen = time.perf_counter()
-    bf16_names = [n for n in names if not WORKLOADS[n].get("nvfp4")]
+    bf16_names = [n for n in names if not WORKLOADS[n].get("nvfp4") and not WORKLOADS[n].get("lm_head")]
     nv_names = [n for n in names if WORKLOADS[n].get("nvfp4")]
+    lh_names = [n for n in names if WORKLOADS[n].get("lm_head")]
     gen_s = {}
     if bf16_names:
         layers, handles = build_bf16_stack(flint, device, L if any(not WORKLOADS[n].get("prefill") for n in bf16_names)
@@ -835,6 +989,11 @@ def run_flint(args, ws, rank, local):
         del layers, handles
         torch.cuda.empty_cache()
 
+    for n in lh_names:
+        cpu_s = HEADLINE_CPU_SECONDS if n == names[0] else CONFIG_CPU_SECONDS
+        results[n] = bench_lm_head(args, dict(WORKLOADS[n], name=n), ws, rank, cpu_s)
+        torch.cuda.empty_cache()
+
     head = dict(results[names[0]])
     line = {"metric": head.pop("metric"), "value": head.pop("value"), "unit": head.pop("unit"),
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
@@ -851,7 +1010,7 @@ def run_flint(args, ws, rank, local):
 
 
 ALL_ORDER = ["decode1", "decode8", "decode32", "prefill8192", "nvfp4_decode1", "nvfp4_decode8", "nvfp4_decode32",
-             "nvfp4_prefill8192"]
+             "nvfp4_prefill8192", "nvfp4_lm_head1", "nvfp4_lm_head32"]
 HEADLINE_CPU_SECONDS = 10.0
 CONFIG_CPU_SECONDS = 4.0
 

@@ -219,6 +219,42 @@ FLINT_API const char* flint_status_string(flint_status_t st);
 FLINT_API flint_status_t flint_permute_static(const int32_t* idx, int T, int32_t* offsets,
                                               int32_t* gather_idx, cudaStream_t s);
 
+/* ---- 4-bit output layer --------------------------------------------------
+ * The pages report that Flint's output layer (lm_head) was quantised to 4
+ * bits as well and is run from the NVFP4 checkpoint (mrchatgpt.org article,
+ * section 4, the quantisation item; qantcore.space review, section 04, the
+ * quantised variants).  The vocabulary size V is not on the pages: any
+ * positive multiple of 16 is accepted.  A decode step's logits are
+ *   logits[t][v] = sum_h x[t][h] * W[v][h],  W[v][h] = e2m1 * e4m3 * s_tensor,
+ * computed by one weight-streaming kernel (W read once per call). */
+typedef struct flint_lm_head* flint_lm_head_t;
+#define FLINT_LM_HEAD_MAX_T 32
+
+/* Build an output-layer handle on the current device.
+ *   out  host: receives the handle (NULL on failure).
+ *   W    host pointer to a flint_nvfp4_t of shape [V][2048] (device data).
+ *   V    rows of W, a positive multiple of 16.
+ * The handle repacks W into memory it owns (V x 1152 bytes) and keeps no
+ * reference to W's buffers: the caller may free them on return.
+ * Errors: INVALID_ARG (null pointer, V not a positive multiple of 16),
+ * UNSUPPORTED (no sm_103 device), OOM, CUDA. */
+FLINT_API flint_status_t flint_lm_head_create(flint_lm_head_t* out, const flint_nvfp4_t* W, int V);
+
+/* Logits of T tokens, enqueued on stream s (asynchronous).
+ *   x       bf16 [T][2048], device, 16-byte aligned.
+ *   T       1 <= T <= FLINT_LM_HEAD_MAX_T.
+ *   logits  fp32 [T][V], device, 16-byte aligned, fully overwritten; must not
+ *           overlap x.
+ * Errors: INVALID_ARG, CUDA; DEVICE_TIMEOUT when an earlier call's bounded
+ * wait gave up (its outputs are then unspecified; the error is reported
+ * once, by the next call on the handle or by destroy). */
+FLINT_API flint_status_t flint_lm_head_forward(flint_lm_head_t h, const void* x, int T, float* logits,
+                                               cudaStream_t s);
+
+/* Synchronise the device, release the handle and report a pending device
+ * status.  NULL is a no-op. */
+FLINT_API flint_status_t flint_lm_head_destroy(flint_lm_head_t h);
+
 /* Test hook: launch one kernel that waits on a device flag nothing sets,
  * with a wait limit of timeout_ns nanoseconds of %globaltimer; returns
  * FLINT_ERR_DEVICE_TIMEOUT when the bounded wait gives up as designed.

@@ -55,23 +55,26 @@ namespace flint {
 // create-time repack into the owned layout
 // ---------------------------------------------------------------------------
 
-// kind 0: gate_up [2I][H] -> 64 units x 4 chunks; kind 1: down [H][I] -> 128 units.
+// kind 0: gate_up [2I][H] -> 64 units x 4 chunks; kind 1: down [H][I] -> 128
+// units of one chunk; kind 2: any [R][H] (the output layer) -> R/16 units of
+// 16 straight rows x 4 chunks.
 // In a chunk, K block kb, lane t = 4g + c holds at 4t the code bytes of
 // (row g, cols 2c..2c+1), (row g+8, same), (row g, cols 8+2c..9+2c),
 // (row g+8, same) -- the m16n8k16 A fragment, low nibble = lower column;
 // the scales of (row g, row g+8) sit at NV_CODES + 16 kb + 2g.
 __global__ void repack_nvfp4_kernel(const uint8_t* __restrict__ packed, const uint8_t* __restrict__ scales,
-                                    int kind, uint8_t* __restrict__ out) {
-    const int K = kind == 0 ? H : I;
-    const int nchunks = kind == 0 ? NV_GU_UNITS * NV_GU_CHUNKS : NV_DN_UNITS;
-    const int total = nchunks * NV_CHUNK_KB * 32;
+                                    int kind, int nchunks, uint8_t* __restrict__ out) {
+    const int K = kind == 1 ? I : H;
+    const int cpu = kind == 1 ? 1 : NV_GU_CHUNKS;          // chunks per unit
+    const size_t total = (size_t)nchunks * NV_CHUNK_KB * 32;
     const size_t prow = K / 2, srow = K / 16;
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
-        const int lane = i & 31, kb = (i >> 5) & (NV_CHUNK_KB - 1), ch = i >> 10;
-        const int unit = kind == 0 ? ch / NV_GU_CHUNKS : ch;
-        const int kbg = (kind == 0 ? ch % NV_GU_CHUNKS : 0) * NV_CHUNK_KB + kb;
-        auto row_of = [&](int arow) {
-            return kind == 0 ? (arow < 8 ? 8 * unit + arow : I + 8 * unit + (arow - 8)) : 16 * unit + arow;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+        const int lane = (int)(i & 31), kb = (int)((i >> 5) & (NV_CHUNK_KB - 1));
+        const int ch = (int)(i >> 10);
+        const int unit = ch / cpu;
+        const int kbg = (ch % cpu) * NV_CHUNK_KB + kb;
+        auto row_of = [&](int arow) -> size_t {
+            return kind == 0 ? (arow < 8 ? 8 * unit + arow : I + 8 * unit + (arow - 8)) : (size_t)16 * unit + arow;
         };
         const int g = lane >> 2, c = lane & 3;
         const size_t rg = row_of(g), rg8 = row_of(g + 8);
@@ -83,17 +86,19 @@ __global__ void repack_nvfp4_kernel(const uint8_t* __restrict__ packed, const ui
         v.w = packed[rg8 * prow + kbg * 8 + 4 + c];
         *reinterpret_cast<uchar4*>(dst + kb * 128 + 4 * lane) = v;
         if (lane < 8) {
-            dst[NV_CODES + kb * 16 + 2 * lane] = scales[(size_t)row_of(lane) * srow + kbg];
-            dst[NV_CODES + kb * 16 + 2 * lane + 1] = scales[(size_t)row_of(lane + 8) * srow + kbg];
+            dst[NV_CODES + kb * 16 + 2 * lane] = scales[row_of(lane) * srow + kbg];
+            dst[NV_CODES + kb * 16 + 2 * lane + 1] = scales[row_of(lane + 8) * srow + kbg];
         }
     }
 }
 
-cudaError_t launch_repack_nvfp4(const uint8_t* packed, const uint8_t* scales, int kind, uint8_t* out,
+cudaError_t launch_repack_nvfp4(const uint8_t* packed, const uint8_t* scales, int kind, int rows, uint8_t* out,
                                 cudaStream_t s) {
-    const int nchunks = kind == 0 ? NV_GU_UNITS * NV_GU_CHUNKS : NV_DN_UNITS;
-    const int total = nchunks * NV_CHUNK_KB * 32;
-    repack_nvfp4_kernel<<<(total + 255) / 256, 256, 0, s>>>(packed, scales, kind, out);
+    const int nchunks = kind == 0 ? NV_GU_UNITS * NV_GU_CHUNKS : kind == 1 ? NV_DN_UNITS : rows / 16 * NV_GU_CHUNKS;
+    const size_t total = (size_t)nchunks * NV_CHUNK_KB * 32;
+    const size_t blocks = (total + 255) / 256;
+    repack_nvfp4_kernel<<<(unsigned)(blocks < 65535 * 16 ? blocks : 65535 * 16), 256, 0, s>>>(packed, scales, kind,
+                                                                                              nchunks, out);
     return cudaGetLastError();
 }
 

@@ -223,8 +223,8 @@ flint_status_t flint_moe_create(flint_moe_t* out, const void* router_W, const fl
             ts[2 * e] = mg->tensor_scale;
             ts[2 * e + 1] = md->tensor_scale;
             uint8_t* b = h->nv + (size_t)e * NV_EXPERT_BYTES;
-            if (launch_repack_nvfp4(mg->packed, mg->block_scales, 0, b, 0) != cudaSuccess ||
-                launch_repack_nvfp4(md->packed, md->block_scales, 1, b + NV_GU_BYTES, 0) != cudaSuccess)
+            if (launch_repack_nvfp4(mg->packed, mg->block_scales, 0, 0, b, 0) != cudaSuccess ||
+                launch_repack_nvfp4(md->packed, md->block_scales, 1, 0, b + NV_GU_BYTES, 0) != cudaSuccess)
                 st = FLINT_ERR_CUDA;
         }
         if (st == FLINT_OK && cudaMemcpy(h->nv_ts, ts, sizeof ts, cudaMemcpyHostToDevice) != cudaSuccess)

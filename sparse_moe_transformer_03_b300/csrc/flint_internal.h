@@ -104,7 +104,9 @@ constexpr size_t NV_GU_BYTES = (size_t)NV_GU_UNITS * NV_GU_CHUNKS * NV_CHUNK;   
 constexpr size_t NV_DN_BYTES = (size_t)NV_DN_UNITS * NV_CHUNK;                 // 589,824
 constexpr size_t NV_EXPERT_BYTES = NV_GU_BYTES + NV_DN_BYTES;                  // 1,769,472
 
-cudaError_t launch_repack_nvfp4(const uint8_t* packed, const uint8_t* scales, int kind, uint8_t* out,
+// kind 0: a gate_up matrix, 1: a down matrix, 2: any [rows][H] matrix (rows a
+// multiple of 16) as rows/16 units of 16 straight rows x 4 chunks
+cudaError_t launch_repack_nvfp4(const uint8_t* packed, const uint8_t* scales, int kind, int rows, uint8_t* out,
                                 cudaStream_t s);
 cudaError_t decode_nvfp4_set_attributes();
 cudaError_t launch_decode_experts_nvfp4(const LaunchCtx& L, const uint8_t* nv, const float* nv_ts,

@@ -32,6 +32,7 @@ STATUS = {
 
 H, I, E, TOPK, CHUNK, DECODE_MAX_T = 2048, 512, 256, 6, 8192, 32
 STACK_MAX_T, STACK_MAX_LAYERS = 8, 64
+LM_HEAD_MAX_T = 32               # FLINT_LM_HEAD_MAX_T
 
 
 class FlintError(RuntimeError):
@@ -74,6 +75,12 @@ def load_library():
     lib.flint_permute_static.argtypes = [P, I32, P, P, P]
     lib.flint_debug_bounded_wait.restype = I32
     lib.flint_debug_bounded_wait.argtypes = [ctypes.c_uint64, P]
+    lib.flint_lm_head_create.restype = I32
+    lib.flint_lm_head_create.argtypes = [ctypes.POINTER(P), ctypes.POINTER(flint_nvfp4_t), I32]
+    lib.flint_lm_head_forward.restype = I32
+    lib.flint_lm_head_forward.argtypes = [P, P, I32, P, P]
+    lib.flint_lm_head_destroy.restype = I32
+    lib.flint_lm_head_destroy.argtypes = [P]
     _lib = lib
     return lib
 
@@ -193,6 +200,25 @@ def flint_moe_destroy(h):
 
 def flint_status_string(code):
     return load_library().flint_status_string(int(code)).decode()
+
+
+def flint_lm_head_create(W, V):
+    """Output-layer handle from W = (packed uint8 [V][1024], block_scales
+    uint8 [V][128], tensor_scale) with CUDA tensors (or device addresses)."""
+    pk, sc, ts = W
+    st = flint_nvfp4_t(_ptr(pk).value, _ptr(sc).value, float(ts))
+    h = ctypes.c_void_p()
+    _check("flint_lm_head_create", load_library().flint_lm_head_create(ctypes.byref(h), ctypes.byref(st), int(V)))
+    return h.value
+
+
+def flint_lm_head_forward(h, x, T, logits, stream=None):
+    _check("flint_lm_head_forward",
+           load_library().flint_lm_head_forward(ctypes.c_void_p(h), _ptr(x), int(T), _ptr(logits), _stream(stream)))
+
+
+def flint_lm_head_destroy(h):
+    _check("flint_lm_head_destroy", load_library().flint_lm_head_destroy(ctypes.c_void_p(h) if h else None))
 
 
 def flint_debug_bounded_wait(timeout_ns, stream=None):

@@ -33,6 +33,7 @@ def test_header_constants_match_binding():
     assert int(consts["FLINT_CHUNK"]) == flint.CHUNK
     assert int(consts["FLINT_DECODE_MAX_T"]) == flint.DECODE_MAX_T
     assert int(consts["FLINT_STACK_MAX_T"]) == flint.STACK_MAX_T
+    assert int(consts["FLINT_LM_HEAD_MAX_T"]) == flint.LM_HEAD_MAX_T
     assert int(consts["FLINT_STACK_MAX_LAYERS"]) == flint.STACK_MAX_LAYERS
     enums = dict(re.findall(r"(FLINT_(?:OK|ERR_\w+)) = (\d+)", src))
     assert {int(v): k for k, v in enums.items()} == flint.STATUS
@@ -92,3 +93,21 @@ def test_nvfp4_create_rejects_null_parts():
     h = ctypes.c_void_p()
     rc = lib.flint_moe_create(ctypes.byref(h), ctypes.c_void_p(16), None, entries, entries, shared, 1)
     assert rc == 1 and not h.value
+
+
+def test_lm_head_host_argument_checks(lib):
+    """The output layer's calls reject bad arguments before any CUDA call."""
+    P = ctypes.c_void_p
+    lib.flint_lm_head_create.argtypes = [ctypes.POINTER(P), ctypes.POINTER(flint.flint_nvfp4_t), ctypes.c_int]
+    h = P()
+    assert lib.flint_lm_head_create(None, None, 16) == 1
+    assert lib.flint_lm_head_create(ctypes.byref(h), None, 16) == 1
+    w = flint.flint_nvfp4_t(4096, 8192, 1.0)
+    null_w = flint.flint_nvfp4_t(None, 8192, 1.0)
+    assert lib.flint_lm_head_create(ctypes.byref(h), ctypes.byref(null_w), 16) == 1
+    for V in (0, -16, 8, 24, 100):
+        assert lib.flint_lm_head_create(ctypes.byref(h), ctypes.byref(w), V) == 1, V
+    assert h.value is None
+    lib.flint_lm_head_forward.argtypes = [P, P, ctypes.c_int, P, P]
+    assert lib.flint_lm_head_forward(None, P(4096), 1, P(1 << 20), None) == 1
+    assert lib.flint_lm_head_destroy(None) == 0
