@@ -116,6 +116,8 @@ cudaError_t launch_decode_experts_nvfp4(const LaunchCtx& L, const uint8_t* nv, c
 // tmap.cu: the owned NVFP4 experts as TMA tensors of 32-bit words
 bool encode_nvfp4_gateup(CUtensorMap* map, const uint8_t* nv, uint32_t box_words, uint32_t box_units);
 bool encode_nvfp4_down(CUtensorMap* map, const uint8_t* nv, uint32_t box_words, uint32_t box_units);
+// a [rows][row_words] array of 32-bit words, boxes of row_words x box_rows, no swizzle
+bool encode_u32_rows(CUtensorMap* map, const void* base, uint64_t rows, uint32_t row_words, uint32_t box_rows);
 
 // prefill_nvfp4.cu -- grouped tcgen05 GEMMs with the NVFP4 weight operand
 // dequantised in shared memory.  maps: gate/up codes, gate/up scales, down

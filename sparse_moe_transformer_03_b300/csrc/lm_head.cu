@@ -10,24 +10,24 @@
 //     4608-byte chunks each (codes in mma.sync A-fragment order, then the E4M3
 //     block scales), 1152 bytes per row;
 //   * one persistent CTA per SM takes a balanced contiguous range of units;
-//     a producer warp streams their chunks by bulk copy into a ring of
-//     4608-byte slots, issued round-robin over the consumer warps (chunk c of
-//     every warp's unit, then chunk c + 1, ...), so each warp has its next
-//     chunk in flight while it works on the current one;
-//   * 16 consumer warps: warp w multiplies whole units (16 rows x K 2048) by
+//     consumer warp w takes units w, w + NW, ... of it and streams their
+//     chunks itself: its lane 0 keeps D chunks in flight in the warp's own D
+//     ring slots (one 2-D TMA box of 9 x 512 bytes per chunk) and issues
+//     chunk k + D into the slot of chunk k once the warp has read it.  No
+//     warp waits on another: an earlier design with one producer thread
+//     feeding every warp in a fixed order streamed at 2.8 TB/s with the
+//     arithmetic removed, each slot waiting on the slowest warp;
+//   * NW consumer warps (16; 8 when T > 16, where x takes more shared
+//     memory): warp w multiplies whole units (16 rows x K 2048) by
 //     the tokens, dequantising each 16 x 16 block straight into an f16 A
 //     fragment (nvfp4_frag.cuh) and multiplying it with x staged in shared
 //     memory as f16 (token t scaled by 2^e_t so that its largest |x| lies in
 //     [2^14, 2^15): exact for every bf16 value within 28 binades of it); the
 //     fp32 accumulators get s_tensor * 2^-e_t at the end and the warp writes
-//     its 16 logits per token;
-//   * a slot's sequence word (release / acquire in shared memory) tells a
-//     consumer that the producer armed the slot for that use before it waits
-//     on the slot's barrier parity, so warps that share a slot at different
-//     uses never see each other's phase.
+//     its 16 logits per token.
 // Every wait is bounded by %globaltimer; a wait that gives up sets the CTA's
 // abort flag, reports FLINT_ERR_DEVICE_TIMEOUT through the status word and
-// the producer drains its copies in flight before the CTA exits.
+// each warp lets its copies in flight land before the CTA exits.
 #include <cuda_fp16.h>
 
 #include <new>
@@ -37,15 +37,23 @@
 #include "flint_internal.h"
 #include "mma_sync.cuh"
 #include "nvfp4_frag.cuh"
+#include "tc_ptx.cuh"
 
 namespace flint {
 namespace {
 
-constexpr int LH_NW = 16;                          // consumer warps
-constexpr int LH_THREADS = 32 * (LH_NW + 1);       // + the producer warp
+template <int NT>
+struct LhCfg {
+    // consumer warps, each with two ring slots beside x (T <= 16: 16 warps,
+    // 32 slots; T <= 32: 8 warps, 16 slots).  Measured at T = 1: 16 x 2 slots
+    // 37.5 us, 20 x 2 37.4, 14 x 3 42.0, 8 x 5 41.6
+    static constexpr int NW = NT <= 2 ? 16 : 8;
+    static constexpr int THREADS = 32 * NW;
+};
 constexpr int LH_XSTRIDE = 2 * H + 16;             // bytes per staged token row (bank spread)
 constexpr int LH_UNIT = NV_GU_CHUNKS * NV_CHUNK;   // 18432 bytes: 16 rows x 2048
 constexpr int LH_MAX_SLOTS = 64;
+constexpr int LH_BOX_ROWS = NV_CHUNK / 512;        // a chunk as 9 rows of 512 bytes (one TMA box)
 
 struct LmParams {
     const uint8_t* nv;          // owned layout, units * LH_UNIT bytes
@@ -57,33 +65,23 @@ struct LmParams {
     uint64_t limit_ns;
 };
 
-// dynamic shared memory: ring | x (8 NT rows) | xinv[32] | seq[nslot] | full | empty | abort
+// dynamic shared memory: ring | x (8 NT rows) | xinv[32] | uses[nslot] | full[nslot] | abort
 __host__ __device__ constexpr uint32_t lh_x_off(int nslot) { return (uint32_t)nslot * NV_CHUNK; }
 __host__ __device__ constexpr uint32_t lh_xinv_off(int nslot, int nt) {
     return lh_x_off(nslot) + (uint32_t)(8 * nt) * LH_XSTRIDE;
 }
-__host__ __device__ constexpr uint32_t lh_seq_off(int nslot, int nt) { return lh_xinv_off(nslot, nt) + 32 * 4; }
+__host__ __device__ constexpr uint32_t lh_uses_off(int nslot, int nt) { return lh_xinv_off(nslot, nt) + 32 * 4; }
 __host__ __device__ constexpr uint32_t lh_bar_off(int nslot, int nt) {
-    return (lh_seq_off(nslot, nt) + (uint32_t)nslot * 4 + 7) & ~7u;
+    return (lh_uses_off(nslot, nt) + (uint32_t)nslot * 4 + 7) & ~7u;
 }
 __host__ __device__ constexpr uint32_t lh_smem_bytes(int nslot, int nt) {
-    return lh_bar_off(nslot, nt) + (uint32_t)nslot * 16 + 16;
-}
-
-__device__ __forceinline__ void lh_st_release(uint32_t* p, uint32_t v) {
-    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
-}
-__device__ __forceinline__ uint32_t lh_ld_acquire(const uint32_t* p) {
-    uint32_t v;
-    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
-    return v;
+    return lh_bar_off(nslot, nt) + (uint32_t)nslot * 8 + 16;
 }
 
 struct LmState {
     uint8_t* ring;
-    uint32_t* seq;
+    uint32_t* uses;         // per slot: how many copies were issued into it
     uint64_t* full;
-    uint64_t* empty;
     volatile uint32_t* abort;
     int nslot;
     uint64_t limit;
@@ -110,37 +108,10 @@ __device__ __forceinline__ bool lh_wait(const LmState& s, uint64_t* bar, uint32_
     }
 }
 
-// ring entry q has landed: first the producer's arming of slot q % nslot for
-// use q / nslot (sequence word q + 1), then that use's barrier phase
-__device__ __forceinline__ bool lh_wait_full(const LmState& s, uint32_t q, uint32_t* status) {
-    const int slot = (int)(q % (uint32_t)s.nslot);
-    if (lh_ld_acquire(&s.seq[slot]) != q + 1u) {
-        const uint64_t t0 = globaltimer_ns();
-        for (;;) {
-            bool armed = false;
-#pragma unroll 1
-            for (int i = 0; i < 64 && !armed; ++i) armed = lh_ld_acquire(&s.seq[slot]) == q + 1u;
-            if (armed) break;
-            if (*s.abort) return false;
-            if (globaltimer_ns() - t0 > s.limit) {
-                lh_fail(s, status);
-                return false;
-            }
-        }
-    }
-    return lh_wait(s, &s.full[slot], (q / (uint32_t)s.nslot) & 1, status);
-}
-
-// Ring entry of chunk c of the unit that warp w takes in round r (n units in
-// the CTA): rounds before r hold 4 LH_NW entries each; round r holds
-// 4 nw_r, chunk-major over its nw_r active warps.
-__device__ __forceinline__ uint32_t lh_entry(int r, int c, int w, int n) {
-    const int nw = min(LH_NW, n - r * LH_NW);
-    return (uint32_t)(4 * LH_NW * r + c * nw + w);
-}
-
 template <int NT>   // token tiles of 8: T <= 8 NT
-__global__ void __launch_bounds__(LH_THREADS, 1) lm_head_nvfp4_kernel(LmParams p) {
+__global__ void __launch_bounds__(LhCfg<NT>::THREADS, 1)
+    lm_head_nvfp4_kernel(const __grid_constant__ CUtensorMap map, LmParams p) {
+    constexpr int NW = LhCfg<NT>::NW;
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     LmState s;
@@ -149,60 +120,48 @@ __global__ void __launch_bounds__(LH_THREADS, 1) lm_head_nvfp4_kernel(LmParams p
     s.ring = smem;
     uint8_t* xs = smem + lh_x_off(p.nslot);
     float* xinv = reinterpret_cast<float*>(smem + lh_xinv_off(p.nslot, NT));
-    s.seq = reinterpret_cast<uint32_t*>(smem + lh_seq_off(p.nslot, NT));
+    s.uses = reinterpret_cast<uint32_t*>(smem + lh_uses_off(p.nslot, NT));
     s.full = reinterpret_cast<uint64_t*>(smem + lh_bar_off(p.nslot, NT));
-    s.empty = s.full + p.nslot;
-    s.abort = reinterpret_cast<volatile uint32_t*>(s.empty + p.nslot);
-    // the CTA's units: a balanced contiguous range
+    s.abort = reinterpret_cast<volatile uint32_t*>(s.full + p.nslot);
+    // the CTA's units: a balanced contiguous range; warp w takes units
+    // w, w + NW, ... of it, i.e. chunks k = 0 .. 4 m - 1 (unit w + (k / 4) NW,
+    // chunk k % 4), streamed through its own D slots (chunk k in slot
+    // w D + k % D, that slot's use k / D)
     const int G = gridDim.x, c = blockIdx.x;
     const int u0 = (int)((long long)p.units * c / G), u1 = (int)((long long)p.units * (c + 1) / G);
-    const int n = u1 - u0, rounds = (n + LH_NW - 1) / LH_NW;
-    const uint32_t nslot = (uint32_t)p.nslot;
+    const int n = u1 - u0;
+    const int D = p.nslot / NW;
+    const int m = warp < n ? (n - warp + NW - 1) / NW : 0;
+    const int nch = NV_GU_CHUNKS * m;
+    uint64_t* full = s.full + warp * D;
+    uint8_t* ring = s.ring + (size_t)warp * D * NV_CHUNK;
+    uint32_t* uses = s.uses + warp * D;
 
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < p.nslot; ++i) {
-            mbar_init(&s.full[i], 1);
-            mbar_init(&s.empty[i], 1);
-            s.seq[i] = 0;
+    if (lane == 0) {
+        for (int i = 0; i < D; ++i) {
+            mbar_init(&full[i], 1);
+            uses[i] = 0;
         }
-        *s.abort = 0;
+        if (warp == 0) *s.abort = 0;
         fence_mbar_init();
     }
     __syncthreads();
 
-    if (warp == LH_NW) {
-        // producer: chunk entries in ring order (round, chunk, warp)
-        if (lane == 0) {
-            uint32_t q = 0;
-            bool ok = true;
-            for (int r = 0; ok && r < rounds; ++r) {
-                const int nw = min(LH_NW, n - r * LH_NW);
-                for (int cc = 0; ok && cc < NV_GU_CHUNKS; ++cc) {
-                    for (int w = 0; w < nw; ++w) {
-                        const uint32_t slot = q % nslot;
-                        if (q >= nslot && !lh_wait(s, &s.empty[slot], (q / nslot - 1) & 1, p.status)) {
-                            ok = false;
-                            break;
-                        }
-                        mbar_arrive_expect_tx(&s.full[slot], NV_CHUNK);
-                        lh_st_release(&s.seq[slot], q + 1u);
-                        bulk_g2s(s.ring + (size_t)slot * NV_CHUNK,
-                                 p.nv + (size_t)(u0 + r * LH_NW + w) * LH_UNIT + (size_t)cc * NV_CHUNK, NV_CHUNK,
-                                 &s.full[slot]);
-                        ++q;
-                    }
-                }
-            }
-            // after an abort: the copies in flight land before the CTA exits
-            if (*s.abort)
-                for (uint32_t k = q > nslot ? q - nslot : 0u; k < q; ++k)
-                    mbar_wait_bounded(&s.full[k % nslot], (k / nslot) & 1, 10000000ull);
-        }
-        return;
+    // lane 0: chunk k into its slot (one 2-D box of 9 x 512 bytes)
+    auto issue = [&](int k) {
+        const int sl = k % D;
+        mbar_arrive_expect_tx(&full[sl], NV_CHUNK);
+        uses[sl] = (uint32_t)(k / D) + 1u;
+        const int chunk = (u0 + warp + (k / NV_GU_CHUNKS) * NW) * NV_GU_CHUNKS + k % NV_GU_CHUNKS;
+        tc::tma_load_2d(ring + (size_t)sl * NV_CHUNK, &map, 0, LH_BOX_ROWS * chunk, &full[sl]);
+    };
+    if (lane == 0) {
+        tc::prefetch_tensormap(&map);
+        for (int k = 0; k < D && k < nch; ++k) issue(k);
     }
 
-    // consumers: x -> f16 x 2^e_t, token t on warp t % LH_NW (rows past T zero)
-    for (int t = warp; t < 8 * NT; t += LH_NW) {
+    // x -> f16 x 2^e_t, token t on warp t % NW (rows past T zero)
+    for (int t = warp; t < 8 * NT; t += NW) {
         uint4* row = reinterpret_cast<uint4*>(xs + (size_t)t * LH_XSTRIDE);
         if (t < p.T) {
             const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)t * H);
@@ -241,47 +200,43 @@ __global__ void __launch_bounds__(LH_THREADS, 1) lm_head_nvfp4_kernel(LmParams p
             if (lane == 0) xinv[t] = 0.f;
         }
     }
-    asm volatile("bar.sync 1, %0;" ::"n"(32 * LH_NW) : "memory");   // the consumer warps only
+    __syncthreads();
 
-    // units: warp w takes unit r LH_NW + w of the range in round r
     constexpr int ACC = NT >= 4 ? 1 : (NT == 1 ? 4 : 2);   // independent accumulator chains per tile
     const int g = lane >> 2, cq = lane & 3;
-    bool ok = true;
-    for (int r = 0; ok && r < rounds; ++r) {
-        const int nw = min(LH_NW, n - r * LH_NW);
-        if (warp >= nw) break;                  // only the last round is partial
-        float acc[ACC][NT][4];
+    float acc[ACC][NT][4];
+    for (int k = 0; k < nch; ++k) {
+        const int cc = k % NV_GU_CHUNKS;
+        if (cc == 0) {
 #pragma unroll
-        for (int a = 0; a < ACC; ++a)
+            for (int a = 0; a < ACC; ++a)
 #pragma unroll
-            for (int j = 0; j < NT; ++j) acc[a][j][0] = acc[a][j][1] = acc[a][j][2] = acc[a][j][3] = 0.f;
-        for (int cc = 0; cc < NV_GU_CHUNKS; ++cc) {
-            const uint32_t q = lh_entry(r, cc, warp, n);
-            if (!__all_sync(0xFFFFFFFFu, lh_wait_full(s, q, p.status))) {
-                ok = false;
-                break;
-            }
-            const uint8_t* buf = s.ring + (size_t)(q % nslot) * NV_CHUNK;
-            // B: token 8 j + g, columns 512 cc + 16 kb + 2 cq (and + 8)
-            const uint8_t* xb = xs + (size_t)g * LH_XSTRIDE + cc * 1024 + 4 * cq;
-#pragma unroll
-            for (int kb = 0; kb < NV_CHUNK_KB; ++kb) {
-                uint32_t a[4];
-                nv_a_frag(*reinterpret_cast<const uint32_t*>(buf + kb * 128 + 4 * lane),
-                          *reinterpret_cast<const uint16_t*>(buf + NV_CODES + kb * 16 + 2 * g), a);
-#pragma unroll
-                for (int j = 0; j < NT; ++j) {
-                    const uint8_t* xj = xb + (size_t)j * 8 * LH_XSTRIDE + kb * 32;
-                    mma_f16_16816(acc[kb % ACC][j], a, *reinterpret_cast<const uint32_t*>(xj),
-                                  *reinterpret_cast<const uint32_t*>(xj + 16));
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s.empty[q % nslot]);
+                for (int j = 0; j < NT; ++j) acc[a][j][0] = acc[a][j][1] = acc[a][j][2] = acc[a][j][3] = 0.f;
         }
-        if (!ok) break;
+        const int sl = k % D;
+        if (!__all_sync(0xFFFFFFFFu, lh_wait(s, &full[sl], (uint32_t)(k / D) & 1, p.status))) break;
+        const uint8_t* buf = ring + (size_t)sl * NV_CHUNK;
+        // B: token 8 j + g, columns 512 cc + 16 kb + 2 cq (and + 8)
+        const uint8_t* xb = xs + (size_t)g * LH_XSTRIDE + cc * 1024 + 4 * cq;
+#pragma unroll
+        for (int kb = 0; kb < NV_CHUNK_KB; ++kb) {
+            uint32_t a[4];
+            nv_a_frag(*reinterpret_cast<const uint32_t*>(buf + kb * 128 + 4 * lane),
+                      *reinterpret_cast<const uint16_t*>(buf + NV_CODES + kb * 16 + 2 * g), a);
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                const uint8_t* xj = xb + (size_t)j * 8 * LH_XSTRIDE + kb * 32;
+                mma_f16_16816(acc[kb % ACC][j], a, *reinterpret_cast<const uint32_t*>(xj),
+                              *reinterpret_cast<const uint32_t*>(xj + 16));
+            }
+        }
+        // the slot's reads are done (generic proxy) before the next copy into it (async proxy)
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && k + D < nch) issue(k + D);
+        if (cc != NV_GU_CHUNKS - 1) continue;
         // lane (g, cq): rows v0 and v0 + 8, tokens 8 j + 2 cq and + 1
-        const size_t v0 = (size_t)16 * (u0 + r * LH_NW + warp) + g;
+        const size_t v0 = (size_t)16 * (u0 + warp + (k / NV_GU_CHUNKS) * NW) + g;
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
             float d[4];
@@ -304,21 +259,26 @@ __global__ void __launch_bounds__(LH_THREADS, 1) lm_head_nvfp4_kernel(LmParams p
             }
         }
     }
+    // after an abort: this warp's copies in flight land before the CTA exits
+    if (lane == 0 && *s.abort)
+        for (int i = 0; i < D; ++i)
+            if (uses[i]) mbar_wait_bounded(&full[i], (uses[i] - 1) & 1, 10000000ull);
 }
 
-// largest ring (<= LH_MAX_SLOTS chunk slots) that fits the opt-in shared memory
-int lh_nslot(int nt, int smem_optin) {
-    int k = LH_MAX_SLOTS;
-    while (k > 0 && lh_smem_bytes(k, nt) > (uint32_t)smem_optin) --k;
-    return k;
+// largest ring that fits the opt-in shared memory: a multiple of the
+// consumer warps, at most LH_MAX_SLOTS; 0 when not even two slots per warp fit
+int lh_nslot(int nt, int nw, int smem_optin) {
+    int k = LH_MAX_SLOTS / nw * nw;
+    while (k >= 2 * nw && lh_smem_bytes(k, nt) > (uint32_t)smem_optin) k -= nw;
+    return k >= 2 * nw ? k : 0;
 }
 
 template <int NT>
-cudaError_t lh_launch(const LmParams& p0, int grid, int smem_optin, cudaStream_t s) {
+cudaError_t lh_launch(const CUtensorMap& map, const LmParams& p0, int grid, int smem_optin, cudaStream_t s) {
     LmParams p = p0;
-    p.nslot = lh_nslot(NT, smem_optin);
-    if (p.nslot < 1) return cudaErrorInvalidConfiguration;
-    lm_head_nvfp4_kernel<NT><<<grid, LH_THREADS, lh_smem_bytes(p.nslot, NT), s>>>(p);
+    p.nslot = lh_nslot(NT, LhCfg<NT>::NW, smem_optin);
+    if (p.nslot == 0) return cudaErrorInvalidConfiguration;
+    lm_head_nvfp4_kernel<NT><<<grid, LhCfg<NT>::THREADS, lh_smem_bytes(p.nslot, NT), s>>>(map, p);
     return cudaGetLastError();
 }
 
@@ -338,6 +298,7 @@ struct flint_lm_head {
     int device, num_sms, smem_optin;
     int V, units;
     uint8_t* nv;                 // owned repacked W
+    CUtensorMap map;             // nv as [units x 4 x 9] rows of 128 32-bit words
     float ts;
     uint32_t* status_host;       // host-mapped status word
     uint32_t* status_dev;
@@ -398,6 +359,9 @@ flint_status_t flint_lm_head_create(flint_lm_head_t* out, const flint_nvfp4_t* W
     if (st == FLINT_OK && cudaMalloc(&h->nv, (size_t)h->units * LH_UNIT) != cudaSuccess) st = FLINT_ERR_OOM;
     if (st == FLINT_OK && launch_repack_nvfp4(W->packed, W->block_scales, 2, V, h->nv, 0) != cudaSuccess)
         st = FLINT_ERR_CUDA;
+    if (st == FLINT_OK &&
+        !encode_u32_rows(&h->map, h->nv, (uint64_t)h->units * NV_GU_CHUNKS * LH_BOX_ROWS, 128, LH_BOX_ROWS))
+        st = FLINT_ERR_CUDA;
     if (st == FLINT_OK) {
         const cudaError_t e = cudaSuccess == lh_set_attr<1>(h->smem_optin) &&
                                       cudaSuccess == lh_set_attr<2>(h->smem_optin) &&
@@ -431,10 +395,10 @@ flint_status_t flint_lm_head_forward(flint_lm_head_t h, const void* x, int T, fl
     const int grid = h->units < h->num_sms ? h->units : h->num_sms;
     cudaError_t e;
     switch ((T + 7) / 8) {
-        case 1: e = lh_launch<1>(p, grid, h->smem_optin, s); break;
-        case 2: e = lh_launch<2>(p, grid, h->smem_optin, s); break;
-        case 3: e = lh_launch<3>(p, grid, h->smem_optin, s); break;
-        default: e = lh_launch<4>(p, grid, h->smem_optin, s); break;
+        case 1: e = lh_launch<1>(h->map, p, grid, h->smem_optin, s); break;
+        case 2: e = lh_launch<2>(h->map, p, grid, h->smem_optin, s); break;
+        case 3: e = lh_launch<3>(h->map, p, grid, h->smem_optin, s); break;
+        default: e = lh_launch<4>(h->map, p, grid, h->smem_optin, s); break;
     }
     return e == cudaSuccess ? FLINT_OK : FLINT_ERR_CUDA;
 }

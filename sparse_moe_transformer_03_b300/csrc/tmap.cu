@@ -70,6 +70,13 @@ static bool encode_u32(CUtensorMap* map, const void* base, int rank, const cuuin
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_u32_rows(CUtensorMap* map, const void* base, uint64_t rows, uint32_t row_words, uint32_t box_rows) {
+    const cuuint64_t gdim[2] = {row_words, rows};
+    const cuuint64_t gstride[1] = {(cuuint64_t)row_words * 4};
+    const cuuint32_t box[2] = {row_words, box_rows};
+    return encode_u32(map, base, 2, gdim, gstride, box);
+}
+
 bool encode_nvfp4_gateup(CUtensorMap* map, const uint8_t* nv, uint32_t box_words, uint32_t box_units) {
     const cuuint64_t gdim[4] = {NV_CHUNK / 4, NV_GU_CHUNKS, NV_GU_UNITS, NEXP};
     const cuuint64_t gstride[3] = {NV_CHUNK, (cuuint64_t)NV_GU_CHUNKS * NV_CHUNK, NV_EXPERT_BYTES};
