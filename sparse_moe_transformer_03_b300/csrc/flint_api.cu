@@ -313,7 +313,7 @@ flint_status_t flint_moe_forward(flint_moe_t h, const void* x, int T, void* y, c
         if (e == cudaSuccess) {
             if (h->dtype == FLINT_NVFP4)
                 e = launch_prefill_experts_nvfp4(L, xc, h->h_map, h->nv_maps, Tc, h->offsets, h->gather,
-                                                 h->pair_slot, h->w, h->nv, h->nv_ts, h->h_perm, h->o_perm,
+                                                 h->pair_slot, h->w, h->nv_ts, h->h_perm, h->o_perm,
                                                  ys + (size_t)t0 * H);
             else
                 e = launch_prefill_experts(L, xc, h->h_map, Tc, h->offsets, h->gather, h->pair_slot, h->w,

@@ -127,8 +127,8 @@ bool encode_nvfp4_prefill_maps(CUtensorMap (&maps)[4], const uint8_t* nv);
 cudaError_t launch_prefill_experts_nvfp4(const LaunchCtx& L, const __nv_bfloat16* x, const CUtensorMap& h_map,
                                          const CUtensorMap (&maps)[4], int T, const int32_t* offsets,
                                          const int32_t* gather, const int32_t* pair_slot, const float* w_route,
-                                         const uint8_t* nv, const float* nv_ts, __nv_bfloat16* h_perm,
-                                         __nv_bfloat16* o_perm, __nv_bfloat16* y);
+                                         const float* nv_ts, __nv_bfloat16* h_perm, __nv_bfloat16* o_perm,
+                                         __nv_bfloat16* y);
 
 // stack_decode.cu -- every layer of a stack in one persistent launch (bf16 or
 // NVFP4 experts, T <= STACK_MAX_T).  Layer l reads x of its own and writes its y; layer l

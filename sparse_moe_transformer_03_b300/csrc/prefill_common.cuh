@@ -124,7 +124,6 @@ struct GroupedParams {
     uint32_t* status;
     uint64_t limit_ns;
     const float* nv_ts;          // NVFP4 experts: tensor scales [NEXP][2] (gate_up, down)
-    const uint8_t* nv;           // NVFP4 experts: the owned layout (NV_EXPERT_BYTES each)
 };
 
 // Per-CTA copy of the unit schedule: expert e covers units

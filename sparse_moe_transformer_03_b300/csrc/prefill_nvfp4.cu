@@ -151,12 +151,6 @@ __global__ void __launch_bounds__(N1_THREADS, 1)
         int kc_all = 0;
         for (int u = blockIdx.x; u < total && !__shfl_sync(0xFFFFFFFFu, *abort, 0); u += gridDim.x) {
             const Unit U = decode_unit(S, u);
-            if (warp == 0 && lane == 0 && u + (int)gridDim.x < total) {
-                // the CTA's next unit: its 128-row block (16 owned units x 4 chunks, contiguous) into L2
-                const Unit N = decode_unit(S, u + gridDim.x);
-                bulk_prefetch_l2(p.nv + (size_t)N.e * NV_EXPERT_BYTES + (size_t)N1_UNITS * N.blk * NV_GU_CHUNKS * NV_CHUNK,
-                                 N1_UNITS * NV_GU_CHUNKS * NV_CHUNK);
-            }
             const int nrows = U.npad >> 3;
             int tk[GP_N / 8];
 #pragma unroll
@@ -371,12 +365,6 @@ __global__ void __launch_bounds__(N2_THREADS, 1)
             int kc_all = 0;
             for (int u = blockIdx.x; u < total && !*abort; u += gridDim.x) {
                 const Unit U = decode_unit(S, u);
-                if (u + (int)gridDim.x < total) {
-                    // the CTA's next unit: its 8 owned down units (contiguous) into L2
-                    const Unit N = decode_unit(S, u + gridDim.x);
-                    bulk_prefetch_l2(p.nv + (size_t)N.e * NV_EXPERT_BYTES + NV_GU_BYTES + (size_t)N2_UNITS * N.blk * NV_CHUNK,
-                                     N2_UNITS * NV_CHUNK);
-                }
                 for (int kc = 0; kc < KC; ++kc) {
                     const int s = kc_all % N2_STAGES;
                     if (!pf_wait(&sempty[s], ((kc_all / N2_STAGES) & 1) ^ 1, p.limit_ns, abort)) break;
@@ -511,9 +499,9 @@ bool encode_nvfp4_prefill_maps(CUtensorMap (&maps)[4], const uint8_t* nv) {
 cudaError_t launch_prefill_experts_nvfp4(const LaunchCtx& L, const __nv_bfloat16* x, const CUtensorMap& h_map,
                                          const CUtensorMap (&maps)[4], int T, const int32_t* offsets,
                                          const int32_t* gather, const int32_t* pair_slot, const float* w_route,
-                                         const uint8_t* nv, const float* nv_ts, __nv_bfloat16* h_perm,
-                                         __nv_bfloat16* o_perm, __nv_bfloat16* y) {
-    GroupedParams gp{T, offsets, gather, w_route, nullptr, h_perm, o_perm, L.status, L.wait_limit_ns, nv_ts, nv};
+                                         const float* nv_ts, __nv_bfloat16* h_perm, __nv_bfloat16* o_perm,
+                                         __nv_bfloat16* y) {
+    GroupedParams gp{T, offsets, gather, w_route, nullptr, h_perm, o_perm, L.status, L.wait_limit_ns, nv_ts};
     cudaError_t e = launch_hooked(L, FLINT_KERNEL_GATE_UP, prefill_gateup_nvfp4_kernel, dim3(L.num_sms),
                                   dim3(N1_THREADS), N1_SMEM, x, maps[0], maps[1], gp);
     if (e != cudaSuccess) return e;
