@@ -116,11 +116,11 @@ FLINT_API flint_status_t flint_moe_create(flint_moe_t* out, const void* router_W
 /* y = layer(x) for T >= 1 tokens.
  *   x  bf16 [T][2048], y bf16 [T][2048] (fully overwritten); x and y must not
  *   overlap.  Runs asynchronously on stream s; allocates nothing; capturable in
- *   a CUDA graph.  FLINT_BF16: T <= 32 takes the weight-streaming decode
- *   kernels, larger T the grouped tensor-core path, in chunks of FLINT_CHUNK
- *   tokens.  FLINT_NVFP4: the W4A16 weight-streaming kernels, in pieces of up
- *   to 32 tokens.  One handle serves one stream at a time (the workspace is
- *   per handle).
+ *   a CUDA graph.  T <= 32 takes the weight-streaming decode kernels
+ *   (FLINT_NVFP4: W4A16, the codes dequantised into the MMA fragments), larger
+ *   T the grouped tensor-core path in chunks of FLINT_CHUNK tokens
+ *   (FLINT_NVFP4: the weight tiles dequantised to bf16 in shared memory).  One
+ *   handle serves one stream at a time (the workspace is per handle).
  * Errors: INVALID_ARG (null, misaligned, T < 1), CUDA (launch failed), or a
  * device status left by an earlier call. */
 FLINT_API flint_status_t flint_moe_forward(flint_moe_t h, const void* x, int T, void* y, cudaStream_t s);
