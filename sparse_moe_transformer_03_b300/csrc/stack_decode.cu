@@ -275,6 +275,35 @@ __host__ __device__ __forceinline__ int sk_rcum(int c, int G, int U) {
 // The producer is released (route_bar) as soon as the slots' experts exist.
 __device__ void sk_build_tables(int T, SkShared* sh, int lane) {
     DecodeTables* tab = &sh->tab;
+    if (T == 1) {
+        // one token: its six (distinct) experts are the routed slots 1..6 in
+        // increasing id order, expert of rank k in slot and pair 1 + k -- the
+        // same tables the general path below builds, from six shuffles
+        const int e = lane < TOPK ? sh->sel_e[lane] : E;
+        int rank = 0;
+#pragma unroll
+        for (int j = 0; j < TOPK; ++j) rank += __shfl_sync(0xFFFFFFFFu, e, j) < e ? 1 : 0;
+        if (lane < TOPK) {
+            tab->slot_expert[1 + rank] = e;
+            tab->slot_pair0[1 + rank] = 1 + rank;
+            sh->tok_pair[1 + rank][0] = 1 + rank;
+            sh->tok_w[1 + rank][0] = sh->sel_w[lane];
+        }
+        if (lane == 0) {
+            tab->n_slots = 1 + TOPK;
+            tab->n_pairs = 1 + TOPK;
+            tab->slot_pair0[1 + TOPK] = 1 + TOPK;
+            tab->T = 1;
+            tab->slot_expert[0] = SHARED;
+            tab->slot_pair0[0] = 0;
+            sh->tok_pair[0][0] = 0;
+            sh->tok_w[0][0] = 1.f;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh->route_bar);
+        __syncwarp();
+        return;
+    }
 #pragma unroll
     for (int k = 0; k < 8; ++k) sh->tmask[lane * 8 + k] = 0u;
     __syncwarp();
