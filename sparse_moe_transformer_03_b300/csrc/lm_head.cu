@@ -56,7 +56,6 @@ constexpr int LH_MAX_SLOTS = 64;
 constexpr int LH_BOX_ROWS = NV_CHUNK / 512;        // a chunk as 9 rows of 512 bytes (one TMA box)
 
 struct LmParams {
-    const uint8_t* nv;          // owned layout, units * LH_UNIT bytes
     float ts;                   // tensor scale
     const __nv_bfloat16* x;     // [T][H]
     float* logits;              // [T][V]
@@ -390,7 +389,7 @@ flint_status_t flint_lm_head_forward(flint_lm_head_t h, const void* x, int T, fl
     if (xb < lb + (size_t)T * h->V * 4 && lb < xb + (size_t)T * H * 2) return FLINT_ERR_INVALID_ARG;
     const flint_status_t st = lh_take_status(h);
     if (st != FLINT_OK) return st;
-    LmParams p{h->nv, h->ts, static_cast<const __nv_bfloat16*>(x), logits, T, h->V, h->units, 0, h->status_dev,
+    LmParams p{h->ts, static_cast<const __nv_bfloat16*>(x), logits, T, h->V, h->units, 0, h->status_dev,
                h->limit_ns};
     const int grid = h->units < h->num_sms ? h->units : h->num_sms;
     cudaError_t e;
